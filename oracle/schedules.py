@@ -1,0 +1,553 @@
+"""Oracle of the pipeline orderings: 1F1B, ZB-H1, ZB-H2 event graphs.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).  Plain Python.
+
+What is followed, and the readings taken where the pages leave a step open
+--------------------------------------------------------------------------
+Dependencies ([ZB-PP summary] §3.4 "critical dependency"; §3 Eqs. 4-5;
+[ZB proven] "Draw the event graph before the Gantt"):
+    F(s,j) after F(s-1,j) (+ T_comm);
+    B(s,j) after F(s,j) and after B(s+1,j) (+ T_comm);
+    W(s,j) after B(s,j) only;  the optimizer marker OPT(s) after every W of s.
+1F1B ([Pipeline schedules] "1F1B: same bubble, bounded memory"; [ZB-PP summary]
+§2 "Synchronous 1F1B"): stage s (0-indexed) runs min(P-1-s, m) warm-up
+forwards, then alternates one forward (while any remain) with one backward,
+then drains.  Its backward is the monolithic B+W, modelled as one fused op BW
+whose input gradient is released only at its end.
+ZB-H1 ([ZB-PP summary] §3.4 "Handcrafted Schedule ZB-H1", Table 2): 1F1B's F/B
+order (warm-up min(P-s, m) forwards counting the first steady one), with W
+split off and placed later.
+ZB-H2 ([ZB-PP summary] §3.4 "Handcrafted Schedule ZB-H2"): stage 0 runs 2P-1
+forwards before its first B; reading: stage s runs min(2(P-1-s)+1, m).
+W placement for both ZB orderings (reading of [ZB-PP summary] §3.4 and the
+heuristic's phases 2 and 4, "W insertion to fill bubbles", "Memory-triggered W
+insertion", "Cool-down"): on a simulated timeline each stage runs its next F/B
+the moment its dependencies are met; when the next F/B is not ready it runs
+its oldest pending W; a W is forced before an F when the stage's live
+microbatches (F done, W not done) reach L = P (H1, peak p M_B) or 2P-1 (H2,
+peak (2p-1) M_B); leftover W's drain in ascending microbatch order.
+With T_F = T_B = T_W this reproduces Table 2's bubbles exactly
+((p-1)(T_F+T_B+T_W), (p-1)(T_F+T_B-T_W), (p-1)(T_F+T_B-2T_W)); with unequal
+times it is a reading, not the paper's Figure 3 (which the pages do not show).
+Global serial order for a one-GPU replay: (simulated start, stage index).
+
+Metrics: per-stage span (Eq. 3: last end - first start), cost = max over
+stages, bubble rate = (cost - m (T_F+T_B+T_W)) / cost ([ZB-PP summary] §5
+"Metrics").  The [ZB proven] checker's denominator (global span x stages) is
+also computed, labelled separately.  Closed forms (P-1)/(m+P-1) and
+(P-1)/(v m + P-1) ([Pipeline schedules] "Interleaved stages").
+Memory model ([ZB-PP summary] "The Memory Model"): F: +M_B, B: +M_W - M_B,
+W: -M_W (BW: -M_B).
+"""
+
+from __future__ import annotations
+
+import itertools
+from collections import deque
+from dataclasses import dataclass, field
+
+KINDS = ("F", "B", "W", "BW", "OPT")
+SCHEDULES = ("1F1B", "ZBH1", "ZBH2")
+
+
+@dataclass(frozen=True)
+class Times:
+    F: float = 1.0
+    B: float = 1.0
+    W: float = 1.0
+    comm: float = 0.0
+
+    def dur(self, kind: str) -> float:
+        if kind == "BW":
+            return self.B + self.W
+        if kind == "OPT":
+            return 0.0
+        return getattr(self, kind)
+
+
+@dataclass
+class Event:
+    kind: str
+    stage: int
+    micro: int
+    start: float
+    end: float
+    deps: tuple = field(default_factory=tuple)
+
+    @property
+    def id(self):
+        return (self.kind, self.stage, self.micro)
+
+
+# --------------------------------------------------------------------------
+# closed forms
+# --------------------------------------------------------------------------
+def bubble_fraction(P: int, m: int, v: int = 1) -> float:
+    """(P-1) / (v m + P-1): GPipe / 1F1B (v = 1) and interleaved 1F1B."""
+    return (P - 1) / (v * m + P - 1)
+
+
+def table2_bubble(kind: str, P: int, t: Times) -> float:
+    """Bubble size of [ZB-PP summary] Table 2 (total idle per stage span)."""
+    if kind == "1F1B":
+        return (P - 1) * (t.F + t.B + t.W)
+    if kind == "ZBH1":
+        return (P - 1) * (t.F + t.B - t.W)
+    if kind == "ZBH2":
+        return (P - 1) * (t.F + t.B - 2 * t.W)
+    raise ValueError(kind)
+
+
+def table2_peak_mb(kind: str, P: int) -> int:
+    """Peak activation memory in units of M_B ([ZB-PP summary] Table 2)."""
+    return {"1F1B": P, "ZBH1": P, "ZBH2": 2 * P - 1}[kind]
+
+
+# --------------------------------------------------------------------------
+# per-stage F/B sequences
+# --------------------------------------------------------------------------
+def warmup_forwards(kind: str, P: int, m: int, s: int) -> int:
+    if kind == "1F1B":
+        return min(P - 1 - s, m)
+    if kind == "ZBH1":
+        return min(P - s, m)
+    if kind == "ZBH2":
+        return min(2 * (P - 1 - s) + 1, m)
+    raise ValueError(kind)
+
+
+def fb_sequence(kind: str, P: int, m: int, s: int):
+    """The fixed F/B (or F/BW) order of stage s; W's are placed by simulate()."""
+    w = warmup_forwards(kind, P, m, s)
+    seq = [("F", j) for j in range(w)]
+    nxt = w
+    for b in range(m):
+        if kind == "1F1B":
+            if nxt < m:
+                seq.append(("F", nxt))
+                nxt += 1
+            seq.append(("BW", b))
+        else:
+            seq.append(("B", b))
+            if nxt < m:
+                seq.append(("F", nxt))
+                nxt += 1
+    return seq
+
+
+def live_limit(kind: str, P: int):
+    return {"1F1B": None, "ZBH1": P, "ZBH2": 2 * P - 1}[kind]
+
+
+# --------------------------------------------------------------------------
+# dependencies
+# --------------------------------------------------------------------------
+def op_deps(kind: str, s: int, j: int, P: int, fused: bool):
+    """Ids this op waits for.  B(s+1,j) is BW(s+1,j) when backward is fused."""
+    bk = "BW" if fused else "B"
+    if kind == "F":
+        return (("F", s - 1, j),) if s > 0 else ()
+    if kind in ("B", "BW"):
+        d = [("F", s, j)]
+        if s < P - 1:
+            d.append((bk, s + 1, j))
+        return tuple(d)
+    if kind == "W":
+        return (("B", s, j),)
+    raise ValueError(kind)
+
+
+def _is_cross_stage(dep, s):
+    return dep[1] != s
+
+
+# --------------------------------------------------------------------------
+# list-scheduling simulator
+# --------------------------------------------------------------------------
+def simulate(kind: str, P: int, m: int, t: Times = Times()):
+    """Simulate one ordering; returns the list of Events (no OPT markers)."""
+    if P < 1 or m < 1:
+        raise ValueError("P and m must be >= 1")
+    fused = kind == "1F1B"
+    seqs = [fb_sequence(kind, P, m, s) for s in range(P)]
+    limit = live_limit(kind, P)
+    ptr = [0] * P
+    pending = [deque() for _ in range(P)]
+    live = [0] * P
+    t_free = [0.0] * P
+    waiting = [False] * P
+    end = {}
+    events = []
+
+    def has_work(s):
+        return ptr[s] < len(seqs[s]) or bool(pending[s])
+
+    def ready_at(s, k, j):
+        tt = 0.0
+        for d in op_deps(k, s, j, P, fused):
+            if d not in end:
+                return None
+            tt = max(tt, end[d] + (t.comm if _is_cross_stage(d, s) else 0.0))
+        return tt
+
+    def run(s, k, j, start):
+        e = start + t.dur(k)
+        deps = op_deps(k, s, j, P, fused)
+        events.append(Event(k, s, j, start, e, deps))
+        end[(k, s, j)] = e
+        t_free[s] = e
+        if k == "F":
+            live[s] += 1
+        elif k == "B":
+            pending[s].append(j)
+        elif k in ("W", "BW"):
+            live[s] -= 1
+
+    while any(has_work(s) for s in range(P)):
+        cands = [s for s in range(P) if has_work(s) and not waiting[s]]
+        if not cands:
+            raise RuntimeError("deadlock in simulate")
+        s = min(cands, key=lambda x: (t_free[x], x))
+        now = t_free[s]
+        nxt = seqs[s][ptr[s]] if ptr[s] < len(seqs[s]) else None
+        r = ready_at(s, nxt[0], nxt[1]) if nxt is not None else None
+        acted = True
+        if nxt is not None and r is not None and r <= now:
+            if (nxt[0] == "F" and limit is not None and live[s] >= limit
+                    and pending[s]):
+                run(s, "W", pending[s].popleft(), now)
+            else:
+                run(s, nxt[0], nxt[1], now)
+                ptr[s] += 1
+        elif pending[s]:
+            run(s, "W", pending[s].popleft(), now)
+        else:
+            acted = False
+            if r is not None:
+                t_free[s] = r
+            else:
+                later = [e for e in end.values() if e > now]
+                later += [t_free[o] for o in range(P)
+                          if o != s and has_work(o) and t_free[o] > now]
+                if later:
+                    t_free[s] = min(later)
+                else:
+                    waiting[s] = True
+        if acted:
+            for o in range(P):
+                waiting[o] = False
+    return events
+
+
+def global_order(events):
+    """One-GPU serial replay order: (start, stage), then append OPT markers."""
+    evs = sorted(events, key=lambda e: (e.start, e.stage))
+    ops = [(e.kind, e.stage, e.micro) for e in evs]
+    P = 1 + max(e.stage for e in events)
+    last = {}
+    for i, (k, s, j) in enumerate(ops):
+        last[s] = i
+    # insert OPT(s) right after the last op of stage s, keeping relative order
+    out = []
+    for i, op in enumerate(ops):
+        out.append(op)
+        for s in range(P):
+            if last.get(s) == i:
+                out.append(("OPT", s, 0))
+    return out
+
+
+def make_schedule(kind: str, P: int, m: int, t: Times = Times()):
+    """Events and the global op list (with OPT markers) of one ordering."""
+    evs = simulate(kind, P, m, t)
+    return evs, global_order(evs)
+
+
+def stage_lists(ops, P: int):
+    """Per-stage op sequences (kind, micro) from a global op list."""
+    out = [[] for _ in range(P)]
+    for k, s, j in ops:
+        out[s].append((k, j))
+    return out
+
+
+# --------------------------------------------------------------------------
+# metrics
+# --------------------------------------------------------------------------
+def stage_spans(events, P: int):
+    spans = []
+    for s in range(P):
+        ev = [e for e in events if e.stage == s]
+        spans.append(max(e.end for e in ev) - min(e.start for e in ev))
+    return spans
+
+
+def cost(events, P: int) -> float:
+    """Eq. 3: max over stages of (end of last pass - start of first pass)."""
+    return max(stage_spans(events, P))
+
+
+def bubble_rate(events, P: int, m: int, t: Times) -> float:
+    """(cost - m (T_F + T_B + T_W)) / cost  ([ZB-PP summary] §5 Metrics)."""
+    c = cost(events, P)
+    return (c - m * (t.F + t.B + t.W)) / c
+
+
+def peak_live(events, P: int):
+    """Peak live microbatches per stage (F done, W / BW not yet done)."""
+    peaks = []
+    for s in range(P):
+        ev = sorted((e for e in events if e.stage == s), key=lambda e: e.start)
+        cur = pk = 0
+        for e in ev:
+            if e.kind == "F":
+                cur += 1
+                pk = max(pk, cur)
+            elif e.kind in ("W", "BW"):
+                cur -= 1
+        peaks.append(pk)
+    return peaks
+
+
+def memory_ledger(ops, P: int, M_B: float, M_W: float):
+    """Running activation memory per stage under the Delta-M model.
+
+    F: +M_B;  B: +M_W - M_B;  W: -M_W;  BW (B then W): -M_B.
+    Returns (peak per stage, final per stage).
+    """
+    cur = [0.0] * P
+    peak = [0.0] * P
+    for k, s, j in ops:
+        if k == "F":
+            cur[s] += M_B
+        elif k == "B":
+            cur[s] += M_W - M_B
+        elif k == "W":
+            cur[s] -= M_W
+        elif k == "BW":
+            cur[s] -= M_B
+        peak[s] = max(peak[s], cur[s])
+    return peak, cur
+
+
+# --------------------------------------------------------------------------
+# validators
+# --------------------------------------------------------------------------
+class ScheduleError(ValueError):
+    """Raised by the validators; ``code`` names the rule that failed."""
+
+    def __init__(self, code: str, detail: str = ""):
+        super().__init__(f"{code}: {detail}" if detail else code)
+        self.code = code
+
+
+def validate_ops(ops, P: int, m: int):
+    """Check a global op list for legal one-GPU replay.
+
+    Rules ([ZB-PP summary] §3.4 dependencies; [ZB proven] "Draw the event
+    graph before the Gantt"): every (s, j) has exactly one F and either one B
+    and one W or one fused BW; each op appears after its producers in list
+    order; W/BW of a stage run in ascending microbatch order (so fp32
+    accumulation follows a fixed order); OPT(s), if present, appears once and
+    after every W/BW of stage s, and nothing of stage s follows it.
+    Raises ScheduleError with code in {"kind", "stage", "micro", "duplicate",
+    "mixed", "missing", "dependency", "w_order", "opt"}.
+    """
+    seen = {}
+    last_w = [-1] * P
+    opt_done = [False] * P
+    for idx, op in enumerate(ops):
+        if len(op) != 3:
+            raise ScheduleError("kind", str(op))
+        k, s, j = op
+        if k not in KINDS:
+            raise ScheduleError("kind", str(op))
+        if not (0 <= s < P):
+            raise ScheduleError("stage", str(op))
+        if k != "OPT" and not (0 <= j < m):
+            raise ScheduleError("micro", str(op))
+        if opt_done[s]:
+            raise ScheduleError("opt", f"{op} after OPT of its stage")
+        if k == "OPT":
+            opt_done[s] = True
+            continue
+        if (k, s, j) in seen:
+            raise ScheduleError("duplicate", str(op))
+        if k == "BW" and (("B", s, j) in seen or ("W", s, j) in seen):
+            raise ScheduleError("mixed", str(op))
+        if k in ("B", "W") and ("BW", s, j) in seen:
+            raise ScheduleError("mixed", str(op))
+        fused_next = ("BW", s + 1, j) in seen
+        if k == "F":
+            need = [("F", s - 1, j)] if s > 0 else []
+        elif k in ("B", "BW"):
+            need = [("F", s, j)]
+            if s < P - 1:
+                need.append(("BW", s + 1, j) if fused_next else ("B", s + 1, j))
+        else:  # W
+            need = [("B", s, j)]
+        for d in need:
+            if d not in seen:
+                raise ScheduleError("dependency", f"{op} before {d}")
+        if k in ("W", "BW"):
+            if j <= last_w[s]:
+                raise ScheduleError("w_order", str(op))
+            last_w[s] = j
+        seen[(k, s, j)] = idx
+    for s in range(P):
+        for j in range(m):
+            has_f = ("F", s, j) in seen
+            split = ("B", s, j) in seen and ("W", s, j) in seen
+            fused = ("BW", s, j) in seen
+            if not has_f or not (split or fused):
+                raise ScheduleError("missing", f"stage {s} micro {j}")
+    return True
+
+
+def inspect_events(events, stage_count: int):
+    """Event-interval validator after [ZB proven] "Validate the schedule as data".
+
+    events: iterable of dicts {id, stage, micro, kind, start, end, dependsOn?}.
+    Rejects (ScheduleError code): "stage_count", "duplicate_task",
+    "invalid_stage", "invalid_interval", "missing_dependency",
+    "dependency_violation", "stage_overlap".
+    Returns dict(span, busy, bubble_ratio_global, bubble_rate_eq3,
+    unfinished_activations_b, unfinished_activations_w).
+      * bubble_ratio_global: 1 - busy / (stage_count * span), span from t=0
+        (the [ZB proven] checker's declared denominator);
+      * bubble_rate_eq3: (cost - busy_per_stage_max...) reported as
+        1 - busy / (stage_count * cost) with cost = max per-stage span (Eq. 3);
+      * unfinished_activations_b: F opens, B closes (the checker's ledger);
+      * unfinished_activations_w: F opens, W or BW closes (the lifetime of
+        deferred-W activations, [ZB-PP summary] "The Memory Model").
+    """
+    if not isinstance(stage_count, int) or stage_count < 2:
+        raise ScheduleError("stage_count")
+    ids = [e["id"] for e in events]
+    by_id = {e["id"]: e for e in events}
+    if len(by_id) != len(ids):
+        raise ScheduleError("duplicate_task")
+    for e in events:
+        st = e["stage"]
+        if not isinstance(st, int) or st < 0 or st >= stage_count:
+            raise ScheduleError("invalid_stage", str(e["id"]))
+        if not (e["start"] >= 0 and e["end"] > e["start"]):
+            raise ScheduleError("invalid_interval", str(e["id"]))
+        for d in e.get("dependsOn", ()) or ():
+            if d not in by_id:
+                raise ScheduleError("missing_dependency", f"{e['id']} -> {d}")
+            if by_id[d]["end"] > e["start"]:
+                raise ScheduleError("dependency_violation", f"{e['id']} -> {d}")
+    per_stage = {}
+    for e in events:
+        per_stage.setdefault(e["stage"], []).append(e)
+    for st, lst in per_stage.items():
+        lst = sorted(lst, key=lambda e: e["start"])
+        for a, b in zip(lst, lst[1:]):
+            if a["end"] > b["start"]:
+                raise ScheduleError("stage_overlap", f"{a['id']} / {b['id']}")
+    span = max(e["end"] for e in events)
+    busy = sum(e["end"] - e["start"] for e in events)
+    cost_eq3 = max(max(e["end"] for e in lst) - min(e["start"] for e in lst)
+                   for lst in per_stage.values())
+    live_b = {}
+    live_w = {}
+    for e in events:
+        key = e["micro"], e["stage"]
+        if e["kind"] == "F":
+            live_b[e["micro"]] = live_b.get(e["micro"], 0) + 1
+            live_w[key] = live_w.get(key, 0) + 1
+        if e["kind"] in ("B", "BW"):
+            live_b[e["micro"]] = max(0, live_b.get(e["micro"], 0) - 1)
+        if e["kind"] in ("W", "BW"):
+            live_w[key] = max(0, live_w.get(key, 0) - 1)
+    return {
+        "span": span,
+        "busy": busy,
+        "bubble_ratio_global": 1.0 - busy / (stage_count * span),
+        "bubble_rate_eq3": 1.0 - busy / (stage_count * cost_eq3),
+        "unfinished_activations_b": sum(live_b.values()),
+        "unfinished_activations_w": sum(live_w.values()),
+    }
+
+
+def events_as_dicts(events):
+    """Convert simulator Events to validator dicts (ids as 'k:s:j' strings)."""
+    def sid(i):
+        return f"{i[0]}:{i[1]}:{i[2]}"
+    return [{"id": sid(e.id), "stage": e.stage, "micro": e.micro, "kind": e.kind,
+             "start": e.start, "end": e.end, "dependsOn": [sid(d) for d in e.deps]}
+            for e in events]
+
+
+# --------------------------------------------------------------------------
+# brute force (tiny cases only)
+# --------------------------------------------------------------------------
+def _stage_orders(P, m, s, split=True):
+    """All per-stage orders of F/B/W (or F/BW) for stage s obeying local deps."""
+    ops = []
+    for j in range(m):
+        ops.append(("F", j))
+        if split:
+            ops += [("B", j), ("W", j)]
+        else:
+            ops.append(("BW", j))
+    res = []
+    for perm in itertools.permutations(ops):
+        pos = {o: i for i, o in enumerate(perm)}
+        ok = True
+        for j in range(m):
+            if split:
+                if not (pos[("F", j)] < pos[("B", j)] < pos[("W", j)]):
+                    ok = False
+                    break
+            elif not pos[("F", j)] < pos[("BW", j)]:
+                ok = False
+                break
+        if ok:
+            res.append(list(perm))
+    return res
+
+
+def evaluate_orders(orders, P, m, t: Times, fused=False):
+    """As-soon-as-possible timeline of fixed per-stage orders; returns cost or
+    None if the orders deadlock."""
+    end = {}
+    ptr = [0] * P
+    t_free = [0.0] * P
+    total = sum(len(o) for o in orders)
+    done = 0
+    progress = True
+    while done < total and progress:
+        progress = False
+        for s in range(P):
+            while ptr[s] < len(orders[s]):
+                k, j = orders[s][ptr[s]]
+                deps = op_deps(k, s, j, P, fused)
+                if any(d not in end for d in deps):
+                    break
+                r = max([t_free[s]] + [end[d] + (t.comm if d[1] != s else 0.0) for d in deps])
+                end[(k, s, j)] = r + t.dur(k)
+                t_free[s] = end[(k, s, j)]
+                ptr[s] += 1
+                done += 1
+                progress = True
+    if done < total:
+        return None
+    spans = []
+    for s in range(P):
+        st = [end[(k, s, j)] - t.dur(k) for k, j in orders[s]]
+        en = [end[(k, s, j)] for k, j in orders[s]]
+        spans.append(max(en) - min(st))
+    return max(spans)
+
+
+def brute_force_min_cost(P, m, t: Times, split=True):
+    """Minimum Eq. 3 cost over all per-stage orders (P, m tiny)."""
+    per_stage = [_stage_orders(P, m, s, split) for s in range(P)]
+    best = None
+    for combo in itertools.product(*per_stage):
+        c = evaluate_orders(list(combo), P, m, t, fused=not split)
+        if c is not None and (best is None or c < best):
+            best = c
+    return best

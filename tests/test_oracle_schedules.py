@@ -1,0 +1,227 @@
+"""Pins of the schedule oracle against what the pages fix.
+
+* the bubble closed forms and their printed table ("Pipeline Schedules",
+  section "Interleaved stages") -> tests/golden/bubble_table.txt;
+* Table 2 of the ZB-PP summary: bubble sizes (p-1)(T_F+T_B+T_W),
+  (p-1)(T_F+T_B-T_W), (p-1)(T_F+T_B-2T_W) at equal times, peak memory
+  p M_B / p M_B / (2p-1) M_B; 1F1B keeps P-s microbatches in flight on stage s;
+* the schedule checker's worked example ("Zero-Bubble Pipeline Parallelism,
+  Proven", section "Validate the schedule as data") ->
+  tests/golden/checker_example.txt, with its four rejection cases;
+* topological validity of every generated list with OPT after all W;
+* brute force over every per-stage order at P=2, m=2.
+"""
+
+import os
+
+import pytest
+
+from oracle import schedules as S
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLD, name)) as fh:
+        return [ln.split() for ln in fh if ln.strip() and not ln.startswith("#")]
+
+
+def test_closed_form_matches_printed_table():
+    rows = _rows("bubble_table.txt")
+    assert len(rows) == 3
+    for P, m, v1, v2, v4 in rows:
+        P, m = int(P), int(m)
+        for v, printed in ((1, v1), (2, v2), (4, v4)):
+            assert round(100 * S.bubble_fraction(P, m, v), 1) == float(printed)
+
+
+@pytest.mark.parametrize("P,m", [(4, 8), (8, 8), (8, 16), (2, 5), (4, 24), (3, 7)])
+def test_simulated_1f1b_equals_closed_form(P, m):
+    t = S.Times()
+    ev, _ = S.make_schedule("1F1B", P, m, t)
+    assert abs(S.bubble_rate(ev, P, m, t) - S.bubble_fraction(P, m)) < 1e-12
+
+
+@pytest.mark.parametrize("P,m", [(4, 8), (8, 16), (4, 24), (8, 24), (3, 9), (2, 6)])
+@pytest.mark.parametrize("kind", S.SCHEDULES)
+def test_table2_bubble_at_equal_times(kind, P, m):
+    # ZB-H2's zero bubble needs m >= 2P-1 (its warm-up); every case here has it.
+    for unit in (1.0, 2.5):
+        t = S.Times(unit, unit, unit)
+        ev, _ = S.make_schedule(kind, P, m, t)
+        idle = S.cost(ev, P) - m * (t.F + t.B + t.W)
+        assert abs(idle - S.table2_bubble(kind, P, t)) < 1e-9
+
+
+@pytest.mark.parametrize("P,m", [(4, 8), (8, 16), (8, 24)])
+def test_table2_bubble_also_at_half_w(P, m):
+    # T_W = T_F / 2 = T_B / 2 is another point where the reading meets Table 2.
+    t = S.Times(1.0, 1.0, 0.5)
+    for kind in S.SCHEDULES:
+        ev, _ = S.make_schedule(kind, P, m, t)
+        idle = S.cost(ev, P) - m * (t.F + t.B + t.W)
+        assert abs(idle - S.table2_bubble(kind, P, t)) < 1e-9
+
+
+@pytest.mark.parametrize("P,m", [(4, 8), (8, 16), (8, 24), (5, 11)])
+def test_peak_in_flight(P, m):
+    ev, _ = S.make_schedule("1F1B", P, m)
+    assert S.peak_live(ev, P) == [min(P - s, m) for s in range(P)]
+    for kind in ("ZBH1", "ZBH2"):
+        ev, _ = S.make_schedule(kind, P, m)
+        assert S.peak_live(ev, P)[0] == min(S.table2_peak_mb(kind, P), m)
+        assert max(S.peak_live(ev, P)) <= S.table2_peak_mb(kind, P)
+
+
+def test_zbh1_stage0_is_one_forward_one_b_one_w():
+    # "typically follows 1F-1B-1W pattern" ([ZB-PP summary] heuristic phase 2).
+    _, ops = S.make_schedule("ZBH1", 4, 8)
+    st0 = [(k, j) for k, s, j in ops if s == 0]
+    exp = [("F", j) for j in range(4)]
+    for j in range(4):
+        exp += [("B", j), ("W", j), ("F", j + 4)]
+    for j in range(4, 8):
+        exp += [("B", j), ("W", j)]
+    exp.append(("OPT", 0))
+    assert st0 == exp
+
+
+def test_zbh2_stage0_warmup_is_2p_minus_1():
+    _, ops = S.make_schedule("ZBH2", 4, 8)
+    st0 = [(k, j) for k, s, j in ops if s == 0]
+    assert st0[:7] == [("F", j) for j in range(7)]
+    assert st0[7] == ("B", 0)
+
+
+@pytest.mark.parametrize("kind", S.SCHEDULES)
+@pytest.mark.parametrize("P,m", [(1, 3), (2, 1), (4, 8), (8, 16), (8, 24), (4, 3), (6, 13)])
+def test_generated_lists_are_valid(kind, P, m):
+    ev, ops = S.make_schedule(kind, P, m)
+    assert S.validate_ops(ops, P, m)
+    n_expect = P * m * (2 if kind == "1F1B" else 3) + P
+    assert len(ops) == n_expect
+    for s in range(P):
+        lst = [op for op in ops if op[1] == s]
+        assert lst[-1][0] == "OPT"
+    if P >= 2:
+        r = S.inspect_events(S.events_as_dicts(ev), P)
+        assert r["unfinished_activations_w"] == 0
+        assert r["unfinished_activations_b"] == 0
+
+
+def _checker_events():
+    evs = []
+    for ident, st, mi, kind, a, b, deps in _rows("checker_example.txt"):
+        evs.append({"id": ident, "stage": int(st), "micro": int(mi), "kind": kind,
+                    "start": float(a), "end": float(b),
+                    "dependsOn": [] if deps == "-" else deps.split(",")})
+    return evs
+
+
+def test_checker_worked_example():
+    evs = _checker_events()
+    r = S.inspect_events(evs, 2)
+    assert r["span"] == 8
+    assert r["unfinished_activations_b"] == 0
+    assert r["unfinished_activations_w"] == 0
+    assert 0 <= r["bubble_ratio_global"] < 0.3
+    assert r["bubble_ratio_global"] == 1 - 12 / 16
+    assert r == S.inspect_events(list(evs), 2)
+
+
+@pytest.mark.parametrize("extra,code", [
+    ({"id": "s0f0", "stage": 0, "micro": 9, "kind": "F", "start": 8, "end": 9}, "duplicate_task"),
+    ({"id": "bad", "stage": 2, "micro": 0, "kind": "W", "start": 8, "end": 9}, "invalid_stage"),
+    ({"id": "bad", "stage": 0, "micro": 2, "kind": "F", "start": 0.5, "end": 1.5}, "stage_overlap"),
+    ({"id": "bad", "stage": 1, "micro": 2, "kind": "B", "start": 0, "end": 1,
+      "dependsOn": ["s0f1"]}, "dependency_violation"),
+    ({"id": "bad", "stage": 1, "micro": 2, "kind": "B", "start": 9, "end": 10,
+      "dependsOn": ["nope"]}, "missing_dependency"),
+    ({"id": "bad", "stage": 1, "micro": 2, "kind": "B", "start": 9, "end": 9}, "invalid_interval"),
+])
+def test_checker_rejections(extra, code):
+    with pytest.raises(S.ScheduleError) as ei:
+        S.inspect_events(_checker_events() + [extra], 2)
+    assert ei.value.code == code
+
+
+def test_validate_ops_rejections():
+    P, m = 2, 2
+    _, ops = S.make_schedule("ZBH1", P, m)
+    ok = list(ops)
+    assert S.validate_ops(ok, P, m)
+    # dependency: B before its F
+    bad = [op for op in ok if op != ("B", 1, 0)]
+    bad.insert(0, ("B", 1, 0))
+    with pytest.raises(S.ScheduleError) as e:
+        S.validate_ops(bad, P, m)
+    assert e.value.code == "dependency"
+    # missing W
+    with pytest.raises(S.ScheduleError) as e:
+        S.validate_ops([op for op in ok if op != ("W", 0, 1)], P, m)
+    assert e.value.code == "missing"
+    # duplicate
+    with pytest.raises(S.ScheduleError) as e:
+        S.validate_ops(ok[:1] + ok, P, m)
+    assert e.value.code == "duplicate"
+    # W descending on a stage
+    i0, i1 = ok.index(("W", 0, 0)), ok.index(("W", 0, 1))
+    sw = list(ok)
+    sw[i0], sw[i1] = sw[i1], sw[i0]
+    with pytest.raises(S.ScheduleError) as e:
+        S.validate_ops(sw, P, m)
+    assert e.value.code in ("w_order", "dependency")
+    # OPT before the last W of its stage
+    o = [op for op in ok if op != ("OPT", 0, 0)]
+    o.insert(o.index(("W", 0, 1)), ("OPT", 0, 0))
+    with pytest.raises(S.ScheduleError) as e:
+        S.validate_ops(o, P, m)
+    assert e.value.code == "opt"
+    # unknown stage / micro / kind
+    for op, code in ((("F", 2, 0), "stage"), (("F", 0, 5), "micro"), (("X", 0, 0), "kind")):
+        with pytest.raises(S.ScheduleError) as e:
+            S.validate_ops(ok + [op], P, m)
+        assert e.value.code == code
+    # B and BW for the same (s, j)
+    with pytest.raises(S.ScheduleError) as e:
+        S.validate_ops(ok[:-1] + [("BW", 0, 1)], P, m)
+    assert e.value.code in ("mixed", "duplicate", "w_order", "opt")
+
+
+def test_brute_force_lower_bounds_the_generators():
+    t = S.Times()
+    best_split = S.brute_force_min_cost(2, 2, t, split=True)
+    best_fused = S.brute_force_min_cost(2, 2, t, split=False)
+    assert best_split <= best_fused
+    for kind in ("ZBH1", "ZBH2"):
+        ev, _ = S.make_schedule(kind, 2, 2, t)
+        assert S.cost(ev, 2) >= best_split
+    ev, _ = S.make_schedule("1F1B", 2, 2, t)
+    assert S.cost(ev, 2) == best_fused  # 1F1B is optimal among fused orders here
+
+
+def test_memory_ledger_peaks():
+    # Delta-M model: 1F1B peak on stage s is (P-s) M_B; ZB-H2 stage 0 is (2P-1) M_B.
+    P, m = 4, 8
+    M_B, M_W = 10.0, 6.0
+    _, ops = S.make_schedule("1F1B", P, m)
+    peak, final = S.memory_ledger(ops, P, M_B, M_W)
+    assert peak == [(P - s) * M_B for s in range(P)]
+    assert final == [0.0] * P
+    _, ops = S.make_schedule("ZBH2", P, m)
+    peak, final = S.memory_ledger(ops, P, M_B, M_W)
+    assert peak[0] == (2 * P - 1) * M_B
+    assert final == [0.0] * P
+    _, ops = S.make_schedule("ZBH1", P, m)
+    peak, _ = S.memory_ledger(ops, P, M_B, M_W)
+    assert peak[0] == P * M_B
+
+
+def test_comm_time_delays_dependents():
+    t = S.Times(1.0, 1.0, 1.0, comm=0.25)
+    ev, _ = S.make_schedule("ZBH1", 3, 6, t)
+    ends = {e.id: e.end for e in ev}
+    for e in ev:
+        for d in e.deps:
+            gap = t.comm if d[1] != e.stage else 0.0
+            assert e.start >= ends[d] + gap - 1e-12
