@@ -1,0 +1,220 @@
+/*
+ * zb.h — C ABI of the GB300 split-backward MLP stage library.
+ *
+ * One pipeline stage's transformer MLP block with its backward split in two,
+ * after "Zero Bubble Pipeline Parallelism" (paper-graph-ui summary of arXiv
+ * 2401.10241, §2 "The Unexploited Opportunity" and §3.4 "The Backward Pass
+ * Decomposition"):
+ *   F  (forward):           H = X W1 (+b1);  A = GeLU(H);  Y = A W2 (+b2)
+ *   B  (input gradient):    dA = dY W2^T;  dH = dA * GeLU'(H);  dX = dH W1^T
+ *   W  (weight gradient):   dW2 += A^T dY;  dW1 += X^T dH  (fp32, accumulated)
+ * For a linear map the two halves are Xbar = Ybar W^T and Wbar = X^T Ybar
+ * ("Pipeline Schedules: GPipe, 1F1B and Zero Bubble", section "Zero bubble:
+ * split the backward pass").  A per-stage F/B/W executor replays 1F1B, ZB-H1
+ * and ZB-H2 orderings for all P stages serially on one GPU (summary §3.4
+ * "Handcrafted Schedule ZB-H1 / ZB-H2", Table 2).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Layout: row-major.  X[M,h], W1[h,f], W2[f,h], H/A/dH[M,f], Y/dY/dX[M,h],
+ *    dW1[h,f] and dW2[f,h] in fp32, b1[f], b2[h] in the block dtype, db1[f],
+ *    db2[h] in fp32.  Leading dimensions are the row widths (dense tensors).
+ *  - Ownership: the caller owns every buffer (device memory unless stated).
+ *    The library never allocates device memory; the schedule executor works
+ *    inside the caller's workspace.  Pointers are not retained after return.
+ *  - Alignment: device pointers must be 16-byte aligned; for bf16 blocks h and
+ *    f must be multiples of 8 (16-byte rows for the tensor-memory-access
+ *    copies).  Violations return ZB_ERR_ALIGN.  M may be any value >= 1.
+ *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream) and the call returns without
+ *    waiting.  A device-side wait that gives up (bounded spin in the GEMM
+ *    pipeline) sets a device error word; it is reported as ZB_ERR_TIMEOUT by
+ *    zb_sync_status().  Launch failures are reported as ZB_ERR_CUDA at once.
+ *  - Errors: every call returns a zb_status; zb_last_error() returns a
+ *    thread-local, human-readable message for the last failing call.
+ *  - Determinism: for fixed shapes the same inputs give the same output bits;
+ *    the W pass adds each microbatch's product into the fp32 gradient with a
+ *    fixed tile order, so deferred-W and fused-backward replays that visit
+ *    microbatches in the same (ascending) order are bit-identical.
+ */
+#ifndef ZB_GB300_H
+#define ZB_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zb_status {
+    ZB_OK = 0,
+    ZB_ERR_INVALID_ARG = 1,  /* NULL where a pointer is required, bad enum   */
+    ZB_ERR_SHAPE = 2,        /* M, h, f, P or m out of range                 */
+    ZB_ERR_ALIGN = 3,        /* pointer not 16-byte aligned, h/f not mult. 8 */
+    ZB_ERR_DTYPE = 4,        /* dtype / activation combination unsupported   */
+    ZB_ERR_SCHEDULE = 5,     /* op list not a legal replay (dependency,
+                                duplicate, missing op, OPT misplaced)        */
+    ZB_ERR_W_ORDER = 6,      /* W / BW of a stage not in ascending micro     */
+    ZB_ERR_BUDGET = 7,       /* peak live activation bytes > mem limit       */
+    ZB_ERR_WORKSPACE = 8,    /* workspace missing or too small               */
+    ZB_ERR_CUDA = 9,         /* a CUDA runtime call or launch failed         */
+    ZB_ERR_TIMEOUT = 10,     /* a bounded device-side wait gave up           */
+    ZB_ERR_UNSUPPORTED = 11  /* no kernel for this device / configuration    */
+} zb_status;
+
+typedef enum zb_dtype { ZB_DT_F32 = 0, ZB_DT_BF16 = 1 } zb_dtype;
+
+/* GeLU(x) = x Phi(x) (exact erf form, the default) or its tanh approximation;
+ * NONE makes the block the single linear map Y = X W1 (W2, H, A unused). */
+typedef enum zb_act { ZB_ACT_NONE = 0, ZB_ACT_GELU_ERF = 1, ZB_ACT_GELU_TANH = 2 } zb_act;
+
+typedef struct zb_block {
+    int64_t M;        /* tokens per microbatch (rows of X)                     */
+    int64_t h;        /* hidden width                                          */
+    int64_t f;        /* ffn width; for ZB_ACT_NONE the output width of W1     */
+    int32_t dtype;    /* zb_dtype of X, W, H, A, Y, dY, dH, dX, b              */
+    int32_t act;      /* zb_act                                                */
+    int32_t has_bias; /* 1: b1/b2 added in F, db1/db2 accumulated in W         */
+    int32_t reserved; /* must be 0                                             */
+} zb_block;
+
+/* Supported combinations: BF16 with any zb_act (tensor-core path, fp32
+ * accumulation); F32 with ZB_ACT_NONE (true fp32 FFMA path, no TF32). */
+
+/* ------------------------------------------------------------------------ */
+/* Single passes                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* F of one microbatch.  Writes H_save and A_save ([M,f], kept for B and W)
+ * and Y ([M,h]).  b1/b2 are read only when has_bias (else may be NULL).
+ * ZB_ACT_NONE: Y = X W1 ([M,f]); W2, b2, H_save, A_save may be NULL. */
+zb_status zb_forward(const zb_block* blk, const void* X, const void* W1,
+                     const void* W2, const void* b1, const void* b2,
+                     void* H_save, void* A_save, void* Y, void* stream);
+
+/* B of one microbatch (the critical-path input gradient).  Reads dY [M,h],
+ * W1, W2 and H_save; writes dH_out ([M,f], kept for W) and dX ([M,h]).
+ * dA = dY W2^T stays in fp32 inside the kernel and is never stored.
+ * ZB_ACT_NONE: dX = dY W1^T with dY [M,f]; W2, H_save, dH_out unused. */
+zb_status zb_backward_input(const zb_block* blk, const void* dY, const void* W1,
+                            const void* W2, const void* H_save, void* dH_out,
+                            void* dX, void* stream);
+
+/* W of one microbatch (the deferrable weight gradient).
+ * accumulate = 0: dW1 = X^T dH, dW2 = A^T dY (db1 = colsum dH, db2 = colsum dY)
+ * accumulate = 1: the same products are added to the fp32 buffers.
+ * ZB_ACT_NONE: dW1 (+)= X^T dY with dY [M,f]; A_save, dH, dW2 unused. */
+zb_status zb_backward_weight(const zb_block* blk, const void* X, const void* A_save,
+                             const void* dH, const void* dY, float* dW1, float* dW2,
+                             float* db1, float* db2, int accumulate, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Schedules                                                                */
+/* ------------------------------------------------------------------------ */
+
+typedef enum zb_op_kind {
+    ZB_OP_F = 0, ZB_OP_B = 1, ZB_OP_W = 2,
+    ZB_OP_BW = 3,  /* fused B then W of one (stage, micro): 1F1B's backward  */
+    ZB_OP_OPT = 4  /* optimizer marker of a stage: after all its W, no-op    */
+} zb_op_kind;
+
+/* Pass id (i, j, c) of the summary's ILP formulation (Appendix G). */
+typedef struct zb_op {
+    uint8_t kind;    /* zb_op_kind */
+    uint8_t pad;     /* must be 0  */
+    uint16_t stage;  /* 0 .. P-1   */
+    uint32_t micro;  /* 0 .. m-1 (ignored for OPT) */
+} zb_op;
+
+typedef enum zb_schedule_kind { ZB_SCHED_1F1B = 0, ZB_SCHED_ZBH1 = 1, ZB_SCHED_ZBH2 = 2 } zb_schedule_kind;
+
+/* Generate the one-GPU replay list of a handcrafted ordering for P stages and
+ * m microbatches at equal pass times (T_F = T_B = T_W, no communication):
+ *   1F1B : warm-up min(P-1-s, m) forwards, then F / fused BW alternation;
+ *   ZB-H1: 1F1B's F/B order, W split off; a W runs when the next F/B is not
+ *          ready, and before an F when P microbatches are live on the stage;
+ *   ZB-H2: warm-up min(2(P-1-s)+1, m) forwards, live limit 2P-1.
+ * Ops are ordered by simulated start time, then stage; OPT(s) follows the
+ * last op of stage s.  out may be NULL to query the length; otherwise *n_ops
+ * holds its capacity on entry and the length on return (ZB_ERR_INVALID_ARG
+ * if too small).  Host only, no device work. */
+zb_status zb_make_schedule(int32_t kind, int32_t P, int32_t m, zb_op* out, size_t* n_ops);
+
+typedef struct zb_pipeline {
+    int32_t P;                 /* stages                                     */
+    int32_t m;                 /* microbatches                               */
+    zb_block blk;              /* every stage has the same block shape; for
+                                  P > 1 the block must map [M,h] to [M,h]    */
+    uint64_t mem_limit_bytes;  /* 0 = unlimited; else ZB_ERR_BUDGET when the
+                                  peak live activation bytes exceed it       */
+    int32_t zero_grads;        /* 1: the first W/BW of each stage overwrites
+                                  dW/db (accumulate = 0); 0: always add      */
+    int32_t timing;            /* 1: record CUDA events around every op and
+                                  GEMM launch, synchronise at the end and
+                                  fill the timing fields of zb_run_stats     */
+} zb_pipeline;
+
+typedef struct zb_stage_params {
+    const void* W1; const void* W2; const void* b1; const void* b2;
+    float* dW1; float* dW2; float* db1; float* db2;
+} zb_stage_params;
+
+typedef struct zb_run_stats {
+    uint64_t workspace_bytes;   /* arena bytes used by this op list            */
+    uint64_t peak_live_bytes;   /* ledger peak of live saved activations       */
+    uint32_t n_ops;             /* ops replayed (OPT included)                 */
+    uint32_t n_gemm_launches;   /* tensor-core / FFMA GEMM launches enqueued   */
+    double total_ms;            /* timing: first op start to last op end       */
+    double kind_ms[4];          /* timing: summed op time per F, B, W, BW      */
+    double gemm_ms;             /* timing: summed GEMM kernel time             */
+    float* op_ms;               /* caller array of n_ops floats or NULL        */
+} zb_run_stats;
+
+/* Validate an op list and size its arena.  Checks: every (stage, micro) has
+ * one F and either one B and one W or one BW; producers precede consumers
+ * (F(s-1,j) -> F(s,j) -> B(s,j) <- B(s+1,j); B(s,j) -> W(s,j)); W/BW of a
+ * stage in ascending micro; OPT at most once per stage, after all its W.
+ * Lifetimes (the deferred-W activation store): F saves X, H, A; B frees H and
+ * saves dH; W frees X, A, dH and dY; a stage's Y is the next stage's X and a
+ * stage's dX the previous stage's dY (pointer hand-off inside the arena).
+ * Returns the arena size (*bytes) and the ledger peak (*peak_live_bytes,
+ * may be NULL).  Host only. */
+zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_op* ops, size_t n_ops,
+                                     size_t* bytes, size_t* peak_live_bytes);
+
+/* Replay an op list over P stages on one GPU.
+ *   stages[P]       weights and fp32 gradient buffers per stage;
+ *   X0[m]           stage-0 inputs [M,h] (device pointers);
+ *   dY_last[m]      output gradients entering stage P-1 [M,h];
+ *   dX0_out[m]      optional (array or entries may be NULL): stage-0 dX;
+ *   Y_last_out[m]   optional: stage P-1 outputs Y;
+ *   workspace       device buffer of >= zb_schedule_workspace_size bytes,
+ *                   256-byte aligned;
+ *   stats           optional (NULL to skip).
+ * Kernels are enqueued on `stream` in list order. */
+zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage_params* stages,
+                                const void* const* X0, const void* const* dY_last,
+                                void* const* dX0_out, void* const* Y_last_out,
+                                const zb_op* ops, size_t n_ops, void* workspace,
+                                size_t ws_bytes, zb_run_stats* stats, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronise `stream`, then report (and clear) the device error word of the
+ * current device: ZB_ERR_TIMEOUT if a bounded device wait gave up,
+ * ZB_ERR_CUDA if the stream reported an error, else ZB_OK. */
+zb_status zb_sync_status(void* stream);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* zb_last_error(void);
+
+/* Library version string, e.g. "zb-gb300 0.1 sm_103a". */
+const char* zb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZB_GB300_H */

@@ -1,0 +1,408 @@
+// api.cu — the C ABI: single passes F / B / W of the MLP block and the
+// serial one-GPU replay of a pipeline op list (the per-stage F/B/W executor
+// with its deferred-W activation arena).
+//
+// The block and its split backward follow "Zero Bubble Pipeline Parallelism"
+// (paper-graph-ui summary of arXiv 2401.10241), §3.4 "The Backward Pass
+// Decomposition"; the replay honours the dependencies of §3.4 / Eqs. 4-5:
+// F(s,j) after F(s-1,j); B(s,j) after F(s,j) and B(s+1,j); W(s,j) after B(s,j).
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "zb_internal.h"
+
+namespace zb {
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+zb_status fail(zb_status st, const std::string& msg) {
+    g_last_error = msg;
+    return st;
+}
+
+void clear_error() { g_last_error.clear(); }
+
+namespace {
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+zb_status check_block(const zb_block* b) {
+    if (!b) return fail(ZB_ERR_INVALID_ARG, "block is NULL");
+    if (b->reserved != 0) return fail(ZB_ERR_INVALID_ARG, "block.reserved must be 0");
+    if (b->M <= 0 || b->h <= 0 || b->f <= 0) return fail(ZB_ERR_SHAPE, "M, h and f must be >= 1");
+    if (b->M > (1LL << 30) || b->h > (1LL << 30) || b->f > (1LL << 30))
+        return fail(ZB_ERR_SHAPE, "M, h and f must be <= 2^30");
+    if (b->act < ZB_ACT_NONE || b->act > ZB_ACT_GELU_TANH) return fail(ZB_ERR_INVALID_ARG, "unknown activation");
+    if (b->dtype == ZB_DT_BF16) {
+        if (b->h % 8 || b->f % 8) return fail(ZB_ERR_ALIGN, "bf16 blocks need h and f to be multiples of 8");
+    } else if (b->dtype == ZB_DT_F32) {
+        if (b->act != ZB_ACT_NONE) return fail(ZB_ERR_DTYPE, "fp32 blocks support the single linear map only (act NONE)");
+        if (b->has_bias) return fail(ZB_ERR_DTYPE, "fp32 blocks have no bias path");
+    } else {
+        return fail(ZB_ERR_DTYPE, "unknown dtype");
+    }
+    return ZB_OK;
+}
+
+// Events bracketing kernel launches of one replay (timing mode only).
+struct Recorder {
+    cudaStream_t st = nullptr;
+    bool on = false;
+    std::vector<cudaEvent_t>* pool = nullptr;
+    size_t used = 0;
+    // (before, after, is_gemm) event indices of every launch
+    struct Span { size_t a, b; bool gemm; };
+    std::vector<Span> spans;
+    zb_status mark(size_t* idx) {
+        if (used == pool->size()) {
+            cudaEvent_t e;
+            cudaError_t r = cudaEventCreate(&e);
+            if (r != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("cudaEventCreate: ") + cudaGetErrorString(r));
+            pool->push_back(e);
+        }
+        cudaError_t r = cudaEventRecord((*pool)[used], st);
+        if (r != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(r));
+        *idx = used++;
+        return ZB_OK;
+    }
+};
+
+std::vector<cudaEvent_t>& event_pool() {
+    static thread_local std::vector<cudaEvent_t> pool;
+    return pool;
+}
+
+template <typename F>
+zb_status timed(Recorder* rec, bool gemm, F&& launch) {
+    if (!rec || !rec->on) return launch();
+    size_t a = 0, b = 0;
+    zb_status s = rec->mark(&a);
+    if (s != ZB_OK) return s;
+    s = launch();
+    if (s != ZB_OK) return s;
+    s = rec->mark(&b);
+    if (s != ZB_OK) return s;
+    rec->spans.push_back({a, b, gemm});
+    return ZB_OK;
+}
+
+thread_local int* g_gemm_counter = nullptr;  // GEMM launch count of the running replay
+
+zb_status run_gemm(const GemmBf16& g, void* stream, Recorder* rec) {
+    if (g_gemm_counter) ++*g_gemm_counter;
+    return timed(rec, true, [&] { return gemm_bf16_tc(g, stream); });
+}
+
+zb_status run_gemm32(const GemmF32& g, void* stream, Recorder* rec) {
+    if (g_gemm_counter) ++*g_gemm_counter;
+    return timed(rec, true, [&] { return gemm_f32_simt(g, stream); });
+}
+
+zb_status forward_impl(const zb_block& b, const void* X, const void* W1, const void* W2, const void* b1,
+                       const void* b2, void* H, void* A, void* Y, void* stream, Recorder* rec) {
+    if (b.dtype == ZB_DT_F32) {
+        GemmF32 g;
+        g.Mg = b.M; g.Ng = b.f; g.Kg = b.h;
+        g.A = static_cast<const float*>(X); g.sam = b.h; g.sak = 1;
+        g.B = static_cast<const float*>(W1); g.sbk = b.f; g.sbn = 1;
+        g.C = static_cast<float*>(Y); g.ldc = b.f;
+        return run_gemm32(g, stream, rec);
+    }
+    if (b.act == ZB_ACT_NONE) {
+        GemmBf16 g;
+        g.Mg = b.M; g.Ng = b.f; g.Kg = b.h;
+        g.A = X; g.lda = b.h; g.a_mn = 0;
+        g.B = W1; g.ldb = b.f; g.b_mn = 1;
+        g.epi = EPI_STORE_BF16; g.out0 = Y; g.ld0 = b.f;
+        g.bias = b.has_bias ? b1 : nullptr;
+        return run_gemm(g, stream, rec);
+    }
+    GemmBf16 g1;  // H = X W1 (+b1), A = GeLU(H)
+    g1.Mg = b.M; g1.Ng = b.f; g1.Kg = b.h;
+    g1.A = X; g1.lda = b.h; g1.a_mn = 0;
+    g1.B = W1; g1.ldb = b.f; g1.b_mn = 1;
+    g1.epi = EPI_GELU_DUAL; g1.out0 = H; g1.ld0 = b.f; g1.out1 = A; g1.ld1 = b.f;
+    g1.bias = b.has_bias ? b1 : nullptr; g1.act = b.act;
+    zb_status s = run_gemm(g1, stream, rec);
+    if (s != ZB_OK) return s;
+    GemmBf16 g2;  // Y = A W2 (+b2)
+    g2.Mg = b.M; g2.Ng = b.h; g2.Kg = b.f;
+    g2.A = A; g2.lda = b.f; g2.a_mn = 0;
+    g2.B = W2; g2.ldb = b.h; g2.b_mn = 1;
+    g2.epi = EPI_STORE_BF16; g2.out0 = Y; g2.ld0 = b.h;
+    g2.bias = b.has_bias ? b2 : nullptr;
+    return run_gemm(g2, stream, rec);
+}
+
+zb_status backward_input_impl(const zb_block& b, const void* dY, const void* W1, const void* W2,
+                              const void* H, void* dH, void* dX, void* stream, Recorder* rec) {
+    if (b.dtype == ZB_DT_F32) {
+        GemmF32 g;  // dX = dY W1^T
+        g.Mg = b.M; g.Ng = b.h; g.Kg = b.f;
+        g.A = static_cast<const float*>(dY); g.sam = b.f; g.sak = 1;
+        g.B = static_cast<const float*>(W1); g.sbk = 1; g.sbn = b.f;
+        g.C = static_cast<float*>(dX); g.ldc = b.h;
+        return run_gemm32(g, stream, rec);
+    }
+    if (b.act == ZB_ACT_NONE) {
+        GemmBf16 g;
+        g.Mg = b.M; g.Ng = b.h; g.Kg = b.f;
+        g.A = dY; g.lda = b.f; g.a_mn = 0;
+        g.B = W1; g.ldb = b.f; g.b_mn = 0;
+        g.epi = EPI_STORE_BF16; g.out0 = dX; g.ld0 = b.h;
+        return run_gemm(g, stream, rec);
+    }
+    GemmBf16 g3;  // dH = (dY W2^T) * GeLU'(H); dA stays in fp32 in TMEM
+    g3.Mg = b.M; g3.Ng = b.f; g3.Kg = b.h;
+    g3.A = dY; g3.lda = b.h; g3.a_mn = 0;
+    g3.B = W2; g3.ldb = b.h; g3.b_mn = 0;
+    g3.epi = EPI_GELU_BWD; g3.out0 = dH; g3.ld0 = b.f; g3.aux = H; g3.ldaux = b.f; g3.act = b.act;
+    zb_status s = run_gemm(g3, stream, rec);
+    if (s != ZB_OK) return s;
+    GemmBf16 g4;  // dX = dH W1^T
+    g4.Mg = b.M; g4.Ng = b.h; g4.Kg = b.f;
+    g4.A = dH; g4.lda = b.f; g4.a_mn = 0;
+    g4.B = W1; g4.ldb = b.f; g4.b_mn = 0;
+    g4.epi = EPI_STORE_BF16; g4.out0 = dX; g4.ld0 = b.h;
+    return run_gemm(g4, stream, rec);
+}
+
+zb_status backward_weight_impl(const zb_block& b, const void* X, const void* A, const void* dH,
+                               const void* dY, float* dW1, float* dW2, float* db1, float* db2,
+                               int accumulate, void* stream, Recorder* rec) {
+    if (b.dtype == ZB_DT_F32) {
+        GemmF32 g;  // dW1 (+)= X^T dY
+        g.Mg = b.h; g.Ng = b.f; g.Kg = b.M;
+        g.A = static_cast<const float*>(X); g.sam = 1; g.sak = b.h;
+        g.B = static_cast<const float*>(dY); g.sbk = b.f; g.sbn = 1;
+        g.C = dW1; g.ldc = b.f; g.accumulate = accumulate;
+        return run_gemm32(g, stream, rec);
+    }
+    if (b.act == ZB_ACT_NONE) {
+        GemmBf16 g;
+        g.Mg = b.h; g.Ng = b.f; g.Kg = b.M;
+        g.A = X; g.lda = b.h; g.a_mn = 1;
+        g.B = dY; g.ldb = b.f; g.b_mn = 1;
+        g.epi = EPI_F32; g.out0 = dW1; g.ld0 = b.f; g.accumulate = accumulate;
+        zb_status s = run_gemm(g, stream, rec);
+        if (s != ZB_OK || !b.has_bias) return s;
+        return timed(rec, false, [&] { return colsum_bf16(dY, b.M, b.f, b.f, db1, accumulate, stream); });
+    }
+    GemmBf16 g5;  // dW2 (+)= A^T dY
+    g5.Mg = b.f; g5.Ng = b.h; g5.Kg = b.M;
+    g5.A = A; g5.lda = b.f; g5.a_mn = 1;
+    g5.B = dY; g5.ldb = b.h; g5.b_mn = 1;
+    g5.epi = EPI_F32; g5.out0 = dW2; g5.ld0 = b.h; g5.accumulate = accumulate;
+    zb_status s = run_gemm(g5, stream, rec);
+    if (s != ZB_OK) return s;
+    GemmBf16 g6;  // dW1 (+)= X^T dH
+    g6.Mg = b.h; g6.Ng = b.f; g6.Kg = b.M;
+    g6.A = X; g6.lda = b.h; g6.a_mn = 1;
+    g6.B = dH; g6.ldb = b.f; g6.b_mn = 1;
+    g6.epi = EPI_F32; g6.out0 = dW1; g6.ld0 = b.f; g6.accumulate = accumulate;
+    s = run_gemm(g6, stream, rec);
+    if (s != ZB_OK || !b.has_bias) return s;
+    s = timed(rec, false, [&] { return colsum_bf16(dH, b.M, b.f, b.f, db1, accumulate, stream); });
+    if (s != ZB_OK) return s;
+    return timed(rec, false, [&] { return colsum_bf16(dY, b.M, b.h, b.h, db2, accumulate, stream); });
+}
+
+}  // namespace
+}  // namespace zb
+
+using namespace zb;
+
+extern "C" const char* zb_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" const char* zb_version(void) { return "zb-gb300 0.1 sm_103a"; }
+
+extern "C" zb_status zb_forward(const zb_block* blk, const void* X, const void* W1, const void* W2,
+                                const void* b1, const void* b2, void* H_save, void* A_save, void* Y,
+                                void* stream) {
+    zb_status s = check_block(blk);
+    if (s != ZB_OK) return s;
+    const bool mlp = blk->act != ZB_ACT_NONE;
+    if (!X || !W1 || !Y || (mlp && (!W2 || !H_save || !A_save)))
+        return fail(ZB_ERR_INVALID_ARG, "zb_forward: required pointer is NULL");
+    if (blk->has_bias && (!b1 || (mlp && !b2))) return fail(ZB_ERR_INVALID_ARG, "zb_forward: bias pointer is NULL");
+    if (misaligned(X) || misaligned(W1) || misaligned(W2) || misaligned(Y) || misaligned(H_save) ||
+        misaligned(A_save) || misaligned(b1) || misaligned(b2))
+        return fail(ZB_ERR_ALIGN, "zb_forward: pointers must be 16-byte aligned");
+    s = forward_impl(*blk, X, W1, W2, b1, b2, H_save, A_save, Y, stream, nullptr);
+    if (s == ZB_OK) clear_error();
+    return s;
+}
+
+extern "C" zb_status zb_backward_input(const zb_block* blk, const void* dY, const void* W1, const void* W2,
+                                       const void* H_save, void* dH_out, void* dX, void* stream) {
+    zb_status s = check_block(blk);
+    if (s != ZB_OK) return s;
+    const bool mlp = blk->act != ZB_ACT_NONE;
+    if (!dY || !W1 || !dX || (mlp && (!W2 || !H_save || !dH_out)))
+        return fail(ZB_ERR_INVALID_ARG, "zb_backward_input: required pointer is NULL");
+    if (misaligned(dY) || misaligned(W1) || misaligned(W2) || misaligned(H_save) || misaligned(dH_out) ||
+        misaligned(dX))
+        return fail(ZB_ERR_ALIGN, "zb_backward_input: pointers must be 16-byte aligned");
+    s = backward_input_impl(*blk, dY, W1, W2, H_save, dH_out, dX, stream, nullptr);
+    if (s == ZB_OK) clear_error();
+    return s;
+}
+
+extern "C" zb_status zb_backward_weight(const zb_block* blk, const void* X, const void* A_save, const void* dH,
+                                        const void* dY, float* dW1, float* dW2, float* db1, float* db2,
+                                        int accumulate, void* stream) {
+    zb_status s = check_block(blk);
+    if (s != ZB_OK) return s;
+    const bool mlp = blk->act != ZB_ACT_NONE;
+    if (!X || !dY || !dW1 || (mlp && (!A_save || !dH || !dW2)))
+        return fail(ZB_ERR_INVALID_ARG, "zb_backward_weight: required pointer is NULL");
+    if (blk->has_bias && (!db1 || (mlp && !db2)))
+        return fail(ZB_ERR_INVALID_ARG, "zb_backward_weight: bias-gradient pointer is NULL");
+    if (misaligned(X) || misaligned(A_save) || misaligned(dH) || misaligned(dY) || misaligned(dW1) ||
+        misaligned(dW2) || misaligned(db1) || misaligned(db2))
+        return fail(ZB_ERR_ALIGN, "zb_backward_weight: pointers must be 16-byte aligned");
+    s = backward_weight_impl(*blk, X, A_save, dH, dY, dW1, dW2, db1, db2, accumulate ? 1 : 0, stream, nullptr);
+    if (s == ZB_OK) clear_error();
+    return s;
+}
+
+extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage_params* stages,
+                                           const void* const* X0, const void* const* dY_last,
+                                           void* const* dX0_out, void* const* Y_last_out, const zb_op* ops,
+                                           size_t n_ops, void* workspace, size_t ws_bytes, zb_run_stats* stats,
+                                           void* stream) {
+    if (!pl || !stages || !X0 || !dY_last) return fail(ZB_ERR_INVALID_ARG, "pipeline, stages, X0 or dY_last is NULL");
+    const zb_block& b = pl->blk;
+    zb_status s = check_block(&b);
+    if (s != ZB_OK) return s;
+    const int P = pl->P, m = pl->m;
+    if (P < 1 || m < 1) return fail(ZB_ERR_SHAPE, "P and m must be >= 1");
+    if (P > 1 && b.act == ZB_ACT_NONE && b.f != b.h)
+        return fail(ZB_ERR_SHAPE, "a multi-stage single-linear pipeline needs f == h");
+    const bool mlp = b.act != ZB_ACT_NONE;
+    for (int st = 0; st < P; ++st) {
+        const zb_stage_params& p = stages[st];
+        if (!p.W1 || !p.dW1 || (mlp && (!p.W2 || !p.dW2)))
+            return fail(ZB_ERR_INVALID_ARG, "stage " + std::to_string(st) + ": weight or gradient pointer is NULL");
+        if (b.has_bias && (!p.b1 || !p.db1 || (mlp && (!p.b2 || !p.db2))))
+            return fail(ZB_ERR_INVALID_ARG, "stage " + std::to_string(st) + ": bias pointer is NULL");
+        if (misaligned(p.W1) || misaligned(p.W2) || misaligned(p.b1) || misaligned(p.b2) || misaligned(p.dW1) ||
+            misaligned(p.dW2) || misaligned(p.db1) || misaligned(p.db2))
+            return fail(ZB_ERR_ALIGN, "stage " + std::to_string(st) + ": pointers must be 16-byte aligned");
+    }
+    bool has_y = Y_last_out != nullptr, has_dx = dX0_out != nullptr;
+    for (int j = 0; j < m; ++j) {
+        if (!X0[j] || !dY_last[j]) return fail(ZB_ERR_INVALID_ARG, "X0 / dY_last entry is NULL");
+        if (misaligned(X0[j]) || misaligned(dY_last[j])) return fail(ZB_ERR_ALIGN, "X0 / dY_last must be 16-byte aligned");
+        if (has_y && !Y_last_out[j]) has_y = false;
+        if (has_dx && !dX0_out[j]) has_dx = false;
+        if (Y_last_out && misaligned(Y_last_out[j])) return fail(ZB_ERR_ALIGN, "Y_last_out must be 16-byte aligned");
+        if (dX0_out && misaligned(dX0_out[j])) return fail(ZB_ERR_ALIGN, "dX0_out must be 16-byte aligned");
+    }
+    OpCheck c = validate_ops(ops, n_ops, P, m);
+    if (c.st != ZB_OK) return fail(c.st, c.msg);
+    ArenaPlan plan;
+    s = plan_arena(*pl, ops, n_ops, has_y, has_dx, &plan);
+    if (s != ZB_OK) return s;
+    if (plan.workspace_bytes > 0) {
+        if (!workspace) return fail(ZB_ERR_WORKSPACE, "workspace is NULL");
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(ZB_ERR_ALIGN, "workspace must be 256-byte aligned");
+        if (ws_bytes < plan.workspace_bytes)
+            return fail(ZB_ERR_WORKSPACE, "workspace too small: need " + std::to_string(plan.workspace_bytes) + " bytes");
+    }
+    char* ws = static_cast<char*>(workspace);
+    auto row_ptr = [&](int slot) -> void* { return ws + static_cast<size_t>(slot) * plan.row_bytes; };
+    auto ffn_ptr = [&](int slot) -> void* {
+        return ws + static_cast<size_t>(plan.row_slots) * plan.row_bytes + static_cast<size_t>(slot) * plan.ffn_bytes;
+    };
+
+    Recorder rec;
+    rec.st = static_cast<cudaStream_t>(stream);
+    rec.on = pl->timing != 0;
+    rec.pool = &event_pool();
+    std::vector<std::pair<size_t, size_t>> op_span(n_ops, {0, 0});  // [first span, end span)
+    int gemms = 0;
+    g_gemm_counter = &gemms;
+    std::vector<char> w_started(P, 0);
+
+    for (size_t i = 0; i < n_ops && s == ZB_OK; ++i) {
+        const zb_op& o = ops[i];
+        const int st = o.stage, j = static_cast<int>(o.micro);
+        const zb_stage_params& p = stages[st];
+        op_span[i].first = rec.spans.size();
+        const void* X = st == 0 ? X0[j] : row_ptr(plan.at(st, j, BUF_X));
+        const void* dY = st == P - 1 ? dY_last[j] : row_ptr(plan.at(st, j, BUF_DY));
+        void* H = mlp ? ffn_ptr(plan.at(st, j, BUF_H)) : nullptr;
+        void* A = mlp ? ffn_ptr(plan.at(st, j, BUF_A)) : nullptr;
+        void* dH = mlp ? ffn_ptr(plan.at(st, j, BUF_DH)) : nullptr;
+        auto run_b = [&]() -> zb_status {
+            void* dX;
+            if (st > 0) dX = row_ptr(plan.at(st - 1, j, BUF_DY));
+            else dX = has_dx ? dX0_out[j] : row_ptr(plan.tmp_slot[i]);
+            return backward_input_impl(b, dY, p.W1, p.W2, H, dH, dX, stream, &rec);
+        };
+        auto run_w = [&]() -> zb_status {
+            const int acc = (pl->zero_grads && !w_started[st]) ? 0 : 1;
+            w_started[st] = 1;
+            const void* Xw = X;
+            return backward_weight_impl(b, Xw, A, dH, dY, p.dW1, p.dW2, p.db1, p.db2, acc, stream, &rec);
+        };
+        switch (o.kind) {
+            case ZB_OP_F: {
+                void* Y;
+                if (st < P - 1) Y = row_ptr(plan.at(st + 1, j, BUF_X));
+                else Y = has_y ? Y_last_out[j] : row_ptr(plan.tmp_slot[i]);
+                s = forward_impl(b, X, p.W1, p.W2, p.b1, p.b2, H, A, Y, stream, &rec);
+                break;
+            }
+            case ZB_OP_B: s = run_b(); break;
+            case ZB_OP_W: s = run_w(); break;
+            case ZB_OP_BW:
+                s = run_b();
+                if (s == ZB_OK) s = run_w();
+                break;
+            default: break;
+        }
+        op_span[i].second = rec.spans.size();
+    }
+    g_gemm_counter = nullptr;
+    if (s != ZB_OK) return s;
+
+    if (stats) {
+        stats->workspace_bytes = plan.workspace_bytes;
+        stats->peak_live_bytes = plan.peak_live_bytes;
+        stats->n_ops = static_cast<uint32_t>(n_ops);
+        stats->n_gemm_launches = static_cast<uint32_t>(gemms);
+        stats->total_ms = 0.0;
+        for (double& k : stats->kind_ms) k = 0.0;
+        stats->gemm_ms = 0.0;
+    }
+    if (rec.on && stats && !rec.spans.empty()) {
+        cudaError_t e = cudaEventSynchronize((*rec.pool)[rec.used - 1]);
+        if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("timing sync: ") + cudaGetErrorString(e));
+        auto ms = [&](size_t a, size_t bb) {
+            float t = 0.f;
+            cudaEventElapsedTime(&t, (*rec.pool)[a], (*rec.pool)[bb]);
+            return static_cast<double>(t);
+        };
+        stats->total_ms = ms(rec.spans.front().a, rec.spans.back().b);
+        for (const auto& sp : rec.spans)
+            if (sp.gemm) stats->gemm_ms += ms(sp.a, sp.b);
+        for (size_t i = 0; i < n_ops; ++i) {
+            double t = 0.0;
+            if (op_span[i].second > op_span[i].first)
+                t = ms(rec.spans[op_span[i].first].a, rec.spans[op_span[i].second - 1].b);
+            if (ops[i].kind < 4) stats->kind_ms[ops[i].kind] += t;
+            if (stats->op_ms) stats->op_ms[i] = static_cast<float>(t);
+        }
+    } else if (stats && stats->op_ms) {
+        for (size_t i = 0; i < n_ops; ++i) stats->op_ms[i] = 0.f;
+    }
+    clear_error();
+    return ZB_OK;
+}

@@ -1,0 +1,171 @@
+// misc.cu — the true-fp32 FFMA GEMM (single-linear fp32 blocks, no TF32),
+// the fixed-order column sums of the bias gradients, and the device error
+// word of the bounded waits.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "zb_internal.h"
+
+namespace {
+
+// ---------------------------------------------------------------- error word
+// Bit-set by a bounded device wait that gave up (see gemm_tc.cu).  One word
+// per device context; read and cleared by zb_sync_status().
+__device__ unsigned int g_zb_error_word;
+
+// ---------------------------------------------------------------- fp32 GEMM
+constexpr int TM = 64, TN = 64, TK = 16;
+
+// C[m*ldc + n] (+)= sum_k A[m*sam + k*sak] * B[k*sbk + n*sbn]; every output
+// sums its products in ascending k with fmaf, so results are deterministic.
+__global__ void __launch_bounds__(256)
+    zb_gemm_f32_simt_kernel(zb::GemmF32 g) {
+    __shared__ float As[TK][TM + 4];
+    __shared__ float Bs[TK][TN + 4];
+    const int tid = threadIdx.x;
+    const int ty = tid / 16, tx = tid % 16;
+    const long long m0 = static_cast<long long>(blockIdx.y) * TM;
+    const long long n0 = static_cast<long long>(blockIdx.x) * TN;
+    float acc[4][4] = {};
+    for (long long k0 = 0; k0 < g.Kg; k0 += TK) {
+#pragma unroll
+        for (int i = 0; i < (TK * TM) / 256; ++i) {
+            const int idx = tid + i * 256;
+            const int kk = idx / TM, mm = idx % TM;
+            const long long m = m0 + mm, k = k0 + kk;
+            As[kk][mm] = (m < g.Mg && k < g.Kg) ? g.A[m * g.sam + k * g.sak] : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < (TK * TN) / 256; ++i) {
+            const int idx = tid + i * 256;
+            const int kk = idx / TN, nn = idx % TN;
+            const long long n = n0 + nn, k = k0 + kk;
+            Bs[kk][nn] = (n < g.Ng && k < g.Kg) ? g.B[k * g.sbk + n * g.sbn] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < TK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const long long m = m0 + ty * 4 + i;
+        if (m >= g.Mg) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const long long n = n0 + tx * 4 + j;
+            if (n >= g.Ng) continue;
+            float* c = g.C + m * g.ldc + n;
+            *c = g.accumulate ? (*c + acc[i][j]) : acc[i][j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- column sums
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// One thread per column, rows summed in ascending order (coalesced across
+// the warp: consecutive threads read consecutive columns of a row).
+template <typename T>
+__global__ void zb_colsum_kernel(const T* __restrict__ X, long long rows, long long cols,
+                                 long long ld, float* __restrict__ db, int accumulate) {
+    const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float acc = 0.0f;
+    for (long long r = 0; r < rows; ++r) acc += to_f<T>(X[r * ld + c]);
+    db[c] = accumulate ? db[c] + acc : acc;
+}
+
+}  // namespace
+
+namespace zb {
+
+unsigned int* device_error_word() {
+    static std::mutex mu;
+    static unsigned int* ptrs[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        fail(ZB_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_zb_error_word);
+        if (e != cudaSuccess) {
+            fail(ZB_ERR_CUDA, std::string("cudaGetSymbolAddress(error word): ") + cudaGetErrorString(e));
+            return nullptr;
+        }
+        ptrs[dev] = static_cast<unsigned int*>(p);
+    }
+    return ptrs[dev];
+}
+
+zb_status gemm_f32_simt(const GemmF32& g, void* stream) {
+    if (g.Mg <= 0 || g.Ng <= 0 || g.Kg <= 0) return fail(ZB_ERR_SHAPE, "fp32 GEMM extents must be >= 1");
+    if (!g.A || !g.B || !g.C) return fail(ZB_ERR_INVALID_ARG, "fp32 GEMM operand is NULL");
+    const long long gx = (g.Ng + TN - 1) / TN, gy = (g.Mg + TM - 1) / TM;
+    if (gy > 65535) return fail(ZB_ERR_SHAPE, "fp32 GEMM M too large");
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+    zb_gemm_f32_simt_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(g);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("fp32 GEMM launch: ") + cudaGetErrorString(e));
+    return ZB_OK;
+}
+
+zb_status colsum_bf16(const void* X, int64_t rows, int64_t cols, int64_t ld, float* db,
+                      int accumulate, void* stream) {
+    const unsigned blocks = static_cast<unsigned>((cols + 255) / 256);
+    zb_colsum_kernel<__nv_bfloat16><<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(X), rows, cols, ld, db, accumulate);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("colsum launch: ") + cudaGetErrorString(e));
+    return ZB_OK;
+}
+
+zb_status colsum_f32(const float* X, int64_t rows, int64_t cols, int64_t ld, float* db,
+                     int accumulate, void* stream) {
+    const unsigned blocks = static_cast<unsigned>((cols + 255) / 256);
+    zb_colsum_kernel<float><<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(X, rows, cols, ld, db,
+                                                                                 accumulate);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("colsum launch: ") + cudaGetErrorString(e));
+    return ZB_OK;
+}
+
+}  // namespace zb
+
+extern "C" zb_status zb_sync_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return zb::fail(ZB_ERR_CUDA, std::string("stream: ") + cudaGetErrorString(e));
+    unsigned int* w = zb::device_error_word();
+    if (!w) return ZB_ERR_CUDA;
+    unsigned int v = 0;
+    e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return zb::fail(ZB_ERR_CUDA, std::string("read error word: ") + cudaGetErrorString(e));
+    if (v != 0) {
+        const unsigned int zero = 0;
+        cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        return zb::fail(ZB_ERR_TIMEOUT, "a bounded device wait gave up (error word " + std::to_string(v) + ")");
+    }
+    zb::clear_error();
+    return ZB_OK;
+}

@@ -1,0 +1,392 @@
+// schedule.cpp — host-side pipeline logic: the handcrafted orderings
+// (1F1B, ZB-H1, ZB-H2), op-list validation and the deferred-W arena plan.
+//
+// Orderings after "Zero Bubble Pipeline Parallelism" (paper-graph-ui summary
+// of arXiv 2401.10241), §3.4 "Handcrafted Schedule ZB-H1 / ZB-H2", Table 2,
+// the heuristic's phases "W insertion to fill bubbles" / "Memory-triggered W
+// insertion" / "Cool-down", and "Pipeline Schedules: GPipe, 1F1B and Zero
+// Bubble", section "1F1B: same bubble, bounded memory".  Pass times are equal
+// (one time unit; the fused 1F1B backward takes two), so the simulator runs
+// on integers.  Lifetimes after the summary's "The Memory Model" (F stores
+// M_B, B trades M_B for M_W, W frees M_W) and "Pipeline Schedules", "Zero
+// bubble": per-stage instruction sequences with gradient-buffer lifetime
+// management.
+#include <algorithm>
+#include <cstring>
+#include <deque>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "zb_internal.h"
+
+namespace {
+
+struct SimEvent {
+    int kind, stage, micro;
+    long long start, end;
+};
+
+int warmup_count(int kind, int P, int m, int s) {
+    int w = 0;
+    if (kind == ZB_SCHED_1F1B) w = P - 1 - s;
+    else if (kind == ZB_SCHED_ZBH1) w = P - s;
+    else w = 2 * (P - 1 - s) + 1;
+    return std::min(w, m);
+}
+
+// Fixed F/B (F/BW for 1F1B) sequence of stage s.
+std::vector<std::pair<int, int>> fb_order(int kind, int P, int m, int s) {
+    std::vector<std::pair<int, int>> q;
+    const int w = warmup_count(kind, P, m, s);
+    for (int j = 0; j < w; ++j) q.push_back({ZB_OP_F, j});
+    int next_f = w;
+    for (int b = 0; b < m; ++b) {
+        if (kind == ZB_SCHED_1F1B) {
+            if (next_f < m) q.push_back({ZB_OP_F, next_f++});
+            q.push_back({ZB_OP_BW, b});
+        } else {
+            q.push_back({ZB_OP_B, b});
+            if (next_f < m) q.push_back({ZB_OP_F, next_f++});
+        }
+    }
+    return q;
+}
+
+long long op_len(int kind) { return kind == ZB_OP_BW ? 2 : 1; }
+
+bool simulate(int kind, int P, int m, std::vector<SimEvent>* out) {
+    const int live_cap = kind == ZB_SCHED_ZBH1 ? P : (kind == ZB_SCHED_ZBH2 ? 2 * P - 1 : 0);
+    struct St {
+        std::vector<std::pair<int, int>> seq;
+        size_t pos = 0;
+        std::deque<int> wq;
+        int live = 0;
+        long long tfree = 0;
+        bool parked = false;
+    };
+    std::vector<St> st(P);
+    for (int s = 0; s < P; ++s) st[s].seq = fb_order(kind, P, m, s);
+    // end times (or -1): fwd_end[s*m+j]; bwd_end = end of B or BW
+    std::vector<long long> fwd_end(static_cast<size_t>(P) * m, -1), bwd_end(static_cast<size_t>(P) * m, -1);
+    std::vector<long long> all_ends;
+    auto busy = [&](int s) { return st[s].pos < st[s].seq.size() || !st[s].wq.empty(); };
+    auto emit = [&](int s, int k, int j, long long t0) {
+        const long long t1 = t0 + op_len(k);
+        out->push_back({k, s, j, t0, t1});
+        all_ends.push_back(t1);
+        st[s].tfree = t1;
+        if (k == ZB_OP_F) {
+            fwd_end[static_cast<size_t>(s) * m + j] = t1;
+            st[s].live++;
+        } else if (k == ZB_OP_B) {
+            bwd_end[static_cast<size_t>(s) * m + j] = t1;
+            st[s].wq.push_back(j);
+        } else if (k == ZB_OP_BW) {
+            bwd_end[static_cast<size_t>(s) * m + j] = t1;
+            st[s].live--;
+        } else {
+            st[s].live--;
+        }
+    };
+    // earliest start of (k, s, j) given its producers, -1 if one is unscheduled
+    auto ready_time = [&](int s, int k, int j) -> long long {
+        long long t = 0;
+        if (k == ZB_OP_F) {
+            if (s > 0) {
+                t = fwd_end[static_cast<size_t>(s - 1) * m + j];
+                if (t < 0) return -1;
+            }
+            return t;
+        }
+        t = fwd_end[static_cast<size_t>(s) * m + j];
+        if (t < 0) return -1;
+        if (s + 1 < P) {
+            const long long u = bwd_end[static_cast<size_t>(s + 1) * m + j];
+            if (u < 0) return -1;
+            t = std::max(t, u);
+        }
+        return t;
+    };
+    for (;;) {
+        int pick = -1;
+        for (int s = 0; s < P; ++s) {
+            if (!busy(s) || st[s].parked) continue;
+            if (pick < 0 || st[s].tfree < st[pick].tfree) pick = s;
+        }
+        if (pick < 0) {
+            bool any = false;
+            for (int s = 0; s < P; ++s) any = any || busy(s);
+            if (!any) break;
+            return false;  // every stage with work is parked: cannot happen for legal orders
+        }
+        St& S = st[pick];
+        const long long now = S.tfree;
+        const bool have_fb = S.pos < S.seq.size();
+        long long ready = -1;
+        if (have_fb) ready = ready_time(pick, S.seq[S.pos].first, S.seq[S.pos].second);
+        bool ran = true;
+        if (have_fb && ready >= 0 && ready <= now) {
+            const bool force_w = S.seq[S.pos].first == ZB_OP_F && live_cap > 0 &&
+                                 S.live >= live_cap && !S.wq.empty();
+            if (force_w) {
+                const int j = S.wq.front();
+                S.wq.pop_front();
+                emit(pick, ZB_OP_W, j, now);
+            } else {
+                emit(pick, S.seq[S.pos].first, S.seq[S.pos].second, now);
+                S.pos++;
+            }
+        } else if (!S.wq.empty()) {
+            const int j = S.wq.front();
+            S.wq.pop_front();
+            emit(pick, ZB_OP_W, j, now);
+        } else {
+            ran = false;
+            if (ready >= 0) {
+                S.tfree = ready;
+            } else {
+                long long nxt = -1;
+                for (long long e : all_ends)
+                    if (e > now && (nxt < 0 || e < nxt)) nxt = e;
+                for (int o = 0; o < P; ++o)
+                    if (o != pick && busy(o) && st[o].tfree > now && (nxt < 0 || st[o].tfree < nxt))
+                        nxt = st[o].tfree;
+                if (nxt < 0) S.parked = true;
+                else S.tfree = nxt;
+            }
+        }
+        if (ran)
+            for (auto& x : st) x.parked = false;
+    }
+    return true;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+namespace zb {
+
+bool block_bytes(const zb_block& b, size_t* row_bytes, size_t* ffn_bytes) {
+    const size_t es = b.dtype == ZB_DT_F32 ? 4 : 2;
+    if (b.M <= 0 || b.h <= 0 || b.f <= 0) return false;
+    // a single linear map's output is [M,f]: row slots then hold max(h, f)
+    const int64_t row_w = b.act == ZB_ACT_NONE ? std::max(b.h, b.f) : b.h;
+    *row_bytes = static_cast<size_t>(b.M) * static_cast<size_t>(row_w) * es;
+    *ffn_bytes = static_cast<size_t>(b.M) * static_cast<size_t>(b.f) * es;
+    return true;
+}
+
+OpCheck validate_ops(const zb_op* ops, size_t n, int P, int m) {
+    OpCheck r;
+    auto bad = [&](zb_status s, const std::string& msg) {
+        r.st = s;
+        r.msg = msg;
+        return r;
+    };
+    auto name = [](const zb_op& o) {
+        static const char* k[] = {"F", "B", "W", "BW", "OPT"};
+        return std::string(o.kind < 5 ? k[o.kind] : "?") + "(" + std::to_string(o.stage) + "," +
+               std::to_string(o.micro) + ")";
+    };
+    if (P <= 0 || m <= 0) return bad(ZB_ERR_SHAPE, "P and m must be >= 1");
+    if (!ops && n) return bad(ZB_ERR_INVALID_ARG, "ops is NULL");
+    const size_t PM = static_cast<size_t>(P) * m;
+    // seen[kind][s*m+j]
+    std::vector<unsigned char> seen(4 * PM, 0);
+    auto has = [&](int k, int s, int j) { return seen[k * PM + static_cast<size_t>(s) * m + j] != 0; };
+    std::vector<long long> last_w(P, -1);
+    std::vector<char> opt_done(P, 0);
+    for (size_t i = 0; i < n; ++i) {
+        const zb_op& o = ops[i];
+        if (o.kind > ZB_OP_OPT || o.pad != 0) return bad(ZB_ERR_SCHEDULE, "op " + std::to_string(i) + ": bad kind");
+        if (o.stage >= P) return bad(ZB_ERR_SCHEDULE, "op " + std::to_string(i) + ": stage out of range " + name(o));
+        if (o.kind != ZB_OP_OPT && o.micro >= static_cast<uint32_t>(m))
+            return bad(ZB_ERR_SCHEDULE, "op " + std::to_string(i) + ": micro out of range " + name(o));
+        const int s = o.stage;
+        if (opt_done[s]) return bad(ZB_ERR_SCHEDULE, name(o) + " after OPT of its stage");
+        if (o.kind == ZB_OP_OPT) {
+            opt_done[s] = 1;
+            continue;
+        }
+        const int j = static_cast<int>(o.micro);
+        if (has(o.kind, s, j)) return bad(ZB_ERR_SCHEDULE, "duplicate " + name(o));
+        if (o.kind == ZB_OP_BW && (has(ZB_OP_B, s, j) || has(ZB_OP_W, s, j)))
+            return bad(ZB_ERR_SCHEDULE, "BW mixed with split B/W for " + name(o));
+        if ((o.kind == ZB_OP_B || o.kind == ZB_OP_W) && has(ZB_OP_BW, s, j))
+            return bad(ZB_ERR_SCHEDULE, "split B/W mixed with BW for " + name(o));
+        bool ok = true;
+        if (o.kind == ZB_OP_F) {
+            ok = s == 0 || has(ZB_OP_F, s - 1, j);
+        } else if (o.kind == ZB_OP_B || o.kind == ZB_OP_BW) {
+            ok = has(ZB_OP_F, s, j) && (s == P - 1 || has(ZB_OP_B, s + 1, j) || has(ZB_OP_BW, s + 1, j));
+        } else {
+            ok = has(ZB_OP_B, s, j);
+        }
+        if (!ok) return bad(ZB_ERR_SCHEDULE, name(o) + " runs before one of its producers");
+        if (o.kind == ZB_OP_W || o.kind == ZB_OP_BW) {
+            if (j <= last_w[s]) return bad(ZB_ERR_W_ORDER, name(o) + ": weight gradients of a stage must run in ascending micro order");
+            last_w[s] = j;
+        }
+        seen[o.kind * PM + static_cast<size_t>(s) * m + j] = 1;
+    }
+    for (int s = 0; s < P; ++s)
+        for (int j = 0; j < m; ++j) {
+            const bool split = has(ZB_OP_B, s, j) && has(ZB_OP_W, s, j);
+            if (!has(ZB_OP_F, s, j) || !(split || has(ZB_OP_BW, s, j)))
+                return bad(ZB_ERR_SCHEDULE, "missing pass for stage " + std::to_string(s) + " micro " + std::to_string(j));
+        }
+    return r;
+}
+
+zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has_y_out,
+                     bool has_dx_out, ArenaPlan* plan) {
+    const int P = pl.P, m = pl.m;
+    size_t rb = 0, fb = 0;
+    if (!block_bytes(pl.blk, &rb, &fb)) return fail(ZB_ERR_SHAPE, "block extents must be >= 1");
+    const bool mlp = pl.blk.act != ZB_ACT_NONE;
+    plan->P = P;
+    plan->m = m;
+    plan->row_bytes = align256(rb);
+    plan->ffn_bytes = align256(fb);
+    plan->slot.assign(static_cast<size_t>(P) * m * BUF_COUNT, -1);
+    plan->tmp_slot.assign(n, -1);
+    // Two pools of equal-size slots; lowest free index first (deterministic).
+    std::set<int> free_row, free_ffn;
+    int n_row = 0, n_ffn = 0;
+    size_t live = 0, peak = 0;
+    // Saved activations enter the ledger; a scratch output (the last stage's Y
+    // or stage 0's dX when the caller gives no buffer) takes a slot only.
+    auto take = [&](bool ffn, bool saved = true) {
+        std::set<int>& fr = ffn ? free_ffn : free_row;
+        int& cnt = ffn ? n_ffn : n_row;
+        int id;
+        if (!fr.empty()) {
+            id = *fr.begin();
+            fr.erase(fr.begin());
+        } else {
+            id = cnt++;
+        }
+        if (saved) {
+            live += ffn ? fb : rb;
+            peak = std::max(peak, live);
+        }
+        return id;
+    };
+    auto give = [&](bool ffn, int id, bool saved = true) {
+        if (id < 0) return;
+        (ffn ? free_ffn : free_row).insert(id);
+        if (saved) live -= ffn ? fb : rb;
+    };
+    auto ref = [&](int s, int j, int k) -> int& {
+        return plan->slot[(static_cast<size_t>(s) * m + j) * BUF_COUNT + k];
+    };
+    auto do_b = [&](int s, int j, size_t i) {
+        if (mlp) ref(s, j, BUF_DH) = take(true);
+        int tmp = -1;
+        if (s > 0) ref(s - 1, j, BUF_DY) = take(false);  // dX(s) = dY(s-1)
+        else if (!has_dx_out) tmp = take(false, false);
+        if (mlp) give(true, ref(s, j, BUF_H));
+        give(false, tmp, false);
+        if (tmp >= 0) plan->tmp_slot[i] = tmp;
+    };
+    auto do_w = [&](int s, int j) {
+        if (s > 0) give(false, ref(s, j, BUF_X));
+        if (mlp) {
+            give(true, ref(s, j, BUF_A));
+            give(true, ref(s, j, BUF_DH));
+        }
+        if (s < P - 1) give(false, ref(s, j, BUF_DY));
+    };
+    for (size_t i = 0; i < n; ++i) {
+        const zb_op& o = ops[i];
+        const int s = o.stage, j = static_cast<int>(o.micro);
+        switch (o.kind) {
+            case ZB_OP_F: {
+                if (mlp) {
+                    ref(s, j, BUF_H) = take(true);
+                    ref(s, j, BUF_A) = take(true);
+                }
+                if (s < P - 1) {
+                    ref(s + 1, j, BUF_X) = take(false);  // Y(s) = X(s+1)
+                } else if (!has_y_out) {
+                    const int tmp = take(false, false);
+                    plan->tmp_slot[i] = tmp;
+                    give(false, tmp, false);
+                }
+                break;
+            }
+            case ZB_OP_B: do_b(s, j, i); break;
+            case ZB_OP_W: do_w(s, j); break;
+            case ZB_OP_BW:
+                do_b(s, j, i);
+                do_w(s, j);
+                break;
+            default: break;
+        }
+    }
+    plan->row_slots = n_row;
+    plan->ffn_slots = n_ffn;
+    plan->workspace_bytes = static_cast<size_t>(n_row) * plan->row_bytes + static_cast<size_t>(n_ffn) * plan->ffn_bytes;
+    plan->peak_live_bytes = peak;
+    if (pl.mem_limit_bytes != 0 && peak > pl.mem_limit_bytes)
+        return fail(ZB_ERR_BUDGET, "peak live activation bytes " + std::to_string(peak) + " exceed the limit " +
+                                       std::to_string(pl.mem_limit_bytes));
+    return ZB_OK;
+}
+
+}  // namespace zb
+
+extern "C" zb_status zb_make_schedule(int32_t kind, int32_t P, int32_t m, zb_op* out, size_t* n_ops) {
+    if (!n_ops) return zb::fail(ZB_ERR_INVALID_ARG, "n_ops is NULL");
+    if (kind < ZB_SCHED_1F1B || kind > ZB_SCHED_ZBH2) return zb::fail(ZB_ERR_INVALID_ARG, "unknown schedule kind");
+    if (P < 1 || m < 1 || P > 65535 || static_cast<long long>(P) * m > (1LL << 24))
+        return zb::fail(ZB_ERR_SHAPE, "P and m must be >= 1 (P <= 65535, P*m <= 2^24)");
+    const size_t per = kind == ZB_SCHED_1F1B ? 2 : 3;
+    const size_t total = static_cast<size_t>(P) * m * per + P;
+    if (!out) {
+        *n_ops = total;
+        zb::clear_error();
+        return ZB_OK;
+    }
+    if (*n_ops < total) {
+        *n_ops = total;
+        return zb::fail(ZB_ERR_INVALID_ARG, "output capacity too small");
+    }
+    std::vector<SimEvent> ev;
+    ev.reserve(total);
+    if (!simulate(kind, P, m, &ev)) return zb::fail(ZB_ERR_SCHEDULE, "schedule simulation deadlocked");
+    std::stable_sort(ev.begin(), ev.end(), [](const SimEvent& a, const SimEvent& b) {
+        return a.start != b.start ? a.start < b.start : a.stage < b.stage;
+    });
+    std::vector<size_t> last(P, 0);
+    for (size_t i = 0; i < ev.size(); ++i) last[ev[i].stage] = i;
+    size_t w = 0;
+    for (size_t i = 0; i < ev.size(); ++i) {
+        out[w++] = zb_op{static_cast<uint8_t>(ev[i].kind), 0, static_cast<uint16_t>(ev[i].stage),
+                         static_cast<uint32_t>(ev[i].micro)};
+        for (int s = 0; s < P; ++s)
+            if (last[s] == i) out[w++] = zb_op{ZB_OP_OPT, 0, static_cast<uint16_t>(s), 0};
+    }
+    *n_ops = w;
+    zb::clear_error();
+    return ZB_OK;
+}
+
+extern "C" zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_op* ops, size_t n_ops,
+                                                size_t* bytes, size_t* peak_live_bytes) {
+    if (!pl || !bytes) return zb::fail(ZB_ERR_INVALID_ARG, "pipeline or bytes is NULL");
+    zb::OpCheck c = zb::validate_ops(ops, n_ops, pl->P, pl->m);
+    if (c.st != ZB_OK) return zb::fail(c.st, c.msg);
+    if (pl->P > 1 && pl->blk.act == ZB_ACT_NONE && pl->blk.f != pl->blk.h)
+        return zb::fail(ZB_ERR_SHAPE, "a multi-stage single-linear pipeline needs f == h");
+    zb::ArenaPlan plan;
+    // sizing assumes no caller output buffers (the largest arena)
+    zb_status st = zb::plan_arena(*pl, ops, n_ops, false, false, &plan);
+    *bytes = plan.workspace_bytes;
+    if (peak_live_bytes) *peak_live_bytes = plan.peak_live_bytes;
+    if (st != ZB_OK) return st;
+    zb::clear_error();
+    return ZB_OK;
+}

@@ -1,0 +1,97 @@
+// zb_internal.h — declarations shared by the library's translation units.
+// Not part of the public ABI (see include/zb.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/zb.h"
+
+namespace zb {
+
+// ---------------------------------------------------------------- errors
+zb_status fail(zb_status st, const std::string& msg);  // sets zb_last_error, returns st
+void clear_error();
+
+// Device error word of the current device (bit set by a bounded wait that
+// gave up).  Returns nullptr with a message on CUDA failure.
+unsigned int* device_error_word();
+
+// ---------------------------------------------------------------- GEMMs
+enum Epilogue : int {
+    EPI_STORE_BF16 = 0,  // out0 = bf16(acc (+ bias[col]))
+    EPI_GELU_DUAL = 1,   // out0 = bf16(acc + bias) = H; out1 = bf16(GeLU(acc + bias)) = A
+    EPI_GELU_BWD = 2,    // out0 = bf16(acc * GeLU'(aux))  (aux = H, bf16)
+    EPI_F32 = 3          // out0 (fp32) = (accumulate ? out0 : 0) + acc
+};
+
+// D[Mg,Ng] = sum_k Aop(m,k) Bop(k,n) with bf16 operands, fp32 accumulation.
+//  a_mn = 0: Aop(m,k) = A[m*lda + k]   (K-major)
+//  a_mn = 1: Aop(m,k) = A[k*lda + m]   (MN-major)
+//  b_mn = 0: Bop(k,n) = B[n*ldb + k]   (K-major)
+//  b_mn = 1: Bop(k,n) = B[k*ldb + n]   (MN-major)
+struct GemmBf16 {
+    int64_t Mg = 0, Ng = 0, Kg = 0;
+    const void* A = nullptr; int64_t lda = 0; int a_mn = 0;
+    const void* B = nullptr; int64_t ldb = 0; int b_mn = 0;
+    int epi = EPI_STORE_BF16;
+    void* out0 = nullptr; int64_t ld0 = 0;
+    void* out1 = nullptr; int64_t ld1 = 0;
+    const void* aux = nullptr; int64_t ldaux = 0;
+    const void* bias = nullptr;  // bf16 [Ng] or nullptr
+    int accumulate = 0;
+    int act = ZB_ACT_GELU_ERF;
+};
+zb_status gemm_bf16_tc(const GemmBf16& g, void* stream);
+
+// fp32 FFMA GEMM (no TF32): C[m*ldc + n] (+)= sum_k A[m*sam + k*sak] * B[k*sbk + n*sbn]
+struct GemmF32 {
+    int64_t Mg = 0, Ng = 0, Kg = 0;
+    const float* A = nullptr; int64_t sam = 0, sak = 0;
+    const float* B = nullptr; int64_t sbk = 0, sbn = 0;
+    float* C = nullptr; int64_t ldc = 0;
+    int accumulate = 0;
+};
+zb_status gemm_f32_simt(const GemmF32& g, void* stream);
+
+// db[n] (+)= sum_{r < rows} X[r*ld + n], fp32 accumulation in row order.
+zb_status colsum_bf16(const void* X, int64_t rows, int64_t cols, int64_t ld, float* db,
+                      int accumulate, void* stream);
+zb_status colsum_f32(const float* X, int64_t rows, int64_t cols, int64_t ld, float* db,
+                     int accumulate, void* stream);
+// out[i] = bf16(x[i]) ... unused helpers kept out.
+
+// ---------------------------------------------------------------- schedules
+struct OpCheck {
+    zb_status st = ZB_OK;
+    std::string msg;
+};
+// Validate an op list against the replay rules.
+OpCheck validate_ops(const zb_op* ops, size_t n, int P, int m);
+
+// Arena plan: for every op, which slots its outputs occupy and which slots
+// it releases.  Two size classes: "row" buffers [M,h] and "ffn" buffers [M,f].
+enum BufKind : int { BUF_X = 0, BUF_H, BUF_A, BUF_DH, BUF_DY, BUF_COUNT };
+struct ArenaPlan {
+    size_t row_bytes = 0, ffn_bytes = 0;  // per-slot (256-B aligned)
+    int row_slots = 0, ffn_slots = 0;     // peak simultaneous slots per class
+    size_t workspace_bytes = 0;
+    size_t peak_live_bytes = 0;
+    // slot index per (stage, micro, BufKind); -1 when the buffer is caller-owned
+    std::vector<int> slot;  // index: ((s*m + j) * BUF_COUNT + kind)
+    // temporary slots for Y of the last stage / dX of stage 0 when no output
+    // pointer is given: one per op index (or -1)
+    std::vector<int> tmp_slot;
+    int P = 0, m = 0;
+    int at(int s, int j, int k) const { return slot[(static_cast<size_t>(s) * m + j) * BUF_COUNT + k]; }
+};
+// has_y_out / has_dx_out: whether the caller supplies the last stage's Y /
+// stage 0's dX for every microbatch (else a temporary slot is used).
+zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has_y_out,
+                     bool has_dx_out, ArenaPlan* plan);
+
+bool block_bytes(const zb_block& b, size_t* row_bytes, size_t* ffn_bytes);
+
+}  // namespace zb

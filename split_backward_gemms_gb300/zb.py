@@ -1,0 +1,241 @@
+"""Thin ctypes binding of the C ABI in ``include/zb.h`` (same names).
+
+Argument marshalling only: every pass runs in the CUDA library
+``libzb_gb300.so`` built in-tree by ``split_backward_gemms_gb300.build``.
+Importing this module loads the library and fails loudly if it is missing;
+there is no CPU fallback.
+
+Pointers may be given as torch tensors (their ``data_ptr()``), plain ints or
+None.  ``stream`` may be a ``torch.cuda.Stream``, an int handle or None (the
+current torch stream when torch's CUDA is initialised, else the legacy
+default stream).  A non-OK status raises ``ZBError`` carrying the status and
+``zb_last_error()``.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+from . import build as _build
+
+# ---------------------------------------------------------------- constants
+ZB_OK = 0
+ZB_ERR_INVALID_ARG = 1
+ZB_ERR_SHAPE = 2
+ZB_ERR_ALIGN = 3
+ZB_ERR_DTYPE = 4
+ZB_ERR_SCHEDULE = 5
+ZB_ERR_W_ORDER = 6
+ZB_ERR_BUDGET = 7
+ZB_ERR_WORKSPACE = 8
+ZB_ERR_CUDA = 9
+ZB_ERR_TIMEOUT = 10
+ZB_ERR_UNSUPPORTED = 11
+STATUS_NAMES = {v: k for k, v in list(globals().items()) if k.startswith("ZB_ERR_") or k == "ZB_OK"}
+
+ZB_DT_F32 = 0
+ZB_DT_BF16 = 1
+ZB_ACT_NONE = 0
+ZB_ACT_GELU_ERF = 1
+ZB_ACT_GELU_TANH = 2
+
+ZB_OP_F, ZB_OP_B, ZB_OP_W, ZB_OP_BW, ZB_OP_OPT = range(5)
+OP_NAMES = ("F", "B", "W", "BW", "OPT")
+ZB_SCHED_1F1B, ZB_SCHED_ZBH1, ZB_SCHED_ZBH2 = range(3)
+SCHED_IDS = {"1F1B": ZB_SCHED_1F1B, "ZBH1": ZB_SCHED_ZBH1, "ZBH2": ZB_SCHED_ZBH2}
+
+
+# ---------------------------------------------------------------- structs
+class zb_block(C.Structure):
+    _fields_ = [("M", C.c_int64), ("h", C.c_int64), ("f", C.c_int64), ("dtype", C.c_int32),
+                ("act", C.c_int32), ("has_bias", C.c_int32), ("reserved", C.c_int32)]
+
+
+class zb_op(C.Structure):
+    _fields_ = [("kind", C.c_uint8), ("pad", C.c_uint8), ("stage", C.c_uint16), ("micro", C.c_uint32)]
+
+
+class zb_pipeline(C.Structure):
+    _fields_ = [("P", C.c_int32), ("m", C.c_int32), ("blk", zb_block),
+                ("mem_limit_bytes", C.c_uint64), ("zero_grads", C.c_int32), ("timing", C.c_int32)]
+
+
+class zb_stage_params(C.Structure):
+    _fields_ = [("W1", C.c_void_p), ("W2", C.c_void_p), ("b1", C.c_void_p), ("b2", C.c_void_p),
+                ("dW1", C.c_void_p), ("dW2", C.c_void_p), ("db1", C.c_void_p), ("db2", C.c_void_p)]
+
+
+class zb_run_stats(C.Structure):
+    _fields_ = [("workspace_bytes", C.c_uint64), ("peak_live_bytes", C.c_uint64),
+                ("n_ops", C.c_uint32), ("n_gemm_launches", C.c_uint32), ("total_ms", C.c_double),
+                ("kind_ms", C.c_double * 4), ("gemm_ms", C.c_double), ("op_ms", C.POINTER(C.c_float))]
+
+
+class ZBError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+# ---------------------------------------------------------------- loading
+def _load():
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run split_backward_gemms_gb300.build.build() "
+                           "(there is no CPU fallback)")
+    lib = C.CDLL(path)
+    vp, sz = C.c_void_p, C.c_size_t
+    sig = {
+        "zb_forward": [C.POINTER(zb_block), vp, vp, vp, vp, vp, vp, vp, vp, vp],
+        "zb_backward_input": [C.POINTER(zb_block), vp, vp, vp, vp, vp, vp, vp],
+        "zb_backward_weight": [C.POINTER(zb_block), vp, vp, vp, vp, vp, vp, vp, vp, C.c_int, vp],
+        "zb_make_schedule": [C.c_int32, C.c_int32, C.c_int32, C.POINTER(zb_op), C.POINTER(sz)],
+        "zb_schedule_workspace_size": [C.POINTER(zb_pipeline), C.POINTER(zb_op), sz, C.POINTER(sz),
+                                       C.POINTER(sz)],
+        "zb_run_stage_schedule": [C.POINTER(zb_pipeline), C.POINTER(zb_stage_params), C.POINTER(vp),
+                                  C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), C.POINTER(zb_op), sz,
+                                  vp, sz, C.POINTER(zb_run_stats), vp],
+        "zb_sync_status": [vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = C.c_int
+    lib.zb_last_error.argtypes = []
+    lib.zb_last_error.restype = C.c_char_p
+    lib.zb_version.argtypes = []
+    lib.zb_version.restype = C.c_char_p
+    return lib
+
+
+LIB = _load()
+
+
+# ---------------------------------------------------------------- helpers
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr() or None
+    raise TypeError(f"cannot take a device pointer of {type(x)!r}")
+
+
+def _stream(s):
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return torch.cuda.current_stream().cuda_stream or None
+        except Exception:  # pragma: no cover - torch missing
+            pass
+        return None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None
+
+
+def _check(st: int, where: str):
+    if st != ZB_OK:
+        raise ZBError(st, where, zb_last_error())
+
+
+def make_block(M: int, h: int, f: int, dtype: int = ZB_DT_BF16, act: int = ZB_ACT_GELU_ERF,
+               has_bias: bool = False) -> zb_block:
+    return zb_block(M, h, f, dtype, act, 1 if has_bias else 0, 0)
+
+
+def ops_array(ops):
+    """(kind, stage, micro) tuples (kind as name or id) -> ctypes zb_op array."""
+    arr = (zb_op * len(ops))()
+    for i, (k, s, j) in enumerate(ops):
+        arr[i].kind = OP_NAMES.index(k) if isinstance(k, str) else int(k)
+        arr[i].pad = 0
+        arr[i].stage = s
+        arr[i].micro = j
+    return arr
+
+
+def ops_tuples(arr, n=None):
+    n = len(arr) if n is None else n
+    return [(OP_NAMES[arr[i].kind], arr[i].stage, arr[i].micro) for i in range(n)]
+
+
+# ---------------------------------------------------------------- ABI
+def zb_last_error() -> str:
+    return LIB.zb_last_error().decode()
+
+
+def zb_version() -> str:
+    return LIB.zb_version().decode()
+
+
+def zb_forward(blk, X, W1, W2, b1, b2, H_save, A_save, Y, stream=None):
+    _check(LIB.zb_forward(C.byref(blk), _ptr(X), _ptr(W1), _ptr(W2), _ptr(b1), _ptr(b2),
+                          _ptr(H_save), _ptr(A_save), _ptr(Y), _stream(stream)), "zb_forward")
+
+
+def zb_backward_input(blk, dY, W1, W2, H_save, dH_out, dX, stream=None):
+    _check(LIB.zb_backward_input(C.byref(blk), _ptr(dY), _ptr(W1), _ptr(W2), _ptr(H_save),
+                                 _ptr(dH_out), _ptr(dX), _stream(stream)), "zb_backward_input")
+
+
+def zb_backward_weight(blk, X, A_save, dH, dY, dW1, dW2, db1, db2, accumulate, stream=None):
+    _check(LIB.zb_backward_weight(C.byref(blk), _ptr(X), _ptr(A_save), _ptr(dH), _ptr(dY),
+                                  _ptr(dW1), _ptr(dW2), _ptr(db1), _ptr(db2),
+                                  1 if accumulate else 0, _stream(stream)), "zb_backward_weight")
+
+
+def zb_make_schedule(kind, P: int, m: int):
+    """Generated op list as (kind_name, stage, micro) tuples."""
+    kid = SCHED_IDS[kind] if isinstance(kind, str) else int(kind)
+    n = C.c_size_t(0)
+    _check(LIB.zb_make_schedule(kid, P, m, None, C.byref(n)), "zb_make_schedule")
+    arr = (zb_op * n.value)()
+    _check(LIB.zb_make_schedule(kid, P, m, arr, C.byref(n)), "zb_make_schedule")
+    return ops_tuples(arr, n.value)
+
+
+def make_pipeline(P, m, blk, mem_limit_bytes=0, zero_grads=True, timing=False) -> zb_pipeline:
+    return zb_pipeline(P, m, blk, mem_limit_bytes, 1 if zero_grads else 0, 1 if timing else 0)
+
+
+def zb_schedule_workspace_size(pl, ops):
+    """Returns (workspace_bytes, peak_live_bytes)."""
+    arr = ops if isinstance(ops, C.Array) else ops_array(ops)
+    b = C.c_size_t(0)
+    pk = C.c_size_t(0)
+    _check(LIB.zb_schedule_workspace_size(C.byref(pl), arr, len(arr), C.byref(b), C.byref(pk)),
+           "zb_schedule_workspace_size")
+    return b.value, pk.value
+
+
+def _ptr_array(xs):
+    if xs is None:
+        return None
+    arr = (C.c_void_p * len(xs))()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def zb_run_stage_schedule(pl, stages, X0, dY_last, dX0_out, Y_last_out, ops, workspace,
+                          ws_bytes, stats=None, stream=None):
+    """stages: list of dicts/objects with W1, W2, b1, b2, dW1, dW2, db1, db2 pointers."""
+    sp = (zb_stage_params * len(stages))()
+    for i, st in enumerate(stages):
+        get = st.get if isinstance(st, dict) else (lambda k, _s=st: getattr(_s, k, None))
+        for k in ("W1", "W2", "b1", "b2", "dW1", "dW2", "db1", "db2"):
+            setattr(sp[i], k, _ptr(get(k)))
+    arr = ops if isinstance(ops, C.Array) else ops_array(ops)
+    st_ptr = C.byref(stats) if stats is not None else None
+    _check(LIB.zb_run_stage_schedule(C.byref(pl), sp, _ptr_array(X0), _ptr_array(dY_last),
+                                     _ptr_array(dX0_out), _ptr_array(Y_last_out), arr, len(arr),
+                                     _ptr(workspace), ws_bytes, st_ptr, _stream(stream)),
+           "zb_run_stage_schedule")
+
+
+def zb_sync_status(stream=None):
+    _check(LIB.zb_sync_status(_stream(stream)), "zb_sync_status")

