@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Benchmark of the split-backward MLP stage on GB300 (one JSON line).
+
+A step is one replay of a stage's whole F/B/W op list over m microbatches
+(every forward, input-gradient and weight-gradient pass, fp32 weight
+gradients accumulated in microbatch order) with the inputs resident in HBM.
+
+Default workload: one stage of a GPT-3-style block, h=6144, ffn=24576,
+seq 3072, microbatch 1, bf16, m=24, replaying the stage-0 list of an 8-stage
+ZB-H2 ordering (all W deferred into the warm-up/cool-down slots).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c4|c3|c2]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun): the
+path has no exchange between GPUs, so "value" sums the replicas' work over
+the slowest replica's time.  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload (host cores), the baseline arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "F/B/W TFLOP/s and stage tokens/sec on 1 GB300; % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+
+WORKLOADS = {
+    # name: (h, f, M, m, schedule, pipeline depth the list comes from, description)
+    "c4": (6144, 24576, 3072, 24, "ZBH2", 8,
+           "one stage h=6144 ffn=24576 seq 3072 microbatch 1 m=24, ZB-H2 stage-0 list of an "
+           "8-stage pipeline, all W deferred, fp32 dW accumulate"),
+    "c3": (4096, 16384, 3072, 16, "ZBH1", 8,
+           "one stage h=4096 ffn=16384 seq 3072 microbatch 1 m=16, ZB-H1 stage-0 list of an "
+           "8-stage pipeline, deferred W held in HBM"),
+    "c2": (1024, 4096, 2048, 8, "ZBH1", 4,
+           "P=4 stages h=1024 ffn=4096 microbatch 4x512 m=8, ZB-H1 replayed for all stages "
+           "on one GPU"),
+}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"],
+                "bf16_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def _gemm_source_sha():
+    h = hashlib.sha256()
+    for n in ("gemm_tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "split_backward_gemms_gb300", "csrc", n), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+    taken on the current GEMM source; else None."""
+    path = os.path.join(ROOT, "profiles", f"gemm_tc_{workload}.md")
+    try:
+        with open(path) as fh:
+            txt = fh.read()
+    except OSError:
+        return None
+    vals = {}
+    for ln in txt.splitlines():
+        if ln.startswith("traffic_bytes_per_launch:") or ln.startswith("source_sha:"):
+            k, v = ln.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha") != _gemm_source_sha():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _cpu_sample(h, f, tokens, seed=0):
+    """Seeded host inputs for the oracle sample (the same draw recipe)."""
+    from split_backward_gemms_gb300 import inputs
+    stages, X0, dY = inputs.pipeline_draws(1, 1, tokens, h, f, seed=seed)
+    return stages[0], X0[0], dY[0]
+
+
+def cpu_oracle_rate(h, f, tokens, repeats=1):
+    """Time the fp64 oracle's F, B and W on a `tokens`-row slice; TFLOP/s."""
+    import numpy as np
+
+    from oracle import block as ob
+    st, X, G = _cpu_sample(h, f, tokens)
+    X, G, W1, W2 = (a.astype(np.float64) for a in (X, G, st.W1, st.W2))
+    best = None
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        H, A, _ = ob.forward(X, W1, W2)
+        _, dH, _ = ob.backward_input(G, W1, W2, H)
+        ob.backward_weight(X, A, dH, G)
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    flops = 12.0 * tokens * h * f
+    return flops / best / 1e12, best
+
+
+def run_reference(args, wl):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    h, f, M, m, sched, Pl, desc = WORKLOADS[wl]
+    tokens = 256
+    from oracle import block as ob  # noqa: F401  (the oracle is the reference arm)
+    import numpy as np
+    st, X, G = _cpu_sample(h, f, tokens)
+    X, G, W1, W2 = (a.astype(np.float64) for a in (X, G, st.W1, st.W2))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        H, A, _ = ob.forward(X, W1, W2)
+        _, dH, _ = ob.backward_input(G, W1, W2, H)
+        ob.backward_weight(X, A, dH, G)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    flops = 12.0 * tokens * h * f
+    tot = sum(times)
+    value = flops * len(times) / tot / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": desc, "h": h, "f": f, "M": M, "m": m, "schedule": sched},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"F+B+W of one microbatch's first {tokens} tokens at "
+                                   f"h={h}, f={f} per step, fp64 numpy on host cores"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=tuple(WORKLOADS), default="c4")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args, args.workload)
+
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from split_backward_gemms_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if ws > 1:
+        dist.barrier()
+    from split_backward_gemms_gb300 import zb
+
+    h, f, M, m, sched, Pl, desc = WORKLOADS[args.workload]
+    multi = args.workload == "c2"
+    P = Pl if multi else 1
+    gen = torch.Generator(device=dev).manual_seed(1000 + rank)
+    bf = torch.bfloat16
+    W = [{"W1": (torch.randn(h, f, device=dev, generator=gen) * 0.02).to(bf),
+          "W2": (torch.randn(f, h, device=dev, generator=gen) * 0.02).to(bf),
+          "dW1": torch.zeros(h, f, device=dev), "dW2": torch.zeros(f, h, device=dev)}
+         for _ in range(P)]
+    X0 = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
+    dY = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
+    ops = zb.zb_make_schedule(sched, Pl, m)
+    if not multi:
+        ops = [(k, 0, j) for k, s, j in ops if s == 0]
+    blk = zb.make_block(M, h, f)
+    pl = zb.make_pipeline(P, m, blk, timing=True)
+    need, peak_live = zb.zb_schedule_workspace_size(pl, ops)
+    ws_t = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    n_ops = len(ops)
+    ops_c = zb.ops_array(ops)
+
+    def step(stats):
+        zb.zb_run_stage_schedule(pl, W, X0, dY, None, None, ops_c, ws_t, ws_t.numel(), stats,
+                                 stream)
+
+    st = zb.zb_run_stats()
+    for _ in range(args.warmup):
+        step(st)
+    torch.cuda.synchronize()
+    zb.zb_sync_status(stream)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    sums = {"gemm_ms": 0.0, "gemm_launches": 0, "kind": [0.0] * 4}
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(st)
+        sums["gemm_ms"] += st.gemm_ms
+        sums["gemm_launches"] += st.n_gemm_launches
+        for i in range(4):
+            sums["kind"][i] += st.kind_ms[i]
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    zb.zb_sync_status(stream)
+    ms = e0.elapsed_time(e1)
+    t = torch.tensor([ms], device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+
+    flop_mb = 12.0 * M * h * f  # F, B and W: 4 M h f each per microbatch
+    step_flops = flop_mb * m * P
+    value = step_flops * args.steps * ws / (ms_max / 1e3) / 1e12
+    tokens_s = m * M * args.steps * ws / (ms_max / 1e3)
+    kind_tf = {}
+    for i, name in enumerate(("F", "B", "W")):
+        kms = sums["kind"][i]
+        kind_tf[name] = (4.0 * M * h * f * m * P * args.steps / (kms / 1e3) / 1e12) if kms > 0 else None
+    peaks = _peaks()
+    gemm_flops = 2.0 * M * h * f
+    avg_launch_ms = sums["gemm_ms"] / max(1, sums["gemm_launches"])
+    achieved = gemm_flops / (avg_launch_ms / 1e3) / 1e12
+    roof_peak = peaks["bf16_sustained"]
+    traffic = _profiled_traffic(args.workload)
+
+    # ------------------------------------------------------------- end to end
+    pin = [x.cpu().pin_memory() for x in X0]
+    pin_g = [g.cpu().pin_memory() for g in dY]
+    host_dW = [(torch.empty(h, f, pin_memory=True), torch.empty(f, h, pin_memory=True))
+               for _ in range(P)]
+    h2d = sum(x.numel() * x.element_size() for x in pin + pin_g)
+    d2h = sum(a.numel() * 4 + b.numel() * 4 for a, b in host_dW)
+
+    def e2e_step():
+        for j in range(m):
+            X0[j].copy_(pin[j], non_blocking=True)
+            dY[j].copy_(pin_g[j], non_blocking=True)
+        step(None)
+        for s in range(P):
+            host_dW[s][0].copy_(W[s]["dW1"], non_blocking=True)
+            host_dW[s][1].copy_(W[s]["dW2"], non_blocking=True)
+
+    pl.timing = 0
+    e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    t = torch.tensor([e2e_ms], device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_value = step_flops * args.e2e_steps * ws / (float(t.item()) / 1e3) / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tokens = 1024
+        rate, secs = cpu_oracle_rate(h, f, tokens)
+        cpu = {"value": rate, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"fp64 numpy F+B+W of one microbatch's first {tokens} tokens at h={h}, "
+                         f"f={f} ({secs:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": desc, "h": h, "f": f, "M": M, "m": m, "P": P,
+                       "schedule": sched, "list_from_P": Pl,
+                       "parallelism": "replicas" if ws > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (W1 %.0f MB, X and dY %.0f MB per microbatch)"
+                             % (h * f * 2 / 1e6, M * h * 2 / 1e6)},
+            "tokens_per_s": tokens_s,
+            "tflops": kind_tf,
+            "pct_of_peak": {"burst": 100.0 * value / ws / peaks["bf16"],
+                            "sustained": 100.0 * value / ws / peaks["bf16_sustained"]},
+            "peak_live_bytes": peak_live, "workspace_bytes": need,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": roof_peak,
+                         "unit": "TFLOP/s", "frac": achieved / roof_peak, "traffic": traffic,
+                         "kernel": "zb_gemm_bf16_tc_kernel (all six GEMMs of F/B/W)",
+                         "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
+                         "frac_of_burst": achieved / peaks["bf16"]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": sums["gemm_launches"],
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -12,10 +12,14 @@
 //   warps 2..5  drain the accumulator with tcgen05.ld (one TMEM lane = one
 //               output row per thread) and apply the epilogue: bf16 store,
 //               bias + GeLU dual store (H and A), GeLU' product with the
-//               saved H (dH), or fp32 read-modify-write of a weight gradient.
+//               saved H (dH), or fp32 accumulation of a weight gradient.
+//               Results leave through swizzled shared-memory staging boxes
+//               and TMA tensor stores; the weight gradient is added in place
+//               with a TMA reduce-add (one fp32 add per element, in L2).
 // The two accumulators let the epilogue of tile t overlap the MMAs of t+1.
 // Tiles are visited in a fixed order (tile = blockIdx.x + i * gridDim.x,
-// M-blocks fastest) and K is never split, so results are deterministic.
+// grouped rasterisation, see tile_coords) and K is never split, so results
+// are deterministic.
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets the
 // device error word, drains its in-flight copies and MMAs, frees TMEM and
 // returns.
@@ -45,6 +49,9 @@ constexpr uint32_t ACC_COLS = 256;
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s
 constexpr uint64_t DRAIN_LIMIT_NS = 500000000ull;  // 0.5 s
 
+constexpr uint32_t STAGING_BOX = 32 * 128;                 // 32 rows x 128 bytes
+constexpr uint32_t STAGING_BYTES = 4 * 2 * STAGING_BOX;      // 2 boxes per epilogue warp
+
 struct SharedCtl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -54,7 +61,8 @@ struct SharedCtl {
     uint32_t tmem_base;
     int abort_flag;
 };
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(SharedCtl) + 64;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + sizeof(SharedCtl) + 64;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct EpiArgs {
     int Mg, Ng, Kg;
@@ -124,81 +132,66 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
     return __bfloat1622float2(v);
 }
 
-// Apply the epilogue to 32 consecutive columns [col0, col0+32) of one row.
-template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const EpiArgs& a, int row, int col0,
-                                               const uint32_t (&v)[32]) {
+// Tile order: groups of GROUP_M M-blocks; inside a group M is fastest, then
+// N.  A wave of resident CTAs then covers about GROUP_M x (grid / GROUP_M)
+// tiles, so the operand panels it touches at each K step are few and shared
+// from L2 (M-fastest over a tall problem would stream a new A panel per CTA).
+constexpr int GROUP_M = 16;
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& mb, int& nb) {
+    const int per_group = GROUP_M * tiles_n;
+    const int g = tile / per_group;
+    const int first = g * GROUP_M;
+    const int gsz = min(tiles_m - first, GROUP_M);
+    const int r = tile - g * per_group;
+    mb = first + r % gsz;
+    nb = r / gsz;
+}
+
+// Write one thread's 128-byte row of a 32-row staging box (TMA 128-byte
+// swizzle: 16-byte chunk k of row r sits at chunk k ^ (r mod 8)).
+__device__ __forceinline__ void stage_row(uint32_t stg, int lane, const uint32_t (&w)[32]) {
+    const uint32_t row = stg + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const int col = col0 + g * 8;
-        if (col >= a.Ng) break;
-        float x[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[g * 8 + i]);
-        if (EPI == zb::EPI_F32) {
-            float* dst = reinterpret_cast<float*>(a.out0) + static_cast<long long>(row) * a.ld0 + col;
-            if (a.accumulate) {
-                const float4 o0 = *reinterpret_cast<const float4*>(dst);
-                const float4 o1 = *reinterpret_cast<const float4*>(dst + 4);
-                x[0] += o0.x; x[1] += o0.y; x[2] += o0.z; x[3] += o0.w;
-                x[4] += o1.x; x[5] += o1.y; x[6] += o1.z; x[7] += o1.w;
-            }
-            *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
-            *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
-        } else {
-            if (EPI == zb::EPI_STORE_BF16 || EPI == zb::EPI_GELU_DUAL) {
-                if (a.bias != nullptr) {
-                    const uint4 b = *reinterpret_cast<const uint4*>(a.bias + col);
-                    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = unpack_bf16x2(bw[i]);
-                        x[2 * i] += f.x;
-                        x[2 * i + 1] += f.y;
-                    }
-                }
-            }
-            if (EPI == zb::EPI_GELU_BWD) {
-                const uint4 hv = *reinterpret_cast<const uint4*>(
-                    a.aux + static_cast<long long>(row) * a.ldaux + col);
-                const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 f = unpack_bf16x2(hw[i]);
-                    x[2 * i] *= gelu_grad_f(f.x, a.act);
-                    x[2 * i + 1] *= gelu_grad_f(f.y, a.act);
-                }
-            }
-            uint4 o;
-            o.x = pack_bf16x2(x[0], x[1]);
-            o.y = pack_bf16x2(x[2], x[3]);
-            o.z = pack_bf16x2(x[4], x[5]);
-            o.w = pack_bf16x2(x[6], x[7]);
-            __nv_bfloat16* dst =
-                reinterpret_cast<__nv_bfloat16*>(a.out0) + static_cast<long long>(row) * a.ld0 + col;
-            *reinterpret_cast<uint4*>(dst) = o;
-            if (EPI == zb::EPI_GELU_DUAL) {
-                uint4 q;
-                q.x = pack_bf16x2(gelu_f(x[0], a.act), gelu_f(x[1], a.act));
-                q.y = pack_bf16x2(gelu_f(x[2], a.act), gelu_f(x[3], a.act));
-                q.z = pack_bf16x2(gelu_f(x[4], a.act), gelu_f(x[5], a.act));
-                q.w = pack_bf16x2(gelu_f(x[6], a.act), gelu_f(x[7], a.act));
-                __nv_bfloat16* dst1 = reinterpret_cast<__nv_bfloat16*>(a.out1) +
-                                      static_cast<long long>(row) * a.ld1 + col;
-                *reinterpret_cast<uint4*>(dst1) = q;
-            }
-        }
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t off = static_cast<uint32_t>((k ^ (lane & 7)) << 4);
+        zbp::st_shared_v4(row + off, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
+}
+
+// Lane 0 makes sure the staging buffer about to be written is no longer read
+// by the bulk store issued two stores ago (buffers alternate).
+__device__ __forceinline__ void staging_acquire(int lane) {
+    if (lane == 0) zbp::bulk_wait_read<1>();
+    __syncwarp();
+}
+
+// Hand a filled staging buffer to the TMA unit.
+template <bool REDUCE>
+__device__ __forceinline__ void staging_release(const CUtensorMap* tm, uint32_t stg, int lane,
+                                                int x, int y) {
+    zbp::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (REDUCE)
+            zbp::tma_reduce_add_2d(tm, stg, x, y);
+        else
+            zbp::tma_store_2d(tm, stg, x, y);
+        zbp::bulk_commit();
     }
 }
 
 template <int EPI, int A_MN, int B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     zb_gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB, const EpiArgs args) {
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmO0,
+                           const __grid_constant__ CUtensorMap tmO1, const EpiArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* staging = smem + STAGES * STAGE_BYTES;
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(staging + STAGING_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -223,6 +216,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         zbp::tma_prefetch_desc(&tmA);
         zbp::tma_prefetch_desc(&tmB);
+        zbp::tma_prefetch_desc(&tmO0);
+        if (EPI == zb::EPI_GELU_DUAL) zbp::tma_prefetch_desc(&tmO1);
     }
     if (warp == 1) {
         zbp::tmem_alloc(zbp::smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -240,8 +235,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % tiles_m) * BM;
-                const int n0 = (tile / tiles_m) * BN;
+                int mb, nb;
+                tile_coords(tile, tiles_m, tiles_n, mb, nb);
+                const int m0 = mb * BM;
+                const int n0 = nb * BN;
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t r = it / STAGES;
@@ -331,31 +328,124 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // Warp w may read TMEM lanes 32*(w%4) .. +31: rows q*32 .. q*32+31 of
+        // the tile, one row per thread.  Results leave through two 4-KiB
+        // swizzled staging boxes per warp (32 rows x 128 bytes) and TMA
+        // stores; the fp32 weight gradient is accumulated with a TMA
+        // reduce-add, so the old values are never read by the SM.
+        const int q = warp & 3;
+        const uint32_t stg0 = zbp::smem_u32(staging + (warp - 2) * 2 * STAGING_BOX);
+        uint32_t flip = 0;
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
             const uint32_t buf = local & 1u;
             const uint32_t tr = local >> 1;
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            const int m0 = mb * BM;
+            const int n0 = nb * BN;
+            const int row0 = m0 + q * 32;
+            const int row = row0 + lane;
+            if (EPI == zb::EPI_GELU_BWD && row < args.Mg) {
+                // warm L2 with this row of H while the MMAs run
+                const int ncols = min(BN, args.Ng - n0);
+                zbp::prefetch_l2(args.aux + static_cast<long long>(row) * args.ldaux + n0,
+                                 static_cast<uint32_t>(ncols) * 2u);
+            }
             if (!wait_bar(zbp::smem_u32(&ctl->tfull[buf]), tr & 1u, abort_flag, args.err,
                           ERR_WAIT_EPI, WAIT_LIMIT_NS, true))
                 break;
             zbp::tc_fence_after();
-            const int m0 = (tile % tiles_m) * BM;
-            const int n0 = (tile / tiles_m) * BN;
-            const int row = m0 + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
+            const bool rows_live = row0 < args.Mg;
+            if (EPI == zb::EPI_F32) {
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                zbp::tmem_ld_32x32b_x32(taddr + c * 32, v);
-                zbp::tmem_ld_wait();
-                const int col0 = n0 + c * 32;
-                if (row < args.Mg && col0 < args.Ng) epilogue_chunk<EPI>(args, row, col0, v);
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    zbp::tmem_ld_32x32b_x32(taddr + c * 32, v);
+                    zbp::tmem_ld_wait();
+                    const int col0 = n0 + c * 32;
+                    if (!rows_live || col0 >= args.Ng) continue;
+                    const uint32_t stg = stg0 + flip * STAGING_BOX;
+                    flip ^= 1u;
+                    staging_acquire(lane);
+                    stage_row(stg, lane, v);
+                    if (args.accumulate)
+                        staging_release<true>(&tmO0, stg, lane, col0, row0);
+                    else
+                        staging_release<false>(&tmO0, stg, lane, col0, row0);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t v0[32], v1[32];
+                    zbp::tmem_ld_32x32b_x32(taddr + c * 64, v0);
+                    zbp::tmem_ld_32x32b_x32(taddr + c * 64 + 32, v1);
+                    zbp::tmem_ld_wait();
+                    const int col0 = n0 + c * 64;
+                    if (!rows_live || col0 >= args.Ng) continue;
+                    float x[64];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        x[i] = __uint_as_float(v0[i]);
+                        x[32 + i] = __uint_as_float(v1[i]);
+                    }
+                    if ((EPI == zb::EPI_STORE_BF16 || EPI == zb::EPI_GELU_DUAL) && args.bias) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            if (col0 + g * 8 >= args.Ng) break;
+                            const uint4 b = *reinterpret_cast<const uint4*>(args.bias + col0 + g * 8);
+                            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 f2 = unpack_bf16x2(bw[i]);
+                                x[g * 8 + 2 * i] += f2.x;
+                                x[g * 8 + 2 * i + 1] += f2.y;
+                            }
+                        }
+                    }
+                    if (EPI == zb::EPI_GELU_BWD && row < args.Mg) {
+                        const __nv_bfloat16* hp = args.aux + static_cast<long long>(row) * args.ldaux + col0;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            if (col0 + g * 8 >= args.Ng) break;
+                            const uint4 hv = *reinterpret_cast<const uint4*>(hp + g * 8);
+                            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 f2 = unpack_bf16x2(hw[i]);
+                                x[g * 8 + 2 * i] *= gelu_grad_f(f2.x, args.act);
+                                x[g * 8 + 2 * i + 1] *= gelu_grad_f(f2.y, args.act);
+                            }
+                        }
+                    }
+                    uint32_t w[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+                    uint32_t stg = stg0 + flip * STAGING_BOX;
+                    flip ^= 1u;
+                    staging_acquire(lane);
+                    stage_row(stg, lane, w);
+                    staging_release<false>(&tmO0, stg, lane, col0, row0);
+                    if (EPI == zb::EPI_GELU_DUAL) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            w[i] = pack_bf16x2(gelu_f(x[2 * i], args.act), gelu_f(x[2 * i + 1], args.act));
+                        stg = stg0 + flip * STAGING_BOX;
+                        flip ^= 1u;
+                        staging_acquire(lane);
+                        stage_row(stg, lane, w);
+                        staging_release<false>(&tmO1, stg, lane, col0, row0);
+                    }
+                }
             }
             zbp::tc_fence_before();
             __syncwarp();
             if (lane == 0) zbp::mbar_arrive(zbp::smem_u32(&ctl->tempty[buf]));
         }
+        // the staging buffers must not be released while a bulk store reads them
+        if (lane == 0) zbp::bulk_wait<0>();
+        __syncwarp();
     }
 
     __syncthreads();
@@ -390,19 +480,21 @@ EncodeTiledFn encode_fn(std::string* why) {
     return fn;
 }
 
-// 2-D bf16 map: inner dimension `inner` (contiguous), `outer` rows of stride
-// ld elements; box of box_inner x box_outer elements, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-              uint32_t box_inner, uint32_t box_outer, std::string* why) {
+// 2-D map: inner dimension `inner` (contiguous), `outer` rows of stride ld
+// elements; box of box_inner x box_outer elements, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t outer,
+              uint64_t ld, uint32_t box_inner, uint32_t box_outer, std::string* why) {
     EncodeTiledFn fn = encode_fn(why);
     if (!fn) return false;
+    const uint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {ld * 2};
+    cuuint64_t strides[1] = {ld * es};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         if (why) *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
         return false;
@@ -423,8 +515,8 @@ int sm_count() {
 }
 
 template <int EPI, int A_MN, int B_MN>
-zb_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const EpiArgs& ea, int grid,
-                 cudaStream_t st) {
+zb_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to0,
+                 const CUtensorMap& to1, const EpiArgs& ea, int grid, cudaStream_t st) {
     auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN>;
     static int configured[64] = {0};
     int dev = 0;
@@ -436,7 +528,7 @@ zb_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const EpiArgs& ea
             return zb::fail(ZB_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
         configured[dev] = 1;
     }
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, ea);
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, to0, to1, ea);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return zb::fail(ZB_ERR_CUDA, std::string("tensor-core GEMM launch: ") + cudaGetErrorString(e));
@@ -445,11 +537,12 @@ zb_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const EpiArgs& ea
 
 template <int EPI>
 zb_status dispatch_major(int a_mn, int b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                         const EpiArgs& ea, int grid, cudaStream_t st) {
-    if (!a_mn && !b_mn) return launch<EPI, 0, 0>(ta, tb, ea, grid, st);
-    if (!a_mn && b_mn) return launch<EPI, 0, 1>(ta, tb, ea, grid, st);
-    if (a_mn && !b_mn) return launch<EPI, 1, 0>(ta, tb, ea, grid, st);
-    return launch<EPI, 1, 1>(ta, tb, ea, grid, st);
+                         const CUtensorMap& to0, const CUtensorMap& to1, const EpiArgs& ea,
+                         int grid, cudaStream_t st) {
+    if (!a_mn && !b_mn) return launch<EPI, 0, 0>(ta, tb, to0, to1, ea, grid, st);
+    if (!a_mn && b_mn) return launch<EPI, 0, 1>(ta, tb, to0, to1, ea, grid, st);
+    if (a_mn && !b_mn) return launch<EPI, 1, 0>(ta, tb, to0, to1, ea, grid, st);
+    return launch<EPI, 1, 1>(ta, tb, to0, to1, ea, grid, st);
 }
 
 }  // namespace
@@ -471,19 +564,30 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     if (g.epi == EPI_GELU_BWD && !g.aux) return fail(ZB_ERR_INVALID_ARG, "GeLU' epilogue needs H");
 
     std::string why;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, to0, to1;
     bool ok;
     if (g.a_mn)
-        ok = make_map(&ta, g.A, g.Mg, g.Kg, g.lda, 64, BK, &why);
+        ok = make_map(&ta, g.A, false, g.Mg, g.Kg, g.lda, 64, BK, &why);
     else
-        ok = make_map(&ta, g.A, g.Kg, g.Mg, g.lda, BK, BM, &why);
+        ok = make_map(&ta, g.A, false, g.Kg, g.Mg, g.lda, BK, BM, &why);
     if (ok) {
         if (g.b_mn)
-            ok = make_map(&tb, g.B, g.Ng, g.Kg, g.ldb, 64, BK, &why);
+            ok = make_map(&tb, g.B, false, g.Ng, g.Kg, g.ldb, 64, BK, &why);
         else
-            ok = make_map(&tb, g.B, g.Kg, g.Ng, g.ldb, BK, BN, &why);
+            ok = make_map(&tb, g.B, false, g.Kg, g.Ng, g.ldb, BK, BN, &why);
+    }
+    // epilogue boxes: 32 rows x 128 bytes (32 fp32 or 64 bf16 columns)
+    const bool f32_out = g.epi == EPI_F32;
+    const uint32_t ocols = f32_out ? 32 : 64;
+    if (ok) ok = make_map(&to0, g.out0, f32_out, g.Ng, g.Mg, g.ld0, ocols, 32, &why);
+    if (ok) {
+        if (g.epi == EPI_GELU_DUAL)
+            ok = make_map(&to1, g.out1, false, g.Ng, g.Mg, g.ld1, ocols, 32, &why);
+        else
+            to1 = to0;
     }
     if (!ok) return fail(ZB_ERR_CUDA, why);
+    if (f32_out && (g.ld0 % 4)) return fail(ZB_ERR_ALIGN, "fp32 output leading dimension must be a multiple of 4");
 
     unsigned int* err = device_error_word();
     if (!err) return ZB_ERR_CUDA;
@@ -509,10 +613,10 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (g.epi) {
-        case EPI_STORE_BF16: return dispatch_major<EPI_STORE_BF16>(g.a_mn, g.b_mn, ta, tb, ea, grid, st);
-        case EPI_GELU_DUAL: return dispatch_major<EPI_GELU_DUAL>(g.a_mn, g.b_mn, ta, tb, ea, grid, st);
-        case EPI_GELU_BWD: return dispatch_major<EPI_GELU_BWD>(g.a_mn, g.b_mn, ta, tb, ea, grid, st);
-        case EPI_F32: return dispatch_major<EPI_F32>(g.a_mn, g.b_mn, ta, tb, ea, grid, st);
+        case EPI_STORE_BF16: return dispatch_major<EPI_STORE_BF16>(g.a_mn, g.b_mn, ta, tb, to0, to1, ea, grid, st);
+        case EPI_GELU_DUAL: return dispatch_major<EPI_GELU_DUAL>(g.a_mn, g.b_mn, ta, tb, to0, to1, ea, grid, st);
+        case EPI_GELU_BWD: return dispatch_major<EPI_GELU_BWD>(g.a_mn, g.b_mn, ta, tb, to0, to1, ea, grid, st);
+        case EPI_F32: return dispatch_major<EPI_F32>(g.a_mn, g.b_mn, ta, tb, to0, to1, ea, grid, st);
         default: return fail(ZB_ERR_INVALID_ARG, "unknown epilogue");
     }
 }
