@@ -199,6 +199,30 @@ zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage_params* st
                                 const zb_op* ops, size_t n_ops, void* workspace,
                                 size_t ws_bytes, zb_run_stats* stats, void* stream);
 
+/* Allocation-free replay.  No counterpart in the paper: this is a library
+ * convenience for callers that cannot allocate device memory themselves
+ * (a custom operator inside a framework that owns all device memory through
+ * its own pool, or a latency-critical loop that must never call cudaMalloc /
+ * cudaFree, which can synchronise the whole device).  Same arguments and
+ * semantics as zb_run_stage_schedule, minus the workspace: the activation
+ * arena is a static device array of ZB_STATIC_ARENA_BYTES (64 MiB) that every
+ * device using this entry point holds from its first call until the process
+ * exits.  Op lists whose arena (zb_schedule_workspace_size) is larger are
+ * rejected with ZB_ERR_WORKSPACE; pl->timing must be 0 (ZB_ERR_INVALID_ARG
+ * otherwise).  No device memory is allocated by the call.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * All calls share the one array: calls whose work overlaps on the GPU (e.g.
+ * on two streams at once) race on it.  The arena needs no clearing (every
+ * buffer is written before it is read); the caller's dW/db follow
+ * pl->zero_grads exactly as in zb_run_stage_schedule. */
+#define ZB_STATIC_ARENA_BYTES (64ull << 20)
+zb_status zb_run_stage_schedule_static(const zb_pipeline* pl, const zb_stage_params* stages,
+                                       const void* const* X0, const void* const* dY_last,
+                                       void* const* dX0_out, void* const* Y_last_out,
+                                       const zb_op* ops, size_t n_ops, zb_run_stats* stats,
+                                       void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status                                                                   */
 /* ------------------------------------------------------------------------ */

@@ -96,6 +96,10 @@ def _load():
         "zb_run_stage_schedule": [C.POINTER(zb_pipeline), C.POINTER(zb_stage_params), C.POINTER(vp),
                                   C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), C.POINTER(zb_op), sz,
                                   vp, sz, C.POINTER(zb_run_stats), vp],
+        "zb_run_stage_schedule_static": [C.POINTER(zb_pipeline), C.POINTER(zb_stage_params),
+                                         C.POINTER(vp), C.POINTER(vp), C.POINTER(vp),
+                                         C.POINTER(vp), C.POINTER(zb_op), sz,
+                                         C.POINTER(zb_run_stats), vp],
         "zb_sync_status": [vp],
     }
     for name, args in sig.items():
@@ -235,6 +239,26 @@ def zb_run_stage_schedule(pl, stages, X0, dY_last, dX0_out, Y_last_out, ops, wor
                                      _ptr_array(dX0_out), _ptr_array(Y_last_out), arr, len(arr),
                                      _ptr(workspace), ws_bytes, st_ptr, _stream(stream)),
            "zb_run_stage_schedule")
+
+
+ZB_STATIC_ARENA_BYTES = 64 << 20
+
+
+def zb_run_stage_schedule_static(pl, stages, X0, dY_last, dX0_out, Y_last_out, ops, stats=None,
+                                 stream=None):
+    """zb_run_stage_schedule with the arena in the library's static device
+    array (no workspace argument; allocates nothing)."""
+    sp = (zb_stage_params * len(stages))()
+    for i, st in enumerate(stages):
+        get = st.get if isinstance(st, dict) else (lambda k, _s=st: getattr(_s, k, None))
+        for k in ("W1", "W2", "b1", "b2", "dW1", "dW2", "db1", "db2"):
+            setattr(sp[i], k, _ptr(get(k)))
+    arr = ops if isinstance(ops, C.Array) else ops_array(ops)
+    st_ptr = C.byref(stats) if stats is not None else None
+    _check(LIB.zb_run_stage_schedule_static(C.byref(pl), sp, _ptr_array(X0), _ptr_array(dY_last),
+                                            _ptr_array(dX0_out), _ptr_array(Y_last_out), arr,
+                                            len(arr), st_ptr, _stream(stream)),
+           "zb_run_stage_schedule_static")
 
 
 def zb_sync_status(stream=None):
