@@ -4,11 +4,11 @@
 // split MLP block (the three passes of "Zero Bubble Pipeline Parallelism",
 // summary §3.4: F, the input gradient B and the weight gradient W):
 //   warp 0      one thread issues TMA tensor copies of A/B tiles into a
-//               4-stage shared-memory ring (128-byte swizzle);
-//   warp 1      allocates 512 TMEM columns and one thread issues
-//               tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into one of
-//               two 256-column accumulators, committing each stage back to
-//               the producer and each finished tile to the epilogue;
+//               shared-memory ring (128-byte swizzle);
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (bf16 -> fp32) into one of two 256-column accumulators,
+//               committing each stage back to the producer and each
+//               finished tile to the epilogue;
 //   warps 2..5  drain the accumulator with tcgen05.ld (one TMEM lane = one
 //               output row per thread) and apply the epilogue: bf16 store,
 //               bias + GeLU dual store (H and A), GeLU' product with the
@@ -17,9 +17,18 @@
 //               and TMA tensor stores; the weight gradient is added in place
 //               with a TMA reduce-add (one fp32 add per element, in L2).
 // The two accumulators let the epilogue of tile t overlap the MMAs of t+1.
-// Tiles are visited in a fixed order (tile = blockIdx.x + i * gridDim.x,
-// grouped rasterisation, see tile_coords) and K is never split, so results
-// are deterministic.
+//
+// Two CTA-group shapes share the code:
+//   CG = 1  one CTA per 128x256 tile (M=128, N=256 MMAs), 4 stages of 48 KB;
+//   CG = 2  a cluster of two CTAs on two SMs per 256x256 tile: each CTA
+//           loads its 128 rows of A and half (128 columns) of B, the even
+//           CTA issues M=256, N=256 MMAs (tcgen05 cta_group::2) that write
+//           each CTA's 128 rows into its own TMEM; 6 stages of 32 KB, half
+//           the B traffic per SM.  Copies of both CTAs complete on the even
+//           CTA's barriers; MMA completion is multicast back to both.
+// Tiles are visited in a fixed order (tile = cluster + i * clusters, grouped
+// rasterisation, see tile_coords) and K is never split, so results are
+// deterministic for a given shape.
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets the
 // device error word, drains its in-flight copies and MMAs, frees TMEM and
 // returns.
@@ -28,6 +37,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -35,23 +46,30 @@
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr uint32_t A_BYTES = BM * BK * 2;          // 16 KiB
-constexpr uint32_t B_BYTES = BN * BK * 2;          // 32 KiB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t MN_ATOM_BYTES = 64 * BK * 2;    // 64 MN x 64 K, one TMA box
+constexpr int BM = 128;  // rows per CTA
+constexpr int BN = 256;  // tile columns (MMA N)
+constexpr int BK = 64;   // K per stage (one 128-byte swizzle row of bf16)
+constexpr uint32_t A_BYTES = BM * BK * 2;        // 16 KiB
+constexpr uint32_t MN_ATOM_BYTES = 64 * BK * 2;  // 64 MN x 64 K, one TMA box
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s
 constexpr uint64_t DRAIN_LIMIT_NS = 500000000ull;  // 0.5 s
+constexpr uint32_t STAGING_BOX = 32 * 128;             // 32 rows x 128 bytes
+constexpr uint32_t STAGING_BYTES = 4 * 2 * STAGING_BOX;  // 2 boxes per epilogue warp
 
-constexpr uint32_t STAGING_BOX = 32 * 128;                 // 32 rows x 128 bytes
-constexpr uint32_t STAGING_BYTES = 4 * 2 * STAGING_BOX;      // 2 boxes per epilogue warp
+template <int CG>
+struct Cfg {
+    static constexpr int B_ROWS = BN / CG;                       // B columns held per CTA
+    static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;         // 32 or 16 KiB
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;   // 48 or 32 KiB
+    static constexpr int STAGES = CG == 1 ? 4 : 6;
+    static constexpr int TILE_M = BM * CG;
+    static constexpr int GROUP_M = CG == 1 ? 16 : 8;             // see tile_coords
+};
 
+template <int STAGES>
 struct SharedCtl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -61,8 +79,14 @@ struct SharedCtl {
     uint32_t tmem_base;
     int abort_flag;
 };
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + sizeof(SharedCtl) + 64;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+template <int CG>
+constexpr size_t smem_bytes() {
+    return 1024 + Cfg<CG>::STAGES * Cfg<CG>::STAGE_BYTES + STAGING_BYTES +
+           sizeof(SharedCtl<Cfg<CG>::STAGES>) + 64;
+}
+static_assert(smem_bytes<1>() <= 232448, "shared memory budget (one CTA)");
+static_assert(smem_bytes<2>() <= 232448, "shared memory budget (CTA pair)");
 
 struct EpiArgs {
     int Mg, Ng, Kg;
@@ -83,14 +107,20 @@ constexpr unsigned ERR_WAIT_PRODUCER = 1u << 0;
 constexpr unsigned ERR_WAIT_MMA = 1u << 1;
 constexpr unsigned ERR_WAIT_EPI = 1u << 2;
 
+// Bounded wait on a local mbarrier phase.  CLUSTER selects acquire at
+// cluster scope (arrivals that come from the other CTA of a pair).
+template <bool CLUSTER>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned int* err, unsigned code, uint64_t limit_ns,
                                          bool honour_abort) {
-    if (zbp::mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() {
+        return CLUSTER ? zbp::mbar_try_wait_cluster(bar, parity) : zbp::mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
     const uint64_t t0 = zbp::globaltimer_ns();
     uint32_t spins = 0;
     while (true) {
-        if (zbp::mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((++spins & 63u) == 0) {
             if (honour_abort && *abort_flag) return false;
             if (zbp::globaltimer_ns() - t0 > limit_ns) {
@@ -132,17 +162,16 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
     return __bfloat1622float2(v);
 }
 
-// Tile order: groups of GROUP_M M-blocks; inside a group M is fastest, then
-// N.  A wave of resident CTAs then covers about GROUP_M x (grid / GROUP_M)
+// Tile order: groups of `group` M-blocks; inside a group M is fastest, then
+// N.  A wave of resident CTAs then covers about group x (clusters / group)
 // tiles, so the operand panels it touches at each K step are few and shared
 // from L2 (M-fastest over a tall problem would stream a new A panel per CTA).
-constexpr int GROUP_M = 16;
-
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& mb, int& nb) {
-    const int per_group = GROUP_M * tiles_n;
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group, int& mb,
+                                            int& nb) {
+    const int per_group = group * tiles_n;
     const int g = tile / per_group;
-    const int first = g * GROUP_M;
-    const int gsz = min(tiles_m - first, GROUP_M);
+    const int first = g * group;
+    const int gsz = min(tiles_m - first, group);
     const int r = tile - g * per_group;
     mb = first + r % gsz;
     nb = r / gsz;
@@ -181,21 +210,28 @@ __device__ __forceinline__ void staging_release(const CUtensorMap* tm, uint32_t 
     }
 }
 
-template <int EPI, int A_MN, int B_MN>
+template <int EPI, int A_MN, int B_MN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     zb_gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmO0,
                            const __grid_constant__ CUtensorMap tmO1, const EpiArgs args) {
+    using C = Cfg<CG>;
+    constexpr int STAGES = C::STAGES;
+    constexpr bool PAIR = CG == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* staging = smem + STAGES * STAGE_BYTES;
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(staging + STAGING_BYTES);
+    uint8_t* staging = smem + STAGES * C::STAGE_BYTES;
+    SharedCtl<STAGES>* ctl = reinterpret_cast<SharedCtl<STAGES>*>(staging + STAGING_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tiles_m = (args.Mg + BM - 1) / BM;
+    const uint32_t rank = PAIR ? zbp::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x / CG;
+    const int clusters = gridDim.x / CG;
+    const int tiles_m = (args.Mg + C::TILE_M - 1) / C::TILE_M;
     const int tiles_n = (args.Ng + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
     const int num_kb = (args.Kg + BK - 1) / BK;
@@ -207,7 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             zbp::mbar_init(zbp::smem_u32(&ctl->tfull[b]), 1);
-            zbp::mbar_init(zbp::smem_u32(&ctl->tempty[b]), 4);
+            zbp::mbar_init(zbp::smem_u32(&ctl->tempty[b]), 4 * CG);
         }
         zbp::mbar_init(zbp::smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
@@ -220,11 +256,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (EPI == zb::EPI_GELU_DUAL) zbp::tma_prefetch_desc(&tmO1);
     }
     if (warp == 1) {
-        zbp::tmem_alloc(zbp::smem_u32(&ctl->tmem_base), TMEM_COLS);
-        zbp::tmem_relinquish();
+        if (PAIR) {
+            zbp::tmem_alloc_pair(zbp::smem_u32(&ctl->tmem_base), TMEM_COLS);
+            zbp::tmem_relinquish_pair();
+        } else {
+            zbp::tmem_alloc(zbp::smem_u32(&ctl->tmem_base), TMEM_COLS);
+            zbp::tmem_relinquish();
+        }
     }
     zbp::tc_fence_before();
     __syncthreads();
+    if (PAIR) zbp::cluster_sync();  // both CTAs' barriers exist before any remote use
     zbp::tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
@@ -234,60 +276,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ------------------------------------------------ TMA producer
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
                 int mb, nb;
-                tile_coords(tile, tiles_m, tiles_n, mb, nb);
-                const int m0 = mb * BM;
-                const int n0 = nb * BN;
+                tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
+                const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
+                const int nb0 = nb * BN + static_cast<int>(rank) * C::B_ROWS;
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t r = it / STAGES;
-                    if (!wait_bar(zbp::smem_u32(&ctl->empty[s]), (r & 1u) ^ 1u, abort_flag,
-                                  args.err, ERR_WAIT_PRODUCER, WAIT_LIMIT_NS, true)) {
+                    if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->empty[s]), (r & 1u) ^ 1u, abort_flag,
+                                        args.err, ERR_WAIT_PRODUCER, WAIT_LIMIT_NS, true)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t full = zbp::smem_u32(&ctl->full[s]);
-                    const uint32_t sa = zbp::smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t full_local = zbp::smem_u32(&ctl->full[s]);
+                    const uint32_t full = PAIR ? zbp::mapa_shared(full_local, 0) : full_local;
+                    const uint32_t sa = zbp::smem_u32(smem + s * C::STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
                     const int k0 = kb * BK;
-                    zbp::mbar_arrive_expect_tx(full, STAGE_BYTES);
+                    if (leader) zbp::mbar_arrive_expect_tx(full_local, C::STAGE_BYTES * CG);
+                    auto load = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) {
+                        if (PAIR)
+                            zbp::tma_load_2d_pair(dst, tm, full, x, y);
+                        else
+                            zbp::tma_load_2d(dst, tm, full, x, y);
+                    };
                     if (A_MN) {
-                        zbp::tma_load_2d(sa, &tmA, full, m0, k0);
-                        zbp::tma_load_2d(sa + MN_ATOM_BYTES, &tmA, full, m0 + 64, k0);
+                        load(sa, &tmA, m0, k0);
+                        load(sa + MN_ATOM_BYTES, &tmA, m0 + 64, k0);
                     } else {
-                        zbp::tma_load_2d(sa, &tmA, full, k0, m0);
+                        load(sa, &tmA, k0, m0);
                     }
                     if (B_MN) {
 #pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)
-                            zbp::tma_load_2d(sb + i * MN_ATOM_BYTES, &tmB, full, n0 + 64 * i, k0);
+                        for (int i = 0; i < C::B_ROWS / 64; ++i)
+                            load(sb + i * MN_ATOM_BYTES, &tmB, nb0 + 64 * i, k0);
                     } else {
-                        zbp::tma_load_2d(sb, &tmB, full, k0, n0);
+                        load(sb, &tmB, k0, nb0);
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 // wait for the copies that were issued but may not have landed
                 const uint32_t first = it > STAGES ? it - STAGES : 0;
                 for (uint32_t i = first; i < it; ++i) {
-                    wait_bar(zbp::smem_u32(&ctl->full[i % STAGES]), (i / STAGES) & 1u, abort_flag,
-                             args.err, ERR_WAIT_PRODUCER, DRAIN_LIMIT_NS, false);
+                    wait_bar<PAIR>(zbp::smem_u32(&ctl->full[i % STAGES]), (i / STAGES) & 1u,
+                                   abort_flag, args.err, ERR_WAIT_PRODUCER, DRAIN_LIMIT_NS, false);
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = zbp::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+            constexpr uint32_t idesc = zbp::idesc_bf16_f32(BM * CG, BN, A_MN, B_MN);
             uint32_t it = 0;
             uint32_t local = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+            for (int tile = cluster; tile < num_tiles && ok; tile += clusters, ++local) {
                 const uint32_t buf = local & 1u;
                 const uint32_t tr = local >> 1;
-                if (!wait_bar(zbp::smem_u32(&ctl->tempty[buf]), (tr & 1u) ^ 1u, abort_flag,
-                              args.err, ERR_WAIT_MMA, WAIT_LIMIT_NS, true)) {
+                if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->tempty[buf]), (tr & 1u) ^ 1u, abort_flag,
+                                    args.err, ERR_WAIT_MMA, WAIT_LIMIT_NS, true)) {
                     ok = false;
                     break;
                 }
@@ -296,13 +345,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t r = it / STAGES;
-                    if (!wait_bar(zbp::smem_u32(&ctl->full[s]), r & 1u, abort_flag, args.err,
-                                  ERR_WAIT_MMA, WAIT_LIMIT_NS, true)) {
+                    if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->full[s]), r & 1u, abort_flag, args.err,
+                                        ERR_WAIT_MMA, WAIT_LIMIT_NS, true)) {
                         ok = false;
                         break;
                     }
                     zbp::tc_fence_after();
-                    const uint32_t sa = zbp::smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t sa = zbp::smem_u32(smem + s * C::STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -314,35 +363,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bd =
                             B_MN ? zbp::smem_desc_sw128(sb + kk * 2048, MN_ATOM_BYTES, 1024)
                                  : zbp::smem_desc_sw128(sb + kk * 32, 16, 1024);
-                        zbp::tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        if (PAIR)
+                            zbp::tc_mma_f16_pair(d_tmem, ad, bd, idesc, acc);
+                        else
+                            zbp::tc_mma_f16(d_tmem, ad, bd, idesc, acc);
                     }
-                    zbp::tc_commit(zbp::smem_u32(&ctl->empty[s]));
+                    if (PAIR)
+                        zbp::tc_commit_pair_multicast(zbp::smem_u32(&ctl->empty[s]), 0x3);
+                    else
+                        zbp::tc_commit(zbp::smem_u32(&ctl->empty[s]));
                 }
                 if (!ok) break;
-                zbp::tc_commit(zbp::smem_u32(&ctl->tfull[buf]));
+                if (PAIR)
+                    zbp::tc_commit_pair_multicast(zbp::smem_u32(&ctl->tfull[buf]), 0x3);
+                else
+                    zbp::tc_commit(zbp::smem_u32(&ctl->tfull[buf]));
             }
             // every MMA issued here completes before TMEM is released
-            zbp::tc_commit(zbp::smem_u32(&ctl->drain));
-            wait_bar(zbp::smem_u32(&ctl->drain), 0, abort_flag, args.err, ERR_WAIT_MMA,
-                     DRAIN_LIMIT_NS, false);
+            if (PAIR)
+                zbp::tc_commit_pair(zbp::smem_u32(&ctl->drain));
+            else
+                zbp::tc_commit(zbp::smem_u32(&ctl->drain));
+            wait_bar<PAIR>(zbp::smem_u32(&ctl->drain), 0, abort_flag, args.err, ERR_WAIT_MMA,
+                           DRAIN_LIMIT_NS, false);
         }
     } else {
         // ---------------------------------------------------- epilogue
         // Warp w may read TMEM lanes 32*(w%4) .. +31: rows q*32 .. q*32+31 of
-        // the tile, one row per thread.  Results leave through two 4-KiB
-        // swizzled staging boxes per warp (32 rows x 128 bytes) and TMA
+        // this CTA's 128 rows, one row per thread.  Results leave through two
+        // 4-KiB swizzled staging boxes per warp (32 rows x 128 bytes) and TMA
         // stores; the fp32 weight gradient is accumulated with a TMA
         // reduce-add, so the old values are never read by the SM.
         const int q = warp & 3;
         const uint32_t stg0 = zbp::smem_u32(staging + (warp - 2) * 2 * STAGING_BOX);
         uint32_t flip = 0;
         uint32_t local = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+        for (int tile = cluster; tile < num_tiles; tile += clusters, ++local) {
             const uint32_t buf = local & 1u;
             const uint32_t tr = local >> 1;
             int mb, nb;
-            tile_coords(tile, tiles_m, tiles_n, mb, nb);
-            const int m0 = mb * BM;
+            tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
+            const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
             const int n0 = nb * BN;
             const int row0 = m0 + q * 32;
             const int row = row0 + lane;
@@ -352,8 +414,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 zbp::prefetch_l2(args.aux + static_cast<long long>(row) * args.ldaux + n0,
                                  static_cast<uint32_t>(ncols) * 2u);
             }
-            if (!wait_bar(zbp::smem_u32(&ctl->tfull[buf]), tr & 1u, abort_flag, args.err,
-                          ERR_WAIT_EPI, WAIT_LIMIT_NS, true))
+            if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->tfull[buf]), tr & 1u, abort_flag, args.err,
+                                ERR_WAIT_EPI, WAIT_LIMIT_NS, true))
                 break;
             zbp::tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
@@ -441,7 +503,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             zbp::tc_fence_before();
             __syncwarp();
-            if (lane == 0) zbp::mbar_arrive(zbp::smem_u32(&ctl->tempty[buf]));
+            if (lane == 0) {
+                const uint32_t te = zbp::smem_u32(&ctl->tempty[buf]);
+                if (PAIR)
+                    zbp::mbar_arrive_cluster(zbp::mapa_shared(te, 0));
+                else
+                    zbp::mbar_arrive(te);
+            }
         }
         // the staging buffers must not be released while a bulk store reads them
         if (lane == 0) zbp::bulk_wait<0>();
@@ -449,9 +517,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     __syncthreads();
+    if (PAIR) zbp::cluster_sync();  // no remote arrivals or copies remain
     if (warp == 1) {
         zbp::tc_fence_after();
-        zbp::tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR)
+            zbp::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            zbp::tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -514,35 +586,109 @@ int sm_count() {
     return cache[dev];
 }
 
-template <int EPI, int A_MN, int B_MN>
-zb_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to0,
-                 const CUtensorMap& to1, const EpiArgs& ea, int grid, cudaStream_t st) {
-    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN>;
-    static int configured[64] = {0};
+struct Maps {
+    CUtensorMap a, b, o0, o1;
+};
+
+// Persistent grid size in CTAs for a CTA-group shape (co-resident clusters x CG).
+template <int EPI, int A_MN, int B_MN, int CG>
+zb_status configure(int* max_ctas) {
+    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG>;
+    static int cached[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    if (dev < 0 || dev >= 64) return zb::fail(ZB_ERR_CUDA, "device ordinal out of range");
+    if (!cached[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(SMEM_BYTES));
+                                             static_cast<int>(smem_bytes<CG>()));
         if (e != cudaSuccess)
             return zb::fail(ZB_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-        configured[dev] = 1;
+        int n = sm_count();
+        if (CG == 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * 256, 1, 1);
+            cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+            cfg.dynamicSmemBytes = smem_bytes<CG>();
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 2;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+            if (e != cudaSuccess || clusters <= 0)
+                return zb::fail(ZB_ERR_UNSUPPORTED, std::string("no co-resident CTA pairs: ") +
+                                                        cudaGetErrorString(e));
+            n = 2 * clusters;
+        }
+        cached[dev] = n;
     }
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, to0, to1, ea);
-    cudaError_t e = cudaGetLastError();
+    *max_ctas = cached[dev];
+    return ZB_OK;
+}
+
+template <int EPI, int A_MN, int B_MN, int CG>
+zb_status launch(const Maps& mp, const EpiArgs& ea, long long tiles, cudaStream_t st) {
+    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG>;
+    int max_ctas = 0;
+    zb_status s = configure<EPI, A_MN, B_MN, CG>(&max_ctas);
+    if (s != ZB_OK) return s;
+    const long long want = tiles * CG;
+    const int grid = static_cast<int>(want < max_ctas ? want : max_ctas);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<CG>();
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = CG;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = CG == 2 ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.o0, mp.o1, ea);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess)
         return zb::fail(ZB_ERR_CUDA, std::string("tensor-core GEMM launch: ") + cudaGetErrorString(e));
     return ZB_OK;
 }
 
-template <int EPI>
-zb_status dispatch_major(int a_mn, int b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                         const CUtensorMap& to0, const CUtensorMap& to1, const EpiArgs& ea,
-                         int grid, cudaStream_t st) {
-    if (!a_mn && !b_mn) return launch<EPI, 0, 0>(ta, tb, to0, to1, ea, grid, st);
-    if (!a_mn && b_mn) return launch<EPI, 0, 1>(ta, tb, to0, to1, ea, grid, st);
-    if (a_mn && !b_mn) return launch<EPI, 1, 0>(ta, tb, to0, to1, ea, grid, st);
-    return launch<EPI, 1, 1>(ta, tb, to0, to1, ea, grid, st);
+template <int EPI, int CG>
+zb_status dispatch_major(int a_mn, int b_mn, const Maps& mp, const EpiArgs& ea, long long tiles,
+                         cudaStream_t st) {
+    if (!a_mn && !b_mn) return launch<EPI, 0, 0, CG>(mp, ea, tiles, st);
+    if (!a_mn && b_mn) return launch<EPI, 0, 1, CG>(mp, ea, tiles, st);
+    if (a_mn && !b_mn) return launch<EPI, 1, 0, CG>(mp, ea, tiles, st);
+    return launch<EPI, 1, 1, CG>(mp, ea, tiles, st);
+}
+
+template <int CG>
+zb_status dispatch(const zb::GemmBf16& g, const Maps& mp, const EpiArgs& ea, long long tiles,
+                   cudaStream_t st) {
+    switch (g.epi) {
+        case zb::EPI_STORE_BF16: return dispatch_major<zb::EPI_STORE_BF16, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st);
+        case zb::EPI_GELU_DUAL: return dispatch_major<zb::EPI_GELU_DUAL, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st);
+        case zb::EPI_GELU_BWD: return dispatch_major<zb::EPI_GELU_BWD, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st);
+        case zb::EPI_F32: return dispatch_major<zb::EPI_F32, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st);
+        default: return zb::fail(ZB_ERR_INVALID_ARG, "unknown epilogue");
+    }
+}
+
+// CTA-group choice: the pair kernel when its 256x256 tiles fill at least one
+// wave of pairs, else one CTA per 128x256 tile (more CTAs for small problems).
+// ZB_GEMM_CTA_GROUP=1 or =2 in the environment forces one shape.
+int choose_cta_group(long long pair_tiles) {
+    static int forced = -1;
+    if (forced < 0) {
+        const char* v = std::getenv("ZB_GEMM_CTA_GROUP");
+        forced = (v && (std::strcmp(v, "1") == 0 || std::strcmp(v, "2") == 0)) ? std::atoi(v) : 0;
+    }
+    if (forced) return forced;
+    const int pairs = sm_count() / 2;
+    return pair_tiles >= pairs ? 2 : 1;
 }
 
 }  // namespace
@@ -562,29 +708,34 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     if (!g.A || !g.B || !g.out0) return fail(ZB_ERR_INVALID_ARG, "GEMM operand is NULL");
     if (g.epi == EPI_GELU_DUAL && !g.out1) return fail(ZB_ERR_INVALID_ARG, "GeLU dual store needs out1");
     if (g.epi == EPI_GELU_BWD && !g.aux) return fail(ZB_ERR_INVALID_ARG, "GeLU' epilogue needs H");
+    if (sm_count() <= 0) return fail(ZB_ERR_CUDA, "cannot query the SM count");
+
+    const long long pair_tiles = ((g.Mg + 2 * BM - 1) / (2 * BM)) * ((g.Ng + BN - 1) / BN);
+    const int cg = choose_cta_group(pair_tiles);
+    const uint32_t b_rows = static_cast<uint32_t>(BN / cg);  // B columns per CTA
 
     std::string why;
-    CUtensorMap ta, tb, to0, to1;
+    Maps mp;
     bool ok;
     if (g.a_mn)
-        ok = make_map(&ta, g.A, false, g.Mg, g.Kg, g.lda, 64, BK, &why);
+        ok = make_map(&mp.a, g.A, false, g.Mg, g.Kg, g.lda, 64, BK, &why);
     else
-        ok = make_map(&ta, g.A, false, g.Kg, g.Mg, g.lda, BK, BM, &why);
+        ok = make_map(&mp.a, g.A, false, g.Kg, g.Mg, g.lda, BK, BM, &why);
     if (ok) {
         if (g.b_mn)
-            ok = make_map(&tb, g.B, false, g.Ng, g.Kg, g.ldb, 64, BK, &why);
+            ok = make_map(&mp.b, g.B, false, g.Ng, g.Kg, g.ldb, 64, BK, &why);
         else
-            ok = make_map(&tb, g.B, false, g.Kg, g.Ng, g.ldb, BK, BN, &why);
+            ok = make_map(&mp.b, g.B, false, g.Kg, g.Ng, g.ldb, BK, b_rows, &why);
     }
     // epilogue boxes: 32 rows x 128 bytes (32 fp32 or 64 bf16 columns)
     const bool f32_out = g.epi == EPI_F32;
     const uint32_t ocols = f32_out ? 32 : 64;
-    if (ok) ok = make_map(&to0, g.out0, f32_out, g.Ng, g.Mg, g.ld0, ocols, 32, &why);
+    if (ok) ok = make_map(&mp.o0, g.out0, f32_out, g.Ng, g.Mg, g.ld0, ocols, 32, &why);
     if (ok) {
         if (g.epi == EPI_GELU_DUAL)
-            ok = make_map(&to1, g.out1, false, g.Ng, g.Mg, g.ld1, ocols, 32, &why);
+            ok = make_map(&mp.o1, g.out1, false, g.Ng, g.Mg, g.ld1, ocols, 32, &why);
         else
-            to1 = to0;
+            mp.o1 = mp.o0;
     }
     if (!ok) return fail(ZB_ERR_CUDA, why);
     if (f32_out && (g.ld0 % 4)) return fail(ZB_ERR_ALIGN, "fp32 output leading dimension must be a multiple of 4");
@@ -607,18 +758,10 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     ea.act = g.act;
     ea.err = err;
 
-    const long long tiles = ((g.Mg + BM - 1) / BM) * ((g.Ng + BN - 1) / BN);
-    const int sms = sm_count();
-    if (sms <= 0) return fail(ZB_ERR_CUDA, "cannot query the SM count");
-    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    switch (g.epi) {
-        case EPI_STORE_BF16: return dispatch_major<EPI_STORE_BF16>(g.a_mn, g.b_mn, ta, tb, to0, to1, ea, grid, st);
-        case EPI_GELU_DUAL: return dispatch_major<EPI_GELU_DUAL>(g.a_mn, g.b_mn, ta, tb, to0, to1, ea, grid, st);
-        case EPI_GELU_BWD: return dispatch_major<EPI_GELU_BWD>(g.a_mn, g.b_mn, ta, tb, to0, to1, ea, grid, st);
-        case EPI_F32: return dispatch_major<EPI_F32>(g.a_mn, g.b_mn, ta, tb, to0, to1, ea, grid, st);
-        default: return fail(ZB_ERR_INVALID_ARG, "unknown epilogue");
-    }
+    if (cg == 2) return dispatch<2>(g, mp, ea, pair_tiles, st);
+    const long long tiles = ((g.Mg + BM - 1) / BM) * ((g.Ng + BN - 1) / BN);
+    return dispatch<1>(g, mp, ea, tiles, st);
 }
 
 }  // namespace zb
