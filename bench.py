@@ -11,6 +11,7 @@ ZB-H2 ordering (all W deferred into the warm-up/cool-down slots).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload c4|c3|c2]
+  python bench.py --sweep [--sweep-points 512x1024,...] [--sweep-m 32]
 
 N > 1 runs N independent replicas (one per GPU, launched by torchrun): the
 path has no exchange between GPUs, so "value" sums the replicas' work over
@@ -214,6 +215,91 @@ def run_reference(args, wl):
     return 0
 
 
+def pass_bytes(M, h, f):
+    """Compulsory HBM bytes of one pass (each tensor read or written once;
+    bf16 activations and weights, fp32 weight gradients read and written)."""
+    F = 2 * (M * h + h * f + 2 * M * f) + 2 * (M * f + f * h + M * h)
+    B = 2 * (M * h + f * h + M * f + M * f) + 2 * (M * f + h * f + M * h)
+    W = 2 * (M * f + M * h) + 8 * f * h + 2 * (M * h + M * f) + 8 * h * f
+    return {"F": F, "B": B, "W": W}
+
+
+def run_sweep(args):
+    """Per-pass kernel sweep: F, B and W standalone at each (M, h), f = 4h,
+    W accumulating over m microbatches (4 distinct input sets, cycled)."""
+    import torch
+
+    from split_backward_gemms_gb300 import build as B
+    B.build()
+    from split_backward_gemms_gb300 import zb
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks = _peaks()
+    stream = torch.cuda.current_stream()
+    if args.sweep_points:
+        points = [tuple(int(v) for v in p.split("x")) for p in args.sweep_points.split(",")]
+    else:
+        points = [(M, h) for M in (512, 2048, 8192, 16384) for h in (1024, 2048, 4096, 8192)]
+    m, sets = args.sweep_m, 4
+    for M, h in points:
+        f = 4 * h
+        gen = torch.Generator(device=dev).manual_seed(M * 31 + h)
+        bf = torch.bfloat16
+        W1 = (torch.randn(h, f, device=dev, generator=gen) * 0.02).to(bf)
+        W2 = (torch.randn(f, h, device=dev, generator=gen) * 0.02).to(bf)
+        dW1 = torch.zeros(h, f, device=dev)
+        dW2 = torch.zeros(f, h, device=dev)
+        blk = zb.make_block(M, h, f)
+        S = []
+        for _ in range(sets):
+            t = {"X": torch.randn(M, h, device=dev, generator=gen).to(bf),
+                 "dY": torch.randn(M, h, device=dev, generator=gen).to(bf),
+                 "H": torch.empty(M, f, device=dev, dtype=bf), "A": torch.empty(M, f, device=dev, dtype=bf),
+                 "Y": torch.empty(M, h, device=dev, dtype=bf), "dH": torch.empty(M, f, device=dev, dtype=bf),
+                 "dX": torch.empty(M, h, device=dev, dtype=bf)}
+            zb.zb_forward(blk, t["X"], W1, W2, None, None, t["H"], t["A"], t["Y"], stream)
+            zb.zb_backward_input(blk, t["dY"], W1, W2, t["H"], t["dH"], t["dX"], stream)
+            S.append(t)
+        passes = {
+            "F": lambda t, j: zb.zb_forward(blk, t["X"], W1, W2, None, None, t["H"], t["A"], t["Y"], stream),
+            "B": lambda t, j: zb.zb_backward_input(blk, t["dY"], W1, W2, t["H"], t["dH"], t["dX"], stream),
+            "W": lambda t, j: zb.zb_backward_weight(blk, t["X"], t["A"], t["dH"], t["dY"], dW1, dW2,
+                                                    None, None, j > 0, stream),
+        }
+        pb = pass_bytes(M, h, f)
+        for name, fn in passes.items():
+            for j in range(3):
+                fn(S[j % sets], j)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for j in range(m):
+                fn(S[j % sets], j)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / m
+            flops = 4.0 * M * h * f
+            t_flop = flops / (peaks["bf16"] * 1e12)
+            t_byte = pb[name] / (peaks["hbm"] * 1e9)
+            bound = "tensor" if t_flop >= t_byte else "hbm"
+            print(json.dumps({
+                "sweep": True, "pass": name, "M": M, "h": h, "f": f, "microbatches": m,
+                "us_per_pass": 1e3 * ms, "tflops": flops / (ms / 1e3) / 1e12,
+                "gb_per_s": pb[name] / (ms / 1e3) / 1e9,
+                "roofline": {"bound": bound, "time_us": 1e6 * max(t_flop, t_byte),
+                             "frac": max(t_flop, t_byte) / (ms / 1e3),
+                             "peak": peaks["bf16"] if bound == "tensor" else peaks["hbm"],
+                             "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                             "peak_kind": "burst (%s)" % peaks["source"]},
+            }), flush=True)
+        zb.zb_sync_status(stream)
+        del S, W1, W2, dW1, dW2
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -221,13 +307,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="c4")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-pass kernel sweep (one JSON line per pass and point)")
+    ap.add_argument("--sweep-points", default="",
+                    help="comma list of MxH points, e.g. 3072x6144 (default: the M x h grid)")
+    ap.add_argument("--sweep-m", type=int, default=32, help="microbatches timed per pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args, args.workload)
+    if args.sweep:
+        return run_sweep(args)
 
     import torch
     import torch.distributed as dist
@@ -322,38 +415,84 @@ def main():
     roof_peak = peaks["bf16_sustained"]
     traffic = _profiled_traffic(args.workload)
 
+    # ----------------------------------------------- projected P-stage pipeline
+    # per-pass times measured above (executor CUDA events), fed to the
+    # library's simulator of the orderings: a projection, not a measurement
+    tfb = [sums["kind"][i] / (m * P * args.steps) for i in range(3)]
+    projection = None
+    if all(t > 0 for t in tfb):
+        projection = {"label": "simulated %d-stage pipeline from the measured per-pass times" % Pl,
+                      "P": Pl, "m": m, "T_F_ms": tfb[0], "T_B_ms": tfb[1], "T_W_ms": tfb[2],
+                      "T_comm_ms": 0.0, "bubble_rate": {}, "pipeline_tokens_per_s": {}}
+        for kind in ("1F1B", "ZBH1", "ZBH2"):
+            res, _ = zb.zb_simulate_schedule(kind, Pl, m, tfb[0], tfb[1], tfb[2], 0.0)
+            projection["bubble_rate"][kind] = res.bubble_rate
+            projection["pipeline_tokens_per_s"][kind] = m * M / (res.cost / 1e3)
+
     # ------------------------------------------------------------- end to end
+    # Through the public API with host buffers: every step uploads its inputs
+    # from pinned host memory and downloads its weight gradients.  Two input
+    # and gradient sets alternate so that step k+1's upload and step k's
+    # download run on a copy stream while the other step computes.
     pin = [x.cpu().pin_memory() for x in X0]
     pin_g = [g.cpu().pin_memory() for g in dY]
     host_dW = [(torch.empty(h, f, pin_memory=True), torch.empty(f, h, pin_memory=True))
                for _ in range(P)]
     h2d = sum(x.numel() * x.element_size() for x in pin + pin_g)
     d2h = sum(a.numel() * 4 + b.numel() * 4 for a, b in host_dW)
-
-    def e2e_step():
-        for j in range(m):
-            X0[j].copy_(pin[j], non_blocking=True)
-            dY[j].copy_(pin_g[j], non_blocking=True)
-        step(None)
-        for s in range(P):
-            host_dW[s][0].copy_(W[s]["dW1"], non_blocking=True)
-            host_dW[s][1].copy_(W[s]["dW2"], non_blocking=True)
-
+    sets = [(X0, dY, W)]
+    X0b = [torch.empty_like(x) for x in X0]
+    dYb = [torch.empty_like(g) for g in dY]
+    Wb = [dict(w, dW1=torch.empty_like(w["dW1"]), dW2=torch.empty_like(w["dW2"])) for w in W]
+    sets.append((X0b, dYb, Wb))
+    up_stream = torch.cuda.Stream(device=dev)
+    down_stream = torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    down_done = [torch.cuda.Event(), torch.cuda.Event()]
     pl.timing = 0
-    e2e_step()
-    torch.cuda.synchronize()
+
+    def upload(a):
+        # set a's inputs were last read by the step two back (done[a])
+        up_stream.wait_event(done[a])
+        with torch.cuda.stream(up_stream):
+            for j in range(m):
+                sets[a][0][j].copy_(pin[j], non_blocking=True)
+                sets[a][1][j].copy_(pin_g[j], non_blocking=True)
+            in_ready[a].record(up_stream)
+
+    def e2e_run(steps):
+        for ev in done + down_done:
+            ev.record(stream)
+        upload(0)
+        for k in range(steps):
+            a = k % 2
+            if k + 1 < steps:
+                upload(1 - a)  # overlaps this step's compute
+            stream.wait_event(in_ready[a])
+            stream.wait_event(down_done[a])  # set a's gradients were downloaded
+            Xs, Gs, Ws = sets[a]
+            zb.zb_run_stage_schedule(pl, Ws, Xs, Gs, None, None, ops_c, ws_t, ws_t.numel(), None, stream)
+            done[a].record(stream)
+            down_stream.wait_event(done[a])
+            with torch.cuda.stream(down_stream):
+                for s_ in range(P):
+                    host_dW[s_][0].copy_(Ws[s_]["dW1"], non_blocking=True)
+                    host_dW[s_][1].copy_(Ws[s_]["dW2"], non_blocking=True)
+                down_done[a].record(down_stream)
+        torch.cuda.synchronize()
+
+    e2e_run(2)
     if ws > 1:
         dist.barrier()
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    t = torch.tensor([e2e_ms], device=dev)
+    t0 = time.perf_counter()
+    e2e_run(args.e2e_steps)
+    e2e_s = time.perf_counter() - t0
+    t = torch.tensor([e2e_s], device=dev)
     if ws > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_value = step_flops * args.e2e_steps * ws / (float(t.item()) / 1e3) / 1e12
+    e2e_value = step_flops * args.e2e_steps * ws / float(t.item()) / 1e12
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -385,7 +524,10 @@ def main():
                          "frac_of_burst": achieved / peaks["bf16"]},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                    "timing": "host wall clock around synchronised steps; uploads and downloads "
+                              "double-buffered on their own streams"},
+            "projection": projection,
             "gpu_launches": sums["gemm_launches"],
             "clocks": clk,
         }

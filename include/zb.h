@@ -141,6 +141,28 @@ typedef enum zb_schedule_kind { ZB_SCHED_1F1B = 0, ZB_SCHED_ZBH1 = 1, ZB_SCHED_Z
  * if too small).  Host only, no device work. */
 zb_status zb_make_schedule(int32_t kind, int32_t P, int32_t m, zb_op* out, size_t* n_ops);
 
+/* Pass times for zb_simulate_schedule (any one unit, e.g. ms). */
+typedef struct zb_sim_times { double t_f, t_b, t_w, t_comm; } zb_sim_times;
+
+typedef struct zb_sim_result {
+    double cost;                     /* max over stages of (end of last pass -
+                                        start of first pass), summary Eq. 3     */
+    double ideal;                    /* m (T_F + T_B + T_W)                     */
+    double bubble_rate;              /* (cost - ideal) / cost, summary §5       */
+    uint32_t peak_live_microbatches; /* max over stages: F done, W not done     */
+    uint32_t peak_live_stage0;       /* the same on stage 0                     */
+} zb_sim_result;
+
+/* Simulate an ordering for P stages, m microbatches and the given pass times
+ * with the same rules as zb_make_schedule (T_comm is added to every
+ * cross-stage dependency, summary Eqs. 4-5): the projected bubble of a
+ * P-GPU pipeline from measured per-pass times.  `out`/`n_ops` may be NULL;
+ * when given they receive the op list ordered by simulated start as in
+ * zb_make_schedule.  Host only.  ZB_ERR_INVALID_ARG for non-positive or
+ * non-finite pass times (T_comm may be 0). */
+zb_status zb_simulate_schedule(int32_t kind, int32_t P, int32_t m, const zb_sim_times* times,
+                               zb_op* out, size_t* n_ops, zb_sim_result* result);
+
 typedef struct zb_pipeline {
     int32_t P;                 /* stages                                     */
     int32_t m;                 /* microbatches                               */
@@ -231,6 +253,13 @@ zb_status zb_run_stage_schedule_static(const zb_pipeline* pl, const zb_stage_par
  * current device: ZB_ERR_TIMEOUT if a bounded device wait gave up,
  * ZB_ERR_CUDA if the stream reported an error, else ZB_OK. */
 zb_status zb_sync_status(void* stream);
+
+/* Self-test of the device-side timeout path: launches one thread that waits
+ * on an mbarrier nothing will ever arrive on, bounded by limit_ns (clamped to
+ * [1 ms, 2 s]); when the bound expires it sets the device error word and
+ * returns.  The next zb_sync_status() then reports ZB_ERR_TIMEOUT (and clears
+ * the word); the context stays usable.  Nothing faults, traps or hangs. */
+zb_status zb_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
 /* Message of the last failing call on this thread ("" if none). */
 const char* zb_last_error(void);

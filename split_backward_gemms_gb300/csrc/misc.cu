@@ -6,6 +6,7 @@
 
 #include <mutex>
 
+#include "ptx.cuh"
 #include "zb_internal.h"
 
 namespace {
@@ -93,6 +94,22 @@ __global__ void zb_colsum_kernel(const T* __restrict__ X, long long rows, long l
     db[c] = accumulate ? db[c] + acc : acc;
 }
 
+// One thread waits on an mbarrier that nothing arrives on, for at most
+// limit_ns, then records the expiry in the error word (bit 31).
+__global__ void zb_selftest_wait_kernel(unsigned int* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = zbp::smem_u32(&bar);
+    zbp::mbar_init(b, 1);
+    zbp::fence_mbar_init();
+    const uint64_t t0 = zbp::globaltimer_ns();
+    while (!zbp::mbar_try_wait(b, 0)) {
+        if (zbp::globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(err, 1u << 31);
+            return;
+        }
+    }
+}
+
 }  // namespace
 
 namespace zb {
@@ -166,6 +183,18 @@ extern "C" zb_status zb_sync_status(void* stream) {
         cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
         return zb::fail(ZB_ERR_TIMEOUT, "a bounded device wait gave up (error word " + std::to_string(v) + ")");
     }
+    zb::clear_error();
+    return ZB_OK;
+}
+
+extern "C" zb_status zb_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+    unsigned int* w = zb::device_error_word();
+    if (!w) return ZB_ERR_CUDA;
+    if (limit_ns < 1000000ull) limit_ns = 1000000ull;
+    if (limit_ns > 2000000000ull) limit_ns = 2000000000ull;
+    zb_selftest_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(w, limit_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return zb::fail(ZB_ERR_CUDA, std::string("self-test launch: ") + cudaGetErrorString(e));
     zb::clear_error();
     return ZB_OK;
 }

@@ -12,6 +12,7 @@
 // bubble": per-stage instruction sequences with gradient-buffer lifetime
 // management.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <deque>
 #include <set>
@@ -24,7 +25,7 @@ namespace {
 
 struct SimEvent {
     int kind, stage, micro;
-    long long start, end;
+    double start, end;
 };
 
 int warmup_count(int kind, int P, int m, int s) {
@@ -53,26 +54,39 @@ std::vector<std::pair<int, int>> fb_order(int kind, int P, int m, int s) {
     return q;
 }
 
-long long op_len(int kind) { return kind == ZB_OP_BW ? 2 : 1; }
+struct PassTimes {
+    double f = 1.0, b = 1.0, w = 1.0, comm = 0.0;
+    double len(int kind) const {
+        if (kind == ZB_OP_F) return f;
+        if (kind == ZB_OP_B) return b;
+        if (kind == ZB_OP_W) return w;
+        return b + w;  // fused BW
+    }
+};
 
-bool simulate(int kind, int P, int m, std::vector<SimEvent>* out) {
+// List-scheduling simulation of one ordering: every stage runs its next F/B
+// as soon as its producers have ended (plus T_comm across stages), else its
+// oldest pending W; a W is forced before an F when the stage's live
+// microbatches reach the ordering's cap.  Decisions are taken in time order,
+// so each one sees every pass that ends by then.
+bool simulate(int kind, int P, int m, const PassTimes& T, std::vector<SimEvent>* out) {
     const int live_cap = kind == ZB_SCHED_ZBH1 ? P : (kind == ZB_SCHED_ZBH2 ? 2 * P - 1 : 0);
     struct St {
         std::vector<std::pair<int, int>> seq;
         size_t pos = 0;
         std::deque<int> wq;
         int live = 0;
-        long long tfree = 0;
+        double tfree = 0.0;
         bool parked = false;
     };
     std::vector<St> st(P);
     for (int s = 0; s < P; ++s) st[s].seq = fb_order(kind, P, m, s);
     // end times (or -1): fwd_end[s*m+j]; bwd_end = end of B or BW
-    std::vector<long long> fwd_end(static_cast<size_t>(P) * m, -1), bwd_end(static_cast<size_t>(P) * m, -1);
-    std::vector<long long> all_ends;
+    std::vector<double> fwd_end(static_cast<size_t>(P) * m, -1.0), bwd_end(static_cast<size_t>(P) * m, -1.0);
+    std::vector<double> all_ends;
     auto busy = [&](int s) { return st[s].pos < st[s].seq.size() || !st[s].wq.empty(); };
-    auto emit = [&](int s, int k, int j, long long t0) {
-        const long long t1 = t0 + op_len(k);
+    auto emit = [&](int s, int k, int j, double t0) {
+        const double t1 = t0 + T.len(k);
         out->push_back({k, s, j, t0, t1});
         all_ends.push_back(t1);
         st[s].tfree = t1;
@@ -90,21 +104,23 @@ bool simulate(int kind, int P, int m, std::vector<SimEvent>* out) {
         }
     };
     // earliest start of (k, s, j) given its producers, -1 if one is unscheduled
-    auto ready_time = [&](int s, int k, int j) -> long long {
-        long long t = 0;
+    auto ready_time = [&](int s, int k, int j) -> double {
+        double t = 0.0;
         if (k == ZB_OP_F) {
             if (s > 0) {
-                t = fwd_end[static_cast<size_t>(s - 1) * m + j];
-                if (t < 0) return -1;
+                const double e = fwd_end[static_cast<size_t>(s - 1) * m + j];
+                if (e < 0) return -1.0;
+                t = e + T.comm;
             }
             return t;
         }
-        t = fwd_end[static_cast<size_t>(s) * m + j];
-        if (t < 0) return -1;
+        const double e = fwd_end[static_cast<size_t>(s) * m + j];
+        if (e < 0) return -1.0;
+        t = e;
         if (s + 1 < P) {
-            const long long u = bwd_end[static_cast<size_t>(s + 1) * m + j];
-            if (u < 0) return -1;
-            t = std::max(t, u);
+            const double u = bwd_end[static_cast<size_t>(s + 1) * m + j];
+            if (u < 0) return -1.0;
+            t = std::max(t, u + T.comm);
         }
         return t;
     };
@@ -121,9 +137,9 @@ bool simulate(int kind, int P, int m, std::vector<SimEvent>* out) {
             return false;  // every stage with work is parked: cannot happen for legal orders
         }
         St& S = st[pick];
-        const long long now = S.tfree;
+        const double now = S.tfree;
         const bool have_fb = S.pos < S.seq.size();
-        long long ready = -1;
+        double ready = -1.0;
         if (have_fb) ready = ready_time(pick, S.seq[S.pos].first, S.seq[S.pos].second);
         bool ran = true;
         if (have_fb && ready >= 0 && ready <= now) {
@@ -146,8 +162,8 @@ bool simulate(int kind, int P, int m, std::vector<SimEvent>* out) {
             if (ready >= 0) {
                 S.tfree = ready;
             } else {
-                long long nxt = -1;
-                for (long long e : all_ends)
+                double nxt = -1.0;
+                for (double e : all_ends)
                     if (e > now && (nxt < 0 || e < nxt)) nxt = e;
                 for (int o = 0; o < P; ++o)
                     if (o != pick && busy(o) && st[o].tfree > now && (nxt < 0 || st[o].tfree < nxt))
@@ -160,6 +176,23 @@ bool simulate(int kind, int P, int m, std::vector<SimEvent>* out) {
             for (auto& x : st) x.parked = false;
     }
     return true;
+}
+
+// Ordered op list (start time, then stage; OPT after each stage's last op).
+size_t emit_ops(std::vector<SimEvent>& ev, int P, zb_op* out) {
+    std::stable_sort(ev.begin(), ev.end(), [](const SimEvent& a, const SimEvent& b) {
+        return a.start != b.start ? a.start < b.start : a.stage < b.stage;
+    });
+    std::vector<size_t> last(P, 0);
+    for (size_t i = 0; i < ev.size(); ++i) last[ev[i].stage] = i;
+    size_t w = 0;
+    for (size_t i = 0; i < ev.size(); ++i) {
+        out[w++] = zb_op{static_cast<uint8_t>(ev[i].kind), 0, static_cast<uint16_t>(ev[i].stage),
+                         static_cast<uint32_t>(ev[i].micro)};
+        for (int s = 0; s < P; ++s)
+            if (last[s] == i) out[w++] = zb_op{ZB_OP_OPT, 0, static_cast<uint16_t>(s), 0};
+    }
+    return w;
 }
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
@@ -338,40 +371,89 @@ zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has
 
 }  // namespace zb
 
-extern "C" zb_status zb_make_schedule(int32_t kind, int32_t P, int32_t m, zb_op* out, size_t* n_ops) {
+namespace {
+
+zb_status check_sched_args(int32_t kind, int32_t P, int32_t m, size_t* n_ops, size_t* total) {
     if (!n_ops) return zb::fail(ZB_ERR_INVALID_ARG, "n_ops is NULL");
     if (kind < ZB_SCHED_1F1B || kind > ZB_SCHED_ZBH2) return zb::fail(ZB_ERR_INVALID_ARG, "unknown schedule kind");
-    if (P < 1 || m < 1 || P > 65535 || static_cast<long long>(P) * m > (1LL << 24))
-        return zb::fail(ZB_ERR_SHAPE, "P and m must be >= 1 (P <= 65535, P*m <= 2^24)");
+    if (P < 1 || m < 1 || P > 65535 || static_cast<long long>(P) * m > (1LL << 20))
+        return zb::fail(ZB_ERR_SHAPE, "P and m must be >= 1 (P <= 65535, P*m <= 2^20)");
     const size_t per = kind == ZB_SCHED_1F1B ? 2 : 3;
-    const size_t total = static_cast<size_t>(P) * m * per + P;
-    if (!out) {
+    *total = static_cast<size_t>(P) * m * per + P;
+    return ZB_OK;
+}
+
+zb_status run_schedule(int32_t kind, int32_t P, int32_t m, const PassTimes& T, zb_op* out, size_t* n_ops,
+                       zb_sim_result* res) {
+    size_t total = 0;
+    zb_status s = check_sched_args(kind, P, m, n_ops, &total);
+    if (s != ZB_OK) return s;
+    if (out && *n_ops < total) {
+        *n_ops = total;
+        return zb::fail(ZB_ERR_INVALID_ARG, "output capacity too small");
+    }
+    if (!out && !res) {
         *n_ops = total;
         zb::clear_error();
         return ZB_OK;
     }
-    if (*n_ops < total) {
-        *n_ops = total;
-        return zb::fail(ZB_ERR_INVALID_ARG, "output capacity too small");
-    }
     std::vector<SimEvent> ev;
     ev.reserve(total);
-    if (!simulate(kind, P, m, &ev)) return zb::fail(ZB_ERR_SCHEDULE, "schedule simulation deadlocked");
-    std::stable_sort(ev.begin(), ev.end(), [](const SimEvent& a, const SimEvent& b) {
-        return a.start != b.start ? a.start < b.start : a.stage < b.stage;
-    });
-    std::vector<size_t> last(P, 0);
-    for (size_t i = 0; i < ev.size(); ++i) last[ev[i].stage] = i;
-    size_t w = 0;
-    for (size_t i = 0; i < ev.size(); ++i) {
-        out[w++] = zb_op{static_cast<uint8_t>(ev[i].kind), 0, static_cast<uint16_t>(ev[i].stage),
-                         static_cast<uint32_t>(ev[i].micro)};
-        for (int s = 0; s < P; ++s)
-            if (last[s] == i) out[w++] = zb_op{ZB_OP_OPT, 0, static_cast<uint16_t>(s), 0};
+    if (!simulate(kind, P, m, T, &ev)) return zb::fail(ZB_ERR_SCHEDULE, "schedule simulation deadlocked");
+    if (res) {
+        // Eq. 3: per-stage span = end of last pass - start of first pass
+        std::vector<double> first(P, -1.0), lastv(P, 0.0);
+        std::vector<int> live(P, 0), peak(P, 0);
+        std::vector<SimEvent> sorted = ev;
+        std::stable_sort(sorted.begin(), sorted.end(), [](const SimEvent& a, const SimEvent& b) {
+            return a.start < b.start;
+        });
+        for (const SimEvent& e : sorted) {
+            if (first[e.stage] < 0 || e.start < first[e.stage]) first[e.stage] = e.start;
+            lastv[e.stage] = std::max(lastv[e.stage], e.end);
+            if (e.kind == ZB_OP_F) peak[e.stage] = std::max(peak[e.stage], ++live[e.stage]);
+            else if (e.kind == ZB_OP_W || e.kind == ZB_OP_BW) --live[e.stage];
+        }
+        double cost = 0.0;
+        int pk = 0;
+        for (int st = 0; st < P; ++st) {
+            cost = std::max(cost, lastv[st] - first[st]);
+            pk = std::max(pk, peak[st]);
+        }
+        res->cost = cost;
+        res->ideal = m * (T.f + T.b + T.w);
+        res->bubble_rate = cost > 0 ? (cost - res->ideal) / cost : 0.0;
+        res->peak_live_microbatches = static_cast<uint32_t>(pk);
+        res->peak_live_stage0 = static_cast<uint32_t>(peak[0]);
     }
-    *n_ops = w;
+    if (out) {
+        *n_ops = emit_ops(ev, P, out);
+    } else {
+        *n_ops = total;
+    }
     zb::clear_error();
     return ZB_OK;
+}
+
+}  // namespace
+
+extern "C" zb_status zb_make_schedule(int32_t kind, int32_t P, int32_t m, zb_op* out, size_t* n_ops) {
+    return run_schedule(kind, P, m, PassTimes(), out, n_ops, nullptr);
+}
+
+extern "C" zb_status zb_simulate_schedule(int32_t kind, int32_t P, int32_t m, const zb_sim_times* times,
+                                          zb_op* out, size_t* n_ops, zb_sim_result* result) {
+    if (!times || !result) return zb::fail(ZB_ERR_INVALID_ARG, "times or result is NULL");
+    PassTimes T;
+    T.f = times->t_f;
+    T.b = times->t_b;
+    T.w = times->t_w;
+    T.comm = times->t_comm;
+    if (!(T.f > 0) || !(T.b > 0) || !(T.w > 0) || !(T.comm >= 0) || !std::isfinite(T.f) ||
+        !std::isfinite(T.b) || !std::isfinite(T.w) || !std::isfinite(T.comm))
+        return zb::fail(ZB_ERR_INVALID_ARG, "pass times must be finite, T_F/T_B/T_W > 0, T_comm >= 0");
+    size_t dummy = 0;
+    return run_schedule(kind, P, m, T, out, n_ops ? n_ops : &dummy, result);
 }
 
 extern "C" zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_op* ops, size_t n_ops,

@@ -72,6 +72,15 @@ class zb_run_stats(C.Structure):
                 ("kind_ms", C.c_double * 4), ("gemm_ms", C.c_double), ("op_ms", C.POINTER(C.c_float))]
 
 
+class zb_sim_times(C.Structure):
+    _fields_ = [("t_f", C.c_double), ("t_b", C.c_double), ("t_w", C.c_double), ("t_comm", C.c_double)]
+
+
+class zb_sim_result(C.Structure):
+    _fields_ = [("cost", C.c_double), ("ideal", C.c_double), ("bubble_rate", C.c_double),
+                ("peak_live_microbatches", C.c_uint32), ("peak_live_stage0", C.c_uint32)]
+
+
 class ZBError(RuntimeError):
     def __init__(self, status: int, where: str, msg: str):
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}")
@@ -100,6 +109,9 @@ def _load():
                                          C.POINTER(vp), C.POINTER(vp), C.POINTER(vp),
                                          C.POINTER(vp), C.POINTER(zb_op), sz,
                                          C.POINTER(zb_run_stats), vp],
+        "zb_simulate_schedule": [C.c_int32, C.c_int32, C.c_int32, C.POINTER(zb_sim_times),
+                                 C.POINTER(zb_op), C.POINTER(sz), C.POINTER(zb_sim_result)],
+        "zb_selftest_wait_timeout": [C.c_uint64, vp],
         "zb_sync_status": [vp],
     }
     for name, args in sig.items():
@@ -200,6 +212,28 @@ def zb_make_schedule(kind, P: int, m: int):
     arr = (zb_op * n.value)()
     _check(LIB.zb_make_schedule(kid, P, m, arr, C.byref(n)), "zb_make_schedule")
     return ops_tuples(arr, n.value)
+
+
+def zb_simulate_schedule(kind, P: int, m: int, t_f: float, t_b: float, t_w: float,
+                         t_comm: float = 0.0, want_ops: bool = False):
+    """Simulated ordering with the given pass times: returns (result, ops or None)."""
+    kid = SCHED_IDS[kind] if isinstance(kind, str) else int(kind)
+    t = zb_sim_times(t_f, t_b, t_w, t_comm)
+    res = zb_sim_result()
+    if not want_ops:
+        _check(LIB.zb_simulate_schedule(kid, P, m, C.byref(t), None, None, C.byref(res)),
+               "zb_simulate_schedule")
+        return res, None
+    n = C.c_size_t(0)
+    _check(LIB.zb_make_schedule(kid, P, m, None, C.byref(n)), "zb_make_schedule")
+    arr = (zb_op * n.value)()
+    _check(LIB.zb_simulate_schedule(kid, P, m, C.byref(t), arr, C.byref(n), C.byref(res)),
+           "zb_simulate_schedule")
+    return res, ops_tuples(arr, n.value)
+
+
+def zb_selftest_wait_timeout(limit_ns: int, stream=None):
+    _check(LIB.zb_selftest_wait_timeout(int(limit_ns), _stream(stream)), "zb_selftest_wait_timeout")
 
 
 def make_pipeline(P, m, blk, mem_limit_bytes=0, zero_grads=True, timing=False) -> zb_pipeline:

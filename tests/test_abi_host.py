@@ -159,3 +159,37 @@ def test_single_linear_multi_stage_needs_square(zb):
     with pytest.raises(zb.ZBError) as e:
         zb.zb_schedule_workspace_size(pl, ops)
     assert e.value.status == zb.ZB_ERR_SHAPE
+
+
+@pytest.mark.parametrize("kind", S.SCHEDULES)
+@pytest.mark.parametrize("P,m", [(2, 3), (4, 8), (8, 24), (5, 11), (3, 2)])
+def test_simulator_with_times_matches_oracle(zb, kind, P, m):
+    # dyadic times (exact in binary) so both simulators see identical sums
+    import random
+    rnd = random.Random(P * 100 + m)
+    for _ in range(4):
+        tf, tb, tw = (rnd.randint(1, 16) / 8 for _ in range(3))
+        tc = rnd.randint(0, 4) / 16
+        t = S.Times(tf, tb, tw, tc)
+        ev, ref_ops = S.make_schedule(kind, P, m, t)
+        res, ops = zb.zb_simulate_schedule(kind, P, m, tf, tb, tw, tc, want_ops=True)
+        assert ops == ref_ops
+        assert res.cost == S.cost(ev, P)
+        assert abs(res.bubble_rate - S.bubble_rate(ev, P, m, t)) < 1e-12
+        assert res.peak_live_microbatches == max(S.peak_live(ev, P))
+        assert res.peak_live_stage0 == S.peak_live(ev, P)[0]
+
+
+def test_simulator_equal_times_is_make_schedule(zb):
+    for kind in S.SCHEDULES:
+        res, ops = zb.zb_simulate_schedule(kind, 4, 8, 1.0, 1.0, 1.0, 0.0, want_ops=True)
+        assert ops == zb.zb_make_schedule(kind, 4, 8)
+        assert res.cost == {"1F1B": 33.0, "ZBH1": 27.0, "ZBH2": 24.0}[kind]
+
+
+def test_simulator_rejects_bad_times(zb):
+    for bad in ((0.0, 1.0, 1.0, 0.0), (1.0, -1.0, 1.0, 0.0), (1.0, 1.0, float("nan"), 0.0),
+                (1.0, 1.0, 1.0, -0.5)):
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_simulate_schedule("ZBH1", 4, 8, *bad)
+        assert e.value.status == zb.ZB_ERR_INVALID_ARG

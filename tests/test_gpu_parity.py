@@ -431,3 +431,23 @@ def test_workspace_errors(zb):
     zb.zb_run_stage_schedule(pl, stages, X0, dY, None, None, ops, ws, need)
     sync(zb)
     assert torch.isfinite(stages[0]["dW1"]).all()
+
+
+def test_device_wait_timeout_is_reported_and_context_survives(zb):
+    # A bounded wait on a barrier nothing arrives on: reported as
+    # ZB_ERR_TIMEOUT by the next status check, then cleared; the context
+    # keeps working (no fault, no trap).
+    zb.zb_sync_status()
+    zb.zb_selftest_wait_timeout(20_000_000)
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_sync_status()
+    assert e.value.status == zb.ZB_ERR_TIMEOUT
+    zb.zb_sync_status()
+    M, h, f = 64, 64, 128
+    t = _block_tensors(M, h, f, seed=2)
+    blk = zb.make_block(M, h, f)
+    H, A, Y = empty_bf16(M, f), empty_bf16(M, f), empty_bf16(M, h)
+    zb.zb_forward(blk, t["X"], t["W1"], t["W2"], None, None, H, A, Y)
+    sync(zb)
+    Hr, _, _ = ob.forward(f64(t["X"]), f64(t["W1"]), f64(t["W2"]))
+    assert ob.rel_fro(f64(H), Hr) < TOL_BF16
