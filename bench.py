@@ -355,7 +355,8 @@ def main():
     if not multi:
         ops = [(k, 0, j) for k, s, j in ops if s == 0]
     blk = zb.make_block(M, h, f)
-    pl = zb.make_pipeline(P, m, blk, timing=True)
+    # multi-stage replays run their stages on P streams (stage-parallel)
+    pl = zb.make_pipeline(P, m, blk, timing=True, streams=P if multi else 1)
     need, peak_live = zb.zb_schedule_workspace_size(pl, ops)
     ws_t = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -420,7 +421,7 @@ def main():
     # library's simulator of the orderings: a projection, not a measurement
     tfb = [sums["kind"][i] / (m * P * args.steps) for i in range(3)]
     projection = None
-    if all(t > 0 for t in tfb):
+    if all(t > 0 for t in tfb) and not multi:  # concurrent stages blur per-pass times
         projection = {"label": "simulated %d-stage pipeline from the measured per-pass times" % Pl,
                       "P": Pl, "m": m, "T_F_ms": tfb[0], "T_B_ms": tfb[1], "T_W_ms": tfb[2],
                       "T_comm_ms": 0.0, "bubble_rate": {}, "pipeline_tokens_per_s": {}}
@@ -508,7 +509,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": desc, "h": h, "f": f, "M": M, "m": m, "P": P,
-                       "schedule": sched, "list_from_P": Pl,
+                       "schedule": sched, "list_from_P": Pl, "streams": pl.streams,
                        "parallelism": "replicas" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2 (W1 %.0f MB, X and dY %.0f MB per microbatch)"
                              % (h * f * 2 / 1e6, M * h * 2 / 1e6)},

@@ -175,6 +175,19 @@ typedef struct zb_pipeline {
     int32_t timing;            /* 1: record CUDA events around every op and
                                   GEMM launch, synchronise at the end and
                                   fill the timing fields of zb_run_stats     */
+    int32_t streams;           /* 0 or 1: every op on `stream`, in list
+                                  order.  n > 1: stage s runs on stream
+                                  s mod min(n, P, 8) (the caller's stream and
+                                  library-owned streams), ordered by events:
+                                  F(s-1,j) -> F(s,j), B(s+1,j) -> B(s,j), and
+                                  an arena slot's next writer after its last
+                                  reader.  The stages' passes then share the
+                                  GPU the way pipeline stages share time; a
+                                  stage's W still run in list order on its
+                                  stream, so results are bit-identical to the
+                                  serial replay.  The call forks from and
+                                  joins back into `stream`.                  */
+    int32_t reserved;          /* must be 0                                  */
 } zb_pipeline;
 
 typedef struct zb_stage_params {
@@ -230,8 +243,8 @@ zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage_params* st
  * arena is a static device array of ZB_STATIC_ARENA_BYTES (64 MiB) that every
  * device using this entry point holds from its first call until the process
  * exits.  Op lists whose arena (zb_schedule_workspace_size) is larger are
- * rejected with ZB_ERR_WORKSPACE; pl->timing must be 0 (ZB_ERR_INVALID_ARG
- * otherwise).  No device memory is allocated by the call.  The first call on
+ * rejected with ZB_ERR_WORKSPACE; pl->timing must be 0 and pl->streams at
+ * most 1 (ZB_ERR_INVALID_ARG otherwise).  No device memory is allocated by the call.  The first call on
  * each device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current; make that first call before any stream capture.
  * All calls share the one array: calls whose work overlaps on the GPU (e.g.

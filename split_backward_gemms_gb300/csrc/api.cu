@@ -8,7 +8,9 @@
 // F(s,j) after F(s-1,j); B(s,j) after F(s,j) and B(s+1,j); W(s,j) after B(s,j).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -75,6 +77,38 @@ struct Recorder {
 std::vector<cudaEvent_t>& event_pool() {
     static thread_local std::vector<cudaEvent_t> pool;
     return pool;
+}
+
+// Events without timing that order ops across streams (one per op).
+zb_status sync_events(size_t n, std::vector<cudaEvent_t>** out) {
+    static thread_local std::vector<cudaEvent_t> pool;
+    while (pool.size() < n) {
+        cudaEvent_t e;
+        cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+        if (r != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("cudaEventCreate: ") + cudaGetErrorString(r));
+        pool.push_back(e);
+    }
+    *out = &pool;
+    return ZB_OK;
+}
+
+// Library-owned non-blocking streams of the current device (created once).
+zb_status helper_streams(int count, std::vector<cudaStream_t>* out) {
+    static std::mutex mu;
+    static std::vector<cudaStream_t> per_dev[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) return fail(ZB_ERR_CUDA, "cudaGetDevice failed");
+    std::lock_guard<std::mutex> lk(mu);
+    auto& v = per_dev[dev];
+    while (static_cast<int>(v.size()) < count) {
+        cudaStream_t st;
+        e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("cudaStreamCreate: ") + cudaGetErrorString(e));
+        v.push_back(st);
+    }
+    out->assign(v.begin(), v.begin() + count);
+    return ZB_OK;
 }
 
 template <typename F>
@@ -282,6 +316,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     if (s != ZB_OK) return s;
     const int P = pl->P, m = pl->m;
     if (P < 1 || m < 1) return fail(ZB_ERR_SHAPE, "P and m must be >= 1");
+    if (pl->reserved != 0 || pl->streams < 0) return fail(ZB_ERR_INVALID_ARG, "pipeline.streams < 0 or reserved != 0");
     if (P > 1 && b.act == ZB_ACT_NONE && b.f != b.h)
         return fail(ZB_ERR_SHAPE, "a multi-stage single-linear pipeline needs f == h");
     const bool mlp = b.act != ZB_ACT_NONE;
@@ -321,8 +356,33 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         return ws + static_cast<size_t>(plan.row_slots) * plan.row_bytes + static_cast<size_t>(slot) * plan.ffn_bytes;
     };
 
+    // Streams: stage s runs on lanes[s % ns]; lanes[0] is the caller's stream.
+    const int ns = std::max(1, std::min(std::min(pl->streams, P), 8));
+    std::vector<cudaStream_t> lanes(1, static_cast<cudaStream_t>(stream));
+    std::vector<cudaEvent_t>* evs = nullptr;
+    if (ns > 1) {
+        std::vector<cudaStream_t> extra;
+        s = helper_streams(ns - 1, &extra);
+        if (s != ZB_OK) return s;
+        lanes.insert(lanes.end(), extra.begin(), extra.end());
+        s = sync_events(n_ops + ns, &evs);
+        if (s != ZB_OK) return s;
+        // fork: helper lanes start after the work already on the caller's stream
+        cudaEvent_t fork = (*evs)[n_ops];
+        cudaError_t e = cudaEventRecord(fork, lanes[0]);
+        for (int k = 1; k < ns && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(lanes[k], fork, 0);
+        if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("fork: ") + cudaGetErrorString(e));
+    }
+    // producer op of F(s,j) and of B/BW(s,j), for cross-stage waits
+    std::vector<int> fwd_op(static_cast<size_t>(P) * m, -1), bwd_op(static_cast<size_t>(P) * m, -1);
+    for (size_t i = 0; i < n_ops; ++i) {
+        const size_t key = static_cast<size_t>(ops[i].stage) * m + ops[i].micro;
+        if (ops[i].kind == ZB_OP_F) fwd_op[key] = static_cast<int>(i);
+        else if (ops[i].kind == ZB_OP_B || ops[i].kind == ZB_OP_BW) bwd_op[key] = static_cast<int>(i);
+    }
+
     Recorder rec;
-    rec.st = static_cast<cudaStream_t>(stream);
+    rec.st = lanes[0];
     rec.on = pl->timing != 0;
     rec.pool = &event_pool();
     std::vector<std::pair<size_t, size_t>> op_span(n_ops, {0, 0});  // [first span, end span)
@@ -334,6 +394,25 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         const zb_op& o = ops[i];
         const int st = o.stage, j = static_cast<int>(o.micro);
         const zb_stage_params& p = stages[st];
+        cudaStream_t lane = lanes[st % ns];
+        void* lane_v = static_cast<void*>(lane);
+        rec.st = lane;
+        if (ns > 1 && o.kind != ZB_OP_OPT) {
+            // wait for producers and slot releases that ran on other lanes
+            std::vector<int> deps = plan.reuse_deps[i];
+            if (o.kind == ZB_OP_F && st > 0) deps.push_back(fwd_op[static_cast<size_t>(st - 1) * m + j]);
+            if ((o.kind == ZB_OP_B || o.kind == ZB_OP_BW) && st < P - 1)
+                deps.push_back(bwd_op[static_cast<size_t>(st + 1) * m + j]);
+            for (int d : deps) {
+                if (d < 0 || lanes[ops[d].stage % ns] == lane) continue;
+                cudaError_t e = cudaStreamWaitEvent(lane, (*evs)[d], 0);
+                if (e != cudaSuccess) {
+                    s = fail(ZB_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(e));
+                    break;
+                }
+            }
+            if (s != ZB_OK) break;
+        }
         op_span[i].first = rec.spans.size();
         const void* X = st == 0 ? X0[j] : row_ptr(plan.at(st, j, BUF_X));
         const void* dY = st == P - 1 ? dY_last[j] : row_ptr(plan.at(st, j, BUF_DY));
@@ -344,20 +423,20 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
             void* dX;
             if (st > 0) dX = row_ptr(plan.at(st - 1, j, BUF_DY));
             else dX = has_dx ? dX0_out[j] : row_ptr(plan.tmp_slot[i]);
-            return backward_input_impl(b, dY, p.W1, p.W2, H, dH, dX, stream, &rec);
+            return backward_input_impl(b, dY, p.W1, p.W2, H, dH, dX, lane_v, &rec);
         };
         auto run_w = [&]() -> zb_status {
             const int acc = (pl->zero_grads && !w_started[st]) ? 0 : 1;
             w_started[st] = 1;
             const void* Xw = X;
-            return backward_weight_impl(b, Xw, A, dH, dY, p.dW1, p.dW2, p.db1, p.db2, acc, stream, &rec);
+            return backward_weight_impl(b, Xw, A, dH, dY, p.dW1, p.dW2, p.db1, p.db2, acc, lane_v, &rec);
         };
         switch (o.kind) {
             case ZB_OP_F: {
                 void* Y;
                 if (st < P - 1) Y = row_ptr(plan.at(st + 1, j, BUF_X));
                 else Y = has_y ? Y_last_out[j] : row_ptr(plan.tmp_slot[i]);
-                s = forward_impl(b, X, p.W1, p.W2, p.b1, p.b2, H, A, Y, stream, &rec);
+                s = forward_impl(b, X, p.W1, p.W2, p.b1, p.b2, H, A, Y, lane_v, &rec);
                 break;
             }
             case ZB_OP_B: s = run_b(); break;
@@ -369,6 +448,20 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
             default: break;
         }
         op_span[i].second = rec.spans.size();
+        if (ns > 1 && s == ZB_OK) {
+            cudaError_t e = cudaEventRecord((*evs)[i], lane);
+            if (e != cudaSuccess) s = fail(ZB_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(e));
+        }
+    }
+    if (ns > 1) {
+        // join: the caller's stream continues after every lane's work
+        for (int k = 1; k < ns; ++k) {
+            cudaEvent_t ev = (*evs)[n_ops + k];
+            cudaError_t e = cudaEventRecord(ev, lanes[k]);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(lanes[0], ev, 0);
+            if (e != cudaSuccess && s == ZB_OK)
+                s = fail(ZB_ERR_CUDA, std::string("join: ") + cudaGetErrorString(e));
+        }
     }
     g_gemm_counter = nullptr;
     if (s != ZB_OK) return s;
@@ -383,14 +476,14 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         stats->gemm_ms = 0.0;
     }
     if (rec.on && stats && !rec.spans.empty()) {
-        cudaError_t e = cudaEventSynchronize((*rec.pool)[rec.used - 1]);
+        cudaError_t e = cudaStreamSynchronize(lanes[0]);  // joined: every lane is done
         if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("timing sync: ") + cudaGetErrorString(e));
         auto ms = [&](size_t a, size_t bb) {
             float t = 0.f;
             cudaEventElapsedTime(&t, (*rec.pool)[a], (*rec.pool)[bb]);
             return static_cast<double>(t);
         };
-        stats->total_ms = ms(rec.spans.front().a, rec.spans.back().b);
+        for (const auto& sp : rec.spans) stats->total_ms = std::max(stats->total_ms, ms(rec.spans.front().a, sp.b));
         for (const auto& sp : rec.spans)
             if (sp.gemm) stats->gemm_ms += ms(sp.a, sp.b);
         for (size_t i = 0; i < n_ops; ++i) {

@@ -132,25 +132,75 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-__device__ __forceinline__ float gelu_f(float x, int act) {
-    if (act == ZB_ACT_GELU_TANH) {
-        const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-        return 0.5f * x * (1.0f + tanhf(u));
-    }
-    return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f));
+// GeLU and its derivative without branches, so that the epilogue can
+// interleave many independent elements (a per-element dependent chain with
+// one warp per scheduler otherwise leaves the math latency-bound).
+//
+// Exact (erf) form: Phi(x) = (1 + erf(x / sqrt 2)) / 2 with erf(z), z >= 0,
+// from Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26 (maximum absolute error 1.5e-7):
+//     erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),
+//     t = 1 / (1 + p z),
+// and erf(-z) = -erf(z).  exp(-z^2) = exp(-x^2 / 2) is also the normal
+// density's exponential, so GeLU'(x) = Phi(x) + x phi(x) reuses it.
+// tanh form: tanh(u) = 1 - 2 / (1 + exp(2u)).
+struct AS71_26 {
+    static constexpr float p = 0.3275911f;
+    static constexpr float a1 = 0.254829592f;
+    static constexpr float a2 = -0.284496736f;
+    static constexpr float a3 = 1.421413741f;
+    static constexpr float a4 = -1.453152027f;
+    static constexpr float a5 = 1.061405429f;
+};
+
+// Phi(x) and exp(-x^2/2); 1 + p z lies in [1, 1 + p z_max], so the fast
+// reciprocal is exact enough (relative error of a few ulp).
+__device__ __forceinline__ void normal_cdf_and_exp(float x, float& Phi, float& e) {
+    using C = AS71_26;
+    const float z = fabsf(x) * 0.7071067811865476f;
+    e = __expf(-0.5f * x * x);
+    const float t = __fdividef(1.0f, fmaf(C::p, z, 1.0f));
+    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, C::a5, C::a4), C::a3), C::a2), C::a1);
+    // q = (1 - erf(|x|/sqrt 2)) / 2 = Phi(-|x|); no cancellation for x < 0
+    const float q = 0.5f * poly * e;
+    Phi = x < 0.0f ? q : 1.0f - q;
 }
 
-__device__ __forceinline__ float gelu_grad_f(float x, int act) {
-    if (act == ZB_ACT_GELU_TANH) {
+// tanh(u) = 1 - 2 / (1 + exp(2u)); exp overflow gives 1, underflow -1.
+__device__ __forceinline__ float tanh_nb(float u) {
+    return 1.0f - __fdividef(2.0f, 1.0f + __expf(2.0f * u));
+}
+
+template <bool TANH>
+__device__ __forceinline__ float gelu_t(float x) {
+    if (TANH) {
+        const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+        return 0.5f * x * (1.0f + tanh_nb(u));
+    }
+    float Phi, e;
+    normal_cdf_and_exp(x, Phi, e);
+    return x * Phi;
+}
+
+template <bool TANH>
+__device__ __forceinline__ float gelu_grad_t(float x) {
+    if (TANH) {
         const float x2 = x * x;
-        const float t = tanhf(0.7978845608028654f * (x + 0.044715f * x * x2));
+        const float t = tanh_nb(0.7978845608028654f * (x + 0.044715f * x * x2));
         return 0.5f * (1.0f + t) +
                0.5f * x * (1.0f - t * t) * 0.7978845608028654f * (1.0f + 3.0f * 0.044715f * x2);
     }
-    // Phi(x) + x phi(x)
-    return 0.5f * (1.0f + erff(x * 0.7071067811865476f)) +
-           x * 0.3989422804014327f * expf(-0.5f * x * x);
+    float Phi, e;
+    normal_cdf_and_exp(x, Phi, e);
+    return fmaf(x * 0.3989422804014327f, e, Phi);  // Phi(x) + x phi(x)
 }
+
+// 64 columns of one row: the activation form is chosen once per chunk so the
+// unrolled element loops have no branches and interleave.
+template <bool TANH>
+__device__ __forceinline__ void gelu_pack64(const float (&x)[64], uint32_t (&w)[32]);
+template <bool TANH>
+__device__ __forceinline__ void gelu_grad_mul64(float (&x)[64], const uint32_t (&h)[32]);
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -160,6 +210,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
     return __bfloat1622float2(v);
+}
+
+template <bool TANH>
+__device__ __forceinline__ void gelu_pack64(const float (&x)[64], uint32_t (&w)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(gelu_t<TANH>(x[2 * i]), gelu_t<TANH>(x[2 * i + 1]));
+}
+
+template <bool TANH>
+__device__ __forceinline__ void gelu_grad_mul64(float (&x)[64], const uint32_t (&h)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float2 f2 = unpack_bf16x2(h[i]);
+        x[2 * i] *= gelu_grad_t<TANH>(f2.x);
+        x[2 * i + 1] *= gelu_grad_t<TANH>(f2.y);
+    }
 }
 
 // Tile order: groups of `group` M-blocks; inside a group M is fastest, then
@@ -466,20 +532,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                     }
-                    if (EPI == zb::EPI_GELU_BWD && row < args.Mg) {
+                    if (EPI == zb::EPI_GELU_BWD) {
+                        // this row's 64 H values (zeros past the matrix edge)
+                        uint32_t hw[32];
                         const __nv_bfloat16* hp = args.aux + static_cast<long long>(row) * args.ldaux + col0;
 #pragma unroll
                         for (int g = 0; g < 8; ++g) {
-                            if (col0 + g * 8 >= args.Ng) break;
-                            const uint4 hv = *reinterpret_cast<const uint4*>(hp + g * 8);
-                            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 f2 = unpack_bf16x2(hw[i]);
-                                x[g * 8 + 2 * i] *= gelu_grad_f(f2.x, args.act);
-                                x[g * 8 + 2 * i + 1] *= gelu_grad_f(f2.y, args.act);
-                            }
+                            uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+                            if (row < args.Mg && col0 + g * 8 < args.Ng)
+                                hv = *reinterpret_cast<const uint4*>(hp + g * 8);
+                            hw[4 * g] = hv.x;
+                            hw[4 * g + 1] = hv.y;
+                            hw[4 * g + 2] = hv.z;
+                            hw[4 * g + 3] = hv.w;
                         }
+                        if (args.act == ZB_ACT_GELU_TANH)
+                            gelu_grad_mul64<true>(x, hw);
+                        else
+                            gelu_grad_mul64<false>(x, hw);
                     }
                     uint32_t w[32];
 #pragma unroll
@@ -490,9 +560,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     stage_row(stg, lane, w);
                     staging_release<false>(&tmO0, stg, lane, col0, row0);
                     if (EPI == zb::EPI_GELU_DUAL) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            w[i] = pack_bf16x2(gelu_f(x[2 * i], args.act), gelu_f(x[2 * i + 1], args.act));
+                        if (args.act == ZB_ACT_GELU_TANH)
+                            gelu_pack64<true>(x, w);
+                        else
+                            gelu_pack64<false>(x, w);
                         stg = stg0 + flip * STAGING_BOX;
                         flip ^= 1u;
                         staging_acquire(lane);

@@ -61,6 +61,8 @@ extern "C" zb_status zb_run_stage_schedule_static(const zb_pipeline* pl, const z
                                                   void* stream) {
     if (!pl) return zb::fail(ZB_ERR_INVALID_ARG, "pipeline is NULL");
     if (pl->timing) return zb::fail(ZB_ERR_INVALID_ARG, "timing mode creates CUDA events; use zb_run_stage_schedule");
+    if (pl->streams > 1)
+        return zb::fail(ZB_ERR_INVALID_ARG, "stage-parallel replay uses library streams; use zb_run_stage_schedule");
     size_t need = 0;
     zb_status s = zb_schedule_workspace_size(pl, ops, n_ops, &need, nullptr);
     if (s != ZB_OK) return s;

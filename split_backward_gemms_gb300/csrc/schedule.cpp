@@ -285,10 +285,13 @@ zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has
     plan->ffn_bytes = align256(fb);
     plan->slot.assign(static_cast<size_t>(P) * m * BUF_COUNT, -1);
     plan->tmp_slot.assign(n, -1);
+    plan->reuse_deps.assign(n, {});
     // Two pools of equal-size slots; lowest free index first (deterministic).
     std::set<int> free_row, free_ffn;
     int n_row = 0, n_ffn = 0;
     size_t live = 0, peak = 0;
+    std::vector<int> row_freed_by, ffn_freed_by;  // op that last released each slot
+    size_t cur = 0;                               // index of the op being planned
     // Saved activations enter the ledger; a scratch output (the last stage's Y
     // or stage 0's dX when the caller gives no buffer) takes a slot only.
     auto take = [&](bool ffn, bool saved = true) {
@@ -298,8 +301,11 @@ zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has
         if (!fr.empty()) {
             id = *fr.begin();
             fr.erase(fr.begin());
+            const int prev = (ffn ? ffn_freed_by : row_freed_by)[id];
+            if (prev >= 0 && prev != static_cast<int>(cur)) plan->reuse_deps[cur].push_back(prev);
         } else {
             id = cnt++;
+            (ffn ? ffn_freed_by : row_freed_by).push_back(-1);
         }
         if (saved) {
             live += ffn ? fb : rb;
@@ -310,6 +316,7 @@ zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has
     auto give = [&](bool ffn, int id, bool saved = true) {
         if (id < 0) return;
         (ffn ? free_ffn : free_row).insert(id);
+        (ffn ? ffn_freed_by : row_freed_by)[id] = static_cast<int>(cur);
         if (saved) live -= ffn ? fb : rb;
     };
     auto ref = [&](int s, int j, int k) -> int& {
@@ -333,6 +340,7 @@ zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has
         if (s < P - 1) give(false, ref(s, j, BUF_DY));
     };
     for (size_t i = 0; i < n; ++i) {
+        cur = i;
         const zb_op& o = ops[i];
         const int s = o.stage, j = static_cast<int>(o.micro);
         switch (o.kind) {

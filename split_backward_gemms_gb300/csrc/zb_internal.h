@@ -84,6 +84,9 @@ struct ArenaPlan {
     // temporary slots for Y of the last stage / dX of stage 0 when no output
     // pointer is given: one per op index (or -1)
     std::vector<int> tmp_slot;
+    // per op: indices of the ops that last released a slot this op takes
+    // (its next writer must follow them when ops run on several streams)
+    std::vector<std::vector<int>> reuse_deps;
     int P = 0, m = 0;
     int at(int s, int j, int k) const { return slot[(static_cast<size_t>(s) * m + j) * BUF_COUNT + k]; }
 };

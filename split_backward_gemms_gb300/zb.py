@@ -58,7 +58,8 @@ class zb_op(C.Structure):
 
 class zb_pipeline(C.Structure):
     _fields_ = [("P", C.c_int32), ("m", C.c_int32), ("blk", zb_block),
-                ("mem_limit_bytes", C.c_uint64), ("zero_grads", C.c_int32), ("timing", C.c_int32)]
+                ("mem_limit_bytes", C.c_uint64), ("zero_grads", C.c_int32), ("timing", C.c_int32),
+                ("streams", C.c_int32), ("reserved", C.c_int32)]
 
 
 class zb_stage_params(C.Structure):
@@ -236,8 +237,10 @@ def zb_selftest_wait_timeout(limit_ns: int, stream=None):
     _check(LIB.zb_selftest_wait_timeout(int(limit_ns), _stream(stream)), "zb_selftest_wait_timeout")
 
 
-def make_pipeline(P, m, blk, mem_limit_bytes=0, zero_grads=True, timing=False) -> zb_pipeline:
-    return zb_pipeline(P, m, blk, mem_limit_bytes, 1 if zero_grads else 0, 1 if timing else 0)
+def make_pipeline(P, m, blk, mem_limit_bytes=0, zero_grads=True, timing=False,
+                  streams=1) -> zb_pipeline:
+    return zb_pipeline(P, m, blk, mem_limit_bytes, 1 if zero_grads else 0, 1 if timing else 0,
+                       int(streams), 0)
 
 
 def zb_schedule_workspace_size(pl, ops):
