@@ -145,6 +145,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(value: float, device, world_size: int) -> float:
+    """Largest value over the ranks (the slowest replica's time)."""
+    import torch
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_step: float, steps: int, world_size: int, seconds_max: float) -> float:
+    """Whole-job throughput of independent replicas: every rank's work over
+    the slowest rank's time."""
+    return work_per_step * steps * world_size / seconds_max
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -395,16 +411,12 @@ def main():
     if ws > 1:
         dist.barrier()
     zb.zb_sync_status(stream)
-    ms = e0.elapsed_time(e1)
-    t = torch.tensor([ms], device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = reduce_max(e0.elapsed_time(e1), dev, ws)
 
     flop_mb = 12.0 * M * h * f  # F, B and W: 4 M h f each per microbatch
     step_flops = flop_mb * m * P
-    value = step_flops * args.steps * ws / (ms_max / 1e3) / 1e12
-    tokens_s = m * M * args.steps * ws / (ms_max / 1e3)
+    value = job_rate(step_flops, args.steps, ws, ms_max / 1e3) / 1e12
+    tokens_s = job_rate(m * M, args.steps, ws, ms_max / 1e3)
     kind_tf = {}
     for i, name in enumerate(("F", "B", "W")):
         kms = sums["kind"][i]
@@ -489,11 +501,8 @@ def main():
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     e2e_run(args.e2e_steps)
-    e2e_s = time.perf_counter() - t0
-    t = torch.tensor([e2e_s], device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_value = step_flops * args.e2e_steps * ws / float(t.item()) / 1e12
+    e2e_s = reduce_max(time.perf_counter() - t0, dev, ws)
+    e2e_value = job_rate(step_flops, args.e2e_steps, ws, e2e_s) / 1e12
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -193,6 +193,12 @@ typedef struct zb_pipeline {
 typedef struct zb_stage_params {
     const void* W1; const void* W2; const void* b1; const void* b2;
     float* dW1; float* dW2; float* db1; float* db2;
+    double* grad_stats;  /* optional device double[2]: at the stage's OPT op,
+                            [0] = sum of squares and [1] = count of non-finite
+                            values over dW1, dW2 (db1, db2) — the stage's local
+                            state for a post-update check of the global
+                            gradient norm and NaN/Inf (summary §4 "Staged
+                            reduce").  NULL: not computed.               */
 } zb_stage_params;
 
 typedef struct zb_run_stats {
@@ -213,6 +219,7 @@ typedef struct zb_run_stats {
  * Lifetimes (the deferred-W activation store): F saves X, H, A; B frees H and
  * saves dH; W frees X, A, dH and dY; a stage's Y is the next stage's X and a
  * stage's dX the previous stage's dY (pointer hand-off inside the arena).
+ * The arena also holds zb_grad_stats scratch for each stage (at its end).
  * Returns the arena size (*bytes) and the ledger peak (*peak_live_bytes,
  * may be NULL).  Host only. */
 zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_op* ops, size_t n_ops,
@@ -257,6 +264,17 @@ zb_status zb_run_stage_schedule_static(const zb_pipeline* pl, const zb_stage_par
                                        void* const* dX0_out, void* const* Y_last_out,
                                        const zb_op* ops, size_t n_ops, zb_run_stats* stats,
                                        void* stream);
+
+/* Gradient statistics of fp32 buffers: out[0] = sum of squares, out[1] =
+ * number of NaN/Inf values (as a double), over every element of the nbufs
+ * device buffers (bufs[i] holds counts[i] floats, 16-byte aligned).  The
+ * reduction order is fixed (per-thread fp32 partial sums over fixed ranges,
+ * then fp64 sums in a fixed tree), so the same inputs give the same bits.
+ * `scratch` is a device buffer of at least zb_grad_stats_scratch_bytes();
+ * `out` is device memory (double[2]).  HBM-bound: reads 4 bytes per element. */
+size_t zb_grad_stats_scratch_bytes(void);
+zb_status zb_grad_stats(const float* const* bufs, const uint64_t* counts, int32_t nbufs,
+                        double* out, void* scratch, size_t scratch_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status                                                                   */

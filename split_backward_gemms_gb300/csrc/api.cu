@@ -327,7 +327,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         if (b.has_bias && (!p.b1 || !p.db1 || (mlp && (!p.b2 || !p.db2))))
             return fail(ZB_ERR_INVALID_ARG, "stage " + std::to_string(st) + ": bias pointer is NULL");
         if (misaligned(p.W1) || misaligned(p.W2) || misaligned(p.b1) || misaligned(p.b2) || misaligned(p.dW1) ||
-            misaligned(p.dW2) || misaligned(p.db1) || misaligned(p.db2))
+            misaligned(p.dW2) || misaligned(p.db1) || misaligned(p.db2) || misaligned(p.grad_stats))
             return fail(ZB_ERR_ALIGN, "stage " + std::to_string(st) + ": pointers must be 16-byte aligned");
     }
     bool has_y = Y_last_out != nullptr, has_dx = dX0_out != nullptr;
@@ -444,6 +444,24 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
             case ZB_OP_BW:
                 s = run_b();
                 if (s == ZB_OK) s = run_w();
+                break;
+            case ZB_OP_OPT:
+                if (p.grad_stats) {
+                    const float* bufs[4];
+                    uint64_t counts[4];
+                    int nb = 0;
+                    const uint64_t hf = static_cast<uint64_t>(b.h) * static_cast<uint64_t>(b.f);
+                    bufs[nb] = p.dW1; counts[nb++] = hf;
+                    if (mlp) { bufs[nb] = p.dW2; counts[nb++] = hf; }
+                    if (b.has_bias) {
+                        bufs[nb] = p.db1; counts[nb++] = static_cast<uint64_t>(b.f);
+                        if (mlp) { bufs[nb] = p.db2; counts[nb++] = static_cast<uint64_t>(b.h); }
+                    }
+                    void* scratch = ws + plan.stats_offset + static_cast<size_t>(st) * plan.stats_bytes;
+                    s = timed(&rec, false, [&] {
+                        return zb_grad_stats(bufs, counts, nb, p.grad_stats, scratch, plan.stats_bytes, lane_v);
+                    });
+                }
                 break;
             default: break;
         }

@@ -110,6 +110,76 @@ __global__ void zb_selftest_wait_kernel(unsigned int* err, unsigned long long li
     }
 }
 
+// ---------------------------------------------------------------- gradient statistics
+// Fixed partition (independent of the device): every buffer is cut into
+// STATS_BLOCKS ranges of float4 groups; each thread sums the squares of its
+// strided groups in fp32, the block combines the threads in fp64 in a fixed
+// tree, and one thread adds the partials in index order.
+constexpr int STATS_BLOCKS = 304;
+constexpr int STATS_THREADS = 256;
+constexpr int STATS_MAX_BUFS = 4;
+
+struct StatsBufs {
+    const float* p[STATS_MAX_BUFS];
+    unsigned long long n[STATS_MAX_BUFS];
+};
+
+__global__ void __launch_bounds__(STATS_THREADS)
+    zb_grad_stats_partial_kernel(StatsBufs b, double* part) {
+    const int buf = blockIdx.y;
+    const float* x = b.p[buf];
+    const unsigned long long n = b.n[buf];
+    const unsigned long long n4 = n / 4;
+    const unsigned long long per = (n4 + STATS_BLOCKS - 1) / STATS_BLOCKS;
+    const unsigned long long lo = per * blockIdx.x;
+    const unsigned long long hi = min(lo + per, n4);
+    float sq = 0.0f;
+    unsigned bad = 0;
+    for (unsigned long long i = lo + threadIdx.x; i < hi; i += STATS_THREADS) {
+        const float4 v = reinterpret_cast<const float4*>(x)[i];
+        sq = fmaf(v.x, v.x, sq);
+        sq = fmaf(v.y, v.y, sq);
+        sq = fmaf(v.z, v.z, sq);
+        sq = fmaf(v.w, v.w, sq);
+        bad += !isfinite(v.x) + !isfinite(v.y) + !isfinite(v.z) + !isfinite(v.w);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < n - 4 * n4) {  // the last n mod 4 elements
+        const float v = x[4 * n4 + threadIdx.x];
+        sq = fmaf(v, v, sq);
+        bad += !isfinite(v);
+    }
+    double dsq = sq, dbad = bad;
+    for (int o = 16; o > 0; o >>= 1) {
+        dsq += __shfl_down_sync(0xffffffffu, dsq, o);
+        dbad += __shfl_down_sync(0xffffffffu, dbad, o);
+    }
+    __shared__ double ssq[STATS_THREADS / 32], sbad[STATS_THREADS / 32];
+    if ((threadIdx.x & 31) == 0) {
+        ssq[threadIdx.x >> 5] = dsq;
+        sbad[threadIdx.x >> 5] = dbad;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double a = 0.0, c = 0.0;
+        for (int w = 0; w < STATS_THREADS / 32; ++w) {
+            a += ssq[w];
+            c += sbad[w];
+        }
+        part[2 * (buf * STATS_BLOCKS + blockIdx.x)] = a;
+        part[2 * (buf * STATS_BLOCKS + blockIdx.x) + 1] = c;
+    }
+}
+
+__global__ void zb_grad_stats_final_kernel(const double* part, int nbufs, double* out) {
+    double a = 0.0, c = 0.0;
+    for (int i = 0; i < nbufs * STATS_BLOCKS; ++i) {
+        a += part[2 * i];
+        c += part[2 * i + 1];
+    }
+    out[0] = a;
+    out[1] = c;
+}
+
 }  // namespace
 
 namespace zb {
@@ -195,6 +265,34 @@ extern "C" zb_status zb_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
     zb_selftest_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(w, limit_ns);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return zb::fail(ZB_ERR_CUDA, std::string("self-test launch: ") + cudaGetErrorString(e));
+    zb::clear_error();
+    return ZB_OK;
+}
+
+extern "C" size_t zb_grad_stats_scratch_bytes(void) {
+    return static_cast<size_t>(2 * STATS_MAX_BUFS * STATS_BLOCKS) * sizeof(double);
+}
+
+extern "C" zb_status zb_grad_stats(const float* const* bufs, const uint64_t* counts, int32_t nbufs,
+                                   double* out, void* scratch, size_t scratch_bytes, void* stream) {
+    if (nbufs < 1 || nbufs > STATS_MAX_BUFS) return zb::fail(ZB_ERR_INVALID_ARG, "nbufs must be in [1, 4]");
+    if (!bufs || !counts || !out || !scratch) return zb::fail(ZB_ERR_INVALID_ARG, "NULL argument");
+    if (scratch_bytes < zb_grad_stats_scratch_bytes()) return zb::fail(ZB_ERR_WORKSPACE, "scratch too small");
+    if ((reinterpret_cast<uintptr_t>(scratch) & 15u) || (reinterpret_cast<uintptr_t>(out) & 7u))
+        return zb::fail(ZB_ERR_ALIGN, "scratch must be 16-byte and out 8-byte aligned");
+    StatsBufs b = {};
+    for (int i = 0; i < nbufs; ++i) {
+        if (!bufs[i] || (reinterpret_cast<uintptr_t>(bufs[i]) & 15u))
+            return zb::fail(ZB_ERR_ALIGN, "gradient buffers must be non-NULL and 16-byte aligned");
+        b.p[i] = bufs[i];
+        b.n[i] = counts[i];
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    double* part = static_cast<double*>(scratch);
+    zb_grad_stats_partial_kernel<<<dim3(STATS_BLOCKS, nbufs), STATS_THREADS, 0, st>>>(b, part);
+    zb_grad_stats_final_kernel<<<1, 1, 0, st>>>(part, nbufs, out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return zb::fail(ZB_ERR_CUDA, std::string("grad stats launch: ") + cudaGetErrorString(e));
     zb::clear_error();
     return ZB_OK;
 }

@@ -369,7 +369,9 @@ zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has
     }
     plan->row_slots = n_row;
     plan->ffn_slots = n_ffn;
-    plan->workspace_bytes = static_cast<size_t>(n_row) * plan->row_bytes + static_cast<size_t>(n_ffn) * plan->ffn_bytes;
+    plan->stats_offset = static_cast<size_t>(n_row) * plan->row_bytes + static_cast<size_t>(n_ffn) * plan->ffn_bytes;
+    plan->stats_bytes = align256(zb_grad_stats_scratch_bytes());
+    plan->workspace_bytes = plan->stats_offset + static_cast<size_t>(P) * plan->stats_bytes;
     plan->peak_live_bytes = peak;
     if (pl.mem_limit_bytes != 0 && peak > pl.mem_limit_bytes)
         return fail(ZB_ERR_BUDGET, "peak live activation bytes " + std::to_string(peak) + " exceed the limit " +

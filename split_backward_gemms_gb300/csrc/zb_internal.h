@@ -79,6 +79,7 @@ struct ArenaPlan {
     int row_slots = 0, ffn_slots = 0;     // peak simultaneous slots per class
     size_t workspace_bytes = 0;
     size_t peak_live_bytes = 0;
+    size_t stats_offset = 0, stats_bytes = 0;  // per-stage gradient-statistics scratch
     // slot index per (stage, micro, BufKind); -1 when the buffer is caller-owned
     std::vector<int> slot;  // index: ((s*m + j) * BUF_COUNT + kind)
     // temporary slots for Y of the last stage / dX of stage 0 when no output

@@ -64,7 +64,8 @@ class zb_pipeline(C.Structure):
 
 class zb_stage_params(C.Structure):
     _fields_ = [("W1", C.c_void_p), ("W2", C.c_void_p), ("b1", C.c_void_p), ("b2", C.c_void_p),
-                ("dW1", C.c_void_p), ("dW2", C.c_void_p), ("db1", C.c_void_p), ("db2", C.c_void_p)]
+                ("dW1", C.c_void_p), ("dW2", C.c_void_p), ("db1", C.c_void_p), ("db2", C.c_void_p),
+                ("grad_stats", C.c_void_p)]
 
 
 class zb_run_stats(C.Structure):
@@ -113,6 +114,7 @@ def _load():
         "zb_simulate_schedule": [C.c_int32, C.c_int32, C.c_int32, C.POINTER(zb_sim_times),
                                  C.POINTER(zb_op), C.POINTER(sz), C.POINTER(zb_sim_result)],
         "zb_selftest_wait_timeout": [C.c_uint64, vp],
+        "zb_grad_stats": [C.POINTER(vp), C.POINTER(C.c_uint64), C.c_int32, vp, vp, sz, vp],
         "zb_sync_status": [vp],
     }
     for name, args in sig.items():
@@ -121,6 +123,8 @@ def _load():
         fn.restype = C.c_int
     lib.zb_last_error.argtypes = []
     lib.zb_last_error.restype = C.c_char_p
+    lib.zb_grad_stats_scratch_bytes.argtypes = []
+    lib.zb_grad_stats_scratch_bytes.restype = C.c_size_t
     lib.zb_version.argtypes = []
     lib.zb_version.restype = C.c_char_p
     return lib
@@ -233,6 +237,18 @@ def zb_simulate_schedule(kind, P: int, m: int, t_f: float, t_b: float, t_w: floa
     return res, ops_tuples(arr, n.value)
 
 
+def zb_grad_stats_scratch_bytes() -> int:
+    return LIB.zb_grad_stats_scratch_bytes()
+
+
+def zb_grad_stats(bufs, counts, out, scratch, scratch_bytes, stream=None):
+    """out (device double[2]) <- [sum of squares, non-finite count] over bufs."""
+    arr = (C.c_void_p * len(bufs))(*[_ptr(b) for b in bufs])
+    cnt = (C.c_uint64 * len(bufs))(*[int(c) for c in counts])
+    _check(LIB.zb_grad_stats(arr, cnt, len(bufs), _ptr(out), _ptr(scratch), scratch_bytes,
+                             _stream(stream)), "zb_grad_stats")
+
+
 def zb_selftest_wait_timeout(limit_ns: int, stream=None):
     _check(LIB.zb_selftest_wait_timeout(int(limit_ns), _stream(stream)), "zb_selftest_wait_timeout")
 
@@ -268,7 +284,7 @@ def zb_run_stage_schedule(pl, stages, X0, dY_last, dX0_out, Y_last_out, ops, wor
     sp = (zb_stage_params * len(stages))()
     for i, st in enumerate(stages):
         get = st.get if isinstance(st, dict) else (lambda k, _s=st: getattr(_s, k, None))
-        for k in ("W1", "W2", "b1", "b2", "dW1", "dW2", "db1", "db2"):
+        for k in ("W1", "W2", "b1", "b2", "dW1", "dW2", "db1", "db2", "grad_stats"):
             setattr(sp[i], k, _ptr(get(k)))
     arr = ops if isinstance(ops, C.Array) else ops_array(ops)
     st_ptr = C.byref(stats) if stats is not None else None
@@ -288,7 +304,7 @@ def zb_run_stage_schedule_static(pl, stages, X0, dY_last, dX0_out, Y_last_out, o
     sp = (zb_stage_params * len(stages))()
     for i, st in enumerate(stages):
         get = st.get if isinstance(st, dict) else (lambda k, _s=st: getattr(_s, k, None))
-        for k in ("W1", "W2", "b1", "b2", "dW1", "dW2", "db1", "db2"):
+        for k in ("W1", "W2", "b1", "b2", "dW1", "dW2", "db1", "db2", "grad_stats"):
             setattr(sp[i], k, _ptr(get(k)))
     arr = ops if isinstance(ops, C.Array) else ops_array(ops)
     st_ptr = C.byref(stats) if stats is not None else None

@@ -512,3 +512,62 @@ def test_activation_epilogues_match_the_math(zb, act):
         # relative to tiny values) the bf16 result is almost always exact
         body = np.abs(r) >= 1e-2
         assert body.mean() > 0.5 and np.mean(g[body] == r[body]) > 0.999
+
+
+def test_grad_stats_sum_of_squares_and_nonfinite_count(zb):
+    # squared L2 norm and NaN/Inf count: the local half of a post-update check
+    rng = np.random.default_rng(3)
+    sizes = [1, 7, 4096 * 3 + 3, 1_000_003]
+    host = [rng.standard_normal(n).astype(np.float32) for n in sizes]
+    host[2][5] = np.nan
+    host[3][17] = np.inf
+    host[3][999_999] = -np.inf
+    bufs = [torch.from_numpy(a).cuda() for a in host]
+    out = torch.zeros(2, dtype=torch.float64, device="cuda")
+    nbytes = zb.zb_grad_stats_scratch_bytes()
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    good = [a[np.isfinite(a)].astype(np.float64) for a in host]
+    for sel in ([0], [1, 3], [0, 1, 2, 3]):
+        zb.zb_grad_stats([bufs[i] for i in sel], [sizes[i] for i in sel], out, scratch, nbytes)
+        sync(zb)
+        got = out.cpu().numpy()
+        bad = sum(int(np.sum(~np.isfinite(host[i]))) for i in sel)
+        assert got[1] == bad
+        if bad == 0:
+            ref = sum(float(np.sum(good[i] ** 2)) for i in sel)
+            assert abs(got[0] - ref) <= 1e-6 * ref
+            first = out.clone()
+            zb.zb_grad_stats([bufs[i] for i in sel], [sizes[i] for i in sel], out, scratch, nbytes)
+            sync(zb)
+            assert torch.equal(out, first)  # fixed reduction order
+        else:
+            assert not np.isfinite(got[0])
+
+
+def test_replay_reports_stage_grad_stats_and_injected_nan(zb):
+    P, m, M, h, f = 2, 3, 136, 72, 200
+    blk = zb.make_block(M, h, f)
+    wts, X0, dY = _pipeline_setup(zb, P, m, M, h, f, seed=5)
+    ops = zb.zb_make_schedule("ZBH1", P, m)
+    pl = zb.make_pipeline(P, m, blk)
+    ws_bytes, _ = zb.zb_schedule_workspace_size(pl, ops)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    for poison in (False, True):
+        X = [x.clone() for x in X0]
+        if poison:
+            X[1][3, 4] = float("nan")  # a host-made input carries a NaN
+        stages = [dict(w, dW1=empty_f32(h, f), dW2=empty_f32(f, h),
+                       grad_stats=torch.full((2,), -1.0, dtype=torch.float64, device="cuda"))
+                  for w in wts]
+        zb.zb_run_stage_schedule(pl, stages, X, dY, None, None, ops, ws, ws_bytes)
+        sync(zb)
+        for s in range(P):
+            st = stages[s]["grad_stats"].cpu().numpy()
+            g1, g2 = f64(stages[s]["dW1"]), f64(stages[s]["dW2"])
+            bad = int(np.sum(~np.isfinite(g1)) + np.sum(~np.isfinite(g2)))
+            assert st[1] == bad
+            if not poison:
+                ref = float(np.sum(g1 ** 2) + np.sum(g2 ** 2))
+                assert bad == 0 and abs(st[0] - ref) <= 1e-6 * ref
+            else:
+                assert bad > 0
