@@ -441,6 +441,12 @@ def main():
             res, _ = zb.zb_simulate_schedule(kind, Pl, m, tfb[0], tfb[1], tfb[2], 0.0)
             projection["bubble_rate"][kind] = res.bubble_rate
             projection["pipeline_tokens_per_s"][kind] = m * M / (res.cost / 1e3)
+        # heuristic schedules under 1F1B-sized and doubled memory; this block's
+        # B swaps H for dH, so M_W = M_B (mw_ratio 1)
+        for name, limit in (("ZB-1p", Pl), ("ZB-2p", 2 * Pl)):
+            res, _, _ = zb.zb_auto_schedule(Pl, m, tfb[0], tfb[1], tfb[2], 0.0, limit, 1.0)
+            projection["bubble_rate"][name] = res.bubble_rate
+            projection["pipeline_tokens_per_s"][name] = m * M / (res.cost / 1e3)
 
     # ------------------------------------------------------------- end to end
     # Through the public API with host buffers: every step uploads its inputs

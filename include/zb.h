@@ -163,6 +163,24 @@ typedef struct zb_sim_result {
 zb_status zb_simulate_schedule(int32_t kind, int32_t P, int32_t m, const zb_sim_times* times,
                                zb_op* out, size_t* n_ops, zb_sim_result* result);
 
+/* Heuristic automatic scheduler for measured pass times (summary §3 "The
+ * Heuristic Scheduling Algorithm" with "The Memory Model"): memory counted in
+ * units of M_B per stage (F +1, B + r - 1, W -r with r = mw_ratio = M_W/M_B),
+ * never above mem_limit (ZB-1p: P, ZB-2p: 2P).  Whenever a stage is free it
+ * runs its next B if ready; else its next F if ready, within memory, and
+ * allowed by two binary hyperparameters (h1: keep adding warm-up forwards
+ * even when one would delay the first B; h2: never run more than one F
+ * ahead of the next stage); else its oldest W if memory blocks the F, the
+ * idle gap is at least T_W, or idling would make the stage's accumulated
+ * idle time the largest of all stages; remaining W drain at the end.  All
+ * four (h1, h2) are simulated and the smallest Eq. 3 cost is returned
+ * (hyper[0..1], may be NULL).  out / n_ops as for zb_simulate_schedule.
+ * Host only.  ZB_ERR_BUDGET if mem_limit < 1; ZB_ERR_INVALID_ARG for bad
+ * times or mw_ratio outside (0, 1]. */
+zb_status zb_auto_schedule(int32_t P, int32_t m, const zb_sim_times* times, double mem_limit,
+                           double mw_ratio, zb_op* out, size_t* n_ops, zb_sim_result* result,
+                           int32_t* hyper);
+
 typedef struct zb_pipeline {
     int32_t P;                 /* stages                                     */
     int32_t m;                 /* microbatches                               */

@@ -551,3 +551,163 @@ def brute_force_min_cost(P, m, t: Times, split=True):
         if c is not None and (best is None or c < best):
             best = c
     return best
+
+
+# --------------------------------------------------------------------------
+# heuristic automatic scheduler (ZB-1p / ZB-2p)
+# --------------------------------------------------------------------------
+def auto_schedule(P: int, m: int, t: Times, mem_limit: float, mw_ratio: float = 0.5,
+                  h1: int = 1, h2: int = 0):
+    """One run of the heuristic scheduler ([ZB-PP summary] §3 "The Heuristic
+    Scheduling Algorithm", phases 1-4, and "The Memory Model").
+
+    Memory is counted in units of M_B: F adds 1, B adds mw_ratio - 1
+    (M_W = mw_ratio * M_B), W subtracts mw_ratio; a stage never starts a pass
+    that would take it above mem_limit.  Reading of the phases, applied by a
+    stage whenever it is free, in time order:
+      * B first: a stage runs its next B as soon as it is ready (the critical
+        path, "Schedule B promptly").
+      * Warm-up / steady F: otherwise it runs its next F if that F is ready,
+        fits in memory, and (h2 = 1) the stage is not already more than one
+        forward ahead of the next stage (phase 3's skip hyperparameter).
+        Before its first B, with h1 = 0 it stops adding forwards once one
+        more F would delay that B (phase 1's hyperparameter); with h1 = 1 it
+        keeps filling until memory stops it.
+      * W: otherwise, with a W pending, it runs the oldest one when memory is
+        what blocks the F (memory-triggered W), when the idle gap before the
+        next F/B is at least T_W, or when idling the gap would make this
+        stage's accumulated idle time the largest of all stages (the greedy
+        "cumulative maximum bubble" rule); else it idles until the next pass
+        becomes ready.
+      * Cool-down: remaining W's run in ascending order.
+    Returns the list of Events.
+    """
+    nF = [0] * P
+    nB = [0] * P
+    pending = [deque() for _ in range(P)]
+    mem = [0.0] * P
+    idle = [0.0] * P
+    t_free = [0.0] * P
+    waiting = [False] * P
+    endF, endB = {}, {}
+    ends = []
+    events = []
+    eps = 1e-9
+
+    def has_work(s):
+        return nF[s] < m or nB[s] < m or bool(pending[s])
+
+    def ready_f(s):
+        j = nF[s]
+        if j >= m:
+            return None
+        if s == 0:
+            return 0.0
+        e = endF.get((s - 1, j))
+        return None if e is None else e + t.comm
+
+    def ready_b(s):
+        j = nB[s]
+        if j >= m or j >= nF[s]:
+            return None
+        e = endF.get((s, j))
+        if e is None:
+            return None
+        if s == P - 1:
+            return e
+        u = endB.get((s + 1, j))
+        return None if u is None else max(e, u + t.comm)
+
+    def run(s, k, j, start):
+        d = t.dur(k)
+        e = start + d
+        deps = op_deps(k, s, j, P, False)
+        events.append(Event(k, s, j, start, e, deps))
+        ends.append(e)
+        t_free[s] = e
+        if k == "F":
+            endF[(s, j)] = e
+            nF[s] += 1
+            mem[s] += 1.0
+        elif k == "B":
+            endB[(s, j)] = e
+            nB[s] += 1
+            mem[s] += mw_ratio - 1.0
+            pending[s].append(j)
+        else:
+            mem[s] -= mw_ratio
+
+    while any(has_work(s) for s in range(P)):
+        cands = [s for s in range(P) if has_work(s) and not waiting[s]]
+        if not cands:
+            raise RuntimeError("deadlock in auto_schedule")
+        s = min(cands, key=lambda x: (t_free[x], x))
+        now = t_free[s]
+        rb = ready_b(s)
+        rf = ready_f(s)
+        f_fits = mem[s] + 1.0 <= mem_limit + eps
+        f_skip = h2 and s < P - 1 and nF[s] - nF[s + 1] > 1
+        if (nB[s] == 0 and not h1 and rf is not None and rb is not None
+                and rb < max(now, rf) + t.F):
+            f_skip = True  # one more warm-up F would delay the first B
+        f_ok = rf is not None and f_fits and not f_skip
+        acted = True
+        if rb is not None and rb <= now:
+            run(s, "B", nB[s], now)
+        elif f_ok and rf <= now:
+            run(s, "F", nF[s], now)
+        elif pending[s]:
+            nxt = [x for x in (rb, rf if f_ok else None) if x is not None]
+            gap = (min(nxt) - now) if nxt else float("inf")
+            mem_block = rf is not None and rf <= now and not f_fits
+            tail = nF[s] == m and nB[s] == m
+            if (tail or mem_block or gap >= t.W - eps
+                    or idle[s] + gap > max(idle) + eps):
+                run(s, "W", pending[s].popleft(), now)
+            else:
+                idle[s] += gap
+                t_free[s] = min(nxt)
+        else:
+            acted = False
+            nxt = [x for x in (rb, rf if f_ok else None) if x is not None and x > now]
+            if nxt:
+                idle[s] += min(nxt) - now
+                t_free[s] = min(nxt)
+            else:
+                later = [e for e in ends if e > now]
+                later += [t_free[o] for o in range(P) if o != s and has_work(o) and t_free[o] > now]
+                if later:
+                    idle[s] += min(later) - now
+                    t_free[s] = min(later)
+                else:
+                    waiting[s] = True
+        if acted:
+            for o in range(P):
+                waiting[o] = False
+    return events
+
+
+def auto_schedule_search(P: int, m: int, t: Times, mem_limit: float, mw_ratio: float = 0.5):
+    """Grid search over the two binary hyperparameters; the smallest Eq. 3
+    cost wins (ties: the first of (0,0), (0,1), (1,0), (1,1)).
+    Returns (events, ops, (h1, h2))."""
+    best = None
+    for h1 in (0, 1):
+        for h2 in (0, 1):
+            ev = auto_schedule(P, m, t, mem_limit, mw_ratio, h1, h2)
+            c = cost(ev, P)
+            if best is None or c < best[0] - 1e-12:
+                best = (c, ev, (h1, h2))
+    return best[1], global_order(best[1]), best[2]
+
+
+def mem_peaks(events, P: int, mw_ratio: float):
+    """Peak activation memory per stage (units of M_B) of an event list."""
+    peaks = []
+    for s in range(P):
+        cur = pk = 0.0
+        for e in sorted((e for e in events if e.stage == s), key=lambda e: e.start):
+            cur += {"F": 1.0, "B": mw_ratio - 1.0, "W": -mw_ratio, "BW": -1.0}[e.kind]
+            pk = max(pk, cur)
+        peaks.append(pk)
+    return peaks

@@ -13,6 +13,7 @@
 // management.
 #include <algorithm>
 #include <cmath>
+#include <limits>
 #include <cstring>
 #include <deque>
 #include <set>
@@ -174,6 +175,127 @@ bool simulate(int kind, int P, int m, const PassTimes& T, std::vector<SimEvent>*
         }
         if (ran)
             for (auto& x : st) x.parked = false;
+    }
+    return true;
+}
+
+// Heuristic automatic scheduler ("Zero Bubble Pipeline Parallelism", summary
+// §3 "The Heuristic Scheduling Algorithm" and "The Memory Model").  Memory in
+// units of M_B: F +1, B + (r - 1), W -r with r = M_W / M_B.  Whenever a stage
+// is free (decisions in time order) it runs, in this priority:
+//   1. its next B if ready (critical path);
+//   2. its next F if ready, within the memory limit, not more than one F
+//      ahead of the next stage when h2 = 1, and - before its first B with
+//      h1 = 0 - not delaying that B;
+//   3. its oldest pending W if memory blocks the F, or the idle gap before
+//      the next F/B is at least T_W, or idling the gap would make this
+//      stage's accumulated idle time the largest of all stages, or only W
+//      remain;
+//   4. otherwise it idles until its next F/B can start.
+bool auto_simulate(int P, int m, const PassTimes& T, double limit, double r, int h1, int h2,
+                   std::vector<SimEvent>* out) {
+    const double eps = 1e-9;
+    std::vector<int> nf(P, 0), nb(P, 0);
+    std::vector<std::deque<int>> wq(P);
+    std::vector<double> mem(P, 0.0), idle(P, 0.0), tfree(P, 0.0);
+    std::vector<char> parked(P, 0);
+    std::vector<double> fend(static_cast<size_t>(P) * m, -1.0), bend(static_cast<size_t>(P) * m, -1.0);
+    std::vector<double> ends;
+    const double NONE = -1.0;
+    auto work = [&](int s) { return nf[s] < m || nb[s] < m || !wq[s].empty(); };
+    auto f_ready = [&](int s) -> double {
+        const int j = nf[s];
+        if (j >= m) return NONE;
+        if (s == 0) return 0.0;
+        const double e = fend[static_cast<size_t>(s - 1) * m + j];
+        return e < 0 ? NONE : e + T.comm;
+    };
+    auto b_ready = [&](int s) -> double {
+        const int j = nb[s];
+        if (j >= m || j >= nf[s]) return NONE;
+        const double e = fend[static_cast<size_t>(s) * m + j];
+        if (e < 0) return NONE;
+        if (s == P - 1) return e;
+        const double u = bend[static_cast<size_t>(s + 1) * m + j];
+        return u < 0 ? NONE : std::max(e, u + T.comm);
+    };
+    auto put = [&](int s, int k, int j, double t0) {
+        const double t1 = t0 + T.len(k);
+        out->push_back({k, s, j, t0, t1});
+        ends.push_back(t1);
+        tfree[s] = t1;
+        if (k == ZB_OP_F) {
+            fend[static_cast<size_t>(s) * m + j] = t1;
+            nf[s]++;
+            mem[s] += 1.0;
+        } else if (k == ZB_OP_B) {
+            bend[static_cast<size_t>(s) * m + j] = t1;
+            nb[s]++;
+            mem[s] += r - 1.0;
+            wq[s].push_back(j);
+        } else {
+            mem[s] -= r;
+        }
+    };
+    for (;;) {
+        int s = -1;
+        for (int k = 0; k < P; ++k)
+            if (work(k) && !parked[k] && (s < 0 || tfree[k] < tfree[s])) s = k;
+        if (s < 0) {
+            for (int k = 0; k < P; ++k)
+                if (work(k)) return false;
+            break;
+        }
+        const double now = tfree[s];
+        const double rb = b_ready(s), rf = f_ready(s);
+        const bool fits = mem[s] + 1.0 <= limit + eps;
+        bool skip = h2 && s < P - 1 && nf[s] - nf[s + 1] > 1;
+        if (nb[s] == 0 && !h1 && rf >= 0 && rb >= 0 && rb < std::max(now, rf) + T.f) skip = true;
+        const bool f_ok = rf >= 0 && fits && !skip;
+        bool acted = true;
+        if (rb >= 0 && rb <= now) {
+            put(s, ZB_OP_B, nb[s], now);
+        } else if (f_ok && rf <= now) {
+            put(s, ZB_OP_F, nf[s], now);
+        } else if (!wq[s].empty()) {
+            double next = NONE;
+            if (rb >= 0) next = rb;
+            if (f_ok && (next < 0 || rf < next)) next = rf;
+            const double gap = next >= 0 ? next - now : std::numeric_limits<double>::infinity();
+            const bool mem_block = rf >= 0 && rf <= now && !fits;
+            const bool tail = nf[s] == m && nb[s] == m;
+            const double most_idle = *std::max_element(idle.begin(), idle.end());
+            if (tail || mem_block || gap >= T.w - eps || idle[s] + gap > most_idle + eps) {
+                const int j = wq[s].front();
+                wq[s].pop_front();
+                put(s, ZB_OP_W, j, now);
+            } else {
+                idle[s] += gap;
+                tfree[s] = next;
+            }
+        } else {
+            acted = false;
+            double next = NONE;
+            if (rb > now) next = rb;
+            if (f_ok && rf > now && (next < 0 || rf < next)) next = rf;
+            if (next >= 0) {
+                idle[s] += next - now;
+                tfree[s] = next;
+            } else {
+                double later = NONE;
+                for (double e : ends)
+                    if (e > now && (later < 0 || e < later)) later = e;
+                for (int o = 0; o < P; ++o)
+                    if (o != s && work(o) && tfree[o] > now && (later < 0 || tfree[o] < later)) later = tfree[o];
+                if (later >= 0) {
+                    idle[s] += later - now;
+                    tfree[s] = later;
+                } else {
+                    parked[s] = 1;
+                }
+            }
+        }
+        if (acted) std::fill(parked.begin(), parked.end(), 0);
     }
     return true;
 }
@@ -383,6 +505,32 @@ zb_status plan_arena(const zb_pipeline& pl, const zb_op* ops, size_t n, bool has
 
 namespace {
 
+// Eq. 3 cost (max per-stage span), bubble rate and peak live microbatches.
+void fill_result(const std::vector<SimEvent>& ev, int P, int m, const PassTimes& T, zb_sim_result* res) {
+    std::vector<double> first(P, -1.0), lastv(P, 0.0);
+    std::vector<int> live(P, 0), peak(P, 0);
+    std::vector<SimEvent> sorted = ev;
+    std::stable_sort(sorted.begin(), sorted.end(),
+                     [](const SimEvent& a, const SimEvent& b) { return a.start < b.start; });
+    for (const SimEvent& e : sorted) {
+        if (first[e.stage] < 0 || e.start < first[e.stage]) first[e.stage] = e.start;
+        lastv[e.stage] = std::max(lastv[e.stage], e.end);
+        if (e.kind == ZB_OP_F) peak[e.stage] = std::max(peak[e.stage], ++live[e.stage]);
+        else if (e.kind == ZB_OP_W || e.kind == ZB_OP_BW) --live[e.stage];
+    }
+    double cost = 0.0;
+    int pk = 0;
+    for (int st = 0; st < P; ++st) {
+        cost = std::max(cost, lastv[st] - first[st]);
+        pk = std::max(pk, peak[st]);
+    }
+    res->cost = cost;
+    res->ideal = m * (T.f + T.b + T.w);
+    res->bubble_rate = cost > 0 ? (cost - res->ideal) / cost : 0.0;
+    res->peak_live_microbatches = static_cast<uint32_t>(pk);
+    res->peak_live_stage0 = static_cast<uint32_t>(peak[0]);
+}
+
 zb_status check_sched_args(int32_t kind, int32_t P, int32_t m, size_t* n_ops, size_t* total) {
     if (!n_ops) return zb::fail(ZB_ERR_INVALID_ARG, "n_ops is NULL");
     if (kind < ZB_SCHED_1F1B || kind > ZB_SCHED_ZBH2) return zb::fail(ZB_ERR_INVALID_ARG, "unknown schedule kind");
@@ -410,32 +558,7 @@ zb_status run_schedule(int32_t kind, int32_t P, int32_t m, const PassTimes& T, z
     std::vector<SimEvent> ev;
     ev.reserve(total);
     if (!simulate(kind, P, m, T, &ev)) return zb::fail(ZB_ERR_SCHEDULE, "schedule simulation deadlocked");
-    if (res) {
-        // Eq. 3: per-stage span = end of last pass - start of first pass
-        std::vector<double> first(P, -1.0), lastv(P, 0.0);
-        std::vector<int> live(P, 0), peak(P, 0);
-        std::vector<SimEvent> sorted = ev;
-        std::stable_sort(sorted.begin(), sorted.end(), [](const SimEvent& a, const SimEvent& b) {
-            return a.start < b.start;
-        });
-        for (const SimEvent& e : sorted) {
-            if (first[e.stage] < 0 || e.start < first[e.stage]) first[e.stage] = e.start;
-            lastv[e.stage] = std::max(lastv[e.stage], e.end);
-            if (e.kind == ZB_OP_F) peak[e.stage] = std::max(peak[e.stage], ++live[e.stage]);
-            else if (e.kind == ZB_OP_W || e.kind == ZB_OP_BW) --live[e.stage];
-        }
-        double cost = 0.0;
-        int pk = 0;
-        for (int st = 0; st < P; ++st) {
-            cost = std::max(cost, lastv[st] - first[st]);
-            pk = std::max(pk, peak[st]);
-        }
-        res->cost = cost;
-        res->ideal = m * (T.f + T.b + T.w);
-        res->bubble_rate = cost > 0 ? (cost - res->ideal) / cost : 0.0;
-        res->peak_live_microbatches = static_cast<uint32_t>(pk);
-        res->peak_live_stage0 = static_cast<uint32_t>(peak[0]);
-    }
+    if (res) fill_result(ev, P, m, T, res);
     if (out) {
         *n_ops = emit_ops(ev, P, out);
     } else {
@@ -479,6 +602,56 @@ extern "C" zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_
     *bytes = plan.workspace_bytes;
     if (peak_live_bytes) *peak_live_bytes = plan.peak_live_bytes;
     if (st != ZB_OK) return st;
+    zb::clear_error();
+    return ZB_OK;
+}
+
+extern "C" zb_status zb_auto_schedule(int32_t P, int32_t m, const zb_sim_times* times, double mem_limit,
+                                      double mw_ratio, zb_op* out, size_t* n_ops, zb_sim_result* result,
+                                      int32_t* hyper) {
+    if (!times || !result) return zb::fail(ZB_ERR_INVALID_ARG, "times or result is NULL");
+    PassTimes T;
+    T.f = times->t_f;
+    T.b = times->t_b;
+    T.w = times->t_w;
+    T.comm = times->t_comm;
+    if (!(T.f > 0) || !(T.b > 0) || !(T.w > 0) || !(T.comm >= 0) || !std::isfinite(T.f) ||
+        !std::isfinite(T.b) || !std::isfinite(T.w) || !std::isfinite(T.comm))
+        return zb::fail(ZB_ERR_INVALID_ARG, "pass times must be finite, T_F/T_B/T_W > 0, T_comm >= 0");
+    if (!(mw_ratio > 0.0 && mw_ratio <= 1.0)) return zb::fail(ZB_ERR_INVALID_ARG, "mw_ratio must be in (0, 1]");
+    if (!(mem_limit >= 1.0) || !std::isfinite(mem_limit))
+        return zb::fail(ZB_ERR_BUDGET, "the memory limit must allow one microbatch (>= 1 M_B)");
+    size_t total = 0;
+    size_t dummy = 0;
+    zb_status st = check_sched_args(ZB_SCHED_ZBH1, P, m, n_ops ? n_ops : &dummy, &total);
+    if (st != ZB_OK) return st;
+    if (out && *n_ops < total) {
+        *n_ops = total;
+        return zb::fail(ZB_ERR_INVALID_ARG, "output capacity too small");
+    }
+    std::vector<SimEvent> best;
+    double best_cost = 0.0;
+    int best_h = -1;
+    for (int h = 0; h < 4; ++h) {  // (h1, h2) = (0,0), (0,1), (1,0), (1,1)
+        std::vector<SimEvent> ev;
+        ev.reserve(total);
+        if (!auto_simulate(P, m, T, mem_limit, mw_ratio, h >> 1, h & 1, &ev)) continue;
+        zb_sim_result r;
+        fill_result(ev, P, m, T, &r);
+        if (best_h < 0 || r.cost < best_cost - 1e-12) {
+            best = std::move(ev);
+            best_cost = r.cost;
+            best_h = h;
+        }
+    }
+    if (best_h < 0) return zb::fail(ZB_ERR_SCHEDULE, "no hyperparameter setting produced a schedule");
+    fill_result(best, P, m, T, result);
+    if (hyper) {
+        hyper[0] = best_h >> 1;
+        hyper[1] = best_h & 1;
+    }
+    if (out) *n_ops = emit_ops(best, P, out);
+    else if (n_ops) *n_ops = total;
     zb::clear_error();
     return ZB_OK;
 }

@@ -114,6 +114,9 @@ def _load():
         "zb_simulate_schedule": [C.c_int32, C.c_int32, C.c_int32, C.POINTER(zb_sim_times),
                                  C.POINTER(zb_op), C.POINTER(sz), C.POINTER(zb_sim_result)],
         "zb_selftest_wait_timeout": [C.c_uint64, vp],
+        "zb_auto_schedule": [C.c_int32, C.c_int32, C.POINTER(zb_sim_times), C.c_double, C.c_double,
+                             C.POINTER(zb_op), C.POINTER(sz), C.POINTER(zb_sim_result),
+                             C.POINTER(C.c_int32)],
         "zb_grad_stats": [C.POINTER(vp), C.POINTER(C.c_uint64), C.c_int32, vp, vp, sz, vp],
         "zb_sync_status": [vp],
     }
@@ -247,6 +250,20 @@ def zb_grad_stats(bufs, counts, out, scratch, scratch_bytes, stream=None):
     cnt = (C.c_uint64 * len(bufs))(*[int(c) for c in counts])
     _check(LIB.zb_grad_stats(arr, cnt, len(bufs), _ptr(out), _ptr(scratch), scratch_bytes,
                              _stream(stream)), "zb_grad_stats")
+
+
+def zb_auto_schedule(P: int, m: int, t_f: float, t_b: float, t_w: float, t_comm: float,
+                     mem_limit: float, mw_ratio: float = 0.5):
+    """Heuristic schedule: returns (result, ops, (h1, h2))."""
+    t = zb_sim_times(t_f, t_b, t_w, t_comm)
+    res = zb_sim_result()
+    n = C.c_size_t(0)
+    _check(LIB.zb_make_schedule(SCHED_IDS["ZBH1"], P, m, None, C.byref(n)), "zb_make_schedule")
+    arr = (zb_op * n.value)()
+    hyper = (C.c_int32 * 2)()
+    _check(LIB.zb_auto_schedule(P, m, C.byref(t), mem_limit, mw_ratio, arr, C.byref(n), C.byref(res),
+                                hyper), "zb_auto_schedule")
+    return res, ops_tuples(arr, n.value), (hyper[0], hyper[1])
 
 
 def zb_selftest_wait_timeout(limit_ns: int, stream=None):

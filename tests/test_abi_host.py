@@ -193,3 +193,41 @@ def test_simulator_rejects_bad_times(zb):
         with pytest.raises(zb.ZBError) as e:
             zb.zb_simulate_schedule("ZBH1", 4, 8, *bad)
         assert e.value.status == zb.ZB_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("P,m", [(2, 4), (4, 8), (4, 12), (8, 24), (3, 7)])
+@pytest.mark.parametrize("limit_x", [1, 2])
+def test_auto_scheduler_matches_oracle(zb, P, m, limit_x):
+    import random
+    rnd = random.Random(P * 31 + m * 7 + limit_x)
+    cases = [(1.0, 1.0, 1.0, 0.0)]
+    for _ in range(3):
+        cases.append((rnd.randint(4, 16) / 8, rnd.randint(4, 16) / 8, rnd.randint(2, 12) / 8,
+                      rnd.randint(0, 3) / 16))
+    for tf, tb, tw, tc in cases:
+        for mw in (0.5, 0.375):
+            t = S.Times(tf, tb, tw, tc)
+            ev, ref_ops, ref_h = S.auto_schedule_search(P, m, t, limit_x * P, mw)
+            res, ops, hyper = zb.zb_auto_schedule(P, m, tf, tb, tw, tc, limit_x * P, mw)
+            assert ops == ref_ops
+            assert hyper == ref_h
+            assert res.cost == S.cost(ev, P)
+
+
+def test_auto_scheduler_reproduces_the_printed_zb1p_bubble(zb):
+    with open(os.path.join(ROOT, "tests", "golden", "table5_zb1p.txt")) as fh:
+        row = [ln.split() for ln in fh if ln.strip() and not ln.startswith("#")][0]
+    P, m = int(row[0]), int(row[1])
+    tf, tb, tw, tc, pct = (float(x) for x in row[2:])
+    res, ops, _ = zb.zb_auto_schedule(P, m, tf, tb, tw, tc, P, 0.366)
+    assert round(100 * res.bubble_rate, 2) == pct
+    assert S.validate_ops(ops, P, m)
+
+
+def test_auto_scheduler_rejects_bad_budget(zb):
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_auto_schedule(4, 8, 1, 1, 1, 0, 0.5)
+    assert e.value.status == zb.ZB_ERR_BUDGET
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_auto_schedule(4, 8, 1, 1, 1, 0, 4, 1.5)
+    assert e.value.status == zb.ZB_ERR_INVALID_ARG

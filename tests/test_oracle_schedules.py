@@ -225,3 +225,44 @@ def test_comm_time_delays_dependents():
         for d in e.deps:
             gap = t.comm if d[1] != e.stage else 0.0
             assert e.start >= ends[d] + gap - 1e-12
+
+
+# ---------------------------------------------------------------- ZB-1p / ZB-2p
+def _table5():
+    P, m, tf, tb, tw, tc, pct = _rows("table5_zb1p.txt")[0]
+    return int(P), int(m), S.Times(float(tf), float(tb), float(tw), float(tc)), float(pct)
+
+
+@pytest.mark.parametrize("mw", [0.366, 0.5, 0.9])
+def test_zb1p_reproduces_the_printed_bubble(mw):
+    P, m, t, pct = _table5()
+    ev, ops, _ = S.auto_schedule_search(P, m, t, P, mw)
+    assert S.validate_ops(ops, P, m)
+    assert round(100 * S.bubble_rate(ev, P, m, t), 2) == pct
+    assert max(S.mem_peaks(ev, P, mw)) <= P + 1e-9
+
+
+@pytest.mark.parametrize("P,m", [(2, 4), (4, 8), (4, 24), (8, 16), (8, 24), (3, 9)])
+def test_zb1p_equals_zbh1_and_zb2p_equals_zbh2_at_equal_times(P, m):
+    # ZB-1p matches ZB-H1 under the 1F1B memory limit; with 2P M_B the
+    # heuristic reaches ZB-H2's zero bubble (m >= 2P-1 here).
+    t = S.Times()
+    for limit, kind in ((P, "ZBH1"), (2 * P, "ZBH2")):
+        ev, ops, _ = S.auto_schedule_search(P, m, t, limit, 0.5)
+        ref, _ = S.make_schedule(kind, P, m, t)
+        assert S.cost(ev, P) == S.cost(ref, P)
+        assert S.validate_ops(ops, P, m)
+        assert max(S.mem_peaks(ev, P, 0.5)) <= limit + 1e-9
+
+
+@pytest.mark.parametrize("times", [(18.522, 18.086, 9.337, 0.601), (11.347, 11.248, 8.132, 0.377),
+                                   (1.0, 1.2, 0.6, 0.0), (1.0, 2.0, 0.5, 0.1)])
+@pytest.mark.parametrize("P,m", [(4, 12), (8, 24)])
+def test_zb2p_bubble_below_zbh2(times, P, m):
+    t = S.Times(*times)
+    ev2, _, _ = S.auto_schedule_search(P, m, t, 2 * P, 0.5)
+    ev1, _, _ = S.auto_schedule_search(P, m, t, P, 0.5)
+    h2, _ = S.make_schedule("ZBH2", P, m, t)
+    assert S.bubble_rate(ev2, P, m, t) <= S.bubble_rate(h2, P, m, t) + 1e-12
+    assert S.bubble_rate(ev2, P, m, t) <= S.bubble_rate(ev1, P, m, t) + 1e-12
+    assert max(S.mem_peaks(ev2, P, 0.5)) <= 2 * P + 1e-9
