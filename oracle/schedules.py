@@ -578,7 +578,8 @@ def auto_schedule(P: int, m: int, t: Times, mem_limit: float, mw_ratio: float = 
         next F/B is at least T_W, or when idling the gap would make this
         stage's accumulated idle time the largest of all stages (the greedy
         "cumulative maximum bubble" rule); else it idles until the next pass
-        becomes ready.
+        becomes ready.  Idle time counts from a stage's first pass (a
+        stage's span, Eq. 3, starts there).
       * Cool-down: remaining W's run in ascending order.
     Returns the list of Events.
     """
@@ -665,19 +666,22 @@ def auto_schedule(P: int, m: int, t: Times, mem_limit: float, mw_ratio: float = 
                     or idle[s] + gap > max(idle) + eps):
                 run(s, "W", pending[s].popleft(), now)
             else:
-                idle[s] += gap
+                if nF[s] > 0:
+                    idle[s] += gap
                 t_free[s] = min(nxt)
         else:
             acted = False
             nxt = [x for x in (rb, rf if f_ok else None) if x is not None and x > now]
             if nxt:
-                idle[s] += min(nxt) - now
+                if nF[s] > 0:
+                    idle[s] += min(nxt) - now
                 t_free[s] = min(nxt)
             else:
                 later = [e for e in ends if e > now]
                 later += [t_free[o] for o in range(P) if o != s and has_work(o) and t_free[o] > now]
                 if later:
-                    idle[s] += min(later) - now
+                    if nF[s] > 0:
+                        idle[s] += min(later) - now
                     t_free[s] = min(later)
                 else:
                     waiting[s] = True

@@ -189,8 +189,8 @@ bool simulate(int kind, int P, int m, const PassTimes& T, std::vector<SimEvent>*
 //      h1 = 0 - not delaying that B;
 //   3. its oldest pending W if memory blocks the F, or the idle gap before
 //      the next F/B is at least T_W, or idling the gap would make this
-//      stage's accumulated idle time the largest of all stages, or only W
-//      remain;
+//      stage's accumulated idle time (counted from its first pass, where its
+//      Eq. 3 span starts) the largest of all stages, or only W remain;
 //   4. otherwise it idles until its next F/B can start.
 bool auto_simulate(int P, int m, const PassTimes& T, double limit, double r, int h1, int h2,
                    std::vector<SimEvent>* out) {
@@ -270,7 +270,7 @@ bool auto_simulate(int P, int m, const PassTimes& T, double limit, double r, int
                 wq[s].pop_front();
                 put(s, ZB_OP_W, j, now);
             } else {
-                idle[s] += gap;
+                if (nf[s] > 0) idle[s] += gap;  // idle counts from the stage's first pass
                 tfree[s] = next;
             }
         } else {
@@ -279,7 +279,7 @@ bool auto_simulate(int P, int m, const PassTimes& T, double limit, double r, int
             if (rb > now) next = rb;
             if (f_ok && rf > now && (next < 0 || rf < next)) next = rf;
             if (next >= 0) {
-                idle[s] += next - now;
+                if (nf[s] > 0) idle[s] += next - now;
                 tfree[s] = next;
             } else {
                 double later = NONE;
@@ -288,7 +288,7 @@ bool auto_simulate(int P, int m, const PassTimes& T, double limit, double r, int
                 for (int o = 0; o < P; ++o)
                     if (o != s && work(o) && tfree[o] > now && (later < 0 || tfree[o] < later)) later = tfree[o];
                 if (later >= 0) {
-                    idle[s] += later - now;
+                    if (nf[s] > 0) idle[s] += later - now;
                     tfree[s] = later;
                 } else {
                     parked[s] = 1;

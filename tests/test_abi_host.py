@@ -214,14 +214,14 @@ def test_auto_scheduler_matches_oracle(zb, P, m, limit_x):
             assert res.cost == S.cost(ev, P)
 
 
-def test_auto_scheduler_reproduces_the_printed_zb1p_bubble(zb):
-    with open(os.path.join(ROOT, "tests", "golden", "table5_zb1p.txt")) as fh:
-        row = [ln.split() for ln in fh if ln.strip() and not ln.startswith("#")][0]
-    P, m = int(row[0]), int(row[1])
-    tf, tb, tw, tc, pct = (float(x) for x in row[2:])
-    res, ops, _ = zb.zb_auto_schedule(P, m, tf, tb, tw, tc, P, 0.366)
-    assert round(100 * res.bubble_rate, 2) == pct
-    assert S.validate_ops(ops, P, m)
+def test_auto_scheduler_reproduces_printed_bubbles(zb):
+    from tests.test_oracle_schedules import table5_rows
+    for name, P, m, t, mw, limit, pct in table5_rows():
+        res, ops, _ = zb.zb_auto_schedule(P, m, t.F, t.B, t.W, t.comm, limit, mw)
+        assert abs(100 * res.bubble_rate - pct) <= 0.015
+        assert S.validate_ops(ops, P, m)
+        ev, ref_ops, _ = S.auto_schedule_search(P, m, t, limit, mw)
+        assert ops == ref_ops
 
 
 def test_auto_scheduler_rejects_bad_budget(zb):
