@@ -316,6 +316,63 @@ def run_sweep(args):
     return 0
 
 
+def measure_post_validated_adamw(zb, h, f, dev, stream, peaks, steps=5, warmup=3):
+    """Post-update validation step of two pipeline stages, each holding one
+    h x f block's weights (W1 and W2, fp32 master copies with AdamW moments and
+    a bf16 weight copy).  max_norm sits between stage 0's partial gradient
+    norm and the global one, so stage 0 steps, rolls back and steps again:
+    the protocol's worst case.  HBM-bound: 30 bytes per element per pass
+    (read theta, m, v, g; write theta, m, v, bf16 theta)."""
+    import torch
+    P = 2
+    gen = torch.Generator(device=dev).manual_seed(77)
+    n = h * f
+    stages, tensors = [], []
+    for s in range(P):
+        st = []
+        for _ in range(2):
+            th = torch.randn(n, device=dev, generator=gen) * 0.02
+            d = {"theta": th, "m": torch.zeros_like(th), "v": torch.zeros_like(th),
+                 "grad": torch.randn(n, device=dev, generator=gen) * (1.0 + s),
+                 "weight_bf16": th.to(torch.bfloat16), "stage": s}
+            st.append(d)
+            tensors.append(d)
+        stages.append(st)
+    nbytes = zb.zb_grad_stats_scratch_bytes()
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    states = []
+    for st in stages:
+        o = torch.zeros(2, dtype=torch.float64, device=dev)
+        zb.zb_grad_stats([d["grad"] for d in st], [n, n], o, scratch, nbytes, stream)
+        torch.cuda.synchronize()
+        states.append(o)
+    sq = [float(o[0]) for o in states]
+    c = (sq[0] * (sq[0] + sq[1])) ** 0.25  # geometric mean of the two partial norms
+    dec = torch.empty(P * 40, dtype=torch.uint8, device=dev)
+    hp = zb.make_adamw(max_norm=c, step=10)
+    for _ in range(warmup):
+        zb.zb_post_validated_adamw(P, states, tensors, hp, dec, stream)
+    torch.cuda.synchronize()
+    rolled = [d["rolled_back"] for d in zb.decisions_from_bytes(dec.cpu().numpy().tobytes(), P)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        zb.zb_post_validated_adamw(P, states, tensors, hp, dec, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    zb.zb_sync_status(stream)
+    ms = e0.elapsed_time(e1) / steps
+    elems = 2 * n * P + 2 * n * sum(rolled)
+    algo = 30.0 * elems
+    gbs = algo / (ms / 1e3) / 1e9
+    return {"workload": f"post-validated AdamW, {P} stages x (W1, W2) of h={h} f={f} "
+                        f"({2 * n / 1e6:.0f}M fp32 parameters per stage), stage 0 rolls back",
+            "ms": ms, "rolled_back": rolled, "algorithmic_bytes": algo,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"]},
+            "launches_per_step": 3}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -325,6 +382,8 @@ def main():
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="c4")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-optimizer", action="store_true",
+                    help="skip the post-validated AdamW measurement (after the timed step)")
     ap.add_argument("--sweep", action="store_true",
                     help="per-pass kernel sweep (one JSON line per pass and point)")
     ap.add_argument("--sweep-points", default="",
@@ -510,6 +569,10 @@ def main():
     e2e_s = reduce_max(time.perf_counter() - t0, dev, ws)
     e2e_value = job_rate(step_flops, args.e2e_steps, ws, e2e_s) / 1e12
 
+    optimizer = None
+    if not args.no_optimizer:
+        optimizer = measure_post_validated_adamw(zb, h, f, dev, stream, _peaks())
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tokens = 1024
@@ -544,6 +607,7 @@ def main():
                     "timing": "host wall clock around synchronised steps; uploads and downloads "
                               "double-buffered on their own streams"},
             "projection": projection,
+            "optimizer": optimizer,
             "gpu_launches": sums["gemm_launches"],
             "clocks": clk,
         }

@@ -295,6 +295,81 @@ zb_status zb_grad_stats(const float* const* bufs, const uint64_t* counts, int32_
                         double* out, void* scratch, size_t scratch_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Post-update validation: staged reduce, optimistic AdamW step, rollback    */
+/* ------------------------------------------------------------------------ */
+
+/* One fp32 tensor of the optimizer: master weights theta, first and second
+ * moments m and v, and its gradient (for example a stage's dW1 after the
+ * schedule ran), all `count` floats, device memory, 16-byte aligned.
+ * weight_bf16, if not NULL, receives bf16(theta) (round to nearest even)
+ * wherever theta is written: the copy the F/B passes read.  `stage` names the
+ * pipeline stage whose decision applies.  reserved must be 0. */
+typedef struct zb_opt_tensor {
+    float* theta;
+    float* m;
+    float* v;
+    const float* grad;
+    void* weight_bf16;
+    uint64_t count;
+    int32_t stage;
+    int32_t reserved;
+} zb_opt_tensor;
+
+/* AdamW hyperparameters for update number `step` (>= 1):
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   theta -= lr wd theta + lr (m / (1-b1^step)) / (sqrt(v / (1-b2^step)) + eps)
+ * with g = clip * grad.  max_norm > 0 enables clipping by the global gradient
+ * norm (clip = max_norm / ||g|| when ||g|| > max_norm, else 1); 0 disables it.
+ * Requires 0 < beta1, beta2 < 1, eps > 0, wd >= 0, lr >= 0, lr*wd < 1. */
+typedef struct zb_adamw_params {
+    float lr, beta1, beta2, eps, weight_decay, max_norm;
+    int32_t step;
+    int32_t reserved; /* must be 0 */
+} zb_adamw_params;
+
+/* Per-stage record of one post-validated step (device memory, written by
+ * zb_post_validated_adamw).  norm_sq_partial is the staged-reduce state the
+ * stage stepped with (sum of squares of stages 0..s), norm_sq_global that of
+ * all stages; scale_* are the clip factors, skip_* are 1 when a NaN/Inf was
+ * seen (no update); rolled_back is 1 when the optimistic decision differed
+ * from the global one and the stage inverted and redid its step. */
+typedef struct zb_stage_decision {
+    double norm_sq_partial;
+    double norm_sq_global;
+    float scale_used;
+    float scale_global;
+    int32_t skip_used;
+    int32_t skip_global;
+    int32_t rolled_back;
+    int32_t reserved;
+} zb_stage_decision;
+
+/* One optimizer step of P stages with post-update validation, after "Zero
+ * Bubble Pipeline Parallelism" (paper-graph-ui summary, §4 "The Optimizer
+ * Synchronization Bypass" and "Why rollback is feasible"):
+ *   1. staged reduce: stage s's partial state is the sum of the local states
+ *      (sum of squares, NaN/Inf count) of stages 0..s; stage P-1's is global;
+ *   2. optimistic step: each stage runs AdamW with its partial clip factor,
+ *      or leaves its tensors untouched if its partial state saw a NaN/Inf;
+ *   3. validation: a stage whose clip factor or skip decision differs from
+ *      the global one inverts its step (the algebraic inverse of the update
+ *      above, given the same gradient) and applies the global decision.
+ * stage_state: host array of P device pointers, each to double[2] = {sum of
+ * squares, NaN/Inf count} of that stage's gradients (what zb_grad_stats and
+ * the executor's OPT marker write).  tensors: host array of n_tensors
+ * descriptors.  decisions: device array of P records (the report).
+ * All decisions are made on the device: the call enqueues work on `stream`
+ * (three kernels per 64 tensors at most) and never waits.  The result equals
+ * the synchronous step (global state first, then one update per stage) up to
+ * fp32 rounding of the inverse.  Errors: ZB_ERR_SHAPE (P outside [1, 64],
+ * n_tensors < 0), ZB_ERR_INVALID_ARG (NULL, bad stage index or
+ * hyperparameters), ZB_ERR_ALIGN; nothing is enqueued on error. */
+zb_status zb_post_validated_adamw(int32_t P, const double* const* stage_state,
+                                  const zb_opt_tensor* tensors, int32_t n_tensors,
+                                  const zb_adamw_params* hp, zb_stage_decision* decisions,
+                                  void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status                                                                   */
 /* ------------------------------------------------------------------------ */
 

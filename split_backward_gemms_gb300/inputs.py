@@ -68,3 +68,24 @@ def pipeline_draws(P: int, m: int, M: int, h: int, f: int, *, seed: int = 0,
 def matrix(seed: int, shape, std: float = 1.0) -> np.ndarray:
     """One seeded fp32 N(0, std^2) matrix (standalone kernel cases)."""
     return normal(np.random.default_rng(seed), shape, std)
+
+
+def optimizer_draws(sizes_per_stage, *, seed: int = 0, grad_std=None, theta_std: float = 0.02):
+    """Optimizer state for P stages: per stage a list of (theta, m, v, grad)
+    fp32 arrays of the given sizes.  theta ~ N(0, theta_std^2), m ~ N(0, 1e-4),
+    v = (N(0, 1e-2))^2 (a second moment, so non-negative), grad ~ N(0,
+    grad_std[s]^2) (1 for every stage by default).  Draw order: stage by
+    stage, tensor by tensor, theta, m, v, grad."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for s, sizes in enumerate(sizes_per_stage):
+        gs = 1.0 if grad_std is None else float(grad_std[s])
+        st = []
+        for n in sizes:
+            theta = normal(rng, (n,), theta_std)
+            m = normal(rng, (n,), 1e-2)
+            v = np.square(normal(rng, (n,), 1e-1))
+            g = normal(rng, (n,), gs)
+            st.append((theta, m, v, g))
+        out.append(st)
+    return out

@@ -83,6 +83,24 @@ class zb_sim_result(C.Structure):
                 ("peak_live_microbatches", C.c_uint32), ("peak_live_stage0", C.c_uint32)]
 
 
+class zb_opt_tensor(C.Structure):
+    _fields_ = [("theta", C.c_void_p), ("m", C.c_void_p), ("v", C.c_void_p), ("grad", C.c_void_p),
+                ("weight_bf16", C.c_void_p), ("count", C.c_uint64), ("stage", C.c_int32),
+                ("reserved", C.c_int32)]
+
+
+class zb_adamw_params(C.Structure):
+    _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("weight_decay", C.c_float), ("max_norm", C.c_float), ("step", C.c_int32),
+                ("reserved", C.c_int32)]
+
+
+class zb_stage_decision(C.Structure):
+    _fields_ = [("norm_sq_partial", C.c_double), ("norm_sq_global", C.c_double),
+                ("scale_used", C.c_float), ("scale_global", C.c_float), ("skip_used", C.c_int32),
+                ("skip_global", C.c_int32), ("rolled_back", C.c_int32), ("reserved", C.c_int32)]
+
+
 class ZBError(RuntimeError):
     def __init__(self, status: int, where: str, msg: str):
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}")
@@ -119,6 +137,8 @@ def _load():
                              C.POINTER(C.c_int32)],
         "zb_grad_stats": [C.POINTER(vp), C.POINTER(C.c_uint64), C.c_int32, vp, vp, sz, vp],
         "zb_sync_status": [vp],
+        "zb_post_validated_adamw": [C.c_int32, C.POINTER(vp), C.POINTER(zb_opt_tensor), C.c_int32,
+                                    C.POINTER(zb_adamw_params), vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -250,6 +270,37 @@ def zb_grad_stats(bufs, counts, out, scratch, scratch_bytes, stream=None):
     cnt = (C.c_uint64 * len(bufs))(*[int(c) for c in counts])
     _check(LIB.zb_grad_stats(arr, cnt, len(bufs), _ptr(out), _ptr(scratch), scratch_bytes,
                              _stream(stream)), "zb_grad_stats")
+
+
+def make_adamw(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, max_norm=0.0,
+               step=1) -> zb_adamw_params:
+    return zb_adamw_params(lr, beta1, beta2, eps, weight_decay, max_norm, int(step), 0)
+
+
+def zb_post_validated_adamw(P: int, stage_state, tensors, hp, decisions, stream=None):
+    """One post-validated AdamW step of P stages.
+
+    stage_state: P device pointers (tensors) to double[2] gradient states;
+    tensors: sequence of dicts with theta, m, v, grad, weight_bf16 (or None),
+    stage (count defaults to theta.numel()); decisions: device buffer of P
+    zb_stage_decision records (40 bytes each)."""
+    st = (C.c_void_p * P)(*[_ptr(x) for x in stage_state])
+    arr = (zb_opt_tensor * max(len(tensors), 1))()
+    for i, t in enumerate(tensors):
+        count = t.get("count")
+        if count is None:
+            count = t["theta"].numel()
+        arr[i] = zb_opt_tensor(_ptr(t["theta"]), _ptr(t["m"]), _ptr(t["v"]), _ptr(t["grad"]),
+                               _ptr(t.get("weight_bf16")), int(count), int(t["stage"]), 0)
+    _check(LIB.zb_post_validated_adamw(P, st, arr, len(tensors), C.byref(hp), _ptr(decisions),
+                                       _stream(stream)), "zb_post_validated_adamw")
+
+
+def decisions_from_bytes(raw: bytes, P: int):
+    """Decode P zb_stage_decision records copied back from the device."""
+    recs = (zb_stage_decision * P).from_buffer_copy(raw[:P * C.sizeof(zb_stage_decision)])
+    return [{name: getattr(r, name) for name, _ in zb_stage_decision._fields_ if name != "reserved"}
+            for r in recs]
 
 
 def zb_auto_schedule(P: int, m: int, t_f: float, t_b: float, t_w: float, t_comm: float,

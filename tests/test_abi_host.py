@@ -231,3 +231,73 @@ def test_auto_scheduler_rejects_bad_budget(zb):
     with pytest.raises(zb.ZBError) as e:
         zb.zb_auto_schedule(4, 8, 1, 1, 1, 0, 4, 1.5)
     assert e.value.status == zb.ZB_ERR_INVALID_ARG
+
+
+ABI_STRUCTS = ["zb_block", "zb_op", "zb_sim_times", "zb_sim_result", "zb_pipeline",
+               "zb_stage_params", "zb_run_stats", "zb_opt_tensor", "zb_adamw_params",
+               "zb_stage_decision"]
+
+
+def test_ctypes_layout_matches_header(zb, tmp_path):
+    """Every struct of the binding has the C compiler's size and field offsets."""
+    import ctypes
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "zb.h"', "int main(void) {"]
+    for name in ABI_STRUCTS:
+        cls = getattr(zb, name)
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {}
+    for ln in out:
+        if ln:
+            n, f, v = ln.split()
+            got[(n, f)] = int(v)
+    for name in ABI_STRUCTS:
+        cls = getattr(zb, name)
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert got[(name, field)] == getattr(cls, field).offset, (name, field)
+
+
+def test_post_validated_adamw_argument_errors(zb):
+    """Argument checks run before anything is enqueued (fake, never dereferenced pointers)."""
+    fake = 1 << 20
+    st = [fake + 8 * i for i in range(2)]
+    dec = fake + 4096
+    t = dict(theta=fake, m=fake + 256, v=fake + 512, grad=fake + 768, weight_bf16=None,
+             count=16, stage=0)
+
+    def code(P=2, states=st, tensors=(t,), hp=None, decisions=dec):
+        hp = zb.make_adamw(max_norm=1.0) if hp is None else hp
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_post_validated_adamw(P, states, list(tensors), hp, decisions)
+        return e.value.status
+
+    assert code(P=0, states=[]) == zb.ZB_ERR_SHAPE
+    assert code(P=65, states=[fake] * 65) == zb.ZB_ERR_SHAPE
+    assert code(decisions=None) == zb.ZB_ERR_INVALID_ARG
+    assert code(decisions=dec + 4) == zb.ZB_ERR_ALIGN
+    assert code(states=[fake, None]) == zb.ZB_ERR_INVALID_ARG
+    assert code(states=[fake, fake + 4]) == zb.ZB_ERR_ALIGN
+    assert code(tensors=[dict(t, stage=2)]) == zb.ZB_ERR_INVALID_ARG
+    assert code(tensors=[dict(t, theta=fake + 4)]) == zb.ZB_ERR_ALIGN
+    assert code(tensors=[dict(t, weight_bf16=fake + 2)]) == zb.ZB_ERR_ALIGN
+    assert code(tensors=[dict(t, grad=None)]) == zb.ZB_ERR_INVALID_ARG
+    for bad in (dict(step=0), dict(beta1=1.0), dict(beta2=0.0), dict(eps=0.0), dict(lr=-1.0),
+                dict(weight_decay=-0.1), dict(lr=1.0, weight_decay=1.0), dict(max_norm=-1.0)):
+        assert code(hp=zb.make_adamw(**bad)) == zb.ZB_ERR_INVALID_ARG, bad
+    hp = zb.make_adamw()
+    hp.reserved = 1
+    assert code(hp=hp) == zb.ZB_ERR_INVALID_ARG
