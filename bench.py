@@ -506,6 +506,16 @@ def main():
             res, _, _ = zb.zb_auto_schedule(Pl, m, tfb[0], tfb[1], tfb[2], 0.0, limit, 1.0)
             projection["bubble_rate"][name] = res.bubble_rate
             projection["pipeline_tokens_per_s"][name] = m * M / (res.cost / 1e3)
+        # two chunks per stage (each half the stage's layers): cyclic 1F1B-I
+        # and the V-shaped ZB-V; peak in M_B = peak chunk activations / 2
+        projection["peak_M_B"] = {}
+        for name, kind in (("1F1B-I", "1F1B-I"), ("ZB-V", "ZBV")):
+            if kind == "1F1B-I" and m % Pl:
+                continue
+            res, _ = zb.zb_simulate_interleaved_schedule(kind, Pl, 2, m, tfb[0], tfb[1], tfb[2], 0.0)
+            projection["bubble_rate"][name] = res.bubble_rate
+            projection["pipeline_tokens_per_s"][name] = m * M / (res.cost / 1e3)
+            projection["peak_M_B"][name] = res.peak_live_microbatches / 2
 
     # ------------------------------------------------------------- end to end
     # Through the public API with host buffers: every step uploads its inputs

@@ -119,15 +119,29 @@ typedef enum zb_op_kind {
     ZB_OP_OPT = 4  /* optimizer marker of a stage: after all its W, no-op    */
 } zb_op_kind;
 
-/* Pass id (i, j, c) of the summary's ILP formulation (Appendix G). */
+/* Pass id (i, j, c) of the summary's ILP formulation (Appendix G), plus the
+ * model chunk for multi-chunk orderings. */
 typedef struct zb_op {
-    uint8_t kind;    /* zb_op_kind */
-    uint8_t pad;     /* must be 0  */
-    uint16_t stage;  /* 0 .. P-1   */
-    uint32_t micro;  /* 0 .. m-1 (ignored for OPT) */
+    uint8_t kind;    /* zb_op_kind                                        */
+    uint8_t chunk;   /* 0 .. chunks-1 (0 for one-chunk orderings)          */
+    uint16_t stage;  /* 0 .. P-1: the pipeline stage (device) running it   */
+    uint32_t micro;  /* 0 .. m-1 (ignored for OPT)                         */
 } zb_op;
 
-typedef enum zb_schedule_kind { ZB_SCHED_1F1B = 0, ZB_SCHED_ZBH1 = 1, ZB_SCHED_ZBH2 = 2 } zb_schedule_kind;
+typedef enum zb_schedule_kind {
+    ZB_SCHED_1F1B = 0, ZB_SCHED_ZBH1 = 1, ZB_SCHED_ZBH2 = 2,
+    ZB_SCHED_1F1B_I = 3, /* interleaved 1F1B: v chunks per stage, cyclic    */
+    ZB_SCHED_ZBV = 4     /* ZB-V: two chunks per stage, V-shaped            */
+} zb_schedule_kind;
+
+/* Model-chunk layouts of multi-chunk pipelines.  With v chunks per stage the
+ * model is a chain of L = v P virtual stages k = 0 .. L-1 (forward order):
+ *   CYCLIC: chunk c of stage s is k = c P + s (stage i holds chunks i, p+i,
+ *           2p+i, ...: "Pipeline Schedules: GPipe, 1F1B and Zero Bubble",
+ *           section "Interleaved stages");
+ *   V:      v = 2, chunk 0 of stage s is k = s and chunk 1 is k = 2P-1-s
+ *           (stage i holds chunks i and 2p-i+1: summary §6 "ZB-V"). */
+typedef enum zb_layout { ZB_LAYOUT_CYCLIC = 0, ZB_LAYOUT_V = 1 } zb_layout;
 
 /* Generate the one-GPU replay list of a handcrafted ordering for P stages and
  * m microbatches at equal pass times (T_F = T_B = T_W, no communication):
@@ -140,6 +154,34 @@ typedef enum zb_schedule_kind { ZB_SCHED_1F1B = 0, ZB_SCHED_ZBH1 = 1, ZB_SCHED_Z
  * holds its capacity on entry and the length on return (ZB_ERR_INVALID_ARG
  * if too small).  Host only, no device work. */
 zb_status zb_make_schedule(int32_t kind, int32_t P, int32_t m, zb_op* out, size_t* n_ops);
+
+/* Multi-chunk orderings for P stages, v chunks per stage, m microbatches.
+ * A chunk pass takes T/v of the stage's per-microbatch pass time T, so the
+ * ideal per-stage time stays m (T_F + T_B + T_W).
+ *   ZB_SCHED_1F1B_I (cyclic layout, v >= 2, m a multiple of P): the
+ *     interleaved 1F1B the pages cite ("Pipeline Schedules", "Interleaved
+ *     stages"; summary §5 "1F1B-I"): stage s runs min(2(P-1-s) + (v-1) P, vm)
+ *     warm-up chunk forwards, then alternates a forward with a fused backward
+ *     BW, then drains; its i-th forward is chunk (i mod vP) div P of
+ *     microbatch (i div vP) P + i mod P, its i-th backward the same
+ *     microbatch of chunk v-1-(that chunk).  At equal times its bubble is
+ *     (P-1)/(vm+P-1).
+ *   ZB_SCHED_ZBV (V layout, v = 2): on a simulated timeline a free stage
+ *     takes, among its passes that can start earliest, a B before an F before
+ *     a W (oldest microbatch first, then the later virtual stage); an F only
+ *     while it holds fewer than 2P live chunk activations (P M_B: summary §6),
+ *     a chunk-0 forward only while it holds fewer than 2P-1; a W from its
+ *     pending ones, oldest first.  Peak: exactly P M_B per stage.
+ * Ops carry (stage, chunk); OPT(stage, chunk) follows the last op of each
+ * virtual stage; list order = (simulated start, stage).
+ * zb_make_interleaved_schedule uses equal times; the simulate variant takes
+ * measured ones (T_comm added between chunks on different stages) and fills
+ * `result`, whose peak_live fields then count chunk activations (M_B / v
+ * each).  out / n_ops as for zb_make_schedule.  Host only.  Errors:
+ * ZB_ERR_INVALID_ARG (kind, v, times), ZB_ERR_SHAPE (P, m, or m not a
+ * multiple of P for 1F1B-I). */
+zb_status zb_make_interleaved_schedule(int32_t kind, int32_t P, int32_t v, int32_t m, zb_op* out,
+                                       size_t* n_ops);
 
 /* Pass times for zb_simulate_schedule (any one unit, e.g. ms). */
 typedef struct zb_sim_times { double t_f, t_b, t_w, t_comm; } zb_sim_times;
@@ -163,6 +205,10 @@ typedef struct zb_sim_result {
 zb_status zb_simulate_schedule(int32_t kind, int32_t P, int32_t m, const zb_sim_times* times,
                                zb_op* out, size_t* n_ops, zb_sim_result* result);
 
+zb_status zb_simulate_interleaved_schedule(int32_t kind, int32_t P, int32_t v, int32_t m,
+                                           const zb_sim_times* times, zb_op* out, size_t* n_ops,
+                                           zb_sim_result* result);
+
 /* Heuristic automatic scheduler for measured pass times (summary §3 "The
  * Heuristic Scheduling Algorithm" with "The Memory Model"): memory counted in
  * units of M_B per stage (F +1, B + r - 1, W -r with r = mw_ratio = M_W/M_B),
@@ -182,7 +228,7 @@ zb_status zb_auto_schedule(int32_t P, int32_t m, const zb_sim_times* times, doub
                            int32_t* hyper);
 
 typedef struct zb_pipeline {
-    int32_t P;                 /* stages                                     */
+    int32_t P;                 /* stages (devices of the pipeline)           */
     int32_t m;                 /* microbatches                               */
     zb_block blk;              /* every stage has the same block shape; for
                                   P > 1 the block must map [M,h] to [M,h]    */
@@ -204,8 +250,15 @@ typedef struct zb_pipeline {
                                   stage's W still run in list order on its
                                   stream, so results are bit-identical to the
                                   serial replay.  The call forks from and
-                                  joins back into `stream`.                  */
-    int32_t reserved;          /* must be 0                                  */
+                                  joins back into `stream`.  With chunks,
+                                  lanes follow the stage (device) of an op.  */
+    int32_t chunks;            /* model chunks per stage: 0 or 1 = one; v > 1
+                                  makes the model a chain of L = v P virtual
+                                  stages placed by `layout`; every per-stage
+                                  array (zb_stage_params, OPT, the arena) is
+                                  then per virtual stage, in chain order     */
+    int32_t layout;            /* zb_layout (V requires chunks = 2); ignored
+                                  for one chunk                              */
 } zb_pipeline;
 
 typedef struct zb_stage_params {
@@ -238,17 +291,25 @@ typedef struct zb_run_stats {
  * saves dH; W frees X, A, dH and dY; a stage's Y is the next stage's X and a
  * stage's dX the previous stage's dY (pointer hand-off inside the arena).
  * The arena also holds zb_grad_stats scratch for each stage (at its end).
+ * With chunks > 1 every op's (stage, chunk) names the virtual stage of the
+ * pipeline's layout and the rules apply to the chain of virtual stages
+ * (ZB_ERR_SCHEDULE for a chunk >= chunks or a stage >= P; ZB_ERR_INVALID_ARG
+ * for a layout other than CYCLIC / V, or V with chunks != 2).
  * Returns the arena size (*bytes) and the ledger peak (*peak_live_bytes,
  * may be NULL).  Host only. */
 zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_op* ops, size_t n_ops,
                                      size_t* bytes, size_t* peak_live_bytes);
 
 /* Replay an op list over P stages on one GPU.
- *   stages[P]       weights and fp32 gradient buffers per stage;
- *   X0[m]           stage-0 inputs [M,h] (device pointers);
- *   dY_last[m]      output gradients entering stage P-1 [M,h];
- *   dX0_out[m]      optional (array or entries may be NULL): stage-0 dX;
- *   Y_last_out[m]   optional: stage P-1 outputs Y;
+ *   stages[L]       weights and fp32 gradient buffers per (virtual) stage,
+ *                   in chain order; L = P, or chunks * P with chunks > 1;
+ *   X0[m]           inputs of the first (virtual) stage [M,h] (device
+ *                   pointers);
+ *   dY_last[m]      output gradients entering the last (virtual) stage
+ *                   [M,h];
+ *   dX0_out[m]      optional (array or entries may be NULL): the first
+ *                   stage's dX;
+ *   Y_last_out[m]   optional: the last stage's outputs Y;
  *   workspace       device buffer of >= zb_schedule_workspace_size bytes,
  *                   256-byte aligned;
  *   stats           optional (NULL to skip).

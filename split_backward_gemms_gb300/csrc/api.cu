@@ -314,9 +314,19 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     const zb_block& b = pl->blk;
     zb_status s = check_block(&b);
     if (s != ZB_OK) return s;
-    const int P = pl->P, m = pl->m;
-    if (P < 1 || m < 1) return fail(ZB_ERR_SHAPE, "P and m must be >= 1");
-    if (pl->reserved != 0 || pl->streams < 0) return fail(ZB_ERR_INVALID_ARG, "pipeline.streams < 0 or reserved != 0");
+    const int m = pl->m;
+    if (pl->P < 1 || m < 1) return fail(ZB_ERR_SHAPE, "P and m must be >= 1");
+    if (pl->streams < 0) return fail(ZB_ERR_INVALID_ARG, "pipeline.streams < 0");
+    // multi-chunk lists run on the chain of virtual stages; dev[i] is the
+    // stage (device) of op i, which picks its stream
+    std::vector<zb_op> vop;
+    std::vector<int> dev;
+    int P = 0;
+    s = virtualize_ops(*pl, ops, n_ops, &vop, &dev, &P);
+    if (s != ZB_OK) return s;
+    zb_pipeline chain = *pl;
+    chain.P = P;
+    chain.chunks = 1;
     if (P > 1 && b.act == ZB_ACT_NONE && b.f != b.h)
         return fail(ZB_ERR_SHAPE, "a multi-stage single-linear pipeline needs f == h");
     const bool mlp = b.act != ZB_ACT_NONE;
@@ -339,10 +349,10 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         if (Y_last_out && misaligned(Y_last_out[j])) return fail(ZB_ERR_ALIGN, "Y_last_out must be 16-byte aligned");
         if (dX0_out && misaligned(dX0_out[j])) return fail(ZB_ERR_ALIGN, "dX0_out must be 16-byte aligned");
     }
-    OpCheck c = validate_ops(ops, n_ops, P, m);
+    OpCheck c = validate_ops(vop.data(), n_ops, P, m);
     if (c.st != ZB_OK) return fail(c.st, c.msg);
     ArenaPlan plan;
-    s = plan_arena(*pl, ops, n_ops, has_y, has_dx, &plan);
+    s = plan_arena(chain, vop.data(), n_ops, has_y, has_dx, &plan);
     if (s != ZB_OK) return s;
     if (plan.workspace_bytes > 0) {
         if (!workspace) return fail(ZB_ERR_WORKSPACE, "workspace is NULL");
@@ -356,8 +366,9 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         return ws + static_cast<size_t>(plan.row_slots) * plan.row_bytes + static_cast<size_t>(slot) * plan.ffn_bytes;
     };
 
-    // Streams: stage s runs on lanes[s % ns]; lanes[0] is the caller's stream.
-    const int ns = std::max(1, std::min(std::min(pl->streams, P), 8));
+    // Streams: ops of stage (device) d run on lanes[d % ns]; lanes[0] is the
+    // caller's stream.
+    const int ns = std::max(1, std::min(std::min(pl->streams, pl->P), 8));
     std::vector<cudaStream_t> lanes(1, static_cast<cudaStream_t>(stream));
     std::vector<cudaEvent_t>* evs = nullptr;
     if (ns > 1) {
@@ -376,9 +387,9 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     // producer op of F(s,j) and of B/BW(s,j), for cross-stage waits
     std::vector<int> fwd_op(static_cast<size_t>(P) * m, -1), bwd_op(static_cast<size_t>(P) * m, -1);
     for (size_t i = 0; i < n_ops; ++i) {
-        const size_t key = static_cast<size_t>(ops[i].stage) * m + ops[i].micro;
-        if (ops[i].kind == ZB_OP_F) fwd_op[key] = static_cast<int>(i);
-        else if (ops[i].kind == ZB_OP_B || ops[i].kind == ZB_OP_BW) bwd_op[key] = static_cast<int>(i);
+        const size_t key = static_cast<size_t>(vop[i].stage) * m + vop[i].micro;
+        if (vop[i].kind == ZB_OP_F) fwd_op[key] = static_cast<int>(i);
+        else if (vop[i].kind == ZB_OP_B || vop[i].kind == ZB_OP_BW) bwd_op[key] = static_cast<int>(i);
     }
 
     Recorder rec;
@@ -391,10 +402,10 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     std::vector<char> w_started(P, 0);
 
     for (size_t i = 0; i < n_ops && s == ZB_OK; ++i) {
-        const zb_op& o = ops[i];
+        const zb_op& o = vop[i];  // stage = virtual stage of the chain
         const int st = o.stage, j = static_cast<int>(o.micro);
         const zb_stage_params& p = stages[st];
-        cudaStream_t lane = lanes[st % ns];
+        cudaStream_t lane = lanes[dev[i] % ns];
         void* lane_v = static_cast<void*>(lane);
         rec.st = lane;
         if (ns > 1 && o.kind != ZB_OP_OPT) {
@@ -404,7 +415,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
             if ((o.kind == ZB_OP_B || o.kind == ZB_OP_BW) && st < P - 1)
                 deps.push_back(bwd_op[static_cast<size_t>(st + 1) * m + j]);
             for (int d : deps) {
-                if (d < 0 || lanes[ops[d].stage % ns] == lane) continue;
+                if (d < 0 || lanes[dev[d] % ns] == lane) continue;
                 cudaError_t e = cudaStreamWaitEvent(lane, (*evs)[d], 0);
                 if (e != cudaSuccess) {
                     s = fail(ZB_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(e));

@@ -355,7 +355,7 @@ OpCheck validate_ops(const zb_op* ops, size_t n, int P, int m) {
     std::vector<char> opt_done(P, 0);
     for (size_t i = 0; i < n; ++i) {
         const zb_op& o = ops[i];
-        if (o.kind > ZB_OP_OPT || o.pad != 0) return bad(ZB_ERR_SCHEDULE, "op " + std::to_string(i) + ": bad kind");
+        if (o.kind > ZB_OP_OPT || o.chunk != 0) return bad(ZB_ERR_SCHEDULE, "op " + std::to_string(i) + ": bad kind or chunk");
         if (o.stage >= P) return bad(ZB_ERR_SCHEDULE, "op " + std::to_string(i) + ": stage out of range " + name(o));
         if (o.kind != ZB_OP_OPT && o.micro >= static_cast<uint32_t>(m))
             return bad(ZB_ERR_SCHEDULE, "op " + std::to_string(i) + ": micro out of range " + name(o));
@@ -592,13 +592,21 @@ extern "C" zb_status zb_simulate_schedule(int32_t kind, int32_t P, int32_t m, co
 extern "C" zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_op* ops, size_t n_ops,
                                                 size_t* bytes, size_t* peak_live_bytes) {
     if (!pl || !bytes) return zb::fail(ZB_ERR_INVALID_ARG, "pipeline or bytes is NULL");
-    zb::OpCheck c = zb::validate_ops(ops, n_ops, pl->P, pl->m);
+    std::vector<zb_op> vops;
+    std::vector<int> dev;
+    int L = 0;
+    zb_status st = zb::virtualize_ops(*pl, ops, n_ops, &vops, &dev, &L);
+    if (st != ZB_OK) return st;
+    zb::OpCheck c = zb::validate_ops(vops.data(), n_ops, L, pl->m);
     if (c.st != ZB_OK) return zb::fail(c.st, c.msg);
-    if (pl->P > 1 && pl->blk.act == ZB_ACT_NONE && pl->blk.f != pl->blk.h)
+    if (L > 1 && pl->blk.act == ZB_ACT_NONE && pl->blk.f != pl->blk.h)
         return zb::fail(ZB_ERR_SHAPE, "a multi-stage single-linear pipeline needs f == h");
     zb::ArenaPlan plan;
+    zb_pipeline chain = *pl;  // the chain of virtual stages
+    chain.P = L;
+    chain.chunks = 1;
     // sizing assumes no caller output buffers (the largest arena)
-    zb_status st = zb::plan_arena(*pl, ops, n_ops, false, false, &plan);
+    st = zb::plan_arena(chain, vops.data(), n_ops, false, false, &plan);
     *bytes = plan.workspace_bytes;
     if (peak_live_bytes) *peak_live_bytes = plan.peak_live_bytes;
     if (st != ZB_OK) return st;

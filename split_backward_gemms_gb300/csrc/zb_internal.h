@@ -71,6 +71,14 @@ struct OpCheck {
 // Validate an op list against the replay rules.
 OpCheck validate_ops(const zb_op* ops, size_t n, int P, int m);
 
+// Map an op list of a (possibly multi-chunk) pipeline onto its chain of
+// virtual stages: vops[i] has stage = the virtual stage of (stage, chunk) and
+// chunk = 0; dev[i] = the op's stage (device); *L = chunks * P (P for one
+// chunk).  Checks the pipeline's chunks / layout and every op's stage and
+// chunk range.
+zb_status virtualize_ops(const zb_pipeline& pl, const zb_op* ops, size_t n, std::vector<zb_op>* vops,
+                         std::vector<int>* dev, int* L);
+
 // Arena plan: for every op, which slots its outputs occupy and which slots
 // it releases.  Two size classes: "row" buffers [M,h] and "ffn" buffers [M,f].
 enum BufKind : int { BUF_X = 0, BUF_H, BUF_A, BUF_DH, BUF_DY, BUF_COUNT };

@@ -42,8 +42,11 @@ ZB_ACT_GELU_TANH = 2
 
 ZB_OP_F, ZB_OP_B, ZB_OP_W, ZB_OP_BW, ZB_OP_OPT = range(5)
 OP_NAMES = ("F", "B", "W", "BW", "OPT")
-ZB_SCHED_1F1B, ZB_SCHED_ZBH1, ZB_SCHED_ZBH2 = range(3)
-SCHED_IDS = {"1F1B": ZB_SCHED_1F1B, "ZBH1": ZB_SCHED_ZBH1, "ZBH2": ZB_SCHED_ZBH2}
+ZB_SCHED_1F1B, ZB_SCHED_ZBH1, ZB_SCHED_ZBH2, ZB_SCHED_1F1B_I, ZB_SCHED_ZBV = range(5)
+SCHED_IDS = {"1F1B": ZB_SCHED_1F1B, "ZBH1": ZB_SCHED_ZBH1, "ZBH2": ZB_SCHED_ZBH2,
+             "1F1B-I": ZB_SCHED_1F1B_I, "ZBV": ZB_SCHED_ZBV}
+ZB_LAYOUT_CYCLIC, ZB_LAYOUT_V = range(2)
+LAYOUT_OF = {"1F1B-I": ZB_LAYOUT_CYCLIC, "ZBV": ZB_LAYOUT_V}
 
 
 # ---------------------------------------------------------------- structs
@@ -53,13 +56,13 @@ class zb_block(C.Structure):
 
 
 class zb_op(C.Structure):
-    _fields_ = [("kind", C.c_uint8), ("pad", C.c_uint8), ("stage", C.c_uint16), ("micro", C.c_uint32)]
+    _fields_ = [("kind", C.c_uint8), ("chunk", C.c_uint8), ("stage", C.c_uint16), ("micro", C.c_uint32)]
 
 
 class zb_pipeline(C.Structure):
     _fields_ = [("P", C.c_int32), ("m", C.c_int32), ("blk", zb_block),
                 ("mem_limit_bytes", C.c_uint64), ("zero_grads", C.c_int32), ("timing", C.c_int32),
-                ("streams", C.c_int32), ("reserved", C.c_int32)]
+                ("streams", C.c_int32), ("chunks", C.c_int32), ("layout", C.c_int32)]
 
 
 class zb_stage_params(C.Structure):
@@ -120,6 +123,11 @@ def _load():
         "zb_backward_input": [C.POINTER(zb_block), vp, vp, vp, vp, vp, vp, vp],
         "zb_backward_weight": [C.POINTER(zb_block), vp, vp, vp, vp, vp, vp, vp, vp, C.c_int, vp],
         "zb_make_schedule": [C.c_int32, C.c_int32, C.c_int32, C.POINTER(zb_op), C.POINTER(sz)],
+        "zb_make_interleaved_schedule": [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(zb_op),
+                                         C.POINTER(sz)],
+        "zb_simulate_interleaved_schedule": [C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                             C.POINTER(zb_sim_times), C.POINTER(zb_op), C.POINTER(sz),
+                                             C.POINTER(zb_sim_result)],
         "zb_schedule_workspace_size": [C.POINTER(zb_pipeline), C.POINTER(zb_op), sz, C.POINTER(sz),
                                        C.POINTER(sz)],
         "zb_run_stage_schedule": [C.POINTER(zb_pipeline), C.POINTER(zb_stage_params), C.POINTER(vp),
@@ -192,18 +200,24 @@ def make_block(M: int, h: int, f: int, dtype: int = ZB_DT_BF16, act: int = ZB_AC
 
 
 def ops_array(ops):
-    """(kind, stage, micro) tuples (kind as name or id) -> ctypes zb_op array."""
+    """(kind, stage, micro) or (kind, stage, chunk, micro) tuples (kind as name
+    or id) -> ctypes zb_op array."""
     arr = (zb_op * len(ops))()
-    for i, (k, s, j) in enumerate(ops):
+    for i, op in enumerate(ops):
+        k, s, c, j = op if len(op) == 4 else (op[0], op[1], 0, op[2])
         arr[i].kind = OP_NAMES.index(k) if isinstance(k, str) else int(k)
-        arr[i].pad = 0
+        arr[i].chunk = c
         arr[i].stage = s
         arr[i].micro = j
     return arr
 
 
-def ops_tuples(arr, n=None):
+def ops_tuples(arr, n=None, chunks=False):
+    """ctypes zb_op array -> (kind_name, stage, micro) tuples, or (kind_name,
+    stage, chunk, micro) with chunks=True."""
     n = len(arr) if n is None else n
+    if chunks:
+        return [(OP_NAMES[arr[i].kind], arr[i].stage, arr[i].chunk, arr[i].micro) for i in range(n)]
     return [(OP_NAMES[arr[i].kind], arr[i].stage, arr[i].micro) for i in range(n)]
 
 
@@ -258,6 +272,34 @@ def zb_simulate_schedule(kind, P: int, m: int, t_f: float, t_b: float, t_w: floa
     _check(LIB.zb_simulate_schedule(kid, P, m, C.byref(t), arr, C.byref(n), C.byref(res)),
            "zb_simulate_schedule")
     return res, ops_tuples(arr, n.value)
+
+
+def zb_make_interleaved_schedule(kind, P: int, v: int, m: int):
+    """Multi-chunk ordering ("1F1B-I" or "ZBV") as (kind_name, stage, chunk, micro)."""
+    kid = SCHED_IDS[kind] if isinstance(kind, str) else int(kind)
+    n = C.c_size_t(0)
+    _check(LIB.zb_make_interleaved_schedule(kid, P, v, m, None, C.byref(n)), "zb_make_interleaved_schedule")
+    arr = (zb_op * n.value)()
+    _check(LIB.zb_make_interleaved_schedule(kid, P, v, m, arr, C.byref(n)), "zb_make_interleaved_schedule")
+    return ops_tuples(arr, n.value, chunks=True)
+
+
+def zb_simulate_interleaved_schedule(kind, P: int, v: int, m: int, t_f: float, t_b: float, t_w: float,
+                                     t_comm: float = 0.0, want_ops: bool = False):
+    """Simulated multi-chunk ordering: (result, ops or None); peaks count chunk activations."""
+    kid = SCHED_IDS[kind] if isinstance(kind, str) else int(kind)
+    t = zb_sim_times(t_f, t_b, t_w, t_comm)
+    res = zb_sim_result()
+    if not want_ops:
+        _check(LIB.zb_simulate_interleaved_schedule(kid, P, v, m, C.byref(t), None, None, C.byref(res)),
+               "zb_simulate_interleaved_schedule")
+        return res, None
+    n = C.c_size_t(0)
+    _check(LIB.zb_make_interleaved_schedule(kid, P, v, m, None, C.byref(n)), "zb_make_interleaved_schedule")
+    arr = (zb_op * n.value)()
+    _check(LIB.zb_simulate_interleaved_schedule(kid, P, v, m, C.byref(t), arr, C.byref(n), C.byref(res)),
+           "zb_simulate_interleaved_schedule")
+    return res, ops_tuples(arr, n.value, chunks=True)
 
 
 def zb_grad_stats_scratch_bytes() -> int:
@@ -322,9 +364,11 @@ def zb_selftest_wait_timeout(limit_ns: int, stream=None):
 
 
 def make_pipeline(P, m, blk, mem_limit_bytes=0, zero_grads=True, timing=False,
-                  streams=1) -> zb_pipeline:
+                  streams=1, chunks=1, layout=ZB_LAYOUT_CYCLIC) -> zb_pipeline:
+    if isinstance(layout, str):
+        layout = LAYOUT_OF[layout]
     return zb_pipeline(P, m, blk, mem_limit_bytes, 1 if zero_grads else 0, 1 if timing else 0,
-                       int(streams), 0)
+                       int(streams), int(chunks), int(layout))
 
 
 def zb_schedule_workspace_size(pl, ops):

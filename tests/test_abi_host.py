@@ -301,3 +301,86 @@ def test_post_validated_adamw_argument_errors(zb):
     hp = zb.make_adamw()
     hp.reserved = 1
     assert code(hp=hp) == zb.ZB_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ multi-chunk orderings
+from oracle import interleaved as IL  # noqa: E402
+
+ILV_CASES = ([("ZBV", P, 2, m) for P in (1, 2, 3, 4, 8) for m in (1, 2 * P - 1, 2 * P, 3 * P)]
+             + [("1F1B-I", P, v, m) for P in (1, 2, 4, 8) for v in (2, 4) for m in (P, 2 * P, 3 * P)])
+
+
+@pytest.mark.parametrize("kind,P,v,m", ILV_CASES)
+def test_interleaved_generator_matches_oracle(zb, kind, P, v, m):
+    _, ref = IL.make_interleaved_schedule(kind, P, v, m)
+    assert zb.zb_make_interleaved_schedule(kind, P, v, m) == ref
+
+
+def test_interleaved_simulator_matches_oracle_at_random_times(zb):
+    import random
+    rng = random.Random(11)
+    for _ in range(60):
+        kind = rng.choice(["ZBV", "1F1B-I"])
+        P = rng.randint(1, 5)
+        v = 2 if kind == "ZBV" else rng.randint(2, 3)
+        m = rng.randint(1, 3 * P) if kind == "ZBV" else P * rng.randint(1, 3)
+        t = S.Times(rng.uniform(0.2, 3), rng.uniform(0.2, 3), rng.uniform(0.1, 3),
+                    rng.choice([0.0, rng.uniform(0, 1)]))
+        res, got = zb.zb_simulate_interleaved_schedule(kind, P, v, m, t.F, t.B, t.W, t.comm, want_ops=True)
+        ev, ref = IL.make_interleaved_schedule(kind, P, v, m, t)
+        assert got == ref
+        assert abs(res.bubble_rate - IL.bubble_rate(ev, P, m, t)) < 1e-12
+        assert res.peak_live_microbatches == max(IL.peak_live_chunks(ev, P))
+        assert res.peak_live_stage0 == IL.peak_live_chunks(ev, P)[0]
+
+
+def test_interleaved_argument_errors(zb):
+    def code(*a):
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_make_interleaved_schedule(*a)
+        return e.value.status
+    assert code("ZBV", 2, 3, 4) == zb.ZB_ERR_INVALID_ARG
+    assert code("1F1B-I", 2, 1, 4) == zb.ZB_ERR_INVALID_ARG
+    assert code("ZBH1", 2, 2, 4) == zb.ZB_ERR_INVALID_ARG
+    assert code("1F1B-I", 4, 2, 6) == zb.ZB_ERR_SHAPE
+    assert code("ZBV", 0, 2, 4) == zb.ZB_ERR_SHAPE
+
+
+@pytest.mark.parametrize("kind,P,v,m", [("ZBV", 2, 2, 4), ("ZBV", 4, 2, 8), ("1F1B-I", 2, 2, 4),
+                                        ("1F1B-I", 2, 3, 4)])
+def test_chunked_list_sizes_like_its_virtual_chain(zb, kind, P, v, m):
+    """A chunked replay is the replay of its chain of v P virtual stages."""
+    ops = zb.zb_make_interleaved_schedule(kind, P, v, m)
+    blk = zb.make_block(64, 32, 128)
+    pl = zb.make_pipeline(P, m, blk, chunks=v, layout=kind)
+    chain = zb.make_pipeline(v * P, m, blk)
+    flat = IL.to_virtual(kind, P, ops)
+    assert zb.zb_schedule_workspace_size(pl, ops) == zb.zb_schedule_workspace_size(chain, flat)
+    # the ledger of the V replay on one GPU: every virtual stage's M_B, chained
+    _, peak_b = zb.zb_schedule_workspace_size(pl, ops)
+    assert peak_b > 0
+
+
+def test_chunked_validation_codes(zb):
+    ops = zb.zb_make_interleaved_schedule("ZBV", 2, 2, 3)
+    blk = zb.make_block(64, 32, 128)
+
+    def code(pl, o):
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_schedule_workspace_size(pl, o)
+        return e.value.status
+
+    pl = zb.make_pipeline(2, 3, blk, chunks=2, layout="ZBV")
+    assert code(zb.make_pipeline(2, 3, blk), ops) == zb.ZB_ERR_SCHEDULE  # chunk 1 without chunks
+    assert code(zb.make_pipeline(2, 3, blk, chunks=3, layout="ZBV"), ops) == zb.ZB_ERR_INVALID_ARG
+    assert code(zb.make_pipeline(2, 3, blk, chunks=2, layout=7), ops) == zb.ZB_ERR_INVALID_ARG
+    bad = [("F", 0, 2, 0)] + ops
+    assert code(pl, bad) == zb.ZB_ERR_SCHEDULE
+    # a V list replayed with the cyclic layout breaks the chain order
+    assert code(zb.make_pipeline(2, 3, blk, chunks=2, layout="1F1B-I"), ops) == zb.ZB_ERR_SCHEDULE
+    # W of a virtual stage out of order
+    i = next(n for n, op in enumerate(ops) if op[0] == "W" and op[3] == 0)
+    k = next(n for n, op in enumerate(ops) if op[0] == "W" and op[1:3] == ops[i][1:3] and op[3] == 1)
+    sw = list(ops)
+    sw[i], sw[k] = sw[k], sw[i]
+    assert code(pl, sw) in (zb.ZB_ERR_W_ORDER, zb.ZB_ERR_SCHEDULE)
