@@ -382,6 +382,8 @@ def main():
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="c4")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--streams", type=int, default=0,
+                    help="streams of the replay (0: one per stage, serial for one stage)")
     ap.add_argument("--no-optimizer", action="store_true",
                     help="skip the post-validated AdamW measurement (after the timed step)")
     ap.add_argument("--sweep", action="store_true",
@@ -431,7 +433,8 @@ def main():
         ops = [(k, 0, j) for k, s, j in ops if s == 0]
     blk = zb.make_block(M, h, f)
     # multi-stage replays run their stages on P streams (stage-parallel)
-    pl = zb.make_pipeline(P, m, blk, timing=True, streams=P if multi else 1)
+    n_streams = args.streams if args.streams > 0 else (P if multi else 1)
+    pl = zb.make_pipeline(P, m, blk, timing=True, streams=n_streams)
     need, peak_live = zb.zb_schedule_workspace_size(pl, ops)
     ws_t = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()

@@ -249,9 +249,16 @@ typedef struct zb_pipeline {
                                   GPU the way pipeline stages share time; a
                                   stage's W still run in list order on its
                                   stream, so results are bit-identical to the
-                                  serial replay.  The call forks from and
-                                  joins back into `stream`.  With chunks,
-                                  lanes follow the stage (device) of an op.  */
+                                  serial replay.  n >= 2 P (2 P <= 8): each
+                                  stage's W and OPT ops also get a stream of
+                                  their own, ordered after the stage's B by
+                                  events and kept in list order, so a weight
+                                  gradient GEMM fills the SMs that an F/B
+                                  kernel's last partial wave leaves idle (the
+                                  one-stage replay with n = 2).  The call
+                                  forks from and joins back into `stream`.
+                                  With chunks, lanes follow the stage
+                                  (device) of an op.                         */
     int32_t chunks;            /* model chunks per stage: 0 or 1 = one; v > 1
                                   makes the model a chain of L = v P virtual
                                   stages placed by `layout`; every per-stage

@@ -366,9 +366,18 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         return ws + static_cast<size_t>(plan.row_slots) * plan.row_bytes + static_cast<size_t>(slot) * plan.ffn_bytes;
     };
 
-    // Streams: ops of stage (device) d run on lanes[d % ns]; lanes[0] is the
-    // caller's stream.
-    const int ns = std::max(1, std::min(std::min(pl->streams, pl->P), 8));
+    // Streams: ops of stage (device) d run on lanes[d % nsd]; lanes[0] is the
+    // caller's stream.  With streams >= 2 P (at most 8) each stage's W and
+    // OPT ops get a lane of their own (lanes[nsd + d]): a weight-gradient
+    // GEMM then starts on the SMs that the stage's last F/B wave leaves idle.
+    const int nsd = std::max(1, std::min(std::min(pl->streams, pl->P), 8));
+    const bool w_lanes = pl->streams >= 2 * pl->P && 2 * pl->P <= 8;
+    const int ns = nsd + (w_lanes ? pl->P : 0);
+    std::vector<int> lane_of(n_ops, 0);
+    for (size_t i = 0; i < n_ops; ++i) {
+        const bool wk = vop[i].kind == ZB_OP_W || vop[i].kind == ZB_OP_OPT;
+        lane_of[i] = (w_lanes && wk) ? nsd + dev[i] : dev[i] % nsd;
+    }
     std::vector<cudaStream_t> lanes(1, static_cast<cudaStream_t>(stream));
     std::vector<cudaEvent_t>* evs = nullptr;
     if (ns > 1) {
@@ -400,22 +409,29 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     int gemms = 0;
     g_gemm_counter = &gemms;
     std::vector<char> w_started(P, 0);
+    std::vector<int> last_w_op(P, -1);  // latest W / BW of each stage, for OPT
 
     for (size_t i = 0; i < n_ops && s == ZB_OK; ++i) {
         const zb_op& o = vop[i];  // stage = virtual stage of the chain
         const int st = o.stage, j = static_cast<int>(o.micro);
         const zb_stage_params& p = stages[st];
-        cudaStream_t lane = lanes[dev[i] % ns];
+        cudaStream_t lane = lanes[lane_of[i]];
         void* lane_v = static_cast<void*>(lane);
         rec.st = lane;
-        if (ns > 1 && o.kind != ZB_OP_OPT) {
+        if (ns > 1) {
             // wait for producers and slot releases that ran on other lanes
-            std::vector<int> deps = plan.reuse_deps[i];
-            if (o.kind == ZB_OP_F && st > 0) deps.push_back(fwd_op[static_cast<size_t>(st - 1) * m + j]);
-            if ((o.kind == ZB_OP_B || o.kind == ZB_OP_BW) && st < P - 1)
-                deps.push_back(bwd_op[static_cast<size_t>(st + 1) * m + j]);
+            std::vector<int> deps;
+            if (o.kind == ZB_OP_OPT) {
+                deps.push_back(last_w_op[st]);
+            } else {
+                deps = plan.reuse_deps[i];
+                if (o.kind == ZB_OP_F && st > 0) deps.push_back(fwd_op[static_cast<size_t>(st - 1) * m + j]);
+                if ((o.kind == ZB_OP_B || o.kind == ZB_OP_BW) && st < P - 1)
+                    deps.push_back(bwd_op[static_cast<size_t>(st + 1) * m + j]);
+                if (o.kind == ZB_OP_W) deps.push_back(bwd_op[static_cast<size_t>(st) * m + j]);
+            }
             for (int d : deps) {
-                if (d < 0 || lanes[dev[d] % ns] == lane) continue;
+                if (d < 0 || lane_of[d] == lane_of[i]) continue;
                 cudaError_t e = cudaStreamWaitEvent(lane, (*evs)[d], 0);
                 if (e != cudaSuccess) {
                     s = fail(ZB_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(e));
@@ -477,6 +493,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
             default: break;
         }
         op_span[i].second = rec.spans.size();
+        if (o.kind == ZB_OP_W || o.kind == ZB_OP_BW) last_w_op[st] = static_cast<int>(i);
         if (ns > 1 && s == ZB_OK) {
             cudaError_t e = cudaEventRecord((*evs)[i], lane);
             if (e != cudaSuccess) s = fail(ZB_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(e));

@@ -212,19 +212,118 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
     return __bfloat1622float2(v);
 }
 
+// ---------------------------------------------------------------------------
+// Exact-erf GeLU / GeLU' on pairs of elements with the packed two-lane fp32
+// instructions of sm_100-class GPUs (fma / mul / add .rn.f32x2): every
+// polynomial and scaling step handles two elements per instruction, which
+// halves the epilogue's arithmetic issue (the epilogue warps share their
+// schedulers with the TMA-producer and MMA-issuer warps, whose loops it
+// would otherwise delay).  Same formulas as normal_cdf_and_exp (A&S 7.1.26),
+// with exp(v) = 2^(v / ln 2) and 1/y taken from the ex2.approx / rcp.approx
+// instructions, the 1/2 of q folded into the coefficients and
+// Phi(x) = 1/2 + sign(x) (1/2 - q) (q = Phi(-|x|)) instead of a select.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void up2(f32x2 v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float ex2_approx(float v) {
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float rcp_approx(float v) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Phi and exp(-x^2/2) of the pair X.
+__device__ __forceinline__ void normal_cdf_and_exp2(f32x2 X, f32x2& PHI, f32x2& E) {
+    using C = AS71_26;
+    float x0, x1;
+    up2(X, x0, x1);
+    // exp(-x^2/2) = 2^(-x^2 / (2 ln 2))
+    const f32x2 arg = mul2(mul2(X, X), pk2(-0.7213475204444817f, -0.7213475204444817f));
+    float a0, a1;
+    up2(arg, a0, a1);
+    E = pk2(ex2_approx(a0), ex2_approx(a1));
+    // t = 1 / (1 + p |x| / sqrt 2)
+    const float pz = C::p * 0.7071067811865476f;
+    const f32x2 den = fma2(pk2(fabsf(x0), fabsf(x1)), pk2(pz, pz), pk2(1.0f, 1.0f));
+    float d0, d1;
+    up2(den, d0, d1);
+    const f32x2 T = pk2(rcp_approx(d0), rcp_approx(d1));
+    // q/e = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) / 2
+    f32x2 P = fma2(T, pk2(0.5f * C::a5, 0.5f * C::a5), pk2(0.5f * C::a4, 0.5f * C::a4));
+    P = fma2(T, P, pk2(0.5f * C::a3, 0.5f * C::a3));
+    P = fma2(T, P, pk2(0.5f * C::a2, 0.5f * C::a2));
+    P = fma2(T, P, pk2(0.5f * C::a1, 0.5f * C::a1));
+    P = mul2(T, P);
+    const f32x2 half_minus_q = fma2(mul2(P, E), pk2(-1.0f, -1.0f), pk2(0.5f, 0.5f));
+    float h0, h1;
+    up2(half_minus_q, h0, h1);
+    PHI = add2(pk2(copysignf(h0, x0), copysignf(h1, x1)), pk2(0.5f, 0.5f));
+}
+
 template <bool TANH>
 __device__ __forceinline__ void gelu_pack64(const float (&x)[64], uint32_t (&w)[32]) {
+    if (TANH) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(gelu_t<TANH>(x[2 * i]), gelu_t<TANH>(x[2 * i + 1]));
+        for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(gelu_t<true>(x[2 * i]), gelu_t<true>(x[2 * i + 1]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const f32x2 X = pk2(x[2 * i], x[2 * i + 1]);
+            f32x2 PHI, E;
+            normal_cdf_and_exp2(X, PHI, E);
+            float g0, g1;
+            up2(mul2(X, PHI), g0, g1);  // GeLU = x Phi(x)
+            w[i] = pack_bf16x2(g0, g1);
+        }
+    }
 }
 
 template <bool TANH>
 __device__ __forceinline__ void gelu_grad_mul64(float (&x)[64], const uint32_t (&h)[32]) {
+    if (TANH) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const float2 f2 = unpack_bf16x2(h[i]);
-        x[2 * i] *= gelu_grad_t<TANH>(f2.x);
-        x[2 * i + 1] *= gelu_grad_t<TANH>(f2.y);
+        for (int i = 0; i < 32; ++i) {
+            const float2 f2 = unpack_bf16x2(h[i]);
+            x[2 * i] *= gelu_grad_t<true>(f2.x);
+            x[2 * i + 1] *= gelu_grad_t<true>(f2.y);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float2 f2 = unpack_bf16x2(h[i]);
+            const f32x2 Hx = pk2(f2.x, f2.y);
+            f32x2 PHI, E;
+            normal_cdf_and_exp2(Hx, PHI, E);
+            // GeLU'(h) = Phi(h) + h phi(h),  phi(h) = exp(-h^2/2) / sqrt(2 pi)
+            const f32x2 G = fma2(mul2(Hx, pk2(0.3989422804014327f, 0.3989422804014327f)), E, PHI);
+            up2(mul2(pk2(x[2 * i], x[2 * i + 1]), G), x[2 * i], x[2 * i + 1]);
+        }
     }
 }
 
@@ -487,6 +586,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
             const bool rows_live = row0 < args.Mg;
             if (EPI == zb::EPI_F32) {
+                // The fp32 stores (TMA reduce-adds) share the TMA unit with the
+                // operand loads of the next tile: issued back to back they
+                // queue ahead of those loads and starve the MMAs.  Spacing the
+                // chunks over the tile (a pause that scales with the K loop,
+                // ~5 ns per K block, at most 250 ns, none after the CTA's last
+                // chunk) keeps the loads flowing.
+                const bool last_tile = tile + clusters >= num_tiles;
+                const unsigned pause_ns = static_cast<unsigned>(min(num_kb * 5, 250));
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t v[32];
@@ -502,6 +609,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         staging_release<true>(&tmO0, stg, lane, col0, row0);
                     else
                         staging_release<false>(&tmO0, stg, lane, col0, row0);
+                    if (!last_tile && pause_ns) __nanosleep(pause_ns);
                 }
             } else {
 #pragma unroll 1
