@@ -255,8 +255,11 @@ typedef struct zb_pipeline {
                                   events and kept in list order, so a weight
                                   gradient GEMM fills the SMs that an F/B
                                   kernel's last partial wave leaves idle (the
-                                  one-stage replay with n = 2).  The call
-                                  forks from and joins back into `stream`.
+                                  one-stage replay with n = 2).  P = 1 and
+                                  n >= 3: the F/B/BW ops of consecutive
+                                  microbatches also alternate over n - 1
+                                  streams (at most 7).  The call forks from
+                                  and joins back into `stream`.
                                   With chunks, lanes follow the stage
                                   (device) of an op.                         */
     int32_t chunks;            /* model chunks per stage: 0 or 1 = one; v > 1

@@ -370,13 +370,22 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     // caller's stream.  With streams >= 2 P (at most 8) each stage's W and
     // OPT ops get a lane of their own (lanes[nsd + d]): a weight-gradient
     // GEMM then starts on the SMs that the stage's last F/B wave leaves idle.
-    const int nsd = std::max(1, std::min(std::min(pl->streams, pl->P), 8));
-    const bool w_lanes = pl->streams >= 2 * pl->P && 2 * pl->P <= 8;
-    const int ns = nsd + (w_lanes ? pl->P : 0);
+    // A one-stage replay with streams >= 3 instead spreads the F/B/BW ops of
+    // consecutive microbatches over streams - 1 lanes (at most 7; the
+    // microbatches are independent until their W) and keeps every W / OPT on
+    // the last lane, in list order: each persistent GEMM then starts on the
+    // SMs that the previous one's partial last wave leaves idle.
+    const bool micro_lanes = pl->P == 1 && pl->streams >= 3;
+    const int nsd = micro_lanes ? std::min(pl->streams - 1, 7) : std::max(1, std::min(std::min(pl->streams, pl->P), 8));
+    const bool w_lanes = micro_lanes || (pl->streams >= 2 * pl->P && 2 * pl->P <= 8);
+    const int ns = nsd + (w_lanes ? (micro_lanes ? 1 : pl->P) : 0);
     std::vector<int> lane_of(n_ops, 0);
     for (size_t i = 0; i < n_ops; ++i) {
         const bool wk = vop[i].kind == ZB_OP_W || vop[i].kind == ZB_OP_OPT;
-        lane_of[i] = (w_lanes && wk) ? nsd + dev[i] : dev[i] % nsd;
+        if (micro_lanes)
+            lane_of[i] = wk ? nsd : static_cast<int>(vop[i].micro % static_cast<uint32_t>(nsd));
+        else
+            lane_of[i] = (w_lanes && wk) ? nsd + dev[i] : dev[i] % nsd;
     }
     std::vector<cudaStream_t> lanes(1, static_cast<cudaStream_t>(stream));
     std::vector<cudaEvent_t>* evs = nullptr;

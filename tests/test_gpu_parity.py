@@ -479,6 +479,36 @@ def test_stage_parallel_replay_is_bit_exact(zb, kind, P, m, streams):
             assert torch.equal(_bits(Yl[j]), _bits(ref[2][j]))
 
 
+@pytest.mark.parametrize("kind,m,streams", [("ZBH2", 6, 2), ("ZBH1", 5, 3), ("1F1B", 4, 2), ("ZBH2", 7, 4)])
+def test_one_stage_lanes_are_bit_exact(zb, kind, m, streams):
+    # One stage: W / OPT on a lane of their own (streams = 2), plus the F/B of
+    # consecutive microbatches alternating over streams - 1 lanes (>= 3):
+    # same bits as the serial replay, gradient statistics included.
+    M, h, f = 512, 256, 1024
+    blk = zb.make_block(M, h, f)
+    wts, X0, dY = _pipeline_setup(zb, 1, m, M, h, f, seed=40 + m)
+    ops = [op for op in zb.zb_make_schedule(kind, 8, m) if op[1] == 0]
+    outs = []
+    for n in (1, streams):
+        pl = zb.make_pipeline(1, m, blk, streams=n)
+        ws_bytes, _ = zb.zb_schedule_workspace_size(pl, ops)
+        ws = torch.full((ws_bytes,), 255, dtype=torch.uint8, device="cuda")
+        stages = [dict(w, dW1=empty_f32(h, f), dW2=empty_f32(f, h),
+                       grad_stats=torch.zeros(2, dtype=torch.float64, device="cuda")) for w in wts]
+        dX0 = [empty_bf16(M, h) for _ in range(m)]
+        Yl = [empty_bf16(M, h) for _ in range(m)]
+        zb.zb_run_stage_schedule(pl, stages, X0, dY, dX0, Yl, ops, ws, ws_bytes)
+        sync(zb)
+        outs.append((stages, dX0, Yl))
+    (sa, xa, ya), (sb, xb, yb) = outs
+    assert torch.equal(_bits(sa[0]["dW1"]), _bits(sb[0]["dW1"]))
+    assert torch.equal(_bits(sa[0]["dW2"]), _bits(sb[0]["dW2"]))
+    assert torch.equal(sa[0]["grad_stats"], sb[0]["grad_stats"])
+    for j in range(m):
+        assert torch.equal(_bits(xa[j]), _bits(xb[j]))
+        assert torch.equal(_bits(ya[j]), _bits(yb[j]))
+
+
 @pytest.mark.parametrize("act", ["gelu_erf", "gelu_tanh"])
 def test_activation_epilogues_match_the_math(zb, act):
     # With W1 = I the F pass stores H = X exactly and A = bf16(GeLU(X)); with
