@@ -385,6 +385,12 @@ def main():
     ap.add_argument("--streams", type=int, default=0,
                     help="streams of the replay (0: one per stage; a one-stage replay puts its W "
                          "passes on a second stream)")
+    ap.add_argument("--e2e-result", choices=("stats", "dW"), default="stats",
+                    help="what the e2e step reads back: the stages' gradient statistics (sum of "
+                         "squares, NaN/Inf count; computed at the OPT markers) or the full fp32 dW")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every step's kernels from the host instead of replaying one "
+                         "captured CUDA graph per step")
     ap.add_argument("--no-optimizer", action="store_true",
                     help="skip the post-validated AdamW measurement (after the timed step)")
     ap.add_argument("--sweep", action="store_true",
@@ -451,6 +457,26 @@ def main():
         step(st)
     torch.cuda.synchronize()
     zb.zb_sync_status(stream)
+    def capture(Ws, Xs, Gs):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                zb.zb_run_stage_schedule(pl, Ws, Xs, Gs, None, None, ops_c, ws_t, ws_t.numel(), None, side)
+        stream.wait_stream(side)
+        return g
+
+    graph = None
+    if not args.no_graph:
+        # the executor only enqueues work: one step captured on a side stream
+        # (its helper streams and events exist already) replays as a graph
+        launches_per_step = st.n_gemm_launches
+        pl.timing = 0
+        graph = capture(W, X0, dY)
+        graph.replay()
+        torch.cuda.synchronize()
+        zb.zb_sync_status(stream)
 
     clocks = ClockSampler(torch.cuda.current_device())
     sums = {"gemm_ms": 0.0, "gemm_launches": 0, "kind": [0.0] * 4}
@@ -463,6 +489,10 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
+        if graph is not None:
+            graph.replay()
+            sums["gemm_launches"] += launches_per_step
+            continue
         step(st)
         sums["gemm_ms"] += st.gemm_ms
         sums["gemm_launches"] += st.n_gemm_launches
@@ -482,7 +512,7 @@ def main():
     tokens_s = job_rate(m * M, args.steps, ws, ms_max / 1e3)
     kind_ms, kind_steps = sums["kind"], args.steps
     kind_basis = "CUDA events around each op in the timed region"
-    if pl.streams > 1:
+    if pl.streams > 1 or graph is not None:
         # per-pass times from a short serial replay: on overlapping streams an
         # op's events also count the time it waited for SMs
         pl_serial = zb.make_pipeline(P, m, blk, timing=True, streams=1)
@@ -502,7 +532,7 @@ def main():
     peaks = _peaks()
     gemm_flops = 2.0 * M * h * f
     avg_launch_ms = sums["gemm_ms"] / max(1, sums["gemm_launches"])
-    overlapped = pl.streams > 1
+    overlapped = pl.streams > 1 or graph is not None
     if overlapped:
         # launches on different streams overlap (a W kernel starts in the
         # tail of an F/B kernel), so events around one launch also count the
@@ -545,20 +575,32 @@ def main():
 
     # ------------------------------------------------------------- end to end
     # Through the public API with host buffers: every step uploads its inputs
-    # from pinned host memory and downloads its weight gradients.  Two input
-    # and gradient sets alternate so that step k+1's upload and step k's
-    # download run on a copy stream while the other step computes.
+    # from pinned host memory and reads back its result: by default the
+    # stages' gradient statistics (the per-step metric a training loop reads;
+    # the weight gradients stay on the GPU for the optimizer), or with
+    # --e2e-result dW the full fp32 weight gradients.  Two input and gradient
+    # sets alternate so that step k+1's upload and step k's read-back run on
+    # copy streams while the other step computes.
     pin = [x.cpu().pin_memory() for x in X0]
     pin_g = [g.cpu().pin_memory() for g in dY]
-    host_dW = [(torch.empty(h, f, pin_memory=True), torch.empty(f, h, pin_memory=True))
-               for _ in range(P)]
+    want_dw = args.e2e_result == "dW"
     h2d = sum(x.numel() * x.element_size() for x in pin + pin_g)
-    d2h = sum(a.numel() * 4 + b.numel() * 4 for a, b in host_dW)
-    sets = [(X0, dY, W)]
-    X0b = [torch.empty_like(x) for x in X0]
-    dYb = [torch.empty_like(g) for g in dY]
-    Wb = [dict(w, dW1=torch.empty_like(w["dW1"]), dW2=torch.empty_like(w["dW2"])) for w in W]
-    sets.append((X0b, dYb, Wb))
+    sets = []
+    for a in range(2):
+        Xs_ = X0 if a == 0 else [torch.empty_like(x) for x in X0]
+        Gs_ = dY if a == 0 else [torch.empty_like(g) for g in dY]
+        Ws_ = [dict(w, dW1=torch.empty_like(w["dW1"]), dW2=torch.empty_like(w["dW2"])) for w in W]
+        if not want_dw:
+            for w in Ws_:
+                w["grad_stats"] = torch.zeros(2, dtype=torch.float64, device=dev)
+        sets.append((Xs_, Gs_, Ws_))
+    if want_dw:
+        host_out = [(torch.empty(h, f, pin_memory=True), torch.empty(f, h, pin_memory=True))
+                    for _ in range(P)]
+        d2h = sum(a.numel() * 4 + b.numel() * 4 for a, b in host_out)
+    else:
+        host_out = [torch.empty(2, dtype=torch.float64, pin_memory=True) for _ in range(P)]
+        d2h = 16 * P
     up_stream = torch.cuda.Stream(device=dev)
     down_stream = torch.cuda.Stream(device=dev)
     in_ready = [torch.cuda.Event(), torch.cuda.Event()]
@@ -575,6 +617,9 @@ def main():
                 sets[a][1][j].copy_(pin_g[j], non_blocking=True)
             in_ready[a].record(up_stream)
 
+    # with graphs: one captured step per input / gradient set
+    e2e_graphs = [capture(Ws_, Xs_, Gs_) for Xs_, Gs_, Ws_ in sets] if graph is not None else None
+
     def e2e_run(steps):
         for ev in done + down_done:
             ev.record(stream)
@@ -586,13 +631,19 @@ def main():
             stream.wait_event(in_ready[a])
             stream.wait_event(down_done[a])  # set a's gradients were downloaded
             Xs, Gs, Ws = sets[a]
-            zb.zb_run_stage_schedule(pl, Ws, Xs, Gs, None, None, ops_c, ws_t, ws_t.numel(), None, stream)
+            if e2e_graphs is not None:
+                e2e_graphs[a].replay()
+            else:
+                zb.zb_run_stage_schedule(pl, Ws, Xs, Gs, None, None, ops_c, ws_t, ws_t.numel(), None, stream)
             done[a].record(stream)
             down_stream.wait_event(done[a])
             with torch.cuda.stream(down_stream):
                 for s_ in range(P):
-                    host_dW[s_][0].copy_(Ws[s_]["dW1"], non_blocking=True)
-                    host_dW[s_][1].copy_(Ws[s_]["dW2"], non_blocking=True)
+                    if want_dw:
+                        host_out[s_][0].copy_(Ws[s_]["dW1"], non_blocking=True)
+                        host_out[s_][1].copy_(Ws[s_]["dW2"], non_blocking=True)
+                    else:
+                        host_out[s_].copy_(Ws[s_]["grad_stats"], non_blocking=True)
                 down_done[a].record(down_stream)
         torch.cuda.synchronize()
 
@@ -624,6 +675,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": desc, "h": h, "f": f, "M": M, "m": m, "P": P,
                        "schedule": sched, "list_from_P": Pl, "streams": pl.streams,
+                       "cuda_graph": graph is not None,
                        "parallelism": "replicas" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2 (W1 %.0f MB, X and dY %.0f MB per microbatch)"
                              % (h * f * 2 / 1e6, M * h * 2 / 1e6)},
@@ -642,6 +694,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                    "result": ("fp32 weight gradients" if want_dw else
+                               "gradient statistics per stage (sum of squares, NaN/Inf count)"),
                     "timing": "host wall clock around synchronised steps; uploads and downloads "
                               "double-buffered on their own streams"},
             "projection": projection,

@@ -601,3 +601,47 @@ def test_replay_reports_stage_grad_stats_and_injected_nan(zb):
                 assert bad == 0 and abs(st[0] - ref) <= 1e-6 * ref
             else:
                 assert bad > 0
+
+
+@pytest.mark.parametrize("P,m,streams,kind", [(4, 8, 4, "ZBH1"), (1, 6, 2, "ZBH2"), (2, 4, 1, "1F1B")])
+def test_replay_captured_in_a_cuda_graph(zb, P, m, streams, kind):
+    # The executor only enqueues work (streams and events of its own are made
+    # on first use, before the capture): a step captured into a CUDA graph and
+    # replayed twice gives the eager replay's bits.
+    M, h, f = 512, 256, 1024
+    blk = zb.make_block(M, h, f)
+    wts, X0, dY = _pipeline_setup(zb, P, m, M, h, f, seed=60 + P)
+    ops = zb.zb_make_schedule(kind, P if P > 1 else 8, m)
+    if P == 1:
+        ops = [op for op in ops if op[1] == 0]
+    pl = zb.make_pipeline(P, m, blk, streams=streams)
+    ws_bytes, _ = zb.zb_schedule_workspace_size(pl, ops)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stages = [dict(w, dW1=empty_f32(h, f), dW2=empty_f32(f, h)) for w in wts]
+    dX0 = [empty_bf16(M, h) for _ in range(m)]
+    Yl = [empty_bf16(M, h) for _ in range(m)]
+    ops_c = zb.ops_array(ops)
+
+    def step(stream=None):
+        zb.zb_run_stage_schedule(pl, stages, X0, dY, dX0, Yl, ops_c, ws, ws_bytes, None, stream)
+
+    step()
+    sync(zb)
+    ref = [(s["dW1"].clone(), s["dW2"].clone()) for s in stages], [x.clone() for x in dX0], [y.clone() for y in Yl]
+    for s in stages:
+        s["dW1"].fill_(float("nan"))
+        s["dW2"].fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            step(side)
+    for _ in range(2):
+        g.replay()
+        sync(zb)
+        for s, (a, b) in zip(stages, ref[0]):
+            assert torch.equal(_bits(s["dW1"]), _bits(a)) and torch.equal(_bits(s["dW2"]), _bits(b))
+        for j in range(m):
+            assert torch.equal(_bits(dX0[j]), _bits(ref[1][j]))
+            assert torch.equal(_bits(Yl[j]), _bits(ref[2][j]))
