@@ -617,10 +617,53 @@ def main():
                 sets[a][1][j].copy_(pin_g[j], non_blocking=True)
             in_ready[a].record(up_stream)
 
-    # with graphs: one captured step per input / gradient set
-    e2e_graphs = [capture(Ws_, Xs_, Gs_) for Xs_, Gs_, Ws_ in sets] if graph is not None else None
+    def read_back(Ws):
+        for s_ in range(P):
+            if want_dw:
+                host_out[s_][0].copy_(Ws[s_]["dW1"], non_blocking=True)
+                host_out[s_][1].copy_(Ws[s_]["dW2"], non_blocking=True)
+            else:
+                host_out[s_].copy_(Ws[s_]["grad_stats"], non_blocking=True)
+
+    def capture_e2e(a):
+        # one graph per set: its step, in parallel the upload of the other
+        # set's inputs (for the next step), then the read-back of its result;
+        # replays follow each other on one stream, one host call per step
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fork = torch.cuda.Event()
+                fork.record(side)
+                up_stream.wait_event(fork)
+                with torch.cuda.stream(up_stream):
+                    for j in range(m):
+                        sets[1 - a][0][j].copy_(pin[j], non_blocking=True)
+                        sets[1 - a][1][j].copy_(pin_g[j], non_blocking=True)
+                    joined = torch.cuda.Event()
+                    joined.record(up_stream)
+                Xs_, Gs_, Ws_ = sets[a]
+                zb.zb_run_stage_schedule(pl, Ws_, Xs_, Gs_, None, None, ops_c, ws_t, ws_t.numel(), None, side)
+                read_back(Ws_)
+                side.wait_event(joined)
+        stream.wait_stream(side)
+        return g
+
+    e2e_graphs = [capture_e2e(0), capture_e2e(1)] if graph is not None else None
 
     def e2e_run(steps):
+        if e2e_graphs is not None:
+            # step 0's inputs, then each replay uploads the next step's
+            with torch.cuda.stream(up_stream):
+                for j in range(m):
+                    sets[0][0][j].copy_(pin[j], non_blocking=True)
+                    sets[0][1][j].copy_(pin_g[j], non_blocking=True)
+            stream.wait_stream(up_stream)
+            for k in range(steps):
+                e2e_graphs[k % 2].replay()
+            torch.cuda.synchronize()
+            return
         for ev in done + down_done:
             ev.record(stream)
         upload(0)
@@ -631,19 +674,11 @@ def main():
             stream.wait_event(in_ready[a])
             stream.wait_event(down_done[a])  # set a's gradients were downloaded
             Xs, Gs, Ws = sets[a]
-            if e2e_graphs is not None:
-                e2e_graphs[a].replay()
-            else:
-                zb.zb_run_stage_schedule(pl, Ws, Xs, Gs, None, None, ops_c, ws_t, ws_t.numel(), None, stream)
+            zb.zb_run_stage_schedule(pl, Ws, Xs, Gs, None, None, ops_c, ws_t, ws_t.numel(), None, stream)
             done[a].record(stream)
             down_stream.wait_event(done[a])
             with torch.cuda.stream(down_stream):
-                for s_ in range(P):
-                    if want_dw:
-                        host_out[s_][0].copy_(Ws[s_]["dW1"], non_blocking=True)
-                        host_out[s_][1].copy_(Ws[s_]["dW2"], non_blocking=True)
-                    else:
-                        host_out[s_].copy_(Ws[s_]["grad_stats"], non_blocking=True)
+                read_back(Ws)
                 down_done[a].record(down_stream)
         torch.cuda.synchronize()
 
@@ -651,9 +686,13 @@ def main():
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    e2e_clocks = ClockSampler(torch.cuda.current_device())
+    e2e_clocks.start()
+    time.sleep(0.3)
     t0 = time.perf_counter()
     e2e_run(args.e2e_steps)
     e2e_s = reduce_max(time.perf_counter() - t0, dev, ws)
+    e2e_clk = e2e_clocks.stop()
     e2e_value = job_rate(step_flops, args.e2e_steps, ws, e2e_s) / 1e12
 
     optimizer = None
@@ -694,10 +733,14 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                    "clocks": e2e_clk,
                     "result": ("fp32 weight gradients" if want_dw else
                                "gradient statistics per stage (sum of squares, NaN/Inf count)"),
-                    "timing": "host wall clock around synchronised steps; uploads and downloads "
-                              "double-buffered on their own streams"},
+                    "timing": ("host wall clock around the steps; per step one CUDA graph: the step, "
+                               "the next step's upload in a parallel branch, the read-back"
+                               if e2e_graphs is not None else
+                               "host wall clock around synchronised steps; uploads and downloads "
+                               "double-buffered on their own streams")},
             "projection": projection,
             "optimizer": optimizer,
             "gpu_launches": sums["gemm_launches"],

@@ -384,3 +384,22 @@ def test_chunked_validation_codes(zb):
     sw = list(ops)
     sw[i], sw[k] = sw[k], sw[i]
     assert code(pl, sw) in (zb.ZB_ERR_W_ORDER, zb.ZB_ERR_SCHEDULE)
+
+
+@pytest.mark.parametrize("kind,P,v,m", [("ZBV", 16, 2, 48), ("ZBV", 32, 2, 96), ("1F1B-I", 16, 2, 64),
+                                        ("1F1B-I", 32, 4, 64)])
+def test_interleaved_at_the_pages_scales(zb, kind, P, v, m):
+    """Table 8 / Figure 9 scales (16-32 stages): generated quickly, valid
+    replays of the chain, ZB-V at exactly P M_B on every stage."""
+    import time
+    t0 = time.perf_counter()
+    res, ops = zb.zb_simulate_interleaved_schedule(kind, P, v, m, 1.0, 1.0, 1.0, 0.0, want_ops=True)
+    assert time.perf_counter() - t0 < 20.0
+    blk = zb.make_block(64, 32, 128)
+    pl = zb.make_pipeline(P, m, blk, chunks=v, layout=kind)
+    zb.zb_schedule_workspace_size(pl, ops)  # validates the list on the chain
+    if kind == "ZBV":
+        assert res.peak_live_microbatches == 2 * P
+        assert res.bubble_rate < S.bubble_rate(S.make_schedule("ZBH1", P, m)[0], P, m, S.Times())
+    else:
+        assert abs(res.bubble_rate - (P - 1) / (v * m + P - 1)) < 1e-12

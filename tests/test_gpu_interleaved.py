@@ -128,3 +128,32 @@ def test_zbv_replay_at_measured_times_and_stats(zb):
         st = stages[k]["grad_stats"].cpu().numpy()
         g = np.concatenate([f64(stages[k]["dW1"]).ravel(), f64(stages[k]["dW2"]).ravel()])
         assert st[1] == 0 and abs(st[0] - float(np.sum(g * g))) <= 1e-6 * st[0]
+
+
+def test_zbv_replay_with_bias_is_the_chain_replay(zb):
+    P, v, m, M, h, f = 2, 2, 3, 136, 72, 200
+    L = v * P
+    blk = zb.make_block(M, h, f, has_bias=True)
+    stages_d, X0, dY = I.pipeline_draws(L, m, M, h, f, seed=8, bias=True)
+    wts = [{"W1": dev_bf16(st.W1), "W2": dev_bf16(st.W2), "b1": dev_bf16(st.b1), "b2": dev_bf16(st.b2)}
+           for st in stages_d]
+    X0 = [dev_bf16(x) for x in X0]
+    dY = [dev_bf16(g) for g in dY]
+
+    def run(pl, ops):
+        ws_bytes, _ = zb.zb_schedule_workspace_size(pl, ops)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        stages = [dict(w, dW1=empty_f32(h, f), dW2=empty_f32(f, h), db1=empty_f32(f), db2=empty_f32(h))
+                  for w in wts]
+        Yl = [empty_bf16(M, h) for _ in range(m)]
+        zb.zb_run_stage_schedule(pl, stages, X0, dY, None, Yl, ops, ws, ws_bytes)
+        sync(zb)
+        return stages, Yl
+
+    a = run(zb.make_pipeline(P, m, blk, chunks=2, layout="ZBV"), zb.zb_make_interleaved_schedule("ZBV", P, 2, m))
+    b = run(zb.make_pipeline(L, m, blk), zb.zb_make_schedule("ZBH1", L, m))
+    for p, q in zip(a[0], b[0]):
+        for key in ("dW1", "dW2", "db1", "db2"):
+            assert torch.equal(p[key], q[key])
+    for p, q in zip(a[1], b[1]):
+        assert torch.equal(p.view(torch.int16), q.view(torch.int16))

@@ -274,3 +274,20 @@ def test_replay_then_post_validated_step(zb):
     sync(zb)
     _, _, Yr = ob.forward(f64(X), f64(stages[0]["W1"]), f64(stages[0]["W2"]), act="gelu_erf")
     assert rel(f64(Y), Yr) <= 5e-3
+
+
+def test_decisions_only_without_tensors(zb):
+    """No tensors: the call still writes every stage's decision."""
+    draws = _draws(seed=50)
+    n = _partial_norms(draws)
+    c = float(np.sqrt(n[2] * n[3]))
+    _, dev = _device_state(zb, draws, lambda s, k: False)
+    states = _stage_states(zb, dev)
+    dec = torch.empty(4 * 40, dtype=torch.uint8, device="cuda")
+    zb.zb_post_validated_adamw(4, states, [], hp_c(zb, c), dec)
+    sync(zb)
+    d = zb.decisions_from_bytes(dec.cpu().numpy().tobytes(), 4)
+    _, report, _ = _oracle(draws, c)
+    assert [x["rolled_back"] for x in d] == [int(r["rolled_back"]) for r in report] == [1, 1, 1, 0]
+    for x, r in zip(d, report):
+        assert abs(x["norm_sq_global"] - n[3] ** 2) <= 1e-6 * n[3] ** 2
