@@ -266,7 +266,11 @@ def run_sweep(args):
         W2 = (torch.randn(f, h, device=dev, generator=gen) * 0.02).to(bf)
         dW1 = torch.zeros(h, f, device=dev)
         dW2 = torch.zeros(f, h, device=dev)
-        blk = zb.make_block(M, h, f)
+        b1 = (torch.randn(f, device=dev, generator=gen) * 0.02).to(bf) if args.bias else None
+        b2 = (torch.randn(h, device=dev, generator=gen) * 0.02).to(bf) if args.bias else None
+        db1 = torch.zeros(f, device=dev) if args.bias else None
+        db2 = torch.zeros(h, device=dev) if args.bias else None
+        blk = zb.make_block(M, h, f, has_bias=args.bias)
         S = []
         for _ in range(sets):
             t = {"X": torch.randn(M, h, device=dev, generator=gen).to(bf),
@@ -274,14 +278,14 @@ def run_sweep(args):
                  "H": torch.empty(M, f, device=dev, dtype=bf), "A": torch.empty(M, f, device=dev, dtype=bf),
                  "Y": torch.empty(M, h, device=dev, dtype=bf), "dH": torch.empty(M, f, device=dev, dtype=bf),
                  "dX": torch.empty(M, h, device=dev, dtype=bf)}
-            zb.zb_forward(blk, t["X"], W1, W2, None, None, t["H"], t["A"], t["Y"], stream)
+            zb.zb_forward(blk, t["X"], W1, W2, b1, b2, t["H"], t["A"], t["Y"], stream)
             zb.zb_backward_input(blk, t["dY"], W1, W2, t["H"], t["dH"], t["dX"], stream)
             S.append(t)
         passes = {
-            "F": lambda t, j: zb.zb_forward(blk, t["X"], W1, W2, None, None, t["H"], t["A"], t["Y"], stream),
+            "F": lambda t, j: zb.zb_forward(blk, t["X"], W1, W2, b1, b2, t["H"], t["A"], t["Y"], stream),
             "B": lambda t, j: zb.zb_backward_input(blk, t["dY"], W1, W2, t["H"], t["dH"], t["dX"], stream),
             "W": lambda t, j: zb.zb_backward_weight(blk, t["X"], t["A"], t["dH"], t["dY"], dW1, dW2,
-                                                    None, None, j > 0, stream),
+                                                    db1, db2, j > 0, stream),
         }
         pb = pass_bytes(M, h, f)
         for name, fn in passes.items():
@@ -301,7 +305,7 @@ def run_sweep(args):
             t_byte = pb[name] / (peaks["hbm"] * 1e9)
             bound = "tensor" if t_flop >= t_byte else "hbm"
             print(json.dumps({
-                "sweep": True, "pass": name, "M": M, "h": h, "f": f, "microbatches": m,
+                "sweep": True, "pass": name, "M": M, "h": h, "f": f, "microbatches": m, "bias": args.bias,
                 "us_per_pass": 1e3 * ms, "tflops": flops / (ms / 1e3) / 1e12,
                 "gb_per_s": pb[name] / (ms / 1e3) / 1e9,
                 "roofline": {"bound": bound, "time_us": 1e6 * max(t_flop, t_byte),
@@ -398,6 +402,8 @@ def main():
     ap.add_argument("--sweep-points", default="",
                     help="comma list of MxH points, e.g. 3072x6144 (default: the M x h grid)")
     ap.add_argument("--sweep-m", type=int, default=32, help="microbatches timed per pass")
+    ap.add_argument("--bias", action="store_true",
+                    help="sweep with biases: F adds b1/b2, W also accumulates db1 = colsum dH, db2 = colsum dY")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -82,16 +82,91 @@ __device__ __forceinline__ float to_f<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// One thread per column, rows summed in ascending order (coalesced across
-// the warp: consecutive threads read consecutive columns of a row).
+// Column sums db[c] (+)= sum_r X[r, c] with a fixed summation order.  A
+// cluster of COLSUM_SPLIT blocks covers 128 columns: block b of the cluster
+// sums the b-th contiguous range of rows; inside it each lane loads 4
+// adjacent elements of a row (8 or 16 bytes, so a warp reads 256 or 512
+// contiguous bytes per row) and warp w sums rows w, w + 8, ... of the range
+// in ascending order; the 8 warp partials are added in warp order, and block
+// 0 adds the blocks' partials in rank order, read from their shared memory
+// (distributed shared memory, no global scratch).  The order depends only on
+// the shape, so the same inputs give the same bits.
+constexpr int COLSUM_WARPS = 8;
+constexpr int COLSUM_COLS = 128;  // 32 lanes x 4 columns
+constexpr int COLSUM_SPLIT = 8;   // blocks (row ranges) per cluster
+
 template <typename T>
-__global__ void zb_colsum_kernel(const T* __restrict__ X, long long rows, long long cols,
-                                 long long ld, float* __restrict__ db, int accumulate) {
-    const long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= cols) return;
-    float acc = 0.0f;
-    for (long long r = 0; r < rows; ++r) acc += to_f<T>(X[r * ld + c]);
-    db[c] = accumulate ? db[c] + acc : acc;
+__device__ __forceinline__ void load4(const T* p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    v[0] = q.x;
+    v[1] = q.y;
+    v[2] = q.z;
+    v[3] = q.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
+    const uint2 q = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xffff0000u);
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+template <typename T>
+__global__ void __cluster_dims__(COLSUM_SPLIT, 1, 1) __launch_bounds__(COLSUM_WARPS * 32)
+    zb_colsum_kernel(const T* __restrict__ X, long long rows, long long cols, long long ld,
+                     float* __restrict__ db, int accumulate, int vec_ok) {
+    __shared__ float part[COLSUM_WARPS][COLSUM_COLS];
+    __shared__ float block_sum[COLSUM_COLS];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t rank = zbp::cluster_ctarank();
+    const long long cb = blockIdx.x / COLSUM_SPLIT;
+    const long long c0 = cb * COLSUM_COLS + 4 * lane;
+    const long long r_begin = rows * rank / COLSUM_SPLIT, r_end = rows * (rank + 1) / COLSUM_SPLIT;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (vec_ok && c0 + 4 <= cols) {
+#pragma unroll 4
+        for (long long r = r_begin + w; r < r_end; r += COLSUM_WARPS) {
+            float v[4];
+            load4<T>(X + r * ld + c0, v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] += v[i];
+        }
+    } else {
+        for (long long r = r_begin + w; r < r_end; r += COLSUM_WARPS)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (c0 + i < cols) acc[i] += to_f<T>(X[r * ld + c0 + i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) part[w][4 * lane + i] = acc[i];
+    __syncthreads();
+    if (threadIdx.x < COLSUM_COLS) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int k = 0; k < COLSUM_WARPS; ++k) sum += part[k][threadIdx.x];
+        block_sum[threadIdx.x] = sum;
+    }
+    zbp::cluster_sync();  // every block's partial is in its shared memory
+    if (rank == 0 && threadIdx.x < COLSUM_COLS) {
+        const long long c = cb * COLSUM_COLS + threadIdx.x;
+        if (c < cols) {
+            const uint32_t local = zbp::smem_u32(&block_sum[threadIdx.x]);
+            float sum = 0.0f;
+#pragma unroll
+            for (int b = 0; b < COLSUM_SPLIT; ++b) sum += ld_shared_cluster_f32(zbp::mapa_shared(local, b));
+            db[c] = accumulate ? db[c] + sum : sum;
+        }
+    }
+    zbp::cluster_sync();  // no block leaves while block 0 may still read it
 }
 
 // One thread waits on an mbarrier that nothing arrives on, for at most
@@ -220,9 +295,11 @@ zb_status gemm_f32_simt(const GemmF32& g, void* stream) {
 
 zb_status colsum_bf16(const void* X, int64_t rows, int64_t cols, int64_t ld, float* db,
                       int accumulate, void* stream) {
-    const unsigned blocks = static_cast<unsigned>((cols + 255) / 256);
-    zb_colsum_kernel<__nv_bfloat16><<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(X), rows, cols, ld, db, accumulate);
+    const unsigned blocks = static_cast<unsigned>((cols + COLSUM_COLS - 1) / COLSUM_COLS * COLSUM_SPLIT);
+    // 8-byte loads need 4-column groups that start 8-byte aligned
+    const int vec_ok = (reinterpret_cast<uintptr_t>(X) & 7u) == 0 && (ld & 3) == 0;
+    zb_colsum_kernel<__nv_bfloat16><<<blocks, COLSUM_WARPS * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(X), rows, cols, ld, db, accumulate, vec_ok);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("colsum launch: ") + cudaGetErrorString(e));
     return ZB_OK;
@@ -230,9 +307,10 @@ zb_status colsum_bf16(const void* X, int64_t rows, int64_t cols, int64_t ld, flo
 
 zb_status colsum_f32(const float* X, int64_t rows, int64_t cols, int64_t ld, float* db,
                      int accumulate, void* stream) {
-    const unsigned blocks = static_cast<unsigned>((cols + 255) / 256);
-    zb_colsum_kernel<float><<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(X, rows, cols, ld, db,
-                                                                                 accumulate);
+    const unsigned blocks = static_cast<unsigned>((cols + COLSUM_COLS - 1) / COLSUM_COLS * COLSUM_SPLIT);
+    const int vec_ok = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ld & 3) == 0;
+    zb_colsum_kernel<float><<<blocks, COLSUM_WARPS * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        X, rows, cols, ld, db, accumulate, vec_ok);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("colsum launch: ") + cudaGetErrorString(e));
     return ZB_OK;
