@@ -344,12 +344,24 @@ def measure_post_validated_adamw(zb, h, f, dev, stream, peaks, steps=5, warmup=3
         stages.append(st)
     nbytes = zb.zb_grad_stats_scratch_bytes()
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    states = []
-    for st in stages:
-        o = torch.zeros(2, dtype=torch.float64, device=dev)
-        zb.zb_grad_stats([d["grad"] for d in st], [n, n], o, scratch, nbytes, stream)
-        torch.cuda.synchronize()
-        states.append(o)
+    states = [torch.zeros(2, dtype=torch.float64, device=dev) for _ in stages]
+
+    def stats_all():
+        for st, o in zip(stages, states):
+            zb.zb_grad_stats([d["grad"] for d in st], [n, n], o, scratch, nbytes, stream)
+
+    for _ in range(warmup):
+        stats_all()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(steps):
+        stats_all()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    stats_ms = g0.elapsed_time(g1) / steps
+    stats_bytes = 4.0 * 2 * n * P  # every gradient element read once
+    stats_gbs = stats_bytes / (stats_ms / 1e3) / 1e9
     sq = [float(o[0]) for o in states]
     c = (sq[0] * (sq[0] + sq[1])) ** 0.25  # geometric mean of the two partial norms
     dec = torch.empty(P * 40, dtype=torch.uint8, device=dev)
@@ -374,7 +386,12 @@ def measure_post_validated_adamw(zb, h, f, dev, stream, peaks, steps=5, warmup=3
             "ms": ms, "rolled_back": rolled, "algorithmic_bytes": algo,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"]},
-            "launches_per_step": 3}
+            "launches_per_step": 3,
+            "grad_stats": {"what": "sum of squares and NaN/Inf count of both stages' gradients "
+                                   "(the staged-reduce inputs), 4 bytes per element",
+                           "ms": stats_ms, "bytes": stats_bytes,
+                           "roofline": {"bound": "hbm", "achieved": stats_gbs, "peak": peaks["hbm"],
+                                        "unit": "GB/s", "frac": stats_gbs / peaks["hbm"]}}}
 
 
 def main():

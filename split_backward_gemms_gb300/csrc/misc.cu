@@ -208,16 +208,29 @@ __global__ void __launch_bounds__(STATS_THREADS)
     const unsigned long long per = (n4 + STATS_BLOCKS - 1) / STATS_BLOCKS;
     const unsigned long long lo = per * blockIdx.x;
     const unsigned long long hi = min(lo + per, n4);
-    float sq = 0.0f;
+    // four float4 loads in flight per thread, four accumulators combined in
+    // a fixed order; the tail goes to the first
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
     unsigned bad = 0;
-    for (unsigned long long i = lo + threadIdx.x; i < hi; i += STATS_THREADS) {
-        const float4 v = reinterpret_cast<const float4*>(x)[i];
-        sq = fmaf(v.x, v.x, sq);
-        sq = fmaf(v.y, v.y, sq);
-        sq = fmaf(v.z, v.z, sq);
-        sq = fmaf(v.w, v.w, sq);
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    auto add = [&](const float4& v, float& a) {
+        a = fmaf(v.x, v.x, a);
+        a = fmaf(v.y, v.y, a);
+        a = fmaf(v.z, v.z, a);
+        a = fmaf(v.w, v.w, a);
         bad += !isfinite(v.x) + !isfinite(v.y) + !isfinite(v.z) + !isfinite(v.w);
+    };
+    unsigned long long i = lo + threadIdx.x;
+    for (; i + 3ull * STATS_THREADS < hi; i += 4ull * STATS_THREADS) {
+        const float4 v0 = x4[i], v1 = x4[i + STATS_THREADS];
+        const float4 v2 = x4[i + 2 * STATS_THREADS], v3 = x4[i + 3 * STATS_THREADS];
+        add(v0, a0);
+        add(v1, a1);
+        add(v2, a2);
+        add(v3, a3);
     }
+    for (; i < hi; i += STATS_THREADS) add(x4[i], a0);
+    float sq = (a0 + a1) + (a2 + a3);
     if (blockIdx.x == 0 && threadIdx.x < n - 4 * n4) {  // the last n mod 4 elements
         const float v = x[4 * n4 + threadIdx.x];
         sq = fmaf(v, v, sq);
