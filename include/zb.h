@@ -76,8 +76,18 @@ typedef struct zb_block {
     int32_t dtype;    /* zb_dtype of X, W, H, A, Y, dY, dH, dX, b              */
     int32_t act;      /* zb_act                                                */
     int32_t has_bias; /* 1: b1/b2 added in F, db1/db2 accumulated in W         */
-    int32_t reserved; /* must be 0                                             */
+    int32_t flags;    /* ZB_BLOCK_* bits; others must be 0                     */
 } zb_block;
+
+/* zb_block.flags.  Split K: when a bf16-output GEMM of zb_forward or
+ * zb_backward_input has too few output tiles to occupy the GPU, those
+ * entry points split its K loop over a cluster of 2 or 4 CTAs and add the
+ * fp32 partial sums in a fixed order (deterministic: the same inputs give
+ * the same bits; the sums differ from the unsplit ones in rounding order
+ * only).  The replay (zb_run_stage_schedule) never splits, so its results
+ * do not depend on how many streams it spreads over; a caller that compares
+ * single passes with a replay bit for bit sets ZB_BLOCK_NO_SPLIT_K. */
+#define ZB_BLOCK_NO_SPLIT_K 1
 
 /* Supported combinations: BF16 with any zb_act (tensor-core path, fp32
  * accumulation); F32 with ZB_ACT_NONE (true fp32 FFMA path, no TF32). */

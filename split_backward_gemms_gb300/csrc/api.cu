@@ -35,7 +35,7 @@ bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) !
 
 zb_status check_block(const zb_block* b) {
     if (!b) return fail(ZB_ERR_INVALID_ARG, "block is NULL");
-    if (b->reserved != 0) return fail(ZB_ERR_INVALID_ARG, "block.reserved must be 0");
+    if (b->flags & ~ZB_BLOCK_NO_SPLIT_K) return fail(ZB_ERR_INVALID_ARG, "unknown bits in block.flags");
     if (b->M <= 0 || b->h <= 0 || b->f <= 0) return fail(ZB_ERR_SHAPE, "M, h and f must be >= 1");
     if (b->M > (1LL << 30) || b->h > (1LL << 30) || b->f > (1LL << 30))
         return fail(ZB_ERR_SHAPE, "M, h and f must be <= 2^30");
@@ -126,11 +126,19 @@ zb_status timed(Recorder* rec, bool gemm, F&& launch) {
 }
 
 thread_local int* g_gemm_counter = nullptr;  // GEMM launch count of the running replay
+// A replay is running: its GEMMs never split K, so its results do not depend
+// on the number of lanes.  With several lanes an under-filled GEMM's idle
+// SMs are taken by other lanes' GEMMs anyway, and splitting would only add
+// the partial-tile exchange (measured on the 4-stage h=1024 replay on four
+// streams: 963 TF/s unsplit, 898 split).
+thread_local bool g_in_replay = false;
 
 zb_status run_gemm(const GemmBf16& g, void* stream, Recorder* rec) {
     if (g_gemm_counter) ++*g_gemm_counter;
     return timed(rec, true, [&] { return gemm_bf16_tc(g, stream); });
 }
+
+int split_allowed(const zb_block& b) { return !g_in_replay && !(b.flags & ZB_BLOCK_NO_SPLIT_K); }
 
 zb_status run_gemm32(const GemmF32& g, void* stream, Recorder* rec) {
     if (g_gemm_counter) ++*g_gemm_counter;
@@ -153,7 +161,7 @@ zb_status forward_impl(const zb_block& b, const void* X, const void* W1, const v
         g.A = X; g.lda = b.h; g.a_mn = 0;
         g.B = W1; g.ldb = b.f; g.b_mn = 1;
         g.epi = EPI_STORE_BF16; g.out0 = Y; g.ld0 = b.f;
-        g.bias = b.has_bias ? b1 : nullptr;
+        g.bias = b.has_bias ? b1 : nullptr; g.allow_split = split_allowed(b);
         return run_gemm(g, stream, rec);
     }
     GemmBf16 g1;  // H = X W1 (+b1), A = GeLU(H)
@@ -161,7 +169,7 @@ zb_status forward_impl(const zb_block& b, const void* X, const void* W1, const v
     g1.A = X; g1.lda = b.h; g1.a_mn = 0;
     g1.B = W1; g1.ldb = b.f; g1.b_mn = 1;
     g1.epi = EPI_GELU_DUAL; g1.out0 = H; g1.ld0 = b.f; g1.out1 = A; g1.ld1 = b.f;
-    g1.bias = b.has_bias ? b1 : nullptr; g1.act = b.act;
+    g1.bias = b.has_bias ? b1 : nullptr; g1.act = b.act; g1.allow_split = split_allowed(b);
     zb_status s = run_gemm(g1, stream, rec);
     if (s != ZB_OK) return s;
     GemmBf16 g2;  // Y = A W2 (+b2)
@@ -169,7 +177,7 @@ zb_status forward_impl(const zb_block& b, const void* X, const void* W1, const v
     g2.A = A; g2.lda = b.f; g2.a_mn = 0;
     g2.B = W2; g2.ldb = b.h; g2.b_mn = 1;
     g2.epi = EPI_STORE_BF16; g2.out0 = Y; g2.ld0 = b.h;
-    g2.bias = b.has_bias ? b2 : nullptr;
+    g2.bias = b.has_bias ? b2 : nullptr; g2.allow_split = split_allowed(b);
     return run_gemm(g2, stream, rec);
 }
 
@@ -188,7 +196,7 @@ zb_status backward_input_impl(const zb_block& b, const void* dY, const void* W1,
         g.Mg = b.M; g.Ng = b.h; g.Kg = b.f;
         g.A = dY; g.lda = b.f; g.a_mn = 0;
         g.B = W1; g.ldb = b.f; g.b_mn = 0;
-        g.epi = EPI_STORE_BF16; g.out0 = dX; g.ld0 = b.h;
+        g.epi = EPI_STORE_BF16; g.out0 = dX; g.ld0 = b.h; g.allow_split = split_allowed(b);
         return run_gemm(g, stream, rec);
     }
     GemmBf16 g3;  // dH = (dY W2^T) * GeLU'(H); dA stays in fp32 in TMEM
@@ -196,13 +204,14 @@ zb_status backward_input_impl(const zb_block& b, const void* dY, const void* W1,
     g3.A = dY; g3.lda = b.h; g3.a_mn = 0;
     g3.B = W2; g3.ldb = b.h; g3.b_mn = 0;
     g3.epi = EPI_GELU_BWD; g3.out0 = dH; g3.ld0 = b.f; g3.aux = H; g3.ldaux = b.f; g3.act = b.act;
+    g3.allow_split = split_allowed(b);
     zb_status s = run_gemm(g3, stream, rec);
     if (s != ZB_OK) return s;
     GemmBf16 g4;  // dX = dH W1^T
     g4.Mg = b.M; g4.Ng = b.h; g4.Kg = b.f;
     g4.A = dH; g4.lda = b.f; g4.a_mn = 0;
     g4.B = W1; g4.ldb = b.f; g4.b_mn = 0;
-    g4.epi = EPI_STORE_BF16; g4.out0 = dX; g4.ld0 = b.h;
+    g4.epi = EPI_STORE_BF16; g4.out0 = dX; g4.ld0 = b.h; g4.allow_split = split_allowed(b);
     return run_gemm(g4, stream, rec);
 }
 
@@ -417,6 +426,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     std::vector<std::pair<size_t, size_t>> op_span(n_ops, {0, 0});  // [first span, end span)
     int gemms = 0;
     g_gemm_counter = &gemms;
+    g_in_replay = true;
     std::vector<char> w_started(P, 0);
     std::vector<int> last_w_op(P, -1);  // latest W / BW of each stage, for OPT
 
@@ -519,6 +529,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         }
     }
     g_gemm_counter = nullptr;
+    g_in_replay = false;
     if (s != ZB_OK) return s;
 
     if (stats) {

@@ -27,8 +27,19 @@
 //           the B traffic per SM.  Copies of both CTAs complete on the even
 //           CTA's barriers; MMA completion is multicast back to both.
 // Tiles are visited in a fixed order (tile = cluster + i * clusters, grouped
-// rasterisation, see tile_coords) and K is never split, so results are
-// deterministic for a given shape.
+// rasterisation, see tile_coords), so results are deterministic for a given
+// shape.
+// Split K (CG = 1 only, bf16-output epilogues): when a problem has too few
+// tiles to occupy the SMs, a cluster of S CTAs (S = 2 or 4) computes one
+// 128x256 tile, CTA r over the r-th of S contiguous K ranges.  CTA r owns
+// columns [r 256/S, (r+1) 256/S) of the tile.  Each CTA writes its fp32
+// partial into its own (then idle) operand ring as S slabs, one per owner;
+// after a cluster barrier (every ring idle, every partial written) each CTA
+// sends slab o to CTA o with one bulk copy through distributed shared memory
+// (the copy engine moves it; completion counted in bytes on CTA o's
+// mbarrier).  CTA o then sums its S slabs from its own shared memory in rank
+// order 0..S-1 (a fixed order, so the result is still deterministic),
+// applies the epilogue and stores it.  No global workspace is involved.
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets the
 // device error word, drains its in-flight copies and MMAs, frees TMEM and
 // returns.
@@ -81,6 +92,7 @@ struct SharedCtl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    uint64_t xchg;  // split K: bytes of the other CTAs' slabs received
 };
 
 template <int CG>
@@ -102,6 +114,7 @@ struct EpiArgs {
     const __nv_bfloat16* bias;
     int accumulate;
     int act;
+    int ksplit;  // CTAs per tile along K (1 = no split; CG = 1 only)
     unsigned int* err;
 };
 
@@ -378,6 +391,146 @@ __device__ __forceinline__ void staging_release(const CUtensorMap* tm, uint32_t 
     }
 }
 
+// ---------------------------------------------------------------- split K
+// GeLU and GeLU' of an element pair (exact-erf form), as in the tile epilogue.
+__device__ __forceinline__ f32x2 gelu_pair(f32x2 X) {
+    f32x2 PHI, E;
+    normal_cdf_and_exp2(X, PHI, E);
+    return mul2(X, PHI);
+}
+__device__ __forceinline__ f32x2 gelu_grad_pair(f32x2 H) {
+    f32x2 PHI, E;
+    normal_cdf_and_exp2(H, PHI, E);
+    return fma2(mul2(H, pk2(0.3989422804014327f, 0.3989422804014327f)), E, PHI);
+}
+
+// The epilogue of one row's 4 consecutive columns (col a multiple of 4, all
+// four inside the matrix), from their fp32 sums.
+template <int EPI>
+__device__ __forceinline__ void epilogue4(const EpiArgs& args, int row, int col, float (&x)[4]) {
+    if ((EPI == zb::EPI_STORE_BF16 || EPI == zb::EPI_GELU_DUAL) && args.bias) {
+        const uint2 b = *reinterpret_cast<const uint2*>(args.bias + col);
+        const float2 b0 = unpack_bf16x2(b.x), b1 = unpack_bf16x2(b.y);
+        x[0] += b0.x;
+        x[1] += b0.y;
+        x[2] += b1.x;
+        x[3] += b1.y;
+    }
+    if (EPI == zb::EPI_GELU_BWD) {
+        const uint2 hv =
+            *reinterpret_cast<const uint2*>(args.aux + static_cast<long long>(row) * args.ldaux + col);
+        const float2 h0 = unpack_bf16x2(hv.x), h1 = unpack_bf16x2(hv.y);
+        if (args.act == ZB_ACT_GELU_TANH) {
+            x[0] *= gelu_grad_t<true>(h0.x);
+            x[1] *= gelu_grad_t<true>(h0.y);
+            x[2] *= gelu_grad_t<true>(h1.x);
+            x[3] *= gelu_grad_t<true>(h1.y);
+        } else {
+            up2(mul2(pk2(x[0], x[1]), gelu_grad_pair(pk2(h0.x, h0.y))), x[0], x[1]);
+            up2(mul2(pk2(x[2], x[3]), gelu_grad_pair(pk2(h1.x, h1.y))), x[2], x[3]);
+        }
+    }
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(args.out0) + static_cast<long long>(row) * args.ld0 +
+                              col) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    if (EPI == zb::EPI_GELU_DUAL) {
+        float g[4];
+        if (args.act == ZB_ACT_GELU_TANH) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) g[i] = gelu_t<true>(x[i]);
+        } else {
+            up2(gelu_pair(pk2(x[0], x[1])), g[0], g[1]);
+            up2(gelu_pair(pk2(x[2], x[3])), g[2], g[3]);
+        }
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(args.out1) +
+                                  static_cast<long long>(row) * args.ld1 + col) =
+            make_uint2(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]));
+    }
+}
+
+// Split-K layout in a CTA's shared memory (ring and staging area, 224 KiB):
+// its own partial tile as ks slabs at slab o (the columns CTA o owns), then
+// ks - 1 receive slots, slot(r) for the slab that CTA r sends.  A slab holds
+// 128 rows of 1024/ks bytes, 16-byte chunk j of row i at chunk j ^ (i mod 8)
+// (a row has at least 8 chunks, so the swizzle stays inside it; the rows
+// written by the 8 lanes of a quarter-warp, or the chunks read by 8
+// consecutive threads, hit 8 different bank groups).
+constexpr uint32_t SPLIT_PARTIAL_BYTES = BM * 1024u;  // one fp32 128 x 256 tile
+constexpr int SPLIT_MAX = 4;
+__host__ __device__ constexpr uint32_t split_slab_bytes(int ks) {
+    return SPLIT_PARTIAL_BYTES / static_cast<uint32_t>(ks);
+}
+static_assert(SPLIT_PARTIAL_BYTES + (SPLIT_MAX - 1) * split_slab_bytes(SPLIT_MAX) <=
+                  Cfg<1>::STAGES * Cfg<1>::STAGE_BYTES + STAGING_BYTES,
+              "split-K slabs and receive slots fit in the ring and staging area");
+__device__ __forceinline__ uint32_t split_chunk_offset(int ks, int row, int j) {
+    return static_cast<uint32_t>(row) * (1024u / static_cast<uint32_t>(ks)) +
+           (static_cast<uint32_t>(j ^ (row & 7)) << 4);
+}
+// receive slot of the slab from CTA r in CTA `owner` (r != owner)
+__device__ __forceinline__ uint32_t split_recv_offset(int ks, int r, int owner) {
+    return SPLIT_PARTIAL_BYTES + static_cast<uint32_t>(r < owner ? r : r - 1) * split_slab_bytes(ks);
+}
+
+// CTA `kslice` of a split-K cluster: sums its 256/ks columns of the tile at
+// (m0, n0) over the ks slabs in its shared memory (from `base`) in rank
+// order, then applies the epilogue.  Consecutive threads take consecutive
+// 16-byte chunks of a row (coalesced global stores); each thread carries
+// SPLIT_ILP chunks at once (loads first), so that the loop is not one
+// dependent chain of shared loads, adds and GeLU per chunk.
+constexpr int SPLIT_ILP = 4;
+template <int EPI>
+__device__ __forceinline__ void split_reduce_store(const EpiArgs& args_in, uint32_t base, int ks,
+                                                   int kslice, int m0, int n0) {
+    const EpiArgs args = args_in;
+    const int lg = ks == 2 ? 5 : 4;  // log2 of the chunks per owned row (ks = 2, 4)
+    const int items = BM << lg;
+    uint32_t src[SPLIT_MAX];
+#pragma unroll
+    for (int q = 0; q < SPLIT_MAX; ++q)
+        src[q] = base + (q == kslice ? static_cast<uint32_t>(kslice) * split_slab_bytes(ks)
+                                     : split_recv_offset(ks, q, kslice));
+    const int col0 = n0 + kslice * (BN / ks);
+    for (int i0 = threadIdx.x; i0 < items; i0 += SPLIT_ILP * NUM_THREADS) {
+        float x[SPLIT_ILP][4];
+        bool live[SPLIT_ILP];
+#pragma unroll
+        for (int u = 0; u < SPLIT_ILP; ++u) {
+            const int i = i0 + u * NUM_THREADS;
+            const int r = i >> lg;
+            const int j = i & ((1 << lg) - 1);
+            live[u] = i < items && m0 + r < args.Mg && col0 + 4 * j < args.Ng;
+            if (live[u]) {
+                const uint32_t off = static_cast<uint32_t>(r) * (16u << lg) +
+                                     (static_cast<uint32_t>(j ^ (r & 7)) << 4);
+                float4 p[SPLIT_MAX];
+#pragma unroll
+                for (int q = 0; q < SPLIT_MAX; ++q)
+                    if (q < ks) p[q] = zbp::ld_shared_v4(src[q] + off);
+                x[u][0] = p[0].x;
+                x[u][1] = p[0].y;
+                x[u][2] = p[0].z;
+                x[u][3] = p[0].w;
+#pragma unroll
+                for (int q = 1; q < SPLIT_MAX; ++q) {
+                    if (q < ks) {
+                        x[u][0] += p[q].x;
+                        x[u][1] += p[q].y;
+                        x[u][2] += p[q].z;
+                        x[u][3] += p[q].w;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < SPLIT_ILP; ++u) {
+            if (live[u]) {
+                const int i = i0 + u * NUM_THREADS;
+                epilogue4<EPI>(args, m0 + (i >> lg), col0 + 4 * (i & ((1 << lg) - 1)), x[u]);
+            }
+        }
+    }
+}
+
 template <int EPI, int A_MN, int B_MN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     zb_gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -395,14 +548,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // split K: CTAs per tile along K, and this CTA's K range (one tile per cluster)
+    constexpr bool SPLITTABLE = !PAIR && EPI != zb::EPI_F32;
+    const int ks = SPLITTABLE ? args.ksplit : 1;
     const uint32_t rank = PAIR ? zbp::cluster_ctarank() : 0u;
+    const int kslice = ks > 1 ? static_cast<int>(zbp::cluster_ctarank()) : 0;
     const bool leader = rank == 0;
-    const int cluster = blockIdx.x / CG;
-    const int clusters = gridDim.x / CG;
+    const int cw = PAIR ? 2 : ks;  // CTAs per cluster
+    const int cluster = blockIdx.x / cw;
+    const int clusters = gridDim.x / cw;
     const int tiles_m = (args.Mg + C::TILE_M - 1) / C::TILE_M;
     const int tiles_n = (args.Ng + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
-    const int num_kb = (args.Kg + BK - 1) / BK;
+    const int num_kb_all = (args.Kg + BK - 1) / BK;
+    const int kb_lo = SPLITTABLE ? static_cast<int>(static_cast<long long>(kslice) * num_kb_all / ks) : 0;
+    const int kb_hi =
+        SPLITTABLE ? static_cast<int>(static_cast<long long>(kslice + 1) * num_kb_all / ks) : num_kb_all;
+    const int num_kb = kb_hi - kb_lo;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -414,6 +576,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             zbp::mbar_init(zbp::smem_u32(&ctl->tempty[b]), 4 * CG);
         }
         zbp::mbar_init(zbp::smem_u32(&ctl->drain), 1);
+        if (SPLITTABLE) zbp::mbar_init(zbp::smem_u32(&ctl->xchg), 1);
         ctl->abort_flag = 0;
         zbp::fence_mbar_init();
     }
@@ -438,6 +601,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     zbp::tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
+    // split K: this CTA receives ks - 1 slabs (before any CTA can send: they
+    // send after the phase-1 cluster barrier, which this thread reaches later)
+    if (SPLITTABLE && ks > 1 && threadIdx.x == 0)
+        zbp::mbar_arrive_expect_tx(zbp::smem_u32(&ctl->xchg), static_cast<uint32_t>(ks - 1) * split_slab_bytes(ks));
 
     if (warp == 0) {
         if (lane == 0) {
@@ -449,7 +616,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
                 const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
                 const int nb0 = nb * BN + static_cast<int>(rank) * C::B_ROWS;
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t r = it / STAGES;
                     if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->empty[s]), (r & 1u) ^ 1u, abort_flag,
@@ -493,6 +660,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        if (SPLITTABLE && ks > 1) {
+            __syncwarp();
+            zbp::cluster_sync();  // split K, phase 1 (see the epilogue)
+        }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer
@@ -510,7 +681,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 zbp::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * ACC_COLS;
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t r = it / STAGES;
                     if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->full[s]), r & 1u, abort_flag, args.err,
@@ -531,7 +702,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bd =
                             B_MN ? zbp::smem_desc_sw128(sb + kk * 2048, MN_ATOM_BYTES, 1024)
                                  : zbp::smem_desc_sw128(sb + kk * 32, 16, 1024);
-                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        const uint32_t acc = (SPLITTABLE ? (kb != kb_lo || kk != 0) : ((kb | kk) != 0)) ? 1u : 0u;
                         if (PAIR)
                             zbp::tc_mma_f16_pair(d_tmem, ad, bd, idesc, acc);
                         else
@@ -555,6 +726,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 zbp::tc_commit(zbp::smem_u32(&ctl->drain));
             wait_bar<PAIR>(zbp::smem_u32(&ctl->drain), 0, abort_flag, args.err, ERR_WAIT_MMA,
                            DRAIN_LIMIT_NS, false);
+        }
+        if (SPLITTABLE && ks > 1) {
+            __syncwarp();
+            zbp::cluster_sync();  // split K, phase 1 (see the epilogue)
+        }
+    } else if (SPLITTABLE && ks > 1) {
+        // ---------------------------------------------- split-K epilogue
+        // One tile per cluster, in accumulator 0: its fp32 partial goes into
+        // this CTA's ring (idle once its MMAs are done) as ks slabs.  Phase 1
+        // (cluster barrier): every CTA's slabs are written and every ring is
+        // idle, so one thread sends slab o to CTA o with a bulk copy.  The
+        // owners sum after their receive barrier (after the role code).
+        const int q = warp & 3;
+        const int prow = q * 32 + lane;
+        const uint32_t base = zbp::smem_u32(smem);
+        const uint32_t slab = split_slab_bytes(ks);
+        const bool ok = cluster < num_tiles &&
+                        wait_bar<false>(zbp::smem_u32(&ctl->tfull[0]), 0, abort_flag, args.err,
+                                        ERR_WAIT_EPI, WAIT_LIMIT_NS, true);
+        zbp::tc_fence_after();
+        if (ok) {
+            const int sw = BN / ks;  // columns per owner
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; c += 2) {
+                uint32_t v[2][32];
+                zbp::tmem_ld_32x32b_x32(taddr + c * 32, v[0]);
+                zbp::tmem_ld_32x32b_x32(taddr + c * 32 + 32, v[1]);
+                zbp::tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int o = ((c + h) * 32) / sw;           // owner of these 32 columns
+                    const int j0 = ((c + h) * 32 - o * sw) / 4;  // their first chunk in its rows
+                    const uint32_t dst = base + static_cast<uint32_t>(o) * slab;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        zbp::st_shared_v4(dst + split_chunk_offset(ks, prow, j0 + k), v[h][4 * k],
+                                          v[h][4 * k + 1], v[h][4 * k + 2], v[h][4 * k + 3]);
+                }
+            }
+        }
+        zbp::fence_proxy_async_smem();  // the slabs are read by the copy engine next
+        __syncwarp();
+        zbp::cluster_sync();
+        if (ok && warp == 2 && lane == 0) {
+            for (int o = 0; o < ks; ++o) {
+                if (o == kslice) continue;
+                const uint32_t dst = zbp::mapa_shared(base + split_recv_offset(ks, kslice, o), static_cast<uint32_t>(o));
+                const uint32_t bar = zbp::mapa_shared(zbp::smem_u32(&ctl->xchg), static_cast<uint32_t>(o));
+                zbp::bulk_copy_s2cluster(dst, base + static_cast<uint32_t>(o) * slab, slab, bar);
+            }
         }
     } else {
         // ---------------------------------------------------- epilogue
@@ -700,6 +922,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     __syncthreads();
     if (PAIR) zbp::cluster_sync();  // no remote arrivals or copies remain
+    if (SPLITTABLE && ks > 1) {
+        // the other CTAs' slabs have landed here (waited for even after an
+        // abort, so that no copy still writes this CTA's shared memory once it
+        // exits; bounded like every wait)
+        const bool got = cluster < num_tiles &&
+                         wait_bar<false>(zbp::smem_u32(&ctl->xchg), 0, abort_flag, args.err, ERR_WAIT_EPI,
+                                         WAIT_LIMIT_NS, false);
+        if (got && !*abort_flag) {
+            int mb, nb;
+            tile_coords(cluster, tiles_m, tiles_n, C::GROUP_M, mb, nb);
+            split_reduce_store<EPI>(args, zbp::smem_u32(smem), ks, kslice, mb * C::TILE_M, nb * BN);
+        }
+        zbp::cluster_sync();  // phase 2: every copy out of this CTA's slabs has landed
+    }
     if (warp == 1) {
         zbp::tc_fence_after();
         if (PAIR)
@@ -811,14 +1047,51 @@ zb_status configure(int* max_ctas) {
     return ZB_OK;
 }
 
+// Co-resident clusters of `ks` one-tile CTAs (split K), per device.
+template <int EPI, int A_MN, int B_MN>
+int split_clusters(int ks) {
+    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, 1>;
+    static int cached[64][4] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int slot = ks == 2 ? 1 : ks == 4 ? 2 : 3;
+    if (dev < 0 || dev >= 64) return 0;
+    if (!cached[dev][slot]) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ks * 64, 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes<1>();
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = ks;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = -1;  // no clusters of this size: never split this far
+        }
+        cached[dev][slot] = n;
+    }
+    return cached[dev][slot];
+}
+
 template <int EPI, int A_MN, int B_MN, int CG>
-zb_status launch(const Maps& mp, const EpiArgs& ea, long long tiles, cudaStream_t st) {
+zb_status launch(const Maps& mp, EpiArgs ea, long long tiles, cudaStream_t st) {
     auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG>;
     int max_ctas = 0;
     zb_status s = configure<EPI, A_MN, B_MN, CG>(&max_ctas);
     if (s != ZB_OK) return s;
+    // a split pays only while every cluster of its grid is resident at once
+    // (one tile each; a second wave of clusters would double the time)
+    int ks = (CG == 1 && EPI != zb::EPI_F32) ? ea.ksplit : 1;
+    while (ks > 1 && split_clusters<EPI, A_MN, B_MN>(ks) < tiles) ks /= 2;
+    ea.ksplit = ks;
     const long long want = tiles * CG;
-    const int grid = static_cast<int>(want < max_ctas ? want : max_ctas);
+    const int grid = ks > 1 ? static_cast<int>(tiles * ks) : static_cast<int>(want < max_ctas ? want : max_ctas);
+    const int cw = CG == 2 ? 2 : ks;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -826,11 +1099,11 @@ zb_status launch(const Maps& mp, const EpiArgs& ea, long long tiles, cudaStream_
     cfg.stream = st;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = CG;
+    attr.val.clusterDim.x = cw;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
-    cfg.numAttrs = CG == 2 ? 1 : 0;
+    cfg.numAttrs = cw > 1 ? 1 : 0;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.o0, mp.o1, ea);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -871,6 +1144,28 @@ int choose_cta_group(long long pair_tiles) {
     if (forced) return forced;
     const int pairs = sm_count() / 2;
     return pair_tiles >= pairs ? 2 : 1;
+}
+
+// Split-K factor for a one-CTA-per-tile GEMM: the largest S in {2, 4}
+// whose S x tiles CTAs fit on the SMs at once with at least min_kb K blocks
+// (of 64) per CTA; 1 when the tiles alone fill the GPU or K is short.
+// ZB_GEMM_SPLIT_K=1 or 2 in the environment caps S (1 disables it);
+// ZB_GEMM_SPLIT_MIN_KB sets min_kb.
+int choose_split(long long tiles, long long num_kb) {
+    static int cap = -1;
+    static int min_kb = 16;
+    if (cap < 0) {
+        const char* v = std::getenv("ZB_GEMM_SPLIT_K");
+        const int c = v ? std::atoi(v) : SPLIT_MAX;
+        cap = (c == 1 || c == 2) ? c : SPLIT_MAX;
+        const char* w = std::getenv("ZB_GEMM_SPLIT_MIN_KB");
+        if (w && std::atoi(w) > 0) min_kb = std::atoi(w);
+    }
+    const int sms = sm_count();
+    int ks = 1;
+    for (int s = 2; s <= cap && s <= SPLIT_MAX; s *= 2)
+        if (tiles * s <= sms && num_kb >= static_cast<long long>(min_kb) * s) ks = s;
+    return ks;
 }
 
 }  // namespace
@@ -938,11 +1233,13 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     ea.bias = static_cast<const __nv_bfloat16*>(g.bias);
     ea.accumulate = g.accumulate;
     ea.act = g.act;
+    ea.ksplit = 1;
     ea.err = err;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cg == 2) return dispatch<2>(g, mp, ea, pair_tiles, st);
     const long long tiles = ((g.Mg + BM - 1) / BM) * ((g.Ng + BN - 1) / BN);
+    if (g.epi != EPI_F32 && g.allow_split) ea.ksplit = choose_split(tiles, (g.Kg + BK - 1) / BK);
     return dispatch<1>(g, mp, ea, tiles, st);
 }
 

@@ -592,6 +592,7 @@ extern "C" zb_status zb_simulate_schedule(int32_t kind, int32_t P, int32_t m, co
 extern "C" zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_op* ops, size_t n_ops,
                                                 size_t* bytes, size_t* peak_live_bytes) {
     if (!pl || !bytes) return zb::fail(ZB_ERR_INVALID_ARG, "pipeline or bytes is NULL");
+    if (pl->blk.flags & ~ZB_BLOCK_NO_SPLIT_K) return zb::fail(ZB_ERR_INVALID_ARG, "unknown bits in block.flags");
     std::vector<zb_op> vops;
     std::vector<int> dev;
     int L = 0;

@@ -43,6 +43,9 @@ struct GemmBf16 {
     const void* bias = nullptr;  // bf16 [Ng] or nullptr
     int accumulate = 0;
     int act = ZB_ACT_GELU_ERF;
+    // split K over a cluster of CTAs when the tiles alone leave SMs idle
+    // (bf16-output epilogues only)
+    int allow_split = 0;
 };
 zb_status gemm_bf16_tc(const GemmBf16& g, void* stream);
 

@@ -39,6 +39,7 @@ ZB_DT_BF16 = 1
 ZB_ACT_NONE = 0
 ZB_ACT_GELU_ERF = 1
 ZB_ACT_GELU_TANH = 2
+ZB_BLOCK_NO_SPLIT_K = 1  # zb_block.flags: single passes never split K
 
 ZB_OP_F, ZB_OP_B, ZB_OP_W, ZB_OP_BW, ZB_OP_OPT = range(5)
 OP_NAMES = ("F", "B", "W", "BW", "OPT")
@@ -52,7 +53,7 @@ LAYOUT_OF = {"1F1B-I": ZB_LAYOUT_CYCLIC, "ZBV": ZB_LAYOUT_V}
 # ---------------------------------------------------------------- structs
 class zb_block(C.Structure):
     _fields_ = [("M", C.c_int64), ("h", C.c_int64), ("f", C.c_int64), ("dtype", C.c_int32),
-                ("act", C.c_int32), ("has_bias", C.c_int32), ("reserved", C.c_int32)]
+                ("act", C.c_int32), ("has_bias", C.c_int32), ("flags", C.c_int32)]
 
 
 class zb_op(C.Structure):
@@ -195,8 +196,10 @@ def _check(st: int, where: str):
 
 
 def make_block(M: int, h: int, f: int, dtype: int = ZB_DT_BF16, act: int = ZB_ACT_GELU_ERF,
-               has_bias: bool = False) -> zb_block:
-    return zb_block(M, h, f, dtype, act, 1 if has_bias else 0, 0)
+               has_bias: bool = False, split_k: bool = True) -> zb_block:
+    """split_k=False sets ZB_BLOCK_NO_SPLIT_K (single passes sum K in the
+    replay's order)."""
+    return zb_block(M, h, f, dtype, act, 1 if has_bias else 0, 0 if split_k else ZB_BLOCK_NO_SPLIT_K)
 
 
 def ops_array(ops):

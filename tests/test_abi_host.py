@@ -403,3 +403,20 @@ def test_interleaved_at_the_pages_scales(zb, kind, P, v, m):
         assert res.bubble_rate < S.bubble_rate(S.make_schedule("ZBH1", P, m)[0], P, m, S.Times())
     else:
         assert abs(res.bubble_rate - (P - 1) / (v * m + P - 1)) < 1e-12
+
+
+def test_block_flags(zb):
+    """zb_block.flags: the binding's ZB_BLOCK_NO_SPLIT_K is the header's, a
+    block carrying it validates, and unknown bits are rejected."""
+    import re
+    hdr = open(os.path.join(ROOT, "include", "zb.h")).read()
+    assert int(re.search(r"#define ZB_BLOCK_NO_SPLIT_K (\d+)", hdr).group(1)) == zb.ZB_BLOCK_NO_SPLIT_K
+    P, m = 2, 3
+    _, ok = S.make_schedule("ZBH1", P, m)
+    blk = zb.make_block(64, 16, 32, split_k=False)
+    assert blk.flags == zb.ZB_BLOCK_NO_SPLIT_K and zb.make_block(64, 16, 32).flags == 0
+    zb.zb_schedule_workspace_size(zb.make_pipeline(P, m, blk), ok)
+    blk.flags = 2
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_schedule_workspace_size(zb.make_pipeline(P, m, blk), ok)
+    assert e.value.status == zb.ZB_ERR_INVALID_ARG

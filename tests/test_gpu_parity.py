@@ -256,7 +256,8 @@ def test_pipeline_p4_replays_bit_exact_and_match_oracle(zb):
             assert torch.equal(_bits(runs[kind][1][j]), _bits(runs["1F1B"][1][j]))
             assert torch.equal(_bits(runs[kind][2][j]), _bits(runs["1F1B"][2][j]))
     # the executor is the single-op passes, in order: compare with a hand chain
-    rec, Xs, dYs, dWs = _hand_chain(zb, blk, P, m, wts, X0, dY)
+    # (single passes with split K off: the replay never splits its K loops)
+    rec, Xs, dYs, dWs = _hand_chain(zb, zb.make_block(M, h, f, split_k=False), P, m, wts, X0, dY)
     for s in range(P):
         assert torch.equal(_bits(runs["ZBH1"][0][s]["dW1"]), _bits(dWs[s][0]))
         assert torch.equal(_bits(runs["ZBH1"][0][s]["dW2"]), _bits(dWs[s][1]))
