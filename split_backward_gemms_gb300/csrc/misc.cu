@@ -83,22 +83,34 @@ template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // Column sums db[c] (+)= sum_r X[r, c] with a fixed summation order.  A
-// cluster of COLSUM_SPLIT blocks covers 128 columns: block b of the cluster
-// sums the b-th contiguous range of rows; inside it each lane loads 4
-// adjacent elements of a row (8 or 16 bytes, so a warp reads 256 or 512
+// cluster of COLSUM_SPLIT blocks covers 32 x CPL columns: block b of the
+// cluster sums the b-th contiguous range of rows; inside it each lane loads
+// CPL adjacent elements of a row (8 or 16 bytes, so a warp reads 256 or 512
 // contiguous bytes per row) and warp w sums rows w, w + 8, ... of the range
 // in ascending order; the 8 warp partials are added in warp order, and block
 // 0 adds the blocks' partials in rank order, read from their shared memory
-// (distributed shared memory, no global scratch).  The order depends only on
-// the shape, so the same inputs give the same bits.
+// (distributed shared memory, no global scratch).  Every column's additions
+// come in the same order whatever CPL is, so the same inputs give the same
+// bits.  bf16
+// matrices take CPL = 8 (16-byte loads) when that still gives two blocks per
+// SM, else CPL = 4 (twice the blocks): the db1 sum of an h=6144 block (24576
+// columns) is then 768 blocks, one wave (1536 with CPL = 4 was a second wave
+// of 26 %), and the db2 sum (6144 columns) keeps 384 blocks.
 constexpr int COLSUM_WARPS = 8;
-constexpr int COLSUM_COLS = 128;  // 32 lanes x 4 columns
-constexpr int COLSUM_SPLIT = 8;   // blocks (row ranges) per cluster
+constexpr int COLSUM_SPLIT = 8;  // blocks (row ranges) per cluster
 
-template <typename T>
-__device__ __forceinline__ void load4(const T* p, float (&v)[4]);
+template <typename T, int CPL>
+__device__ __forceinline__ void load_cols(const T* p, float (&v)[CPL]);
 template <>
-__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+__device__ __forceinline__ void load_cols<__nv_bfloat16, 4>(const __nv_bfloat16* p, float (&v)[4]) {
+    const uint2 q = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xffff0000u);
+}
+template <>
+__device__ __forceinline__ void load_cols<float, 4>(const float* p, float (&v)[4]) {
     const float4 q = *reinterpret_cast<const float4*>(p);
     v[0] = q.x;
     v[1] = q.y;
@@ -106,12 +118,26 @@ __device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
     v[3] = q.w;
 }
 template <>
-__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
-    const uint2 q = *reinterpret_cast<const uint2*>(p);
-    v[0] = __uint_as_float(q.x << 16);
-    v[1] = __uint_as_float(q.x & 0xffff0000u);
-    v[2] = __uint_as_float(q.y << 16);
-    v[3] = __uint_as_float(q.y & 0xffff0000u);
+__device__ __forceinline__ void load_cols<__nv_bfloat16, 8>(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+int sm_count_misc() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
 }
 
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
@@ -120,50 +146,56 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
     return v;
 }
 
-template <typename T>
+template <typename T, int CPL>
 __global__ void __cluster_dims__(COLSUM_SPLIT, 1, 1) __launch_bounds__(COLSUM_WARPS * 32)
     zb_colsum_kernel(const T* __restrict__ X, long long rows, long long cols, long long ld,
                      float* __restrict__ db, int accumulate, int vec_ok) {
-    __shared__ float part[COLSUM_WARPS][COLSUM_COLS];
-    __shared__ float block_sum[COLSUM_COLS];
+    constexpr int COLS = 32 * CPL;  // columns per cluster
+    __shared__ float part[COLSUM_WARPS][COLS];
+    __shared__ float block_sum[COLS];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t rank = zbp::cluster_ctarank();
     const long long cb = blockIdx.x / COLSUM_SPLIT;
-    const long long c0 = cb * COLSUM_COLS + 4 * lane;
+    const long long c0 = cb * COLS + CPL * lane;
     const long long r_begin = rows * rank / COLSUM_SPLIT, r_end = rows * (rank + 1) / COLSUM_SPLIT;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (vec_ok && c0 + 4 <= cols) {
-#pragma unroll 4
-        for (long long r = r_begin + w; r < r_end; r += COLSUM_WARPS) {
-            float v[4];
-            load4<T>(X + r * ld + c0, v);
+    float acc[CPL];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] += v[i];
+    for (int i = 0; i < CPL; ++i) acc[i] = 0.0f;
+    if (vec_ok && c0 + CPL <= cols) {
+        // 8 rows' loads in flight per lane (128 bytes)
+#pragma unroll 8
+        for (long long r = r_begin + w; r < r_end; r += COLSUM_WARPS) {
+            float v[CPL];
+            load_cols<T, CPL>(X + r * ld + c0, v);
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) acc[i] += v[i];
         }
     } else {
         for (long long r = r_begin + w; r < r_end; r += COLSUM_WARPS)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < CPL; ++i)
                 if (c0 + i < cols) acc[i] += to_f<T>(X[r * ld + c0 + i]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) part[w][4 * lane + i] = acc[i];
+    for (int i = 0; i < CPL; ++i) part[w][CPL * lane + i] = acc[i];
     __syncthreads();
-    if (threadIdx.x < COLSUM_COLS) {
+    for (int c = threadIdx.x; c < COLS; c += COLSUM_WARPS * 32) {
         float sum = 0.0f;
 #pragma unroll
-        for (int k = 0; k < COLSUM_WARPS; ++k) sum += part[k][threadIdx.x];
-        block_sum[threadIdx.x] = sum;
+        for (int k = 0; k < COLSUM_WARPS; ++k) sum += part[k][c];
+        block_sum[c] = sum;
     }
     zbp::cluster_sync();  // every block's partial is in its shared memory
-    if (rank == 0 && threadIdx.x < COLSUM_COLS) {
-        const long long c = cb * COLSUM_COLS + threadIdx.x;
-        if (c < cols) {
-            const uint32_t local = zbp::smem_u32(&block_sum[threadIdx.x]);
-            float sum = 0.0f;
+    if (rank == 0) {
+        for (int t = threadIdx.x; t < COLS; t += COLSUM_WARPS * 32) {
+            const long long c = cb * COLS + t;
+            if (c < cols) {
+                const uint32_t local = zbp::smem_u32(&block_sum[t]);
+                float sum = 0.0f;
 #pragma unroll
-            for (int b = 0; b < COLSUM_SPLIT; ++b) sum += ld_shared_cluster_f32(zbp::mapa_shared(local, b));
-            db[c] = accumulate ? db[c] + sum : sum;
+                for (int b = 0; b < COLSUM_SPLIT; ++b) sum += ld_shared_cluster_f32(zbp::mapa_shared(local, b));
+                db[c] = accumulate ? db[c] + sum : sum;
+            }
         }
     }
     zbp::cluster_sync();  // no block leaves while block 0 may still read it
@@ -189,7 +221,7 @@ __global__ void zb_selftest_wait_kernel(unsigned int* err, unsigned long long li
 // Fixed partition (independent of the device): every buffer is cut into
 // STATS_BLOCKS ranges of float4 groups; each thread sums the squares of its
 // strided groups in fp32, the block combines the threads in fp64 in a fixed
-// tree, and one thread adds the partials in index order.
+// tree, and one block adds the partials in a fixed order (the final kernel).
 constexpr int STATS_BLOCKS = 304;
 constexpr int STATS_THREADS = 256;
 constexpr int STATS_MAX_BUFS = 4;
@@ -258,14 +290,37 @@ __global__ void __launch_bounds__(STATS_THREADS)
     }
 }
 
-__global__ void zb_grad_stats_final_kernel(const double* part, int nbufs, double* out) {
+// One block adds the partials: thread t takes partials t, t + 256, ... in
+// index order, then a fixed tree (shuffles, then the warps in order).  A
+// single thread walking all of them would wait on one dependent load after
+// another (~0.1 ms for 1216 partials, longer than the partial kernel itself
+// on a few hundred MB).
+__global__ void __launch_bounds__(STATS_THREADS)
+    zb_grad_stats_final_kernel(const double* part, int nbufs, double* out) {
     double a = 0.0, c = 0.0;
-    for (int i = 0; i < nbufs * STATS_BLOCKS; ++i) {
+    for (int i = threadIdx.x; i < nbufs * STATS_BLOCKS; i += STATS_THREADS) {
         a += part[2 * i];
         c += part[2 * i + 1];
     }
-    out[0] = a;
-    out[1] = c;
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_down_sync(0xffffffffu, a, o);
+        c += __shfl_down_sync(0xffffffffu, c, o);
+    }
+    __shared__ double sa[STATS_THREADS / 32], sc[STATS_THREADS / 32];
+    if ((threadIdx.x & 31) == 0) {
+        sa[threadIdx.x >> 5] = a;
+        sc[threadIdx.x >> 5] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double ta = 0.0, tc = 0.0;
+        for (int w = 0; w < STATS_THREADS / 32; ++w) {
+            ta += sa[w];
+            tc += sc[w];
+        }
+        out[0] = ta;
+        out[1] = tc;
+    }
 }
 
 }  // namespace
@@ -308,11 +363,20 @@ zb_status gemm_f32_simt(const GemmF32& g, void* stream) {
 
 zb_status colsum_bf16(const void* X, int64_t rows, int64_t cols, int64_t ld, float* db,
                       int accumulate, void* stream) {
-    const unsigned blocks = static_cast<unsigned>((cols + COLSUM_COLS - 1) / COLSUM_COLS * COLSUM_SPLIT);
-    // 8-byte loads need 4-column groups that start 8-byte aligned
-    const int vec_ok = (reinterpret_cast<uintptr_t>(X) & 7u) == 0 && (ld & 3) == 0;
-    zb_colsum_kernel<__nv_bfloat16><<<blocks, COLSUM_WARPS * 32, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(X), rows, cols, ld, db, accumulate, vec_ok);
+    const auto* x = static_cast<const __nv_bfloat16*>(X);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long wide_blocks = (cols + 255) / 256 * COLSUM_SPLIT;
+    if (wide_blocks >= 2LL * sm_count_misc()) {
+        // 16-byte loads need 8-column groups that start 16-byte aligned
+        const int vec_ok = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ld & 7) == 0;
+        zb_colsum_kernel<__nv_bfloat16, 8><<<static_cast<unsigned>(wide_blocks), COLSUM_WARPS * 32, 0, st>>>(
+            x, rows, cols, ld, db, accumulate, vec_ok);
+    } else {
+        const unsigned blocks = static_cast<unsigned>((cols + 127) / 128 * COLSUM_SPLIT);
+        const int vec_ok = (reinterpret_cast<uintptr_t>(X) & 7u) == 0 && (ld & 3) == 0;
+        zb_colsum_kernel<__nv_bfloat16, 4><<<blocks, COLSUM_WARPS * 32, 0, st>>>(x, rows, cols, ld, db,
+                                                                                accumulate, vec_ok);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("colsum launch: ") + cudaGetErrorString(e));
     return ZB_OK;
@@ -320,9 +384,9 @@ zb_status colsum_bf16(const void* X, int64_t rows, int64_t cols, int64_t ld, flo
 
 zb_status colsum_f32(const float* X, int64_t rows, int64_t cols, int64_t ld, float* db,
                      int accumulate, void* stream) {
-    const unsigned blocks = static_cast<unsigned>((cols + COLSUM_COLS - 1) / COLSUM_COLS * COLSUM_SPLIT);
+    const unsigned blocks = static_cast<unsigned>((cols + 127) / 128 * COLSUM_SPLIT);
     const int vec_ok = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ld & 3) == 0;
-    zb_colsum_kernel<float><<<blocks, COLSUM_WARPS * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+    zb_colsum_kernel<float, 4><<<blocks, COLSUM_WARPS * 32, 0, static_cast<cudaStream_t>(stream)>>>(
         X, rows, cols, ld, db, accumulate, vec_ok);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("colsum launch: ") + cudaGetErrorString(e));
@@ -381,7 +445,7 @@ extern "C" zb_status zb_grad_stats(const float* const* bufs, const uint64_t* cou
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     double* part = static_cast<double*>(scratch);
     zb_grad_stats_partial_kernel<<<dim3(STATS_BLOCKS, nbufs), STATS_THREADS, 0, st>>>(b, part);
-    zb_grad_stats_final_kernel<<<1, 1, 0, st>>>(part, nbufs, out);
+    zb_grad_stats_final_kernel<<<1, STATS_THREADS, 0, st>>>(part, nbufs, out);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return zb::fail(ZB_ERR_CUDA, std::string("grad stats launch: ") + cudaGetErrorString(e));
     zb::clear_error();
