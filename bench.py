@@ -706,6 +706,18 @@ def main():
         torch.cuda.synchronize()
 
     e2e_run(2)
+    # the host link's rate for this step's inputs, alone (CUDA events on the
+    # copy stream): an upload slower than a step makes e2e copy-bound
+    torch.cuda.synchronize()
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(up_stream)
+    with torch.cuda.stream(up_stream):
+        for j in range(m):
+            sets[0][0][j].copy_(pin[j], non_blocking=True)
+            sets[0][1][j].copy_(pin_g[j], non_blocking=True)
+    u1.record(up_stream)
+    torch.cuda.synchronize()
+    upload_ms = u0.elapsed_time(u1)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -756,6 +768,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                    "upload_alone_ms": upload_ms, "h2d_gb_per_s": h2d / (upload_ms * 1e6),
                     "clocks": e2e_clk,
                     "result": ("fp32 weight gradients" if want_dw else
                                "gradient statistics per stage (sum of squares, NaN/Inf count)"),

@@ -132,10 +132,17 @@ thread_local int* g_gemm_counter = nullptr;  // GEMM launch count of the running
 // the partial-tile exchange (measured on the 4-stage h=1024 replay on four
 // streams: 963 TF/s unsplit, 898 split).
 thread_local bool g_in_replay = false;
+// The running replay uses more than one stream.
+thread_local bool g_multi_lane = false;
 
 zb_status run_gemm(const GemmBf16& g, void* stream, Recorder* rec) {
     if (g_gemm_counter) ++*g_gemm_counter;
-    return timed(rec, true, [&] { return gemm_bf16_tc(g, stream); });
+    GemmBf16 h = g;
+    // programmatic dependent launch only where a GEMM's waiting CTAs cannot
+    // keep another lane's kernels off idle SMs, and with no events between
+    // launches (per-op timing)
+    h.allow_pdl = !g_multi_lane && !(rec && rec->on);
+    return timed(rec, true, [&] { return gemm_bf16_tc(h, stream); });
 }
 
 int split_allowed(const zb_block& b) { return !g_in_replay && !(b.flags & ZB_BLOCK_NO_SPLIT_K); }
@@ -427,6 +434,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     int gemms = 0;
     g_gemm_counter = &gemms;
     g_in_replay = true;
+    g_multi_lane = ns > 1;
     std::vector<char> w_started(P, 0);
     std::vector<int> last_w_op(P, -1);  // latest W / BW of each stage, for OPT
 
@@ -530,6 +538,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     }
     g_gemm_counter = nullptr;
     g_in_replay = false;
+    g_multi_lane = false;
     if (s != ZB_OK) return s;
 
     if (stats) {

@@ -605,6 +605,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // send after the phase-1 cluster barrier, which this thread reaches later)
     if (SPLITTABLE && ks > 1 && threadIdx.x == 0)
         zbp::mbar_arrive_expect_tx(zbp::smem_u32(&ctl->xchg), static_cast<uint32_t>(ks - 1) * split_slab_bytes(ks));
+    // Launched as a programmatic dependent of the previous GEMM in its stream,
+    // the setup above overlaps that GEMM's tail; nothing in global memory is
+    // read or written before it has completed.  The next GEMM may then be
+    // scheduled at once: its CTAs can only take SMs this grid leaves free
+    // (each needs most of an SM's shared memory) and wait there.
+    zbp::grid_dependency_wait();
+    zbp::allow_dependent_launch();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1079,7 +1086,7 @@ int split_clusters(int ks) {
 }
 
 template <int EPI, int A_MN, int B_MN, int CG>
-zb_status launch(const Maps& mp, EpiArgs ea, long long tiles, cudaStream_t st) {
+zb_status launch(const Maps& mp, EpiArgs ea, long long tiles, cudaStream_t st, bool pdl) {
     auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG>;
     int max_ctas = 0;
     zb_status s = configure<EPI, A_MN, B_MN, CG>(&max_ctas);
@@ -1097,13 +1104,22 @@ zb_status launch(const Maps& mp, EpiArgs ea, long long tiles, cudaStream_t st) {
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<CG>();
     cfg.stream = st;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = cw;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = cw > 1 ? 1 : 0;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (cw > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cw;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.o0, mp.o1, ea);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -1113,21 +1129,25 @@ zb_status launch(const Maps& mp, EpiArgs ea, long long tiles, cudaStream_t st) {
 
 template <int EPI, int CG>
 zb_status dispatch_major(int a_mn, int b_mn, const Maps& mp, const EpiArgs& ea, long long tiles,
-                         cudaStream_t st) {
-    if (!a_mn && !b_mn) return launch<EPI, 0, 0, CG>(mp, ea, tiles, st);
-    if (!a_mn && b_mn) return launch<EPI, 0, 1, CG>(mp, ea, tiles, st);
-    if (a_mn && !b_mn) return launch<EPI, 1, 0, CG>(mp, ea, tiles, st);
-    return launch<EPI, 1, 1, CG>(mp, ea, tiles, st);
+                         cudaStream_t st, bool pdl) {
+    if (!a_mn && !b_mn) return launch<EPI, 0, 0, CG>(mp, ea, tiles, st, pdl);
+    if (!a_mn && b_mn) return launch<EPI, 0, 1, CG>(mp, ea, tiles, st, pdl);
+    if (a_mn && !b_mn) return launch<EPI, 1, 0, CG>(mp, ea, tiles, st, pdl);
+    return launch<EPI, 1, 1, CG>(mp, ea, tiles, st, pdl);
 }
 
 template <int CG>
 zb_status dispatch(const zb::GemmBf16& g, const Maps& mp, const EpiArgs& ea, long long tiles,
                    cudaStream_t st) {
+    const bool pdl = g.allow_pdl != 0;
     switch (g.epi) {
-        case zb::EPI_STORE_BF16: return dispatch_major<zb::EPI_STORE_BF16, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st);
-        case zb::EPI_GELU_DUAL: return dispatch_major<zb::EPI_GELU_DUAL, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st);
-        case zb::EPI_GELU_BWD: return dispatch_major<zb::EPI_GELU_BWD, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st);
-        case zb::EPI_F32: return dispatch_major<zb::EPI_F32, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st);
+        case zb::EPI_STORE_BF16:
+            return dispatch_major<zb::EPI_STORE_BF16, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
+        case zb::EPI_GELU_DUAL:
+            return dispatch_major<zb::EPI_GELU_DUAL, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
+        case zb::EPI_GELU_BWD:
+            return dispatch_major<zb::EPI_GELU_BWD, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
+        case zb::EPI_F32: return dispatch_major<zb::EPI_F32, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
         default: return zb::fail(ZB_ERR_INVALID_ARG, "unknown epilogue");
     }
 }

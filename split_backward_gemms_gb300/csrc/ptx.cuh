@@ -244,6 +244,15 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, uint32
         : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (a no-op when launched without
+// the programmatic-serialization attribute), and allow the next such grid
+// in the stream to be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                      "memory");

@@ -46,6 +46,10 @@ struct GemmBf16 {
     // split K over a cluster of CTAs when the tiles alone leave SMs idle
     // (bf16-output epilogues only)
     int allow_split = 0;
+    // launch as a programmatic dependent of the previous kernel in the stream
+    // (its setup overlaps that kernel's tail); only where no other stream's
+    // kernels compete for the SMs its waiting CTAs would hold
+    int allow_pdl = 0;
 };
 zb_status gemm_bf16_tc(const GemmBf16& g, void* stream);
 
