@@ -132,16 +132,20 @@ thread_local int* g_gemm_counter = nullptr;  // GEMM launch count of the running
 // the partial-tile exchange (measured on the 4-stage h=1024 replay on four
 // streams: 963 TF/s unsplit, 898 split).
 thread_local bool g_in_replay = false;
-// The running replay uses more than one stream.
-thread_local bool g_multi_lane = false;
+// The running replay's GEMMs may launch as programmatic dependents: one lane,
+// or one F/B lane beside the W lane(s) of a one-stage replay (measured: the
+// h=6144 and h=4096 one-stage steps +0.3 % and +1.0 %).  Not with
+// stage-parallel lanes, whose small GEMMs share the SMs: a GEMM's waiting
+// CTAs keep other stages' GEMMs off free SMs there (the P=4, h=1024 pipeline
+// on four streams: 956 -> 938 TF/s).
+thread_local bool g_pdl_lanes = true;
 
 zb_status run_gemm(const GemmBf16& g, void* stream, Recorder* rec) {
     if (g_gemm_counter) ++*g_gemm_counter;
     GemmBf16 h = g;
-    // programmatic dependent launch only where a GEMM's waiting CTAs cannot
-    // keep another lane's kernels off idle SMs, and with no events between
-    // launches (per-op timing)
-    h.allow_pdl = !g_multi_lane && !(rec && rec->on);
+    // programmatic dependent launch where the lanes allow it, and with no
+    // events between launches (per-op timing)
+    h.allow_pdl = g_pdl_lanes && !(rec && rec->on);
     return timed(rec, true, [&] { return gemm_bf16_tc(h, stream); });
 }
 
@@ -434,7 +438,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     int gemms = 0;
     g_gemm_counter = &gemms;
     g_in_replay = true;
-    g_multi_lane = ns > 1;
+    g_pdl_lanes = ns == 1 || (w_lanes && !micro_lanes && nsd == 1);
     std::vector<char> w_started(P, 0);
     std::vector<int> last_w_op(P, -1);  // latest W / BW of each stage, for OPT
 
@@ -538,7 +542,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     }
     g_gemm_counter = nullptr;
     g_in_replay = false;
-    g_multi_lane = false;
+    g_pdl_lanes = true;
     if (s != ZB_OK) return s;
 
     if (stats) {
