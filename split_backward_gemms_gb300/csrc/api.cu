@@ -8,6 +8,8 @@
 // F(s,j) after F(s-1,j); B(s,j) after F(s,j) and B(s+1,j); W(s,j) after B(s,j).
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -145,7 +147,13 @@ zb_status run_gemm(const GemmBf16& g, void* stream, Recorder* rec) {
     GemmBf16 h = g;
     // programmatic dependent launch where the lanes allow it, and with no
     // events between launches (per-op timing)
-    h.allow_pdl = g_pdl_lanes && !(rec && rec->on);
+    // ZB_GEMM_PDL=0 turns it off, =1 on inside every lane (else the rule above)
+    static const int pdl_env = [] {
+        const char* v = std::getenv("ZB_GEMM_PDL");
+        return v && (v[0] == '0' || v[0] == '1') ? v[0] - '0' : -1;
+    }();
+    const bool lanes_ok = pdl_env < 0 ? g_pdl_lanes : pdl_env == 1;
+    h.allow_pdl = lanes_ok && !(rec && rec->on);
     return timed(rec, true, [&] { return gemm_bf16_tc(h, stream); });
 }
 
