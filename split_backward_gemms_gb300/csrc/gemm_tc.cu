@@ -9,8 +9,10 @@
 //               (bf16 -> fp32) into one of two 256-column accumulators,
 //               committing each stage back to the producer and each
 //               finished tile to the epilogue;
-//   warps 2..5  drain the accumulator with tcgen05.ld (one TMEM lane = one
-//               output row per thread) and apply the epilogue: bf16 store,
+//   warps 2..9  drain the accumulator with tcgen05.ld (one TMEM lane = one
+//               output row per thread; 8 warps for the bf16 epilogues, two
+//               per lane quadrant, 4 for the fp32 one) and apply the
+//               epilogue: bf16 store,
 //               bias + GeLU dual store (H and A), GeLU' product with the
 //               saved H (dH), or fp32 accumulation of a weight gradient.
 //               Results leave through swizzled shared-memory staging boxes
@@ -62,13 +64,28 @@ constexpr int BN = 256;  // tile columns (MMA N)
 constexpr int BK = 64;   // K per stage (one 128-byte swizzle row of bf16)
 constexpr uint32_t A_BYTES = BM * BK * 2;        // 16 KiB
 constexpr uint32_t MN_ATOM_BYTES = 64 * BK * 2;  // 64 MN x 64 K, one TMA box
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 64 + 32 * 8;  // producer, MMA issuer, up to 8 epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s
 constexpr uint64_t DRAIN_LIMIT_NS = 500000000ull;  // 0.5 s
-constexpr uint32_t STAGING_BOX = 32 * 128;             // 32 rows x 128 bytes
-constexpr uint32_t STAGING_BYTES = 4 * 2 * STAGING_BOX;  // 2 boxes per epilogue warp
+constexpr uint32_t STAGING_BYTES = 32 * 1024;  // 2 staging boxes per epilogue warp
+
+// Epilogue shape.  The bf16-output epilogues run 8 warps, two per TMEM lane
+// quadrant, each over half of the tile's 256 columns in chunks of 32 (a
+// 32-row x 64-byte staging box, 64-byte swizzle): their GeLU / GeLU'
+// arithmetic is latency-bound, and with one warp per scheduler the last
+// tile's epilogue of a short-K GEMM (K = 1024) took longer than its K loop.
+// The fp32 weight-gradient epilogue runs 4 warps over all 256 columns in
+// chunks of 32 (32 x 128-byte boxes, 128-byte swizzle) and leaves warps 6-9
+// idle: its reduce-adds are few and large, and spaced on purpose.
+template <int EPI>
+struct EpiShape {
+    static constexpr int WARPS = EPI == zb::EPI_F32 ? 4 : 8;
+    static constexpr int COLS = BN * 4 / WARPS;                         // columns per warp
+    static constexpr uint32_t BOX = EPI == zb::EPI_F32 ? 32 * 128 : 32 * 64;  // bytes per staging box
+};
+static_assert(2 * 8 * 32 * 64 <= STAGING_BYTES && 2 * 4 * 32 * 128 <= STAGING_BYTES, "staging boxes");
 
 template <int CG>
 struct Cfg {
@@ -211,12 +228,12 @@ __device__ __forceinline__ float gelu_grad_t(float x) {
     return fmaf(x * 0.3989422804014327f, e, Phi);  // Phi(x) + x phi(x)
 }
 
-// 64 columns of one row: the activation form is chosen once per chunk so the
+// N columns of one row: the activation form is chosen once per chunk so the
 // unrolled element loops have no branches and interleave.
-template <bool TANH>
-__device__ __forceinline__ void gelu_pack64(const float (&x)[64], uint32_t (&w)[32]);
-template <bool TANH>
-__device__ __forceinline__ void gelu_grad_mul64(float (&x)[64], const uint32_t (&h)[32]);
+template <bool TANH, int N>
+__device__ __forceinline__ void gelu_pack(const float (&x)[N], uint32_t (&w)[N / 2]);
+template <bool TANH, int N>
+__device__ __forceinline__ void gelu_grad_mul(float (&x)[N], const uint32_t (&h)[N / 2]);
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -302,14 +319,14 @@ __device__ __forceinline__ void normal_cdf_and_exp2(f32x2 X, f32x2& PHI, f32x2& 
     PHI = add2(pk2(copysignf(h0, x0), copysignf(h1, x1)), pk2(0.5f, 0.5f));
 }
 
-template <bool TANH>
-__device__ __forceinline__ void gelu_pack64(const float (&x)[64], uint32_t (&w)[32]) {
+template <bool TANH, int N>
+__device__ __forceinline__ void gelu_pack(const float (&x)[N], uint32_t (&w)[N / 2]) {
     if (TANH) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(gelu_t<true>(x[2 * i]), gelu_t<true>(x[2 * i + 1]));
+        for (int i = 0; i < N / 2; ++i) w[i] = pack_bf16x2(gelu_t<true>(x[2 * i]), gelu_t<true>(x[2 * i + 1]));
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < N / 2; ++i) {
             const f32x2 X = pk2(x[2 * i], x[2 * i + 1]);
             f32x2 PHI, E;
             normal_cdf_and_exp2(X, PHI, E);
@@ -320,18 +337,18 @@ __device__ __forceinline__ void gelu_pack64(const float (&x)[64], uint32_t (&w)[
     }
 }
 
-template <bool TANH>
-__device__ __forceinline__ void gelu_grad_mul64(float (&x)[64], const uint32_t (&h)[32]) {
+template <bool TANH, int N>
+__device__ __forceinline__ void gelu_grad_mul(float (&x)[N], const uint32_t (&h)[N / 2]) {
     if (TANH) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < N / 2; ++i) {
             const float2 f2 = unpack_bf16x2(h[i]);
             x[2 * i] *= gelu_grad_t<true>(f2.x);
             x[2 * i + 1] *= gelu_grad_t<true>(f2.y);
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < N / 2; ++i) {
             const float2 f2 = unpack_bf16x2(h[i]);
             const f32x2 Hx = pk2(f2.x, f2.y);
             f32x2 PHI, E;
@@ -365,6 +382,18 @@ __device__ __forceinline__ void stage_row(uint32_t stg, int lane, const uint32_t
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t off = static_cast<uint32_t>((k ^ (lane & 7)) << 4);
+        zbp::st_shared_v4(row + off, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
+}
+
+// Write one thread's 64-byte row of a 32-row staging box (TMA 64-byte swizzle:
+// 16-byte chunk k of row r sits at chunk k ^ ((r / 2) mod 4); the 8 rows a
+// quarter-warp writes then hit 8 different bank groups).
+__device__ __forceinline__ void stage_row64(uint32_t stg, int lane, const uint32_t (&w)[16]) {
+    const uint32_t row = stg + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t off = static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) << 4);
         zbp::st_shared_v4(row + off, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
     }
 }
@@ -573,7 +602,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             zbp::mbar_init(zbp::smem_u32(&ctl->tfull[b]), 1);
-            zbp::mbar_init(zbp::smem_u32(&ctl->tempty[b]), 4 * CG);
+            zbp::mbar_init(zbp::smem_u32(&ctl->tempty[b]), EpiShape<EPI>::WARPS * CG);
         }
         zbp::mbar_init(zbp::smem_u32(&ctl->drain), 1);
         if (SPLITTABLE) zbp::mbar_init(zbp::smem_u32(&ctl->xchg), 1);
@@ -746,6 +775,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // idle, so one thread sends slab o to CTA o with a bulk copy.  The
         // owners sum after their receive barrier (after the role code).
         const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;  // column half (8 warps: two per lane quadrant)
         const int prow = q * 32 + lane;
         const uint32_t base = zbp::smem_u32(smem);
         const uint32_t slab = split_slab_bytes(ks);
@@ -757,7 +787,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int sw = BN / ks;  // columns per owner
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; c += 2) {
+            for (int c = hf * 4; c < hf * 4 + 4; c += 2) {
                 uint32_t v[2][32];
                 zbp::tmem_ld_32x32b_x32(taddr + c * 32, v[0]);
                 zbp::tmem_ld_32x32b_x32(taddr + c * 32 + 32, v[1]);
@@ -788,143 +818,145 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ---------------------------------------------------- epilogue
         // Warp w may read TMEM lanes 32*(w%4) .. +31: rows q*32 .. q*32+31 of
-        // this CTA's 128 rows, one row per thread.  Results leave through two
-        // 4-KiB swizzled staging boxes per warp (32 rows x 128 bytes) and TMA
-        // stores; the fp32 weight gradient is accumulated with a TMA
-        // reduce-add, so the old values are never read by the SM.
-        const int q = warp & 3;
-        const uint32_t stg0 = zbp::smem_u32(staging + (warp - 2) * 2 * STAGING_BOX);
-        uint32_t flip = 0;
-        uint32_t local = 0;
-        for (int tile = cluster; tile < num_tiles; tile += clusters, ++local) {
-            const uint32_t buf = local & 1u;
-            const uint32_t tr = local >> 1;
-            int mb, nb;
-            tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
-            const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
-            const int n0 = nb * BN;
-            const int row0 = m0 + q * 32;
-            const int row = row0 + lane;
-            if (EPI == zb::EPI_GELU_BWD && row < args.Mg) {
-                // warm L2 with this row of H while the MMAs run
-                const int ncols = min(BN, args.Ng - n0);
-                zbp::prefetch_l2(args.aux + static_cast<long long>(row) * args.ldaux + n0,
-                                 static_cast<uint32_t>(ncols) * 2u);
-            }
-            if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->tfull[buf]), tr & 1u, abort_flag, args.err,
-                                ERR_WAIT_EPI, WAIT_LIMIT_NS, true))
-                break;
-            zbp::tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
-            const bool rows_live = row0 < args.Mg;
-            if (EPI == zb::EPI_F32) {
-                // The fp32 stores (TMA reduce-adds) share the TMA unit with the
-                // operand loads of the next tile: issued back to back they
-                // queue ahead of those loads and starve the MMAs.  Spacing the
-                // chunks over the tile (a pause that scales with the K loop,
-                // ~5 ns per K block, at most 250 ns, none after the CTA's last
-                // chunk) keeps the loads flowing.
-                const bool last_tile = tile + clusters >= num_tiles;
-                const unsigned pause_ns = static_cast<unsigned>(min(num_kb * 5, 250));
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
-                    zbp::tmem_ld_32x32b_x32(taddr + c * 32, v);
-                    zbp::tmem_ld_wait();
-                    const int col0 = n0 + c * 32;
-                    if (!rows_live || col0 >= args.Ng) continue;
-                    const uint32_t stg = stg0 + flip * STAGING_BOX;
-                    flip ^= 1u;
-                    staging_acquire(lane);
-                    stage_row(stg, lane, v);
-                    if (args.accumulate)
-                        staging_release<true>(&tmO0, stg, lane, col0, row0);
-                    else
-                        staging_release<false>(&tmO0, stg, lane, col0, row0);
-                    if (!last_tile && pause_ns) __nanosleep(pause_ns);
+        // this CTA's 128 rows, one row per thread; with 8 epilogue warps the
+        // two warps of a quadrant take one half of the columns each (see
+        // EpiShape).  Results leave through two swizzled staging boxes per
+        // warp and TMA stores; the fp32 weight gradient is accumulated with a
+        // TMA reduce-add, so the old values are never read by the SM.
+        using E = EpiShape<EPI>;
+        const int ew = warp - 2;  // epilogue warp index
+        if (ew < E::WARPS) {
+            const int q = warp & 3;
+            const int c_lo = (ew >> 2) * E::COLS;  // first tile column of this warp
+            const uint32_t stg0 = zbp::smem_u32(staging + ew * 2 * E::BOX);
+            uint32_t flip = 0;
+            uint32_t local = 0;
+            for (int tile = cluster; tile < num_tiles; tile += clusters, ++local) {
+                const uint32_t buf = local & 1u;
+                const uint32_t tr = local >> 1;
+                int mb, nb;
+                tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
+                const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
+                const int n0 = nb * BN;
+                const int row0 = m0 + q * 32;
+                const int row = row0 + lane;
+                if (EPI == zb::EPI_GELU_BWD && row < args.Mg && n0 + c_lo < args.Ng) {
+                    // warm L2 with this warp's part of the row of H while the MMAs run
+                    const int ncols = min(E::COLS, args.Ng - n0 - c_lo);
+                    zbp::prefetch_l2(args.aux + static_cast<long long>(row) * args.ldaux + n0 + c_lo,
+                                     static_cast<uint32_t>(ncols) * 2u);
                 }
-            } else {
+                if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->tfull[buf]), tr & 1u, abort_flag, args.err,
+                                    ERR_WAIT_EPI, WAIT_LIMIT_NS, true))
+                    break;
+                zbp::tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
+                const bool rows_live = row0 < args.Mg;
+                if (EPI == zb::EPI_F32) {
+                    // The fp32 stores (TMA reduce-adds) share the TMA unit with the
+                    // operand loads of the next tile: issued back to back they
+                    // queue ahead of those loads and starve the MMAs.  Spacing the
+                    // chunks over the tile (a pause that scales with the K loop,
+                    // ~5 ns per K block, at most 250 ns, none after the CTA's last
+                    // chunk) keeps the loads flowing.
+                    const bool last_tile = tile + clusters >= num_tiles;
+                    const unsigned pause_ns = static_cast<unsigned>(min(num_kb * 5, 250));
 #pragma unroll 1
-                for (int c = 0; c < BN / 64; ++c) {
-                    uint32_t v0[32], v1[32];
-                    zbp::tmem_ld_32x32b_x32(taddr + c * 64, v0);
-                    zbp::tmem_ld_32x32b_x32(taddr + c * 64 + 32, v1);
-                    zbp::tmem_ld_wait();
-                    const int col0 = n0 + c * 64;
-                    if (!rows_live || col0 >= args.Ng) continue;
-                    float x[64];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        x[i] = __uint_as_float(v0[i]);
-                        x[32 + i] = __uint_as_float(v1[i]);
-                    }
-                    if ((EPI == zb::EPI_STORE_BF16 || EPI == zb::EPI_GELU_DUAL) && args.bias) {
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            if (col0 + g * 8 >= args.Ng) break;
-                            const uint4 b = *reinterpret_cast<const uint4*>(args.bias + col0 + g * 8);
-                            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 f2 = unpack_bf16x2(bw[i]);
-                                x[g * 8 + 2 * i] += f2.x;
-                                x[g * 8 + 2 * i + 1] += f2.y;
-                            }
-                        }
-                    }
-                    if (EPI == zb::EPI_GELU_BWD) {
-                        // this row's 64 H values (zeros past the matrix edge)
-                        uint32_t hw[32];
-                        const __nv_bfloat16* hp = args.aux + static_cast<long long>(row) * args.ldaux + col0;
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            uint4 hv = make_uint4(0u, 0u, 0u, 0u);
-                            if (row < args.Mg && col0 + g * 8 < args.Ng)
-                                hv = *reinterpret_cast<const uint4*>(hp + g * 8);
-                            hw[4 * g] = hv.x;
-                            hw[4 * g + 1] = hv.y;
-                            hw[4 * g + 2] = hv.z;
-                            hw[4 * g + 3] = hv.w;
-                        }
-                        if (args.act == ZB_ACT_GELU_TANH)
-                            gelu_grad_mul64<true>(x, hw);
-                        else
-                            gelu_grad_mul64<false>(x, hw);
-                    }
-                    uint32_t w[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
-                    uint32_t stg = stg0 + flip * STAGING_BOX;
-                    flip ^= 1u;
-                    staging_acquire(lane);
-                    stage_row(stg, lane, w);
-                    staging_release<false>(&tmO0, stg, lane, col0, row0);
-                    if (EPI == zb::EPI_GELU_DUAL) {
-                        if (args.act == ZB_ACT_GELU_TANH)
-                            gelu_pack64<true>(x, w);
-                        else
-                            gelu_pack64<false>(x, w);
-                        stg = stg0 + flip * STAGING_BOX;
+                    for (int c = 0; c < E::COLS / 32; ++c) {
+                        uint32_t v[32];
+                        zbp::tmem_ld_32x32b_x32(taddr + c_lo + c * 32, v);
+                        zbp::tmem_ld_wait();
+                        const int col0 = n0 + c_lo + c * 32;
+                        if (!rows_live || col0 >= args.Ng) continue;
+                        const uint32_t stg = stg0 + flip * E::BOX;
                         flip ^= 1u;
                         staging_acquire(lane);
-                        stage_row(stg, lane, w);
-                        staging_release<false>(&tmO1, stg, lane, col0, row0);
+                        stage_row(stg, lane, v);
+                        if (args.accumulate)
+                            staging_release<true>(&tmO0, stg, lane, col0, row0);
+                        else
+                            staging_release<false>(&tmO0, stg, lane, col0, row0);
+                        if (!last_tile && pause_ns) __nanosleep(pause_ns);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < E::COLS / 32; ++c) {
+                        uint32_t v[32];
+                        zbp::tmem_ld_32x32b_x32(taddr + c_lo + c * 32, v);
+                        zbp::tmem_ld_wait();
+                        const int col0 = n0 + c_lo + c * 32;
+                        if (!rows_live || col0 >= args.Ng) continue;
+                        float x[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
+                        if ((EPI == zb::EPI_STORE_BF16 || EPI == zb::EPI_GELU_DUAL) && args.bias) {
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                if (col0 + g * 8 >= args.Ng) break;
+                                const uint4 b = *reinterpret_cast<const uint4*>(args.bias + col0 + g * 8);
+                                const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float2 f2 = unpack_bf16x2(bw[i]);
+                                    x[g * 8 + 2 * i] += f2.x;
+                                    x[g * 8 + 2 * i + 1] += f2.y;
+                                }
+                            }
+                        }
+                        if (EPI == zb::EPI_GELU_BWD) {
+                            // this row's 32 H values (zeros past the matrix edge)
+                            uint32_t hw[16];
+                            const __nv_bfloat16* hp = args.aux + static_cast<long long>(row) * args.ldaux + col0;
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+                                if (row < args.Mg && col0 + g * 8 < args.Ng)
+                                    hv = *reinterpret_cast<const uint4*>(hp + g * 8);
+                                hw[4 * g] = hv.x;
+                                hw[4 * g + 1] = hv.y;
+                                hw[4 * g + 2] = hv.z;
+                                hw[4 * g + 3] = hv.w;
+                            }
+                            if (args.act == ZB_ACT_GELU_TANH)
+                                gelu_grad_mul<true, 32>(x, hw);
+                            else
+                                gelu_grad_mul<false, 32>(x, hw);
+                        }
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+                        uint32_t stg = stg0 + flip * E::BOX;
+                        flip ^= 1u;
+                        staging_acquire(lane);
+                        stage_row64(stg, lane, w);
+                        staging_release<false>(&tmO0, stg, lane, col0, row0);
+                        if (EPI == zb::EPI_GELU_DUAL) {
+                            if (args.act == ZB_ACT_GELU_TANH)
+                                gelu_pack<true, 32>(x, w);
+                            else
+                                gelu_pack<false, 32>(x, w);
+                            stg = stg0 + flip * E::BOX;
+                            flip ^= 1u;
+                            staging_acquire(lane);
+                            stage_row64(stg, lane, w);
+                            staging_release<false>(&tmO1, stg, lane, col0, row0);
+                        }
                     }
                 }
+                zbp::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t te = zbp::smem_u32(&ctl->tempty[buf]);
+                    if (PAIR)
+                        zbp::mbar_arrive_cluster(zbp::mapa_shared(te, 0));
+                    else
+                        zbp::mbar_arrive(te);
+                }
             }
-            zbp::tc_fence_before();
+            // the staging buffers must not be released while a bulk store reads them
+            if (lane == 0) zbp::bulk_wait<0>();
             __syncwarp();
-            if (lane == 0) {
-                const uint32_t te = zbp::smem_u32(&ctl->tempty[buf]);
-                if (PAIR)
-                    zbp::mbar_arrive_cluster(zbp::mapa_shared(te, 0));
-                else
-                    zbp::mbar_arrive(te);
-            }
         }
-        // the staging buffers must not be released while a bulk store reads them
-        if (lane == 0) zbp::bulk_wait<0>();
-        __syncwarp();
     }
 
     __syncthreads();
@@ -978,9 +1010,11 @@ EncodeTiledFn encode_fn(std::string* why) {
 }
 
 // 2-D map: inner dimension `inner` (contiguous), `outer` rows of stride ld
-// elements; box of box_inner x box_outer elements, 128-byte swizzle.
+// elements; box of box_inner x box_outer elements, 128-byte swizzle unless
+// given (the inner box extent in bytes must not exceed the swizzle span).
 bool make_map(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t outer,
-              uint64_t ld, uint32_t box_inner, uint32_t box_outer, std::string* why) {
+              uint64_t ld, uint32_t box_inner, uint32_t box_outer, std::string* why,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn(why);
     if (!fn) return false;
     const uint64_t es = f32 ? 4 : 2;
@@ -990,7 +1024,7 @@ bool make_map(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         if (why) *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
@@ -1224,13 +1258,14 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
         else
             ok = make_map(&mp.b, g.B, false, g.Kg, g.Ng, g.ldb, BK, b_rows, &why);
     }
-    // epilogue boxes: 32 rows x 128 bytes (32 fp32 or 64 bf16 columns)
+    // epilogue boxes: 32 rows x 32 columns (fp32: 128 bytes, 128-byte
+    // swizzle; bf16: 64 bytes, 64-byte swizzle)
     const bool f32_out = g.epi == EPI_F32;
-    const uint32_t ocols = f32_out ? 32 : 64;
-    if (ok) ok = make_map(&mp.o0, g.out0, f32_out, g.Ng, g.Mg, g.ld0, ocols, 32, &why);
+    const CUtensorMapSwizzle osw = f32_out ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (ok) ok = make_map(&mp.o0, g.out0, f32_out, g.Ng, g.Mg, g.ld0, 32, 32, &why, osw);
     if (ok) {
         if (g.epi == EPI_GELU_DUAL)
-            ok = make_map(&mp.o1, g.out1, false, g.Ng, g.Mg, g.ld1, ocols, 32, &why);
+            ok = make_map(&mp.o1, g.out1, false, g.Ng, g.Mg, g.ld1, 32, 32, &why, osw);
         else
             mp.o1 = mp.o0;
     }
