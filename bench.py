@@ -240,6 +240,54 @@ def pass_bytes(M, h, f):
     return {"F": F, "B": B, "W": W}
 
 
+class SmClockReader:
+    """SM clock read through NVML (libnvidia-ml, read-only queries), sampled
+    every 5 ms by a thread while a sweep point's passes run."""
+
+    def __init__(self, index: int = 0):
+        import ctypes
+        import threading
+        self._threading = threading
+        self.ok = False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                return
+            self.mhz = ctypes.c_uint()
+            self.ok = True
+        except OSError:
+            pass
+        self.samples, self.thread, self.run = [], None, False
+
+    def read(self):
+        import ctypes
+        if self.ok and self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(self.mhz)) == 0:
+            return self.mhz.value
+        return None
+
+    def start(self):
+        self.samples, self.run = [], True
+
+        def loop():
+            while self.run:
+                v = self.read()
+                if v is not None:
+                    self.samples.append(v)
+                time.sleep(0.005)
+        if self.ok:
+            self.thread = self._threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        self.run = False
+        if self.thread is not None:
+            self.thread.join()
+        return statistics.median(self.samples) if self.samples else None
+
+
 def run_sweep(args):
     """Per-pass kernel sweep: F, B and W standalone at each (M, h), f = 4h,
     W accumulating over m microbatches (4 distinct input sets, cycled)."""
@@ -288,17 +336,23 @@ def run_sweep(args):
                                                     db1, db2, j > 0, stream),
         }
         pb = pass_bytes(M, h, f)
+        clock = SmClockReader(torch.cuda.current_device())
         for name, fn in passes.items():
             for j in range(3):
                 fn(S[j % sets], j)
             torch.cuda.synchronize()
+            # each point is compared with the burst peak: let the previous
+            # (possibly power-capped) point's clock recover first
+            time.sleep(args.sweep_rest)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            clock.start()
             e0.record(stream)
             for j in range(m):
                 fn(S[j % sets], j)
             e1.record(stream)
             torch.cuda.synchronize()
+            sm_mhz = clock.stop()
             ms = e0.elapsed_time(e1) / m
             flops = 4.0 * M * h * f
             t_flop = flops / (peaks["bf16"] * 1e12)
@@ -306,7 +360,7 @@ def run_sweep(args):
             bound = "tensor" if t_flop >= t_byte else "hbm"
             print(json.dumps({
                 "sweep": True, "pass": name, "M": M, "h": h, "f": f, "microbatches": m, "bias": args.bias,
-                "us_per_pass": 1e3 * ms, "tflops": flops / (ms / 1e3) / 1e12,
+                "us_per_pass": 1e3 * ms, "tflops": flops / (ms / 1e3) / 1e12, "sm_mhz": sm_mhz,
                 "gb_per_s": pb[name] / (ms / 1e3) / 1e9,
                 "roofline": {"bound": bound, "time_us": 1e6 * max(t_flop, t_byte),
                              "frac": max(t_flop, t_byte) / (ms / 1e3),
@@ -419,6 +473,8 @@ def main():
     ap.add_argument("--sweep-points", default="",
                     help="comma list of MxH points, e.g. 3072x6144 (default: the M x h grid)")
     ap.add_argument("--sweep-m", type=int, default=32, help="microbatches timed per pass")
+    ap.add_argument("--sweep-rest", type=float, default=0.5,
+                    help="seconds of idle before each timed pass of the sweep (clock recovery)")
     ap.add_argument("--bias", action="store_true",
                     help="sweep with biases: F adds b1/b2, W also accumulates db1 = colsum dH, db2 = colsum dY")
     args = ap.parse_args()
