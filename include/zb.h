@@ -30,6 +30,13 @@
  *    waiting.  A device-side wait that gives up (bounded spin in the GEMM
  *    pipeline) sets a device error word; it is reported as ZB_ERR_TIMEOUT by
  *    zb_sync_status().  Launch failures are reported as ZB_ERR_CUDA at once.
+ *    A GEMM that follows another of this library's GEMMs on the same stream
+ *    may start its setup before that one ends (programmatic dependent
+ *    launch); it touches no memory until every earlier work item of the
+ *    stream has completed, so stream order holds as usual.  Environment:
+ *    ZB_GEMM_PDL=0 disables this, ZB_GEMM_SPLIT_K=1 disables split K (see
+ *    zb_block.flags), ZB_GEMM_CTA_GROUP=1|2 forces a GEMM tile shape; all
+ *    are read once per process.
  *  - Errors: every call returns a zb_status; zb_last_error() returns a
  *    thread-local, human-readable message for the last failing call.
  *  - Determinism: for fixed shapes the same inputs give the same output bits;
