@@ -41,7 +41,12 @@ ACTS = {"gelu_erf": 1, "gelu_tanh": 2}
 #   (256, 2048, 8192):  64 tiles, 32 K blocks -> S=2;  16 tiles, 128 K blocks -> S=4
 #   (200, 2056, 2104):  18 tiles, 33 K blocks -> S=2;  18 tiles, 33 K blocks -> S=2 (all ragged)
 #   (2048, 1024, 4096): CTA-pair tiles for F1;  64 tiles, 64 K blocks -> S=2
-SHAPES = [(256, 1024, 4096), (200, 520, 2056), (256, 2048, 8192), (200, 2056, 2104), (2048, 1024, 4096)]
+# degenerate shapes:
+#   (1, 1024, 4096) and (3, 520, 4104): one or three rows, F2 S=4 (4 and 3 tiles)
+#   (130, 8, 4096):     F2 two tiles of 8 live columns, S=4 (three owners hold no column)
+#   (1, 2048, 8):       F1 one tile of 8 live columns, 32 K blocks -> S=2
+SHAPES = [(256, 1024, 4096), (200, 520, 2056), (256, 2048, 8192), (200, 2056, 2104), (2048, 1024, 4096),
+          (1, 1024, 4096), (3, 520, 4104), (130, 8, 4096), (1, 2048, 8)]
 
 
 @pytest.fixture(scope="module")
