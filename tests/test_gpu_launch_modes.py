@@ -6,7 +6,10 @@ waits for it to complete).  ZB_GEMM_PDL=0 turns that off and ZB_GEMM_PDL=1
 turns it on inside every replay lane; the setting is read once per process,
 so each mode runs in a fresh process on the same seeded inputs: single passes
 (with and without split K) and replays on one lane, on an F/B lane beside a W
-lane, and on four stage lanes must give the same bits in every mode.
+lane, and on four stage lanes must give the same bits in every mode.  And a
+process whose first library calls are made inside a CUDA graph capture (the
+split-K occupancy query and the programmatic launches among them) replays
+the graph to the bits of the same passes run eagerly.
 """
 
 import os
@@ -101,3 +104,58 @@ def test_programmatic_launches_change_no_bits(tmp_path):
         assert res[mode].files == keys
         for k in keys:
             assert np.array_equal(res[mode][k], res["default"][k]), (mode, k)
+
+
+def _graph_child(out_path):
+    """The first library calls of the process happen inside a CUDA graph
+    capture: single passes at a split-K shape (its occupancy query and
+    programmatic launches included), then the graph is replayed and
+    compared with the same passes run eagerly afterwards."""
+    from split_backward_gemms_gb300 import zb
+    M, h, f = 256, 1024, 4096
+    stages, X0, dY = I.pipeline_draws(1, 1, M, h, f, seed=21, bias=True)
+    st = stages[0]
+    X, G = dev_bf16(X0[0]), dev_bf16(dY[0])
+    W1, W2, b1, b2 = dev_bf16(st.W1), dev_bf16(st.W2), dev_bf16(st.b1), dev_bf16(st.b2)
+    blk = zb.make_block(M, h, f, has_bias=True)
+
+    def outs():
+        return dict(H=empty_bf16(M, f), A=empty_bf16(M, f), Y=empty_bf16(M, h), dH=empty_bf16(M, f),
+                    dX=empty_bf16(M, h))
+
+    def run(o, stream):
+        zb.zb_forward(blk, X, W1, W2, b1, b2, o["H"], o["A"], o["Y"], stream)
+        zb.zb_backward_input(blk, G, W1, W2, o["H"], o["dH"], o["dX"], stream)
+
+    torch.cuda.synchronize()
+    g_out = outs()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            run(g_out, side)
+    torch.cuda.current_stream().wait_stream(side)
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    e_out = outs()
+    run(e_out, torch.cuda.current_stream())
+    sync(zb)
+    np.savez(out_path, **{f"g_{k}": _bits(v) for k, v in g_out.items()},
+             **{f"e_{k}": _bits(v) for k, v in e_out.items()})
+
+
+def test_first_calls_inside_graph_capture(tmp_path):
+    if not have_gpu():
+        pytest.skip("no CUDA device")
+    from split_backward_gemms_gb300 import build as B
+    B.build()
+    out = str(tmp_path / "graph.npz")
+    code = f"import tests.test_gpu_launch_modes as t; t._graph_child({out!r})"
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    res = np.load(out)
+    for k in ("H", "A", "Y", "dH", "dX"):
+        assert np.array_equal(res[f"g_{k}"], res[f"e_{k}"]), k
+        assert not np.array_equal(res[f"g_{k}"], np.full_like(res[f"g_{k}"], res[f"g_{k}"].flat[0])), k
