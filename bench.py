@@ -458,8 +458,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--streams", type=int, default=0,
-                    help="streams of the replay (0: one per stage; a one-stage replay puts its W "
-                         "passes on a second stream)")
+                    help="streams of the replay (0: one per stage plus a W lane per stage when "
+                         "2P <= 8; a one-stage replay puts its W passes on a second stream)")
     ap.add_argument("--e2e-result", choices=("stats", "dW"), default="stats",
                     help="what the e2e step reads back: the stages' gradient statistics (sum of "
                          "squares, NaN/Inf count; computed at the OPT markers) or the full fp32 dW")
@@ -519,7 +519,9 @@ def main():
         ops = [(k, 0, j) for k, s, j in ops if s == 0]
     blk = zb.make_block(M, h, f)
     # multi-stage replays run their stages on P streams (stage-parallel)
-    n_streams = args.streams if args.streams > 0 else (P if multi else 2)
+    # stage lanes, plus a W lane per stage where 2P streams fit (the P=4,
+    # h=1024 pipeline: 995 TF/s on 4 streams, 1008 on 8)
+    n_streams = args.streams if args.streams > 0 else (min(2 * P, 8) if multi else 2)
     pl = zb.make_pipeline(P, m, blk, timing=True, streams=n_streams)
     need, peak_live = zb.zb_schedule_workspace_size(pl, ops)
     ws_t = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)

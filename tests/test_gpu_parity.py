@@ -455,7 +455,7 @@ def test_device_wait_timeout_is_reported_and_context_survives(zb):
 
 
 @pytest.mark.parametrize("kind,P,m,streams", [("ZBH1", 4, 8, 4), ("ZBH2", 4, 8, 4), ("1F1B", 4, 8, 4),
-                                              ("ZBH2", 8, 16, 3), ("ZBH1", 3, 5, 8)])
+                                              ("ZBH2", 8, 16, 3), ("ZBH1", 3, 5, 8), ("ZBH1", 4, 8, 8)])
 def test_stage_parallel_replay_is_bit_exact(zb, kind, P, m, streams):
     # Stages on several streams, ordered by events: same bits as the serial replay.
     M, h, f = 512, 256, 1024
