@@ -12,9 +12,9 @@
 //   warps 2..9  drain the accumulator with tcgen05.ld (one TMEM lane = one
 //               output row per thread; 8 warps for the bf16 epilogues, two
 //               per lane quadrant, 4 for the fp32 one) and apply the
-//               epilogue: bf16 store,
-//               bias + GeLU dual store (H and A), GeLU' product with the
-//               saved H (dH), or fp32 accumulation of a weight gradient.
+//               epilogue: bf16 store, bias + GeLU dual store (H and A),
+//               GeLU' product with the saved H (dH), or fp32 accumulation
+//               of a weight gradient.
 //               Results leave through swizzled shared-memory staging boxes
 //               and TMA tensor stores; the weight gradient is added in place
 //               with a TMA reduce-add (one fp32 add per element, in L2).
@@ -42,6 +42,9 @@
 // mbarrier).  CTA o then sums its S slabs from its own shared memory in rank
 // order 0..S-1 (a fixed order, so the result is still deterministic),
 // applies the epilogue and stores it.  No global workspace is involved.
+// Launched as a programmatic dependent of the previous GEMM in a stream, a
+// CTA runs its setup early and waits (griddepcontrol.wait) before its first
+// global access.
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets the
 // device error word, drains its in-flight copies and MMAs, frees TMEM and
 // returns.
