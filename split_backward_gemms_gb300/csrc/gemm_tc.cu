@@ -363,6 +363,21 @@ __device__ __forceinline__ void gelu_grad_mul(float (&x)[N], const uint32_t (&h)
     }
 }
 
+// 32 bf16 values of row `row` from column col0 of H (GeLU' epilogue), zeros
+// past the matrix edge.  Plain loads: the caller issues them ahead of use.
+__device__ __forceinline__ void load_h32(const EpiArgs& args, int row, int col0, uint32_t (&hw)[16]) {
+    const __nv_bfloat16* hp = args.aux + static_cast<long long>(row) * args.ldaux + col0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+        if (row < args.Mg && col0 + g * 8 < args.Ng) hv = *reinterpret_cast<const uint4*>(hp + g * 8);
+        hw[4 * g] = hv.x;
+        hw[4 * g + 1] = hv.y;
+        hw[4 * g + 2] = hv.z;
+        hw[4 * g + 3] = hv.w;
+    }
+}
+
 // Tile order: groups of `group` M-blocks; inside a group M is fastest, then
 // N.  A wave of resident CTAs then covers about group x (clusters / group)
 // tiles, so the operand panels it touches at each K step are few and shared
@@ -843,11 +858,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int n0 = nb * BN;
                 const int row0 = m0 + q * 32;
                 const int row = row0 + lane;
-                if (EPI == zb::EPI_GELU_BWD && row < args.Mg && n0 + c_lo < args.Ng) {
-                    // warm L2 with this warp's part of the row of H while the MMAs run
-                    const int ncols = min(E::COLS, args.Ng - n0 - c_lo);
-                    zbp::prefetch_l2(args.aux + static_cast<long long>(row) * args.ldaux + n0 + c_lo,
-                                     static_cast<uint32_t>(ncols) * 2u);
+                // GeLU': the first chunk's H values are loaded while the MMAs
+                // run, each next chunk's during the current chunk's arithmetic
+                uint32_t h_next[16];
+                if (EPI == zb::EPI_GELU_BWD) {
+                    if (row < args.Mg && n0 + c_lo < args.Ng) {
+                        // warm L2 with this warp's part of the row of H
+                        const int ncols = min(E::COLS, args.Ng - n0 - c_lo);
+                        zbp::prefetch_l2(args.aux + static_cast<long long>(row) * args.ldaux + n0 + c_lo,
+                                         static_cast<uint32_t>(ncols) * 2u);
+                    }
+                    load_h32(args, row, n0 + c_lo, h_next);
                 }
                 if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->tfull[buf]), tr & 1u, abort_flag, args.err,
                                     ERR_WAIT_EPI, WAIT_LIMIT_NS, true))
@@ -884,10 +905,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 } else {
 #pragma unroll 1
                     for (int c = 0; c < E::COLS / 32; ++c) {
+                        const int col0 = n0 + c_lo + c * 32;
+                        uint32_t hw[16];
+                        if (EPI == zb::EPI_GELU_BWD) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) hw[i] = h_next[i];
+                            if (c + 1 < E::COLS / 32) load_h32(args, row, col0 + 32, h_next);
+                        }
                         uint32_t v[32];
                         zbp::tmem_ld_32x32b_x32(taddr + c_lo + c * 32, v);
                         zbp::tmem_ld_wait();
-                        const int col0 = n0 + c_lo + c * 32;
                         if (!rows_live || col0 >= args.Ng) continue;
                         float x[32];
 #pragma unroll
@@ -907,19 +934,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                         if (EPI == zb::EPI_GELU_BWD) {
-                            // this row's 32 H values (zeros past the matrix edge)
-                            uint32_t hw[16];
-                            const __nv_bfloat16* hp = args.aux + static_cast<long long>(row) * args.ldaux + col0;
-#pragma unroll
-                            for (int g = 0; g < 4; ++g) {
-                                uint4 hv = make_uint4(0u, 0u, 0u, 0u);
-                                if (row < args.Mg && col0 + g * 8 < args.Ng)
-                                    hv = *reinterpret_cast<const uint4*>(hp + g * 8);
-                                hw[4 * g] = hv.x;
-                                hw[4 * g + 1] = hv.y;
-                                hw[4 * g + 2] = hv.z;
-                                hw[4 * g + 3] = hv.w;
-                            }
                             if (args.act == ZB_ACT_GELU_TANH)
                                 gelu_grad_mul<true, 32>(x, hw);
                             else
