@@ -391,33 +391,38 @@ def test_one_stage_lists_full_size_deferred_equals_eager(zb, kind, m, h):
     assert a[4] == peak_mb * 2 * M * f * 2 + M * f * 2  # + the running B's dH
 
 
-def test_full_size_step_as_benchmarked(zb):
-    """The h=6144 stage step in the launch configuration the benchmark times:
-    the stage-0 ZB-H2 list of an 8-stage ordering (m=24, seq 3072) on two
-    streams (F/B lane and W lane, programmatic launches inside), captured once
-    into a CUDA graph on a side stream after an eager warm-up, replayed twice.
-    Its outputs and fp32 weight gradients equal the serial eager replay's bit
-    for bit (which the test above ties to eager F+BW, and the sampled
-    full-size checks to the oracle)."""
-    M, h, f, m = 3072, 6144, 24576, 24
+@pytest.mark.parametrize("P,m,M,h,kind,list_P,streams", [(1, 24, 3072, 6144, "ZBH2", 8, 2),
+                                                        (4, 8, 2048, 1024, "ZBH1", 4, 8)])
+def test_full_size_step_as_benchmarked(zb, P, m, M, h, kind, list_P, streams):
+    """A step in the launch configuration the benchmark times: the h=6144
+    stage (the stage-0 ZB-H2 list of an 8-stage ordering, m=24, seq 3072, an
+    F/B lane and a W lane) and the P=4, h=1024 pipeline (ZB-H1, m=8, a lane
+    and a W lane per stage), each captured once into a CUDA graph on a side
+    stream after an eager warm-up and replayed twice.  Outputs and fp32
+    weight gradients equal the serial eager replay's bit for bit (which the
+    tests above tie to eager F+BW, a hand chain of single passes and the
+    oracle)."""
+    f = 4 * h
     blk = zb.make_block(M, h, f)
-    gen = torch.Generator(device="cuda").manual_seed(7)
-    W1 = (torch.randn(h, f, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
-    W2 = (torch.randn(f, h, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+    gen = torch.Generator(device="cuda").manual_seed(7 + P)
+    wts = [{"W1": (torch.randn(h, f, device="cuda", generator=gen) * 0.02).to(torch.bfloat16),
+            "W2": (torch.randn(f, h, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)} for _ in range(P)]
     X0 = [torch.randn(M, h, device="cuda", generator=gen).to(torch.bfloat16) for _ in range(m)]
     dY = [torch.randn(M, h, device="cuda", generator=gen).to(torch.bfloat16) for _ in range(m)]
-    ops = [(k, 0, j) for k, s, j in zb.zb_make_schedule("ZBH2", 8, m) if s == 0]
-    ref = _run_schedule(zb, blk, 1, m, [{"W1": W1, "W2": W2}], X0, dY, ops)
-    pl = zb.make_pipeline(1, m, blk, streams=2)
+    ops = zb.zb_make_schedule(kind, list_P, m)
+    if P == 1:
+        ops = [(k, 0, j) for k, s, j in ops if s == 0]
+    ref = _run_schedule(zb, blk, P, m, wts, X0, dY, ops)
+    pl = zb.make_pipeline(P, m, blk, streams=streams)
     ws_bytes, _ = zb.zb_schedule_workspace_size(pl, ops)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    st = [{"W1": W1, "W2": W2, "dW1": empty_f32(h, f), "dW2": empty_f32(f, h)}]
+    st = [dict(w, dW1=empty_f32(h, f), dW2=empty_f32(f, h)) for w in wts]
     dX0 = [empty_bf16(M, h) for _ in range(m)]
     Yl = [empty_bf16(M, h) for _ in range(m)]
     stream = torch.cuda.current_stream()
     zb.zb_run_stage_schedule(pl, st, X0, dY, dX0, Yl, ops, ws, ws_bytes, None, stream)
     sync(zb)
-    for t in [st[0]["dW1"], st[0]["dW2"]] + dX0 + Yl:
+    for t in [x["dW1"] for x in st] + [x["dW2"] for x in st] + dX0 + Yl:
         t.fill_(float("nan"))
     graph = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
@@ -429,8 +434,9 @@ def test_full_size_step_as_benchmarked(zb):
     for _ in range(2):
         graph.replay()
     sync(zb)
-    for key in ("dW1", "dW2"):
-        assert torch.equal(_bits(st[0][key]), _bits(ref[0][0][key])), key
+    for s_ in range(P):
+        for key in ("dW1", "dW2"):
+            assert torch.equal(_bits(st[s_][key]), _bits(ref[0][s_][key])), (s_, key)
     for j in range(m):
         assert torch.equal(_bits(dX0[j]), _bits(ref[1][j])), j
         assert torch.equal(_bits(Yl[j]), _bits(ref[2][j])), j
