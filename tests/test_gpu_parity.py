@@ -392,12 +392,14 @@ def test_one_stage_lists_full_size_deferred_equals_eager(zb, kind, m, h):
 
 
 @pytest.mark.parametrize("P,m,M,h,kind,list_P,streams", [(1, 24, 3072, 6144, "ZBH2", 8, 2),
+                                                        (1, 16, 3072, 4096, "ZBH1", 8, 2),
                                                         (4, 8, 2048, 1024, "ZBH1", 4, 8)])
 def test_full_size_step_as_benchmarked(zb, P, m, M, h, kind, list_P, streams):
     """A step in the launch configuration the benchmark times: the h=6144
     stage (the stage-0 ZB-H2 list of an 8-stage ordering, m=24, seq 3072, an
-    F/B lane and a W lane) and the P=4, h=1024 pipeline (ZB-H1, m=8, a lane
-    and a W lane per stage), each captured once into a CUDA graph on a side
+    F/B lane and a W lane), the h=4096 stage (ZB-H1, m=16) and the P=4,
+    h=1024 pipeline (ZB-H1, m=8, a lane and a W lane per stage), each
+    captured once into a CUDA graph on a side
     stream after an eager warm-up and replayed twice.  Outputs and fp32
     weight gradients equal the serial eager replay's bit for bit (which the
     tests above tie to eager F+BW, a hand chain of single passes and the
