@@ -456,6 +456,10 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="c4")
     ap.add_argument("--e2e-steps", type=int, default=12)
+    ap.add_argument("--e2e-mode", choices=("graph", "hybrid"), default="graph",
+                    help="graph: one graph per step holds the step, the next step's upload and the "
+                         "read-back; hybrid: a graph holds the step and read-back, the uploads are "
+                         "issued from the host on a copy stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--streams", type=int, default=0,
                     help="streams of the replay (0: one per stage plus a W lane per stage when "
@@ -731,9 +735,38 @@ def main():
         stream.wait_stream(side)
         return g
 
-    e2e_graphs = [capture_e2e(0), capture_e2e(1)] if graph is not None else None
+    def capture_step(a):
+        # --e2e-mode hybrid: one graph per set holds its step and read-back;
+        # the uploads are issued from the host on their own stream
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                Xs_, Gs_, Ws_ = sets[a]
+                zb.zb_run_stage_schedule(pl, Ws_, Xs_, Gs_, None, None, ops_c, ws_t, ws_t.numel(), None, side)
+                read_back(Ws_)
+        stream.wait_stream(side)
+        return g
+
+    hybrid = graph is not None and args.e2e_mode == "hybrid"
+    e2e_graphs = [capture_e2e(0), capture_e2e(1)] if graph is not None and not hybrid else None
+    step_graphs = [capture_step(0), capture_step(1)] if hybrid else None
 
     def e2e_run(steps):
+        if step_graphs is not None:
+            for ev in done:
+                ev.record(stream)
+            upload(0)
+            for k in range(steps):
+                a = k % 2
+                if k + 1 < steps:
+                    upload(1 - a)  # overlaps this step's compute
+                stream.wait_event(in_ready[a])
+                step_graphs[a].replay()
+                done[a].record(stream)
+            torch.cuda.synchronize()
+            return
         if e2e_graphs is not None:
             # step 0's inputs, then each replay uploads the next step's
             with torch.cuda.stream(up_stream):
@@ -827,12 +860,16 @@ def main():
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "upload_alone_ms": upload_ms, "h2d_gb_per_s": h2d / (upload_ms * 1e6),
+                    "mode": args.e2e_mode if graph is not None else "eager",
                     "clocks": e2e_clk,
                     "result": ("fp32 weight gradients" if want_dw else
                                "gradient statistics per stage (sum of squares, NaN/Inf count)"),
                     "timing": ("host wall clock around the steps; per step one CUDA graph: the step, "
                                "the next step's upload in a parallel branch, the read-back"
                                if e2e_graphs is not None else
+                               "host wall clock around the steps; per step one CUDA graph (the step, "
+                               "the read-back), the next step's upload issued from the host on a "
+                               "copy stream" if step_graphs is not None else
                                "host wall clock around synchronised steps; uploads and downloads "
                                "double-buffered on their own streams")},
             "projection": projection,
