@@ -833,6 +833,15 @@ def main():
                "sample": f"fp64 numpy F+B+W of one microbatch's first {tokens} tokens at h={h}, "
                          f"f={f} ({secs:.1f} s)"}
 
+    # bytes one step touches: per stage W1, W2 (bf16) and dW1, dW2 (fp32,
+    # read and written); per stage and microbatch X, dY, Y and dX (M x h)
+    # and H, A and dH (M x f), all bf16
+    wt_b = P * (2 * h * f * 2 + 2 * h * f * 4)
+    act_b = P * m * (4 * M * h * 2 + 3 * M * f * 2)
+    l2_b = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)
+    l2_note = ("inputs larger than L2: a step touches %.0f MB of weights and fp32 gradients and %.0f MB "
+               "of activations, against %.0f MB of L2" % (wt_b / 1e6, act_b / 1e6, l2_b / 1e6))
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -842,8 +851,7 @@ def main():
                        "schedule": sched, "list_from_P": Pl, "streams": pl.streams,
                        "cuda_graph": graph is not None,
                        "parallelism": "replicas" if ws > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (W1 %.0f MB, X and dY %.0f MB per microbatch)"
-                             % (h * f * 2 / 1e6, M * h * 2 / 1e6)},
+                       "l2": l2_note},
             "tokens_per_s": tokens_s,
             "tflops": kind_tf, "tflops_basis": kind_basis,
             "pct_of_peak": {"burst": 100.0 * value / ws / peaks["bf16"],
