@@ -76,14 +76,34 @@ struct Recorder {
     }
 };
 
-std::vector<cudaEvent_t>& event_pool() {
-    static thread_local std::vector<cudaEvent_t> pool;
-    return pool;
+// The current device's ordinal, in [0, 64).  Events belong to the device
+// that was current when they were created, so the pools below keep one list
+// per device.
+zb_status current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    if (*dev < 0 || *dev >= 64) return fail(ZB_ERR_CUDA, "device ordinal out of range");
+    return ZB_OK;
 }
 
-// Events without timing that order ops across streams (one per op).
+// Timing events of this thread on the current device.
+zb_status event_pool(std::vector<cudaEvent_t>** out) {
+    static thread_local std::vector<cudaEvent_t> pools[64];
+    int dev = 0;
+    zb_status s = current_device(&dev);
+    if (s != ZB_OK) return s;
+    *out = &pools[dev];
+    return ZB_OK;
+}
+
+// Events without timing that order ops across streams (one per op), this
+// thread's on the current device.
 zb_status sync_events(size_t n, std::vector<cudaEvent_t>** out) {
-    static thread_local std::vector<cudaEvent_t> pool;
+    static thread_local std::vector<cudaEvent_t> pools[64];
+    int dev = 0;
+    zb_status s = current_device(&dev);
+    if (s != ZB_OK) return s;
+    std::vector<cudaEvent_t>& pool = pools[dev];
     while (pool.size() < n) {
         cudaEvent_t e;
         cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
@@ -441,7 +461,8 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     Recorder rec;
     rec.st = lanes[0];
     rec.on = pl->timing != 0;
-    rec.pool = &event_pool();
+    s = event_pool(&rec.pool);
+    if (s != ZB_OK) return s;
     std::vector<std::pair<size_t, size_t>> op_span(n_ops, {0, 0});  // [first span, end span)
     int gemms = 0;
     g_gemm_counter = &gemms;

@@ -52,6 +52,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -1051,15 +1052,15 @@ bool make_map(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64
 }
 
 int sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cache[dev] == 0) {
+    if (cache[dev].load(std::memory_order_relaxed) == 0) {
         int n = 0;
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return cache[dev].load(std::memory_order_relaxed);
 }
 
 struct Maps {
@@ -1070,11 +1071,12 @@ struct Maps {
 template <int EPI, int A_MN, int B_MN, int CG>
 zb_status configure(int* max_ctas) {
     auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG>;
-    static int cached[64] = {0};
+    // per device; a first call racing another computes the same value
+    static std::atomic<int> cached[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return zb::fail(ZB_ERR_CUDA, "device ordinal out of range");
-    if (!cached[dev]) {
+    if (!cached[dev].load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem_bytes<CG>()));
         if (e != cudaSuccess)
@@ -1099,9 +1101,9 @@ zb_status configure(int* max_ctas) {
                                                         cudaGetErrorString(e));
             n = 2 * clusters;
         }
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    *max_ctas = cached[dev];
+    *max_ctas = cached[dev].load(std::memory_order_relaxed);
     return ZB_OK;
 }
 
@@ -1109,12 +1111,12 @@ zb_status configure(int* max_ctas) {
 template <int EPI, int A_MN, int B_MN>
 int split_clusters(int ks) {
     auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, 1>;
-    static int cached[64][4] = {};
+    static std::atomic<int> cached[64][4];
     int dev = 0;
     cudaGetDevice(&dev);
     const int slot = ks == 2 ? 1 : ks == 4 ? 2 : 3;
     if (dev < 0 || dev >= 64) return 0;
-    if (!cached[dev][slot]) {
+    if (!cached[dev][slot].load(std::memory_order_relaxed)) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(ks * 64, 1, 1);
         cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -1131,9 +1133,9 @@ int split_clusters(int ks) {
             cudaGetLastError();
             n = -1;  // no clusters of this size: never split this far
         }
-        cached[dev][slot] = n;
+        cached[dev][slot].store(n, std::memory_order_relaxed);
     }
-    return cached[dev][slot];
+    return cached[dev][slot].load(std::memory_order_relaxed);
 }
 
 template <int EPI, int A_MN, int B_MN, int CG>
@@ -1207,11 +1209,10 @@ zb_status dispatch(const zb::GemmBf16& g, const Maps& mp, const EpiArgs& ea, lon
 // wave of pairs, else one CTA per 128x256 tile (more CTAs for small problems).
 // ZB_GEMM_CTA_GROUP=1 or =2 in the environment forces one shape.
 int choose_cta_group(long long pair_tiles) {
-    static int forced = -1;
-    if (forced < 0) {
+    static const int forced = [] {
         const char* v = std::getenv("ZB_GEMM_CTA_GROUP");
-        forced = (v && (std::strcmp(v, "1") == 0 || std::strcmp(v, "2") == 0)) ? std::atoi(v) : 0;
-    }
+        return (v && (std::strcmp(v, "1") == 0 || std::strcmp(v, "2") == 0)) ? std::atoi(v) : 0;
+    }();
     if (forced) return forced;
     const int pairs = sm_count() / 2;
     return pair_tiles >= pairs ? 2 : 1;
@@ -1223,19 +1224,22 @@ int choose_cta_group(long long pair_tiles) {
 // ZB_GEMM_SPLIT_K=1 or 2 in the environment caps S (1 disables it);
 // ZB_GEMM_SPLIT_MIN_KB sets min_kb.
 int choose_split(long long tiles, long long num_kb) {
-    static int cap = -1;
-    static int min_kb = 16;
-    if (cap < 0) {
+    struct Knobs {
+        int cap, min_kb;
+    };
+    static const Knobs knobs = [] {
+        Knobs k{SPLIT_MAX, 16};
         const char* v = std::getenv("ZB_GEMM_SPLIT_K");
         const int c = v ? std::atoi(v) : SPLIT_MAX;
-        cap = (c == 1 || c == 2) ? c : SPLIT_MAX;
+        k.cap = (c == 1 || c == 2) ? c : SPLIT_MAX;
         const char* w = std::getenv("ZB_GEMM_SPLIT_MIN_KB");
-        if (w && std::atoi(w) > 0) min_kb = std::atoi(w);
-    }
+        if (w && std::atoi(w) > 0) k.min_kb = std::atoi(w);
+        return k;
+    }();
     const int sms = sm_count();
     int ks = 1;
-    for (int s = 2; s <= cap && s <= SPLIT_MAX; s *= 2)
-        if (tiles * s <= sms && num_kb >= static_cast<long long>(min_kb) * s) ks = s;
+    for (int s = 2; s <= knobs.cap && s <= SPLIT_MAX; s *= 2)
+        if (tiles * s <= sms && num_kb >= static_cast<long long>(knobs.min_kb) * s) ks = s;
     return ks;
 }
 

@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -129,15 +130,15 @@ __device__ __forceinline__ void load_cols<__nv_bfloat16, 8>(const __nv_bfloat16*
 }
 
 int sm_count_misc() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cache[dev] == 0) {
+    if (cache[dev].load(std::memory_order_relaxed) == 0) {
         int n = 0;
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n > 0 ? n : 148;
+        cache[dev].store(n > 0 ? n : 148, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return cache[dev].load(std::memory_order_relaxed);
 }
 
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {

@@ -19,6 +19,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <string>
 
@@ -209,18 +210,18 @@ __global__ void __launch_bounds__(THREADS)
 // wave, so no block starts in a partial second wave).
 template <int PASS>
 unsigned resident_blocks() {
-    static unsigned cached[64] = {};
+    static std::atomic<unsigned> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152u * 4;
-    if (cached[dev]) return cached[dev];
+    if (const unsigned c = cached[dev].load(std::memory_order_relaxed)) return c;
     int per_sm = 0, sms = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, zb_adamw_kernel<PASS>, THREADS, 0) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per_sm < 1 || sms < 1) {
         cudaGetLastError();
         return 152u * 4;
     }
-    cached[dev] = static_cast<unsigned>(per_sm * sms);
-    return cached[dev];
+    cached[dev].store(static_cast<unsigned>(per_sm * sms), std::memory_order_relaxed);
+    return static_cast<unsigned>(per_sm * sms);
 }
 
 bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
