@@ -39,6 +39,14 @@
  *    are read once per process.
  *  - Errors: every call returns a zb_status; zb_last_error() returns a
  *    thread-local, human-readable message for the last failing call.
+ *  - Threads and devices: calls may come from several host threads and for
+ *    several devices; each works on the device current on its thread.  Per
+ *    device and shared by all threads: kernel configuration (made on first
+ *    use), the helper streams of multi-lane replays (two threads replaying at
+ *    once on one device interleave on them, in order, so correctly but not
+ *    concurrently) and the device error word read by zb_sync_status().  Per
+ *    thread and device: the events that order a replay's lanes and time its
+ *    ops.  zb_run_stage_schedule_static's arena is one per process.
  *  - Determinism: for fixed shapes the same inputs give the same output bits;
  *    the W pass adds each microbatch's product into the fp32 gradient with a
  *    fixed tile order, so deferred-W and fused-backward replays that visit
