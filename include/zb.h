@@ -46,7 +46,7 @@
  *    once on one device interleave on them, in order, so correctly but not
  *    concurrently) and the device error word read by zb_sync_status().  Per
  *    thread and device: the events that order a replay's lanes and time its
- *    ops.  zb_run_stage_schedule_static's arena is one per process.
+ *    ops.  zb_run_stage_schedule_static's arena is one per device.
  *  - Determinism: for fixed shapes the same inputs give the same output bits;
  *    the W pass adds each microbatch's product into the fp32 gradient with a
  *    fixed tile order, so deferred-W and fused-backward replays that visit
