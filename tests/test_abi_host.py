@@ -420,3 +420,22 @@ def test_block_flags(zb):
     with pytest.raises(zb.ZBError) as e:
         zb.zb_schedule_workspace_size(zb.make_pipeline(P, m, blk), ok)
     assert e.value.status == zb.ZB_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built library the binding refuses to import: there is no
+    CPU fallback for any entry point."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    missing = str(tmp_path / "libzb_gb300.so")
+    code = ("import split_backward_gemms_gb300.build as b; b.LIB_PATH = %r\n"
+            "try:\n"
+            "    from split_backward_gemms_gb300 import zb\n"
+            "except RuntimeError as e:\n"
+            "    print('refused:', e)\n"
+            "else:\n"
+            "    print('imported')\n" % missing)
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.startswith("refused:") and "no CPU fallback" in r.stdout, r.stdout
