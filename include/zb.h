@@ -33,7 +33,10 @@
  *    A GEMM that follows another of this library's GEMMs on the same stream
  *    may start its setup before that one ends (programmatic dependent
  *    launch); it touches no memory until every earlier work item of the
- *    stream has completed, so stream order holds as usual.  Environment:
+ *    stream has completed, so stream order holds as usual.  One exception:
+ *    zb_backward_weight's dW1 GEMM runs beside its dW2 GEMM (neither reads
+ *    or writes what the other writes, unless the caller's buffers overlap,
+ *    which the library checks) and ends only after it.  Environment:
  *    ZB_GEMM_PDL=0 disables this, ZB_GEMM_SPLIT_K=1 disables split K (see
  *    zb_block.flags), ZB_GEMM_CTA_GROUP=1|2 forces a GEMM tile shape; all
  *    are read once per process.

@@ -177,6 +177,12 @@ zb_status run_gemm(const GemmBf16& g, void* stream, Recorder* rec) {
     return timed(rec, true, [&] { return gemm_bf16_tc(h, stream); });
 }
 
+// Byte ranges [a, a + na) and [b, b + nb) do not overlap.
+bool disjoint(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa + na <= pb || pb + nb <= pa;
+}
+
 int split_allowed(const zb_block& b) { return !g_in_replay && !(b.flags & ZB_BLOCK_NO_SPLIT_K); }
 
 zb_status run_gemm32(const GemmF32& g, void* stream, Recorder* rec) {
@@ -287,6 +293,15 @@ zb_status backward_weight_impl(const zb_block& b, const void* X, const void* A, 
     g6.A = X; g6.lda = b.h; g6.a_mn = 1;
     g6.B = dH; g6.ldb = b.f; g6.b_mn = 1;
     g6.epi = EPI_F32; g6.out0 = dW1; g6.ld0 = b.f; g6.accumulate = accumulate;
+    // the two GEMMs share no output and neither reads the other's, so the
+    // second may run beside the first (unless the caller's buffers overlap)
+    {
+        const size_t hf4 = static_cast<size_t>(b.h) * b.f * 4;
+        const size_t act_f = static_cast<size_t>(b.M) * b.f * 2, act_h = static_cast<size_t>(b.M) * b.h * 2;
+        g6.independent_of_prev = disjoint(dW1, hf4, dW2, hf4) && disjoint(dW1, hf4, A, act_f) &&
+                                 disjoint(dW1, hf4, dY, act_h) && disjoint(dW2, hf4, X, act_h) &&
+                                 disjoint(dW2, hf4, dH, act_f);
+    }
     s = run_gemm(g6, stream, rec);
     if (s != ZB_OK || !b.has_bias) return s;
     s = timed(rec, false, [&] { return colsum_bf16(dH, b.M, b.f, b.f, db1, accumulate, stream); });

@@ -136,6 +136,7 @@ struct EpiArgs {
     int accumulate;
     int act;
     int ksplit;  // CTAs per tile along K (1 = no split; CG = 1 only)
+    int late_wait;  // wait for the previous kernel in the stream at exit, not at start
     unsigned int* err;
 };
 
@@ -657,8 +658,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the setup above overlaps that GEMM's tail; nothing in global memory is
     // read or written before it has completed.  The next GEMM may then be
     // scheduled at once: its CTAs can only take SMs this grid leaves free
-    // (each needs most of an SM's shared memory) and wait there.
-    zbp::grid_dependency_wait();
+    // (each needs most of an SM's shared memory) and wait there.  A GEMM
+    // independent of the previous kernel (late_wait) waits at its exit
+    // instead: it runs beside that kernel's tail and still ends after it.
+    if (!args.late_wait) zbp::grid_dependency_wait();
     zbp::allow_dependent_launch();
 
     if (warp == 0) {
@@ -1000,6 +1003,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else
             zbp::tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    if (args.late_wait) zbp::grid_dependency_wait();
 }
 
 // ---------------------------------------------------------------- host side
@@ -1310,6 +1314,7 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     ea.accumulate = g.accumulate;
     ea.act = g.act;
     ea.ksplit = 1;
+    ea.late_wait = g.independent_of_prev && g.allow_pdl ? 1 : 0;
     ea.err = err;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -50,6 +50,11 @@ struct GemmBf16 {
     // (its setup overlaps that kernel's tail); only where no other stream's
     // kernels compete for the SMs its waiting CTAs would hold
     int allow_pdl = 0;
+    // with allow_pdl: this GEMM reads and writes nothing the previous kernel
+    // in the stream writes, so it starts without waiting for that kernel and
+    // waits for it just before exiting instead (its own completion then still
+    // implies that kernel's, for whatever follows in the stream)
+    int independent_of_prev = 0;
 };
 zb_status gemm_bf16_tc(const GemmBf16& g, void* stream);
 

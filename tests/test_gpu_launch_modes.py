@@ -2,7 +2,8 @@
 
 GEMMs that follow each other on one stream launch as programmatic dependents
 (their setup overlaps the previous GEMM's tail, their first global access
-waits for it to complete).  ZB_GEMM_PDL=0 turns that off and ZB_GEMM_PDL=1
+waits for it to complete; the W pass's second GEMM, independent of the
+first, runs beside it and waits for it before exiting).  ZB_GEMM_PDL=0 turns that off and ZB_GEMM_PDL=1
 turns it on inside every replay lane; the setting is read once per process,
 so each mode runs in a fresh process on the same seeded inputs: single passes
 (with and without split K) and replays on one lane, on an F/B lane beside a W
@@ -50,6 +51,9 @@ def _child(out_path):
         zb.zb_backward_input(blk, G, W1, W2, H, dH, dX)
         dW1, dW2, db1, db2 = empty_f32(h, f), empty_f32(f, h), empty_f32(f), empty_f32(h)
         zb.zb_backward_weight(blk, X, A, dH, G, dW1, dW2, db1, db2, 0)
+        # a second, accumulating W pass right behind the first: its dW1 GEMM
+        # starts beside its dW2 GEMM and must still follow the first pass
+        zb.zb_backward_weight(blk, X, A, dH, G, dW1, dW2, db1, db2, 1)
         sync(zb)
         for k, v in dict(H=H, A=A, Y=Y, dH=dH, dX=dX, dW1=dW1, dW2=dW2, db1=db1, db2=db2).items():
             res[f"pass{M}_{k}"] = _bits(v)
