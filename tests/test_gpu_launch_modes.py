@@ -51,9 +51,16 @@ def _child(out_path):
         zb.zb_backward_input(blk, G, W1, W2, H, dH, dX)
         dW1, dW2, db1, db2 = empty_f32(h, f), empty_f32(f, h), empty_f32(f), empty_f32(h)
         zb.zb_backward_weight(blk, X, A, dH, G, dW1, dW2, db1, db2, 0)
-        # a second, accumulating W pass right behind the first: its dW1 GEMM
-        # starts beside its dW2 GEMM and must still follow the first pass
-        zb.zb_backward_weight(blk, X, A, dH, G, dW1, dW2, db1, db2, 1)
+        # fifteen accumulating W passes right behind the first, on alternating
+        # operands: each pass's dW1 GEMM starts beside its dW2 GEMM and must
+        # still follow the previous pass's dW1 GEMM (a lost or reordered
+        # update changes the fp32 bits)
+        dH_alt, G_alt = dH.flip(0).contiguous(), G.flip(0).contiguous()
+        for k in range(15):
+            if k % 2:
+                zb.zb_backward_weight(blk, X, A, dH, G, dW1, dW2, db1, db2, 1)
+            else:
+                zb.zb_backward_weight(blk, X, A, dH_alt, G_alt, dW1, dW2, db1, db2, 1)
         sync(zb)
         for k, v in dict(H=H, A=A, Y=Y, dH=dH, dX=dX, dW1=dW1, dW2=dW2, db1=db1, db2=db2).items():
             res[f"pass{M}_{k}"] = _bits(v)
