@@ -44,7 +44,8 @@
 // applies the epilogue and stores it.  No global workspace is involved.
 // Launched as a programmatic dependent of the previous GEMM in a stream, a
 // CTA runs its setup early and waits (griddepcontrol.wait) before its first
-// global access.
+// global access; a GEMM that touches nothing the previous one writes (the W
+// pass's second) waits only before it exits, and runs beside that one.
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets the
 // device error word, drains its in-flight copies and MMAs, frees TMEM and
 // returns.
