@@ -44,7 +44,9 @@ reaches exactly P M_B on every device.  At equal times it leaves a tail bubble (
 microbatch's backward crosses the whole V while device 0 has run out of
 deferred W's); ``v_zero_bubble_exists`` shows by exhaustive search that
 gap-free V schedules exist at P M_B for small P -- the pages' claim -- and
-not below it.
+not below it.  ``v_gap_free_schedule_ilp`` asks the same question of the same
+model as a 0/1 integer program (scipy's HiGHS) and reaches larger P;
+``check_gap_free_v`` checks any schedule it returns independently.
 """
 
 from __future__ import annotations
@@ -396,3 +398,149 @@ def v_zero_bubble_exists(P: int, m: int, limit: int, max_nodes: int = 2_000_000)
 
     z = tuple([0] * L)
     return rec(z, z, z, 0, tuple([0] * P))
+
+
+# --------------------------------------------------------------------------
+# the same question as an integer program (larger P than the search reaches)
+# --------------------------------------------------------------------------
+def v_gap_free_schedule_ilp(P: int, m: int, limit: int, max_delay: int | None = None,
+                            time_limit: float = 60.0):
+    """The model of ``v_zero_bubble_exists`` (unit slots, no T_comm, F and B
+    of a virtual stage in microbatch order, W in any order; a device may
+    delay its first pass, here by at most ``max_delay`` slots, default 4P) as
+    a 0/1 integer program solved by scipy's HiGHS: x[op, t] = 1 when op
+    starts in slot t; each op once; a device's slots from its first pass on
+    hold exactly one op each for 6m slots (gap-free); every dependency ends
+    before its consumer starts; at every slot a device holds at most `limit`
+    live chunk activations (F done, W not done).  Returns {device: [(slot,
+    kind, k, j), ...]} for a schedule, None when there is none, and raises
+    RuntimeError when the solver stops at its time limit."""
+    import numpy as np
+    from scipy.optimize import Bounds, LinearConstraint, milp
+    from scipy.sparse import coo_matrix
+
+    L = 2 * P
+    dmax = 4 * P if max_delay is None else max_delay
+    T = dmax + 6 * m
+    dev = [device_chunk("V", P, k)[0] for k in range(L)]
+    ops = [(kd, k, j) for j in range(m) for k in range(L) for kd in "FBW"]
+    # earliest and latest starts along each microbatch's chain
+    es, ls = {}, {}
+    for j in range(m):
+        for k in range(L):
+            es[("F", k, j)] = k
+            es[("B", k, j)] = L + (L - 1 - k)
+            es[("W", k, j)] = L + (L - 1 - k) + 1
+            ls[("W", k, j)] = T - 1
+            ls[("B", k, j)] = T - 2 - k
+        for k in range(L):
+            ls[("F", k, j)] = ls[("B", L - 1, j)] - 1 - (L - 1 - k)
+    var = [(op, t) for op in ops for t in range(es[op], ls[op] + 1)]
+    nx = len(var)
+    n = nx + P * (dmax + 1)  # then one-hot first-slot offsets per device
+    byop = {}
+    for i, (op, t) in enumerate(var):
+        byop.setdefault(op, []).append((i, t))
+    rows, cols, vals, lo, hi = [], [], [], [], []
+
+    def add(coefs, a, b):
+        r = len(lo)
+        for i, v in coefs.items():
+            rows.append(r)
+            cols.append(i)
+            vals.append(v)
+        lo.append(a)
+        hi.append(b)
+
+    for op in ops:
+        add({i: 1 for i, _ in byop[op]}, 1, 1)
+    for s in range(P):
+        add({nx + s * (dmax + 1) + o: 1 for o in range(dmax + 1)}, 1, 1)
+    bydt = {}
+    for i, ((kd, k, j), t) in enumerate(var):
+        bydt.setdefault((dev[k], t), []).append(i)
+    for s in range(P):
+        for t in range(T):
+            c = {i: 1 for i in bydt.get((s, t), [])}
+            for o in range(max(0, t - 6 * m + 1), min(t, dmax) + 1):
+                c[nx + s * (dmax + 1) + o] = -1
+            add(c, 0, 0)
+
+    def before(a, b):  # start(a) + 1 <= start(b)
+        c = {i: t for i, t in byop[b]}
+        for i, t in byop[a]:
+            c[i] = c.get(i, 0) - t
+        add(c, 1, np.inf)
+
+    for j in range(m):
+        for k in range(L):
+            if k > 0:
+                before(("F", k - 1, j), ("F", k, j))
+            before(("F", k, j), ("B", k, j))
+            if k < L - 1:
+                before(("B", k + 1, j), ("B", k, j))
+            before(("B", k, j), ("W", k, j))
+            if j + 1 < m:
+                before(("F", k, j), ("F", k, j + 1))
+                before(("B", k, j), ("B", k, j + 1))
+    for s in range(P):
+        fs = [(i, t) for i, ((kd, k, j), t) in enumerate(var) if kd == "F" and dev[k] == s]
+        ws = [(i, t) for i, ((kd, k, j), t) in enumerate(var) if kd == "W" and dev[k] == s]
+        for t in range(T):
+            c = {i: 1 for i, tt in fs if tt <= t}
+            for i, tt in ws:
+                if tt < t:
+                    c[i] = c.get(i, 0) - 1
+            add(c, -np.inf, limit)
+    A = coo_matrix((vals, (rows, cols)), shape=(len(lo), n)).tocsr()
+    res = milp(c=np.zeros(n), constraints=LinearConstraint(A, np.array(lo, float), np.array(hi, float)),
+               integrality=np.ones(n), bounds=Bounds(0, 1), options={"time_limit": time_limit})
+    if res.status == 2:
+        return None
+    if res.status != 0 or res.x is None:
+        raise RuntimeError(f"integer program not decided: {res.message}")
+    out = {s: [] for s in range(P)}
+    for i, ((kd, k, j), t) in enumerate(var):
+        if res.x[i] > 0.5:
+            out[dev[k]].append((t, kd, k, j))
+    for s in out:
+        out[s].sort()
+    return out
+
+
+def check_gap_free_v(P: int, m: int, limit: int, sched) -> None:
+    """Independent check of a unit-slot V schedule {device: [(slot, kind, k,
+    j)]}: every pass once on its own device, one pass per slot with no idle
+    slot between a device's first and last, each dependency in an earlier
+    slot, at most `limit` live chunk activations on a device at any slot.
+    Raises AssertionError on the first violation."""
+    L = 2 * P
+    when = {}
+    for s, row in sched.items():
+        slots = [t for t, *_ in row]
+        assert slots == list(range(slots[0], slots[0] + len(slots))), f"device {s} idles"
+        assert len(row) == 6 * m, f"device {s} runs {len(row)} passes"
+        live = peak = 0
+        for t, kd, k, j in row:
+            assert device_chunk("V", P, k)[0] == s, f"{kd}{k},{j} on device {s}"
+            assert (kd, k, j) not in when, f"{kd}{k},{j} twice"
+            when[(kd, k, j)] = t
+            if kd == "F":
+                live += 1
+                peak = max(peak, live)
+            elif kd == "W":
+                live -= 1
+        assert peak <= limit, f"device {s} holds {peak} > {limit}"
+    assert len(when) == 3 * L * m
+    for (kd, k, j), t in when.items():
+        deps = []
+        if kd == "F" and k > 0:
+            deps.append(("F", k - 1, j))
+        if kd == "B":
+            deps.append(("F", k, j))
+            if k < L - 1:
+                deps.append(("B", k + 1, j))
+        if kd == "W":
+            deps.append(("B", k, j))
+        for d in deps:
+            assert when[d] < t, f"{kd}{k},{j} at {t} before {d} at {when[d]}"

@@ -117,6 +117,45 @@ def test_gap_free_v_needs_m_at_least_2p_minus_1(P):
     assert not I.v_zero_bubble_exists(P, 2 * P - 2, 2 * P)
 
 
+@pytest.mark.parametrize("P,m,limit", [(1, 3, 2), (1, 2, 1), (2, 2, 4), (2, 3, 4), (2, 4, 4), (2, 4, 3),
+                                       (3, 4, 6), (3, 5, 6), (3, 5, 5)])
+def test_integer_program_agrees_with_the_search(P, m, limit):
+    # two independent methods on the same model: depth-first search over
+    # slots and a 0/1 program; every schedule found passes the checker
+    sched = I.v_gap_free_schedule_ilp(P, m, limit)
+    assert (sched is not None) == I.v_zero_bubble_exists(P, m, limit)
+    if sched is not None:
+        I.check_gap_free_v(P, m, limit, sched)
+
+
+def test_gap_free_checker_rejects_planted_mistakes():
+    P, m, limit = 2, 4, 4
+    good = I.v_gap_free_schedule_ilp(P, m, limit)
+    I.check_gap_free_v(P, m, limit, good)
+
+    def planted(edit):
+        bad = {s: list(row) for s, row in good.items()}
+        edit(bad)
+        with pytest.raises(AssertionError):
+            I.check_gap_free_v(P, m, limit, bad)
+
+    # an idle slot: shift the last pass of device 0 one slot later
+    planted(lambda b: b[0].__setitem__(-1, (b[0][-1][0] + 1,) + b[0][-1][1:]))
+    # a dependency broken: device 0's first B trades slots with its first
+    # pass, so it runs no later than the F it needs (same device, later)
+    def swap(b):
+        row = b[0]
+        p = next(i for i, (_, kd, _, _) in enumerate(row) if kd == "B")
+        (t0, *o0), (tp, *op) = row[0], row[p]
+        row[0], row[p] = (t0, *op), (tp, *o0)
+    planted(swap)
+    # a pass missing (and another duplicated)
+    planted(lambda b: b[0].__setitem__(-1, (b[0][-1][0],) + b[0][-2][1:]))
+    # too little memory for this schedule
+    with pytest.raises(AssertionError):
+        I.check_gap_free_v(P, m, limit - 1, good)
+
+
 TIMES = [S.Times(), S.Times(1.0, 1.2, 0.6, 0.0), S.Times(18.522, 18.086, 9.337, 0.601),
          S.Times(1.0, 1.0, 1.5, 0.1)]
 
