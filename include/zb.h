@@ -195,11 +195,14 @@ zb_status zb_make_schedule(int32_t kind, int32_t P, int32_t m, zb_op* out, size_
  *     microbatch of chunk v-1-(that chunk).  At equal times its bubble is
  *     (P-1)/(vm+P-1).
  *   ZB_SCHED_ZBV (V layout, v = 2): on a simulated timeline a free stage
- *     takes, among its passes that can start earliest, a B before an F before
- *     a W (oldest microbatch first, then the later virtual stage); an F only
- *     while it holds fewer than 2P live chunk activations (P M_B: summary §6),
- *     a chunk-0 forward only while it holds fewer than 2P-1; a W from its
- *     pending ones, oldest first.  Peak: exactly P M_B per stage.
+ *     takes, among its passes that can start earliest, a W when it holds 2P
+ *     live chunk activations, else an F before a B before a W (oldest
+ *     microbatch first, then the later virtual stage); an F only while it
+ *     holds fewer than 2P (P M_B: summary §6), a chunk-0 forward only while
+ *     it holds fewer than 2P-1 or has a W pending; a W from its pending
+ *     ones, oldest first.  Peak: exactly P M_B per stage; at equal times no
+ *     stage idles between its first and last pass (summary §6: zero bubble
+ *     at T_F = T_B = T_W) for any m >= 2P-1; it never deadlocks.
  * Ops carry (stage, chunk); OPT(stage, chunk) follows the last op of each
  * virtual stage; list order = (simulated start, stage).
  * zb_make_interleaved_schedule uses equal times; the simulate variant takes

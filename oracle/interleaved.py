@@ -30,23 +30,24 @@ At equal times this reproduces the printed bubble (P-1)/(vm+P-1).
 
 ZB-V (reading; the pages give the assignment and the properties -- zero
 bubble at T_F = T_B = T_W with peak activation memory p M_B -- but not the
-layout of its figure): the V assignment with the W-placement rules of the
-handcrafted orderings, on a simulated timeline.  Whenever a device is free it
-takes, among the passes that can start at the earliest moment, a B before an
-F before a W; within a kind the oldest microbatch first, then the later
-virtual stage; an F only while the device holds fewer than 2P live chunk
-activations (F done, W not done; P M_B, since a chunk activation is M_B/2),
-and a chunk-a forward (new work entering the device) only while it holds
-fewer than 2P-1, so that a chunk-b forward always finds room (the forward
-of the oldest unfinished microbatch can always advance, hence no deadlock at
-any pass times); a W only from the device's pending ones (oldest first).  It
-reaches exactly P M_B on every device.  At equal times it leaves a tail bubble (the last
-microbatch's backward crosses the whole V while device 0 has run out of
-deferred W's); ``v_zero_bubble_exists`` shows by exhaustive search that
-gap-free V schedules exist at P M_B for small P -- the pages' claim -- and
-not below it.  ``v_gap_free_schedule_ilp`` asks the same question of the same
-model as a 0/1 integer program (scipy's HiGHS) and reaches larger P;
-``check_gap_free_v`` checks any schedule it returns independently.
+layout of its figure): the V assignment on a simulated timeline.  Whenever a
+device is free it takes, among the passes that can start at the earliest
+moment: a W when it holds 2P live chunk activations (F done, W not done;
+P M_B, since a chunk activation is M_B/2), as only a W frees one; else an F
+before a B before a W; within a kind the oldest microbatch first, then the
+later virtual stage.  An F needs fewer than 2P live activations, and a
+chunk-a forward (new work entering the device) fewer than 2P-1 unless a W of
+the device is pending: the last slot either stays free for a chunk-b
+forward or is freed by that W next, so the forward of the oldest unfinished
+microbatch can always advance (no deadlock at any pass times, T_comm
+included).  A W comes from the device's pending ones, oldest first.  At
+equal times this leaves no device idle between its first and last pass and
+peaks at exactly P M_B -- both properties the pages state (pinned for P up
+to 8).  ``v_zero_bubble_exists`` shows by exhaustive search that no gap-free
+V schedule holds less memory and none exists below m = 2P-1;
+``v_gap_free_schedule_ilp`` asks the same question of the same model as a
+0/1 integer program (scipy's HiGHS) and reaches larger P;
+``check_gap_free_v`` checks any unit-slot schedule independently.
 """
 
 from __future__ import annotations
@@ -195,10 +196,12 @@ def simulate_zbv(P: int, m: int, t: Times = Times(), limit: int | None = None):
                         r = end[dep]
                         if k < L - 1 and device_chunk(layout, P, k + 1)[0] != s:
                             r += t.comm
-                        cands.append((max(r, free[s]), 0, j, -k, "B", k))
+                        cands.append((max(r, free[s]), 2, j, -k, "B", k))
                 j = nF[k]
-                room = limit - (1 if k < P else 0)  # chunk-a forwards leave one slot
-                if j < m and live[s] < room and (k == 0 or ("F", k - 1, j) in end):
+                # a chunk-a forward leaves the last slot to chunk b unless a W
+                # is pending (a full device runs that W next)
+                room = live[s] < limit and (k >= P or live[s] < limit - 1 or bool(pend[s]))
+                if j < m and room and (k == 0 or ("F", k - 1, j) in end):
                     r = 0.0
                     if k > 0:
                         r = end[("F", k - 1, j)]
@@ -207,7 +210,8 @@ def simulate_zbv(P: int, m: int, t: Times = Times(), limit: int | None = None):
                     cands.append((max(r, free[s]), 1, j, -k, "F", k))
             if pend[s]:
                 j, k = min(pend[s], key=lambda x: (x[0], -x[1]))
-                cands.append((max(end[("B", k, j)], free[s]), 2, j, -k, "W", k))
+                wrank = 0 if live[s] >= limit else 3
+                cands.append((max(end[("B", k, j)], free[s]), wrank, j, -k, "W", k))
             if not cands:
                 continue
             s0 = min(c[0] for c in cands)

@@ -145,12 +145,15 @@ bool sim_ilv(int P, int v, int m, const Tm& T, std::vector<Ev>* out) {
 
 // ------------------------------------------------------------------ ZB-V
 // Whenever a stage is free it takes, among its passes that can start at the
-// earliest moment, a B before an F before a W; within a kind the oldest
+// earliest moment: a W when it holds `limit` live chunk activations (only a
+// W frees one), else an F before a B before a W; within a kind the oldest
 // microbatch first, then the later virtual stage.  An F needs fewer than
-// `limit` live chunk activations on the stage (a chunk-0 forward fewer than
-// limit - 1, so a chunk-1 forward always finds room and the oldest
-// unfinished forward can always advance); a W comes from the stage's pending
-// ones, oldest first.  Stages are served in order of their pass's start.
+// `limit` live activations; a chunk-0 forward fewer than limit - 1 unless a
+// W of the stage is pending, so the last slot either stays free for a
+// chunk-1 forward or is freed by that W next, and the oldest unfinished
+// forward can always advance.  A W comes from the stage's pending ones,
+// oldest first.  Stages are served in order of their pass's start.  At
+// T_F = T_B = T_W this leaves no stage idle between its first and last pass.
 bool sim_zbv(int P, int m, const Tm& T, std::vector<Ev>* out) {
     const int layout = ZB_LAYOUT_V, v = 2, L = 2 * P, limit = 2 * P;
     const size_t LM = static_cast<size_t>(L) * m;
@@ -196,11 +199,13 @@ bool sim_zbv(int P, int m, const Tm& T, std::vector<Ev>* out) {
                         dev_chunk(layout, P, k + 1, &ds, &dc);
                         if (ds != s) r += T.comm;
                     }
-                    if (dep_done) offer({std::max(r, freeT[s]), 0, j, -k, ZB_OP_B, k});
+                    if (dep_done) offer({std::max(r, freeT[s]), 2, j, -k, ZB_OP_B, k});
                 }
                 j = nF[k];
-                const int room = limit - (k < P ? 1 : 0);
-                if (j < m && live[s] < room && (k == 0 || nF[k - 1] > j)) {
+                // a chunk-0 forward leaves the last slot to chunk 1 unless a W
+                // is pending (a full stage runs that W next)
+                const bool room = live[s] < limit && (k >= P || live[s] < limit - 1 || !pend[s].empty());
+                if (j < m && room && (k == 0 || nF[k - 1] > j)) {
                     double r = 0.0;
                     if (k > 0) {
                         r = endF[static_cast<size_t>(k - 1) * m + j];
@@ -216,7 +221,8 @@ bool sim_zbv(int P, int m, const Tm& T, std::vector<Ev>* out) {
                     return a.first != b.first ? a.first < b.first : a.second > b.second;
                 });
                 const int j = it->first, k = it->second;
-                offer({std::max(endB[static_cast<size_t>(k) * m + j], freeT[s]), 2, j, -k, ZB_OP_W, k});
+                const int wrank = live[s] >= limit ? 0 : 3;
+                offer({std::max(endB[static_cast<size_t>(k) * m + j], freeT[s]), wrank, j, -k, ZB_OP_W, k});
             }
             if (!any) continue;
             if (!have || c.start < best.start) {

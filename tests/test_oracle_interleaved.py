@@ -18,6 +18,7 @@
 
 import os
 
+import numpy as np
 import pytest
 
 from oracle import interleaved as I
@@ -126,6 +127,36 @@ def test_integer_program_agrees_with_the_search(P, m, limit):
     assert (sched is not None) == I.v_zero_bubble_exists(P, m, limit)
     if sched is not None:
         I.check_gap_free_v(P, m, limit, sched)
+
+
+@pytest.mark.parametrize("P", list(range(1, 9)))
+def test_zbv_rule_is_gap_free_at_equal_times(P):
+    # the summary's ZB-V properties: no bubble at T_F = T_B = T_W with peak
+    # p M_B (2P chunk activations); the rule's schedule, in unit slots of
+    # one chunk pass, also passes the independent gap-free checker
+    t = S.Times()
+    for m in sorted({max(1, 2 * P - 1), 2 * P, 3 * P, 3 * P + 1, 4 * P + 3}):
+        ev = I.simulate_zbv(P, m, t)
+        assert I.bubble_rate(ev, P, m, t) == 0.0, (P, m)
+        assert max(I.peak_live_chunks(ev, P)) == min(2 * P, 2 * m)
+        sched = {s: [] for s in range(P)}
+        for kind, s, c, j, st, en in ev:
+            k = I.virtual_stage("V", P, s, c)
+            sched[s].append((int(round(st * 2)), kind, k, j))
+        for s in sched:
+            sched[s].sort()
+        I.check_gap_free_v(P, m, 2 * P, sched)
+
+
+def test_zbv_rule_never_deadlocks_at_random_times():
+    rng = np.random.default_rng(5)
+    for _ in range(40):
+        t = S.Times(*rng.uniform(0.3, 2.0, 3), float(rng.choice([0.0, rng.uniform(0.0, 0.6)])))
+        P = int(rng.integers(1, 9))
+        m = int(rng.integers(1, 4 * P + 4))
+        ev = I.simulate_zbv(P, m, t)
+        assert len(ev) == 6 * P * m
+        assert max(I.peak_live_chunks(ev, P)) <= 2 * P
 
 
 def test_gap_free_checker_rejects_planted_mistakes():
