@@ -404,70 +404,135 @@ def validate_ops(ops, P: int, m: int):
     return True
 
 
-def inspect_events(events, stage_count: int):
-    """Event-interval validator after [ZB proven] "Validate the schedule as data".
+def _producers(kind, s, j, stages, present):
+    """The passes an event needs before it may start, by the dependency rules.
 
-    events: iterable of dicts {id, stage, micro, kind, start, end, dependsOn?}.
-    Rejects (ScheduleError code): "stage_count", "duplicate_task",
-    "invalid_stage", "invalid_interval", "missing_dependency",
-    "dependency_violation", "stage_overlap".
-    Returns dict(span, busy, bubble_ratio_global, bubble_rate_eq3,
-    unfinished_activations_b, unfinished_activations_w).
-      * bubble_ratio_global: 1 - busy / (stage_count * span), span from t=0
-        (the [ZB proven] checker's declared denominator);
-      * bubble_rate_eq3: (cost - busy_per_stage_max...) reported as
-        1 - busy / (stage_count * cost) with cost = max per-stage span (Eq. 3);
-      * unfinished_activations_b: F opens, B closes (the checker's ledger);
-      * unfinished_activations_w: F opens, W or BW closes (the lifetime of
-        deferred-W activations, [ZB-PP summary] "The Memory Model").
+    [ZB proven] "Draw the event graph before the Gantt": a forward consumes
+    the previous stage's forward output; an input-gradient pass consumes its
+    own forward context and the next stage's input gradient (that stage's BW
+    when its backward is fused); a weight-gradient pass consumes its own B;
+    the optimizer consumes every weight gradient of its stage that the trace
+    began (a forward without its W leaves the update waiting).
+    ``present`` is the set of (kind, stage, micro) keys in the trace.
     """
-    if not isinstance(stage_count, int) or stage_count < 2:
-        raise ScheduleError("stage_count")
-    ids = [e["id"] for e in events]
-    by_id = {e["id"]: e for e in events}
-    if len(by_id) != len(ids):
-        raise ScheduleError("duplicate_task")
-    for e in events:
-        st = e["stage"]
-        if not isinstance(st, int) or st < 0 or st >= stage_count:
-            raise ScheduleError("invalid_stage", str(e["id"]))
-        if not (e["start"] >= 0 and e["end"] > e["start"]):
-            raise ScheduleError("invalid_interval", str(e["id"]))
-        for d in e.get("dependsOn", ()) or ():
-            if d not in by_id:
-                raise ScheduleError("missing_dependency", f"{e['id']} -> {d}")
-            if by_id[d]["end"] > e["start"]:
-                raise ScheduleError("dependency_violation", f"{e['id']} -> {d}")
-    per_stage = {}
-    for e in events:
-        per_stage.setdefault(e["stage"], []).append(e)
-    for st, lst in per_stage.items():
-        lst = sorted(lst, key=lambda e: e["start"])
-        for a, b in zip(lst, lst[1:]):
-            if a["end"] > b["start"]:
-                raise ScheduleError("stage_overlap", f"{a['id']} / {b['id']}")
-    span = max(e["end"] for e in events)
-    busy = sum(e["end"] - e["start"] for e in events)
-    cost_eq3 = max(max(e["end"] for e in lst) - min(e["start"] for e in lst)
-                   for lst in per_stage.values())
-    live_b = {}
-    live_w = {}
-    for e in events:
-        key = e["micro"], e["stage"]
-        if e["kind"] == "F":
-            live_b[e["micro"]] = live_b.get(e["micro"], 0) + 1
-            live_w[key] = live_w.get(key, 0) + 1
-        if e["kind"] in ("B", "BW"):
-            live_b[e["micro"]] = max(0, live_b.get(e["micro"], 0) - 1)
-        if e["kind"] in ("W", "BW"):
-            live_w[key] = max(0, live_w.get(key, 0) - 1)
+    if kind == "F":
+        return [] if s == 0 else [("F", s - 1, j)]
+    if kind == "W":
+        return [("B", s, j)]
+    if kind in ("B", "BW"):
+        need = [("F", s, j)]
+        if s + 1 < stages:
+            nxt = "BW" if ("BW", s + 1, j) in present else "B"
+            need.append((nxt, s + 1, j))
+        return need
+    # OPT
+    began = sorted(i for (k, t, i) in present if k == "F" and t == s)
+    return [("BW" if ("BW", s, i) in present else "W", s, i) for i in began]
+
+
+def check_trace(events, stages: int):
+    """Legality and bubble accounting of a timed event trace of one step.
+
+    Written from the prose of [ZB proven] "Draw the event graph before the
+    Gantt" and "Validate the schedule as data".  A trace is a list of dicts
+    {id, stage, micro, kind, start, end, dependsOn (optional)} with kind in
+    F, B, W, BW (fused backward) or OPT (the stage's optimizer barrier, which
+    may take no time).  The check builds the event graph: one node per
+    (kind, stage, micro), producer edges both from the trace's own
+    ``dependsOn`` claims and from the dependency rules (``_producers``), and
+    resource edges that keep one stage's passes apart.  Failures raise
+    ScheduleError with these codes:
+        "stages"           the stage count is not a positive integer;
+        "duplicate_id"     two events carry one id;
+        "unknown_kind", "unknown_stage", "bad_interval"  (start < 0, end before
+                           start, or a pass of zero length);
+        "duplicate_work"   two events for one (kind, stage, micro);
+        "missing_producer" a claimed or required producer is not in the trace;
+        "early_consumer"   an event starts before a producer has ended;
+        "stage_collision"  two events of one stage overlap in time.
+    Producer edges are checked event by event in order of start time (ties
+    by id), the trace's claims before the rules' requirements, so the error
+    names the earliest offending consumer.
+
+    Returns a dict:
+        makespan           last end - first start;
+        busy               the summed length of every pass;
+        bubble_global      1 - busy / (stages x makespan): the checker's
+                           denominator of [ZB proven];
+        bubble_eq3         1 - busy / (stages x cost), cost = the longest
+                           per-stage span (Eq. 3 of the summary, §5 Metrics);
+        open_after_b       (stage, micro) pairs with a forward and no B / BW:
+                           activations the input-gradient pass never released;
+        open_after_w       pairs with a forward and no W / BW: activations of
+                           the memory model ("The Memory Model") still held.
+    """
+    if isinstance(stages, bool) or not isinstance(stages, int) or stages < 1:
+        raise ScheduleError("stages", repr(stages))
+    by_id = {}
+    for ev in events:
+        if ev["id"] in by_id:
+            raise ScheduleError("duplicate_id", str(ev["id"]))
+        by_id[ev["id"]] = ev
+    by_key = {}
+    for ident, ev in by_id.items():
+        kind, s = ev["kind"], ev["stage"]
+        if kind not in KINDS:
+            raise ScheduleError("unknown_kind", f"{ident}: {kind!r}")
+        if isinstance(s, bool) or not isinstance(s, int) or not 0 <= s < stages:
+            raise ScheduleError("unknown_stage", f"{ident}: {s!r}")
+        a, b = float(ev["start"]), float(ev["end"])
+        zero_ok = kind == "OPT"
+        if not (0.0 <= a and (b > a or (zero_ok and b == a))) or b == float("inf"):
+            raise ScheduleError("bad_interval", f"{ident}: [{a}, {b}]")
+        key = (kind, s, 0 if kind == "OPT" else ev["micro"])
+        if key in by_key:
+            raise ScheduleError("duplicate_work", f"{by_key[key]} and {ident}")
+        by_key[key] = ident
+    present = set(by_key)
+
+    # producer edges, in order of the consumers' start times
+    for ident in sorted(by_id, key=lambda i: (float(by_id[i]["start"]), str(i))):
+        ev = by_id[ident]
+        claimed = list(ev.get("dependsOn") or ())
+        key = (ev["kind"], ev["stage"], 0 if ev["kind"] == "OPT" else ev["micro"])
+        required = [by_key.get(p, p) for p in _producers(*key, stages, present)]
+        for p in claimed + required:
+            if p not in by_id:
+                raise ScheduleError("missing_producer", f"{ident} needs {p}")
+            if float(by_id[p]["end"]) > float(ev["start"]):
+                raise ScheduleError("early_consumer", f"{ident} starts before {p} ends")
+
+    # resource edges: one pass at a time per stage
+    lanes = {}
+    for ident, ev in by_id.items():
+        lanes.setdefault(ev["stage"], []).append((float(ev["start"]), float(ev["end"]), str(ident)))
+    first = float("inf")
+    last = float("-inf")
+    longest_span = 0.0
+    busy = 0.0
+    for s, lane in lanes.items():
+        lane.sort()
+        free_at, holder = float("-inf"), None
+        for a, b, ident in lane:
+            if a < free_at:
+                raise ScheduleError("stage_collision", f"{holder} and {ident} on stage {s}")
+            free_at, holder = b, ident
+            busy += b - a
+        first = min(first, lane[0][0])
+        last = max(last, free_at)
+        longest_span = max(longest_span, free_at - lane[0][0])
+
+    began = {(ev["stage"], ev["micro"]) for ev in by_id.values() if ev["kind"] == "F"}
+    done_b = {(ev["stage"], ev["micro"]) for ev in by_id.values() if ev["kind"] in ("B", "BW")}
+    done_w = {(ev["stage"], ev["micro"]) for ev in by_id.values() if ev["kind"] in ("W", "BW")}
+    makespan = last - first if by_id else 0.0
     return {
-        "span": span,
+        "makespan": makespan,
         "busy": busy,
-        "bubble_ratio_global": 1.0 - busy / (stage_count * span),
-        "bubble_rate_eq3": 1.0 - busy / (stage_count * cost_eq3),
-        "unfinished_activations_b": sum(live_b.values()),
-        "unfinished_activations_w": sum(live_w.values()),
+        "bubble_global": 1.0 - busy / (stages * makespan) if makespan > 0 else 0.0,
+        "bubble_eq3": 1.0 - busy / (stages * longest_span) if longest_span > 0 else 0.0,
+        "open_after_b": len(began - done_b),
+        "open_after_w": len(began - done_w),
     }
 
 

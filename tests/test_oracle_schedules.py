@@ -7,7 +7,9 @@
   p M_B / p M_B / (2p-1) M_B; 1F1B keeps P-s microbatches in flight on stage s;
 * the schedule checker's worked example ("Zero-Bubble Pipeline Parallelism,
   Proven", section "Validate the schedule as data") ->
-  tests/golden/checker_example.txt, with its four rejection cases;
+  tests/golden/checker_example.txt, with its four rejection cases (the
+  event values the page prints are data here; the checker itself follows
+  the page's prose rules, not its listing);
 * topological validity of every generated list with OPT after all W;
 * brute force over every per-stage order at P=2, m=2.
 """
@@ -103,10 +105,12 @@ def test_generated_lists_are_valid(kind, P, m):
     for s in range(P):
         lst = [op for op in ops if op[1] == s]
         assert lst[-1][0] == "OPT"
-    if P >= 2:
-        r = S.inspect_events(S.events_as_dicts(ev), P)
-        assert r["unfinished_activations_w"] == 0
-        assert r["unfinished_activations_b"] == 0
+    r = S.check_trace(S.events_as_dicts(ev), P)
+    assert r["open_after_w"] == 0
+    assert r["open_after_b"] == 0
+    # the checker's Eq. 3 figure is the simulator's bubble rate
+    t = S.Times()
+    assert abs(r["bubble_eq3"] - S.bubble_rate(ev, P, m, t)) < 1e-12
 
 
 def _checker_events():
@@ -119,30 +123,117 @@ def _checker_events():
 
 
 def test_checker_worked_example():
+    # The page's two-stage example: span 8, nothing left open, a bubble ratio
+    # in [0, 0.3) under the global denominator (12 busy units of 2 x 8).
     evs = _checker_events()
-    r = S.inspect_events(evs, 2)
-    assert r["span"] == 8
-    assert r["unfinished_activations_b"] == 0
-    assert r["unfinished_activations_w"] == 0
-    assert 0 <= r["bubble_ratio_global"] < 0.3
-    assert r["bubble_ratio_global"] == 1 - 12 / 16
-    assert r == S.inspect_events(list(evs), 2)
+    r = S.check_trace(evs, 2)
+    assert r["makespan"] == 8
+    assert r["busy"] == 12
+    assert r["open_after_b"] == 0
+    assert r["open_after_w"] == 0
+    assert 0 <= r["bubble_global"] < 0.3
+    assert r["bubble_global"] == 1 - 12 / 16
+    # stage 0 spans [0, 8], stage 1 [1, 7]: Eq. 3 takes the longer
+    assert r["bubble_eq3"] == 1 - 12 / 16
+    # the same trace in another order gives the same report
+    assert r == S.check_trace(list(reversed(evs)), 2)
 
 
+# The page's rejection cases (its four malformed additions to the example),
+# plus an unknown producer and an empty interval; each must be rejected for
+# the stated reason.
 @pytest.mark.parametrize("extra,code", [
-    ({"id": "s0f0", "stage": 0, "micro": 9, "kind": "F", "start": 8, "end": 9}, "duplicate_task"),
-    ({"id": "bad", "stage": 2, "micro": 0, "kind": "W", "start": 8, "end": 9}, "invalid_stage"),
-    ({"id": "bad", "stage": 0, "micro": 2, "kind": "F", "start": 0.5, "end": 1.5}, "stage_overlap"),
+    ({"id": "s0f0", "stage": 0, "micro": 9, "kind": "F", "start": 8, "end": 9}, "duplicate_id"),
+    ({"id": "bad", "stage": 2, "micro": 0, "kind": "W", "start": 8, "end": 9}, "unknown_stage"),
+    ({"id": "bad", "stage": 0, "micro": 2, "kind": "F", "start": 0.5, "end": 1.5}, "stage_collision"),
     ({"id": "bad", "stage": 1, "micro": 2, "kind": "B", "start": 0, "end": 1,
-      "dependsOn": ["s0f1"]}, "dependency_violation"),
+      "dependsOn": ["s0f1"]}, "early_consumer"),
     ({"id": "bad", "stage": 1, "micro": 2, "kind": "B", "start": 9, "end": 10,
-      "dependsOn": ["nope"]}, "missing_dependency"),
-    ({"id": "bad", "stage": 1, "micro": 2, "kind": "B", "start": 9, "end": 9}, "invalid_interval"),
+      "dependsOn": ["nope"]}, "missing_producer"),
+    ({"id": "bad", "stage": 1, "micro": 2, "kind": "B", "start": 9, "end": 9}, "bad_interval"),
 ])
 def test_checker_rejections(extra, code):
     with pytest.raises(S.ScheduleError) as ei:
-        S.inspect_events(_checker_events() + [extra], 2)
+        S.check_trace(_checker_events() + [extra], 2)
     assert ei.value.code == code
+
+
+def _drop_claims(evs):
+    return [{k: v for k, v in e.items() if k != "dependsOn"} for e in evs]
+
+
+def _retime(evs, ident, start, end):
+    out = [dict(e) for e in evs]
+    for e in out:
+        if e["id"] == ident:
+            e["start"], e["end"] = start, end
+    return out
+
+
+def test_checker_rules_without_claims():
+    # With every dependsOn claim removed the event graph's own rules still
+    # hold the example legal, and still catch each kind of early start.
+    evs = _drop_claims(_checker_events())
+    assert S.check_trace(evs, 2)["makespan"] == 8
+    cases = [
+        ("s1f0", 0.5, 0.9),   # F(1,0) before F(0,0) has ended
+        ("s0b0", 2.5, 2.9),   # B(0,0) before the downstream B(1,0)
+        ("s0w1", 6.5, 6.9),   # W(0,1) before its own B(0,1) ... and overlapping it
+        ("s1b1", 3.5, 3.9),   # B(1,1) before its forward F(1,1) ends
+    ]
+    for ident, a, b in cases:
+        with pytest.raises(S.ScheduleError) as ei:
+            S.check_trace(_retime(evs, ident, a, b), 2)
+        assert ei.value.code in ("early_consumer", "stage_collision"), ident
+    # W(0,1) moved before its B with no overlap on the stage: the rule alone
+    with pytest.raises(S.ScheduleError) as ei:
+        S.check_trace(_retime(evs, "s0w1", 5.0, 5.5), 2)
+    assert ei.value.code == "early_consumer"
+
+
+def test_checker_optimizer_barrier():
+    evs = _drop_claims(_checker_events())
+    ok = evs + [{"id": "opt0", "stage": 0, "micro": 0, "kind": "OPT", "start": 8, "end": 8}]
+    assert S.check_trace(ok, 2)["open_after_w"] == 0
+    early = evs + [{"id": "opt0", "stage": 0, "micro": 0, "kind": "OPT", "start": 7.5, "end": 7.5}]
+    with pytest.raises(S.ScheduleError) as ei:
+        S.check_trace(early, 2)
+    assert ei.value.code == "early_consumer"   # W(0,1) ends at 8
+
+
+def test_checker_missing_rule_producer_and_open_markers():
+    evs = _drop_claims(_checker_events())
+    # a B with no forward of its own
+    orphan = evs + [{"id": "x", "stage": 1, "micro": 5, "kind": "B", "start": 9, "end": 10}]
+    with pytest.raises(S.ScheduleError) as ei:
+        S.check_trace(orphan, 2)
+    assert ei.value.code == "missing_producer"
+    # dropping the W passes of micro 1 leaves two activations held under the
+    # memory model, none under the input-gradient ledger
+    r = S.check_trace([e for e in evs if e["id"] not in ("s0w1", "s1w1")], 2)
+    assert (r["open_after_b"], r["open_after_w"]) == (0, 2)
+    # dropping the stage-0 B of micro 1 (and its W) leaves one open on each
+    r = S.check_trace([e for e in evs if e["id"] not in ("s0b1", "s0w1")], 2)
+    assert (r["open_after_b"], r["open_after_w"]) == (1, 1)
+    # the same (kind, stage, micro) twice under two ids
+    dup = evs + [{"id": "again", "stage": 0, "micro": 0, "kind": "F", "start": 8, "end": 9}]
+    with pytest.raises(S.ScheduleError) as ei:
+        S.check_trace(dup, 2)
+    assert ei.value.code == "duplicate_work"
+
+
+def test_checker_fused_backward_trace():
+    # 1F1B's fused BW: B(s) then needs the downstream BW, and the simulated
+    # trace at unequal times passes; shifting one BW earlier fails.
+    t = S.Times(1.0, 1.3, 0.7, 0.1)
+    ev, _ = S.make_schedule("1F1B", 4, 8, t)
+    d = _drop_claims(S.events_as_dicts(ev))
+    assert S.check_trace(d, 4)["open_after_w"] == 0
+    bw = [e for e in d if e["kind"] == "BW" and e["stage"] == 2][0]
+    moved = _retime(d, bw["id"], 0.0, 0.01)
+    with pytest.raises(S.ScheduleError) as ei:
+        S.check_trace(moved, 4)
+    assert ei.value.code in ("early_consumer", "stage_collision")
 
 
 def test_validate_ops_rejections():
