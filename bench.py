@@ -73,24 +73,17 @@ def _gemm_source_sha():
 
 
 def _profiled_traffic(workload):
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
-    taken on the current GEMM source; else None."""
-    path = os.path.join(ROOT, "profiles", f"gemm_tc_{workload}.md")
+    """DRAM bytes per GEMM launch of the workload's step mix, from the ncu
+    figures committed as data under profiles/ (gemm_tc_<workload>.json),
+    while they were taken on the current GEMM source; else None."""
+    path = os.path.join(ROOT, "profiles", f"gemm_tc_{workload}.json")
     try:
         with open(path) as fh:
-            txt = fh.read()
-    except OSError:
-        return None
-    vals = {}
-    for ln in txt.splitlines():
-        if ln.startswith("traffic_bytes_per_launch:") or ln.startswith("source_sha:"):
-            k, v = ln.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("source_sha") != _gemm_source_sha():
-        return None
-    try:
-        return float(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
+            d = json.load(fh)
+        if d.get("source_sha") != _gemm_source_sha():
+            return None
+        return float(d["traffic_bytes_per_launch"])
+    except (OSError, KeyError, TypeError, ValueError):
         return None
 
 
@@ -199,6 +192,7 @@ def run_reference(args, wl):
     if rank != 0:
         return 0
     h, f, M, m, sched, Pl, desc = WORKLOADS[wl]
+    sched = args.schedule or sched
     tokens = 256
     from oracle import block as ob  # noqa: F401  (the oracle is the reference arm)
     import numpy as np
@@ -448,6 +442,117 @@ def measure_post_validated_adamw(zb, h, f, dev, stream, peaks, steps=5, warmup=3
                                         "unit": "GB/s", "frac": stats_gbs / peaks["hbm"]}}}
 
 
+class Workload:
+    """Device tensors, op list and executor plan of one benchmark workload."""
+
+
+def make_ops(zb, sched, Pl, m, multi):
+    """The op list a workload replays: the whole pipeline, or the stage-0
+    list of a Pl-stage ordering replayed as one stage."""
+    ops = zb.zb_make_schedule(sched, Pl, m)
+    if not multi:
+        ops = [(k, 0, j) for k, s, j in ops if s == 0]
+    return ops
+
+
+def setup_workload(zb, dev, name, schedule=None, streams=0, seed=1000):
+    """Seeded synthetic weights (N(0, 0.02)), inputs and last-stage gradients
+    (N(0, 1)) in HBM, the op list and a planned workspace."""
+    import torch
+    w = Workload()
+    w.name = name
+    w.h, w.f, w.M, w.m, sched, w.Pl, w.desc = WORKLOADS[name]
+    w.sched = schedule or sched
+    w.multi = name == "c2"
+    w.P = w.Pl if w.multi else 1
+    h, f, M, m = w.h, w.f, w.M, w.m
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    bf = torch.bfloat16
+    w.W = [{"W1": (torch.randn(h, f, device=dev, generator=gen) * 0.02).to(bf),
+            "W2": (torch.randn(f, h, device=dev, generator=gen) * 0.02).to(bf),
+            "dW1": torch.zeros(h, f, device=dev), "dW2": torch.zeros(f, h, device=dev)}
+           for _ in range(w.P)]
+    w.X0 = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
+    w.dY = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
+    w.ops = make_ops(zb, w.sched, w.Pl, m, w.multi)
+    w.blk = zb.make_block(M, h, f)
+    # multi-stage replays run their stages on P streams (stage-parallel)
+    # plus a W lane per stage where 2P streams fit (the P=4, h=1024
+    # pipeline: 995 TF/s on 4 streams, 1008 on 8); a one-stage replay puts
+    # its W passes on a second stream
+    n_streams = streams if streams > 0 else (min(2 * w.P, 8) if w.multi else 2)
+    w.pl = zb.make_pipeline(w.P, m, w.blk, timing=True, streams=n_streams)
+    w.need, w.peak_live = zb.zb_schedule_workspace_size(w.pl, w.ops)
+    w.ws_t = torch.empty(max(w.need, 256), dtype=torch.uint8, device=dev)
+    w.ops_c = zb.ops_array(w.ops)
+    w.step_flops = 12.0 * M * h * f * m * w.P  # F, B and W: 4 M h f each per microbatch
+    return w
+
+
+def time_workload(zb, dev, w, steps, warmup, use_graph=True):
+    """Warm-up replays, then `steps` replays of one captured CUDA graph
+    between CUDA events on the launching stream (no per-op timing)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    st = zb.zb_run_stats()
+    for _ in range(warmup):
+        zb.zb_run_stage_schedule(w.pl, w.W, w.X0, w.dY, None, None, w.ops_c, w.ws_t, w.ws_t.numel(), st,
+                                 stream)
+    torch.cuda.synchronize()
+    zb.zb_sync_status(stream)
+    launches = st.n_gemm_launches
+    w.pl.timing = 0
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                zb.zb_run_stage_schedule(w.pl, w.W, w.X0, w.dY, None, None, w.ops_c, w.ws_t,
+                                         w.ws_t.numel(), None, side)
+        stream.wait_stream(side)
+        graph.replay()
+        torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        if graph is not None:
+            graph.replay()
+        else:
+            zb.zb_run_stage_schedule(w.pl, w.W, w.X0, w.dY, None, None, w.ops_c, w.ws_t, w.ws_t.numel(),
+                                     None, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    zb.zb_sync_status(stream)
+    ms = e0.elapsed_time(e1) / steps
+    w.pl.timing = 1
+    return {"ms_per_step": ms, "value": w.step_flops / (ms / 1e3) / 1e12,
+            "tokens_per_s": w.m * w.M / (ms / 1e3),
+            "gemm_launches_per_step": launches}
+
+
+def other_workloads(zb, dev, steps, warmup):
+    """The other configurations in the same run, each as its own short
+    timed region: the P=4, h=1024 pipeline under 1F1B (fused backward) and
+    under ZB-H1 (split backward, W lanes), same streams and graphs, and the
+    h=4096 one-stage ZB-H1 step."""
+    import torch
+    out = {}
+    for name, sched in (("c2", "1F1B"), ("c2", "ZBH1"), ("c3", "ZBH1")):
+        w = setup_workload(zb, dev, name, sched)
+        r = time_workload(zb, dev, w, steps, warmup)
+        r.update({"workload": w.desc.split(",")[0] if name != "c2" else
+                  "P=4 stages h=1024 ffn=4096 microbatch 4x512 m=8, all stages on one GPU",
+                  "schedule": sched, "streams": w.pl.streams, "unit": UNIT,
+                  "pct_of_burst_peak": 100.0 * r["value"] / _peaks()["bf16"]})
+        out[f"{name}_{sched}"] = r
+        del w
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -455,6 +560,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="c4")
+    ap.add_argument("--schedule", choices=("1F1B", "ZBH1", "ZBH2"), default=None,
+                    help="ordering to replay instead of the workload's own (c4: ZBH2, c3 and c2: ZBH1)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other configurations' short timed regions (the P=4, h=1024 "
+                         "pipeline under 1F1B and ZB-H1, the h=4096 step)")
+    ap.add_argument("--extra-steps", type=int, default=10, help="timed steps of each other configuration")
+    ap.add_argument("--no-e2e-both", action="store_true",
+                    help="measure e2e with the --e2e-result read-back only (default: both modes)")
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--e2e-mode", choices=("graph", "hybrid"), default="graph",
                     help="graph: one graph per step holds the step, the next step's upload and the "
@@ -465,8 +578,9 @@ def main():
                     help="streams of the replay (0: one per stage plus a W lane per stage when "
                          "2P <= 8; a one-stage replay puts its W passes on a second stream)")
     ap.add_argument("--e2e-result", choices=("stats", "dW"), default="stats",
-                    help="what the e2e step reads back: the stages' gradient statistics (sum of "
-                         "squares, NaN/Inf count; computed at the OPT markers) or the full fp32 dW")
+                    help="what the e2e step reads back for the line's e2e value: the stages' "
+                         "gradient statistics (sum of squares, NaN/Inf count; computed at the OPT "
+                         "markers) or the full fp32 dW; the other mode is reported beside it")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every step's kernels from the host instead of replaying one "
                          "captured CUDA graph per step")
@@ -507,31 +621,11 @@ def main():
         dist.barrier()
     from split_backward_gemms_gb300 import zb
 
-    h, f, M, m, sched, Pl, desc = WORKLOADS[args.workload]
-    multi = args.workload == "c2"
-    P = Pl if multi else 1
-    gen = torch.Generator(device=dev).manual_seed(1000 + rank)
-    bf = torch.bfloat16
-    W = [{"W1": (torch.randn(h, f, device=dev, generator=gen) * 0.02).to(bf),
-          "W2": (torch.randn(f, h, device=dev, generator=gen) * 0.02).to(bf),
-          "dW1": torch.zeros(h, f, device=dev), "dW2": torch.zeros(f, h, device=dev)}
-         for _ in range(P)]
-    X0 = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
-    dY = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
-    ops = zb.zb_make_schedule(sched, Pl, m)
-    if not multi:
-        ops = [(k, 0, j) for k, s, j in ops if s == 0]
-    blk = zb.make_block(M, h, f)
-    # multi-stage replays run their stages on P streams (stage-parallel)
-    # stage lanes, plus a W lane per stage where 2P streams fit (the P=4,
-    # h=1024 pipeline: 995 TF/s on 4 streams, 1008 on 8)
-    n_streams = args.streams if args.streams > 0 else (min(2 * P, 8) if multi else 2)
-    pl = zb.make_pipeline(P, m, blk, timing=True, streams=n_streams)
-    need, peak_live = zb.zb_schedule_workspace_size(pl, ops)
-    ws_t = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wk = setup_workload(zb, dev, args.workload, args.schedule, args.streams, seed=1000 + rank)
+    h, f, M, m, sched, Pl, desc = wk.h, wk.f, wk.M, wk.m, wk.sched, wk.Pl, wk.desc
+    multi, P, W, X0, dY = wk.multi, wk.P, wk.W, wk.X0, wk.dY
+    blk, pl, need, peak_live, ws_t, ops_c = wk.blk, wk.pl, wk.need, wk.peak_live, wk.ws_t, wk.ops_c
     stream = torch.cuda.current_stream()
-    n_ops = len(ops)
-    ops_c = zb.ops_array(ops)
 
     def step(stats, pipe=None):
         zb.zb_run_stage_schedule(pipe or pl, W, X0, dY, None, None, ops_c, ws_t, ws_t.numel(), stats,
@@ -657,105 +751,141 @@ def main():
             projection["bubble_rate"][name] = res.bubble_rate
             projection["pipeline_tokens_per_s"][name] = m * M / (res.cost / 1e3)
             projection["peak_M_B"][name] = res.peak_live_microbatches / 2
+        projection["pinned"] = {
+            "1F1B": "closed form (P-1)/(m+P-1) at any times",
+            "ZBH1": "Table 2 at equal times and at T_W = T_F/2; a reading of the W placement otherwise",
+            "ZBH2": "Table 2 at equal times and at T_W = T_F/2; a reading of the W placement otherwise",
+            "ZB-1p": "Table 5's printed bubbles at Table 9's times; = ZB-H1 at equal times",
+            "ZB-2p": "Table 5's printed bubbles at Table 9's times; = ZB-H2 at equal times",
+            "1F1B-I": "closed form (P-1)/(vm+P-1) at equal times",
+            "ZB-V": "ordering rule pinned only at equal times (zero bubble, peak p M_B); the value "
+                    "at these unequal measured times comes from an unpinned reading"}
 
     # ------------------------------------------------------------- end to end
     # Through the public API with host buffers: every step uploads its inputs
-    # from pinned host memory and reads back its result: by default the
-    # stages' gradient statistics (the per-step metric a training loop reads;
-    # the weight gradients stay on the GPU for the optimizer), or with
-    # --e2e-result dW the full fp32 weight gradients.  Two input and gradient
-    # sets alternate so that step k+1's upload and step k's read-back run on
-    # copy streams while the other step computes.
+    # from pinned host memory and reads back its result, in two modes: the
+    # stages' gradient statistics (the per-step metric a training loop
+    # reads; the weight gradients stay on the GPU for the optimizer) and the
+    # full fp32 weight gradients.  Two input and gradient sets alternate so
+    # that step k+1's upload and step k's read-back run on copy streams
+    # while the other step computes.
     pin = [x.cpu().pin_memory() for x in X0]
     pin_g = [g.cpu().pin_memory() for g in dY]
-    want_dw = args.e2e_result == "dW"
     h2d = sum(x.numel() * x.element_size() for x in pin + pin_g)
-    sets = []
-    for a in range(2):
-        Xs_ = X0 if a == 0 else [torch.empty_like(x) for x in X0]
-        Gs_ = dY if a == 0 else [torch.empty_like(g) for g in dY]
-        Ws_ = [dict(w, dW1=torch.empty_like(w["dW1"]), dW2=torch.empty_like(w["dW2"])) for w in W]
-        if not want_dw:
-            for w in Ws_:
-                w["grad_stats"] = torch.zeros(2, dtype=torch.float64, device=dev)
-        sets.append((Xs_, Gs_, Ws_))
-    if want_dw:
-        host_out = [(torch.empty(h, f, pin_memory=True), torch.empty(f, h, pin_memory=True))
-                    for _ in range(P)]
-        d2h = sum(a.numel() * 4 + b.numel() * 4 for a, b in host_out)
-    else:
-        host_out = [torch.empty(2, dtype=torch.float64, pin_memory=True) for _ in range(P)]
-        d2h = 16 * P
     up_stream = torch.cuda.Stream(device=dev)
     down_stream = torch.cuda.Stream(device=dev)
-    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
-    done = [torch.cuda.Event(), torch.cuda.Event()]
-    down_done = [torch.cuda.Event(), torch.cuda.Event()]
     pl.timing = 0
 
-    def upload(a):
-        # set a's inputs were last read by the step two back (done[a])
-        up_stream.wait_event(done[a])
-        with torch.cuda.stream(up_stream):
-            for j in range(m):
-                sets[a][0][j].copy_(pin[j], non_blocking=True)
-                sets[a][1][j].copy_(pin_g[j], non_blocking=True)
-            in_ready[a].record(up_stream)
+    def measure_e2e(want_dw):
+        sets = []
+        for a in range(2):
+            Xs_ = X0 if a == 0 else [torch.empty_like(x) for x in X0]
+            Gs_ = dY if a == 0 else [torch.empty_like(g) for g in dY]
+            Ws_ = [dict(w, dW1=torch.empty_like(w["dW1"]), dW2=torch.empty_like(w["dW2"])) for w in W]
+            if not want_dw:
+                for w in Ws_:
+                    w["grad_stats"] = torch.zeros(2, dtype=torch.float64, device=dev)
+            sets.append((Xs_, Gs_, Ws_))
+        if want_dw:
+            host_out = [(torch.empty(h, f, pin_memory=True), torch.empty(f, h, pin_memory=True))
+                        for _ in range(P)]
+            d2h = sum(a.numel() * 4 + b.numel() * 4 for a, b in host_out)
+        else:
+            host_out = [torch.empty(2, dtype=torch.float64, pin_memory=True) for _ in range(P)]
+            d2h = 16 * P
+        in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        down_done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def read_back(Ws):
-        for s_ in range(P):
-            if want_dw:
-                host_out[s_][0].copy_(Ws[s_]["dW1"], non_blocking=True)
-                host_out[s_][1].copy_(Ws[s_]["dW2"], non_blocking=True)
-            else:
-                host_out[s_].copy_(Ws[s_]["grad_stats"], non_blocking=True)
+        def upload(a):
+            # set a's inputs were last read by the step two back (done[a])
+            up_stream.wait_event(done[a])
+            with torch.cuda.stream(up_stream):
+                for j in range(m):
+                    sets[a][0][j].copy_(pin[j], non_blocking=True)
+                    sets[a][1][j].copy_(pin_g[j], non_blocking=True)
+                in_ready[a].record(up_stream)
 
-    def capture_e2e(a):
-        # one graph per set: its step, in parallel the upload of the other
-        # set's inputs (for the next step), then the read-back of its result;
-        # replays follow each other on one stream, one host call per step
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(device=dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(g, stream=side):
-                fork = torch.cuda.Event()
-                fork.record(side)
-                up_stream.wait_event(fork)
+        def read_back(Ws):
+            for s_ in range(P):
+                if want_dw:
+                    host_out[s_][0].copy_(Ws[s_]["dW1"], non_blocking=True)
+                    host_out[s_][1].copy_(Ws[s_]["dW2"], non_blocking=True)
+                else:
+                    host_out[s_].copy_(Ws[s_]["grad_stats"], non_blocking=True)
+
+        def capture_e2e(a):
+            # one graph per set: its step, in parallel the upload of the other
+            # set's inputs (for the next step), then the read-back of its
+            # result; replays follow each other on one stream, one host call
+            # per step
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    fork = torch.cuda.Event()
+                    fork.record(side)
+                    up_stream.wait_event(fork)
+                    with torch.cuda.stream(up_stream):
+                        for j in range(m):
+                            sets[1 - a][0][j].copy_(pin[j], non_blocking=True)
+                            sets[1 - a][1][j].copy_(pin_g[j], non_blocking=True)
+                        joined = torch.cuda.Event()
+                        joined.record(up_stream)
+                    Xs_, Gs_, Ws_ = sets[a]
+                    zb.zb_run_stage_schedule(pl, Ws_, Xs_, Gs_, None, None, ops_c, ws_t, ws_t.numel(), None,
+                                             side)
+                    read_back(Ws_)
+                    side.wait_event(joined)
+            stream.wait_stream(side)
+            return g
+
+        def capture_step(a):
+            # --e2e-mode hybrid: one graph per set holds its step and read-back;
+            # the uploads are issued from the host on their own stream
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    Xs_, Gs_, Ws_ = sets[a]
+                    zb.zb_run_stage_schedule(pl, Ws_, Xs_, Gs_, None, None, ops_c, ws_t, ws_t.numel(), None,
+                                             side)
+                    read_back(Ws_)
+            stream.wait_stream(side)
+            return g
+
+        hybrid = graph is not None and args.e2e_mode == "hybrid"
+        e2e_graphs = [capture_e2e(0), capture_e2e(1)] if graph is not None and not hybrid else None
+        step_graphs = [capture_step(0), capture_step(1)] if hybrid else None
+
+        def e2e_run(steps):
+            if step_graphs is not None:
+                for ev in done:
+                    ev.record(stream)
+                upload(0)
+                for k in range(steps):
+                    a = k % 2
+                    if k + 1 < steps:
+                        upload(1 - a)  # overlaps this step's compute
+                    stream.wait_event(in_ready[a])
+                    step_graphs[a].replay()
+                    done[a].record(stream)
+                torch.cuda.synchronize()
+                return
+            if e2e_graphs is not None:
+                # step 0's inputs, then each replay uploads the next step's
                 with torch.cuda.stream(up_stream):
                     for j in range(m):
-                        sets[1 - a][0][j].copy_(pin[j], non_blocking=True)
-                        sets[1 - a][1][j].copy_(pin_g[j], non_blocking=True)
-                    joined = torch.cuda.Event()
-                    joined.record(up_stream)
-                Xs_, Gs_, Ws_ = sets[a]
-                zb.zb_run_stage_schedule(pl, Ws_, Xs_, Gs_, None, None, ops_c, ws_t, ws_t.numel(), None, side)
-                read_back(Ws_)
-                side.wait_event(joined)
-        stream.wait_stream(side)
-        return g
-
-    def capture_step(a):
-        # --e2e-mode hybrid: one graph per set holds its step and read-back;
-        # the uploads are issued from the host on their own stream
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(device=dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(g, stream=side):
-                Xs_, Gs_, Ws_ = sets[a]
-                zb.zb_run_stage_schedule(pl, Ws_, Xs_, Gs_, None, None, ops_c, ws_t, ws_t.numel(), None, side)
-                read_back(Ws_)
-        stream.wait_stream(side)
-        return g
-
-    hybrid = graph is not None and args.e2e_mode == "hybrid"
-    e2e_graphs = [capture_e2e(0), capture_e2e(1)] if graph is not None and not hybrid else None
-    step_graphs = [capture_step(0), capture_step(1)] if hybrid else None
-
-    def e2e_run(steps):
-        if step_graphs is not None:
-            for ev in done:
+                        sets[0][0][j].copy_(pin[j], non_blocking=True)
+                        sets[0][1][j].copy_(pin_g[j], non_blocking=True)
+                stream.wait_stream(up_stream)
+                for k in range(steps):
+                    e2e_graphs[k % 2].replay()
+                torch.cuda.synchronize()
+                return
+            for ev in done + down_done:
                 ev.record(stream)
             upload(0)
             for k in range(steps):
@@ -763,67 +893,69 @@ def main():
                 if k + 1 < steps:
                     upload(1 - a)  # overlaps this step's compute
                 stream.wait_event(in_ready[a])
-                step_graphs[a].replay()
+                stream.wait_event(down_done[a])  # set a's gradients were downloaded
+                Xs, Gs, Ws = sets[a]
+                zb.zb_run_stage_schedule(pl, Ws, Xs, Gs, None, None, ops_c, ws_t, ws_t.numel(), None, stream)
                 done[a].record(stream)
+                down_stream.wait_event(done[a])
+                with torch.cuda.stream(down_stream):
+                    read_back(Ws)
+                    down_done[a].record(down_stream)
             torch.cuda.synchronize()
-            return
-        if e2e_graphs is not None:
-            # step 0's inputs, then each replay uploads the next step's
-            with torch.cuda.stream(up_stream):
-                for j in range(m):
-                    sets[0][0][j].copy_(pin[j], non_blocking=True)
-                    sets[0][1][j].copy_(pin_g[j], non_blocking=True)
-            stream.wait_stream(up_stream)
-            for k in range(steps):
-                e2e_graphs[k % 2].replay()
-            torch.cuda.synchronize()
-            return
-        for ev in done + down_done:
-            ev.record(stream)
-        upload(0)
-        for k in range(steps):
-            a = k % 2
-            if k + 1 < steps:
-                upload(1 - a)  # overlaps this step's compute
-            stream.wait_event(in_ready[a])
-            stream.wait_event(down_done[a])  # set a's gradients were downloaded
-            Xs, Gs, Ws = sets[a]
-            zb.zb_run_stage_schedule(pl, Ws, Xs, Gs, None, None, ops_c, ws_t, ws_t.numel(), None, stream)
-            done[a].record(stream)
-            down_stream.wait_event(done[a])
-            with torch.cuda.stream(down_stream):
-                read_back(Ws)
-                down_done[a].record(down_stream)
-        torch.cuda.synchronize()
 
-    e2e_run(2)
-    # the host link's rate for this step's inputs, alone (CUDA events on the
-    # copy stream): an upload slower than a step makes e2e copy-bound
-    torch.cuda.synchronize()
-    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    u0.record(up_stream)
-    with torch.cuda.stream(up_stream):
-        for j in range(m):
-            sets[0][0][j].copy_(pin[j], non_blocking=True)
-            sets[0][1][j].copy_(pin_g[j], non_blocking=True)
-    u1.record(up_stream)
-    torch.cuda.synchronize()
-    upload_ms = u0.elapsed_time(u1)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e2e_clocks = ClockSampler(torch.cuda.current_device())
-    e2e_clocks.start()
-    time.sleep(0.3)
-    t0 = time.perf_counter()
-    e2e_run(args.e2e_steps)
-    e2e_s = reduce_max(time.perf_counter() - t0, dev, ws)
-    e2e_clk = e2e_clocks.stop()
-    e2e_value = job_rate(step_flops, args.e2e_steps, ws, e2e_s) / 1e12
+        e2e_run(2)
+        # the host link's rate for this step's inputs, alone (CUDA events on
+        # the copy stream): an upload slower than a step makes e2e copy-bound
+        torch.cuda.synchronize()
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(up_stream)
+        with torch.cuda.stream(up_stream):
+            for j in range(m):
+                sets[0][0][j].copy_(pin[j], non_blocking=True)
+                sets[0][1][j].copy_(pin_g[j], non_blocking=True)
+        u1.record(up_stream)
+        torch.cuda.synchronize()
+        upload_ms = u0.elapsed_time(u1)
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e2e_clocks = ClockSampler(torch.cuda.current_device())
+        e2e_clocks.start()
+        time.sleep(0.3)
+        t0 = time.perf_counter()
+        e2e_run(args.e2e_steps)
+        e2e_s = reduce_max(time.perf_counter() - t0, dev, ws)
+        e2e_clk = e2e_clocks.stop()
+        zb.zb_sync_status(stream)
+        return {"value": job_rate(step_flops, args.e2e_steps, ws, e2e_s) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "upload_alone_ms": upload_ms, "h2d_gb_per_s": h2d / (upload_ms * 1e6),
+                "mode": args.e2e_mode if graph is not None else "eager",
+                "clocks": e2e_clk,
+                "result": ("fp32 weight gradients" if want_dw else
+                           "gradient statistics per stage (sum of squares, NaN/Inf count)"),
+                "timing": ("host wall clock around the steps; per step one CUDA graph: the step, "
+                           "the next step's upload in a parallel branch, the read-back"
+                           if e2e_graphs is not None else
+                           "host wall clock around the steps; per step one CUDA graph (the step, "
+                           "the read-back), the next step's upload issued from the host on a "
+                           "copy stream" if step_graphs is not None else
+                           "host wall clock around synchronised steps; uploads and downloads "
+                           "double-buffered on their own streams")}
+
+    first = args.e2e_result
+    e2e = measure_e2e(first == "dW")
+    if not args.no_e2e_both:
+        other = measure_e2e(first != "dW")
+        e2e["other_result"] = {k: other[k] for k in ("value", "d2h_bytes_per_step", "result", "clocks")}
 
     optimizer = None
     if not args.no_optimizer:
         optimizer = measure_post_validated_adamw(zb, h, f, dev, stream, _peaks())
+
+    extra = None
+    if not args.no_extra and ws == 1:
+        extra = other_workloads(zb, dev, args.extra_steps, args.warmup)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -865,23 +997,10 @@ def main():
                          "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
                          "frac_of_burst": achieved / peaks["bf16"]},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-                    "upload_alone_ms": upload_ms, "h2d_gb_per_s": h2d / (upload_ms * 1e6),
-                    "mode": args.e2e_mode if graph is not None else "eager",
-                    "clocks": e2e_clk,
-                    "result": ("fp32 weight gradients" if want_dw else
-                               "gradient statistics per stage (sum of squares, NaN/Inf count)"),
-                    "timing": ("host wall clock around the steps; per step one CUDA graph: the step, "
-                               "the next step's upload in a parallel branch, the read-back"
-                               if e2e_graphs is not None else
-                               "host wall clock around the steps; per step one CUDA graph (the step, "
-                               "the read-back), the next step's upload issued from the host on a "
-                               "copy stream" if step_graphs is not None else
-                               "host wall clock around synchronised steps; uploads and downloads "
-                               "double-buffered on their own streams")},
+            "e2e": e2e,
             "projection": projection,
             "optimizer": optimizer,
+            "other_configs": extra,
             "gpu_launches": sums["gemm_launches"],
             "clocks": clk,
         }

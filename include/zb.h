@@ -367,14 +367,21 @@ zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage_params* st
  * its own pool, or a latency-critical loop that must never call cudaMalloc /
  * cudaFree, which can synchronise the whole device).  Same arguments and
  * semantics as zb_run_stage_schedule, minus the workspace: the activation
- * arena is a static device array of ZB_STATIC_ARENA_BYTES (64 MiB) that every
- * device using this entry point holds from its first call until the process
- * exits.  Op lists whose arena (zb_schedule_workspace_size) is larger are
+ * arena is a static device array of ZB_STATIC_ARENA_BYTES (64 MiB).  Under
+ * CUDA's default lazy module loading a device holds it from this entry
+ * point's first call on that device until the process exits; under eager
+ * loading (CUDA_MODULE_LOADING=EAGER) every process that loads the library
+ * holds it on each device from that device's context creation, whether or
+ * not it ever calls this entry point.  Op lists whose arena
+ * (zb_schedule_workspace_size) is larger are
  * rejected with ZB_ERR_WORKSPACE; pl->timing must be 0 and pl->streams at
  * most 1 (ZB_ERR_INVALID_ARG otherwise).  No device memory is allocated by the call.  The first call on
  * each device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.
- * All calls share the one array: calls whose work overlaps on the GPU (e.g.
+ * with that device current and caches it for the life of the process; make
+ * that first call before any stream capture.  The cache is not refreshed
+ * after cudaDeviceReset (which ends the context the address belongs to), so
+ * do not call this entry point on a device after resetting it in the same
+ * process.  All calls share the one array: calls whose work overlaps on the GPU (e.g.
  * on two streams at once) race on it.  The arena needs no clearing (every
  * buffer is written before it is read); the caller's dW/db follow
  * pl->zero_grads exactly as in zb_run_stage_schedule. */

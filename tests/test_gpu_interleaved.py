@@ -157,3 +157,50 @@ def test_zbv_replay_with_bias_is_the_chain_replay(zb):
             assert torch.equal(p[key], q[key])
     for p, q in zip(a[1], b[1]):
         assert torch.equal(p.view(torch.int16), q.view(torch.int16))
+
+
+@pytest.mark.parametrize("kind,P,v,m", [("ZBV", 2, 2, 4), ("ZBV", 3, 2, 5), ("1F1B-I", 2, 2, 4)])
+def test_chunked_replay_per_pass_against_oracle(zb, kind, P, v, m):
+    """Every pass of a chunked replay at the one-pass bound (5e-3).
+
+    Single-pass calls along the chain of virtual stages reproduce the
+    chunked replay bit for bit; each of their passes is then compared with
+    the fp64 oracle from the exact bf16 tensors it consumed, so no part of
+    the replay is checked only through the chain bound above.
+    """
+    from tests.test_gpu_parity import _hand_chain
+    M, h, f = 136, 72, 200
+    L = v * P
+    wts, X0, dY = _setup(L, m, M, h, f, seed=41 + L + m)
+    ops = zb.zb_make_interleaved_schedule(kind, P, v, m)
+    blk = zb.make_block(M, h, f)
+    stages, dX0, Yl = _replay(zb, zb.make_pipeline(P, m, blk, chunks=v, layout=kind), wts, X0, dY, ops,
+                              M, h, f)
+    rec, Xs, dYs, dWs = _hand_chain(zb, zb.make_block(M, h, f, split_k=False), L, m, wts, X0, dY)
+    for k in range(L):
+        assert torch.equal(stages[k]["dW1"], dWs[k][0]) and torch.equal(stages[k]["dW2"], dWs[k][1])
+    for j in range(m):
+        assert torch.equal(dX0[j].view(torch.int16), rec[("B", 0, j)][1].view(torch.int16))
+        assert torch.equal(Yl[j].view(torch.int16), rec[("F", L - 1, j)][2].view(torch.int16))
+    for k in range(L):
+        W1, W2 = f64(wts[k]["W1"]), f64(wts[k]["W2"])
+        for j in (0, m - 1):
+            H, A, Y = rec[("F", k, j)]
+            Hr, Ar, Yr = ob.forward(f64(Xs[(k, j)]), W1, W2)
+            assert ob.rel_fro(f64(H), Hr) < TOL_BF16
+            assert ob.rel_fro(f64(A), Ar) < TOL_BF16
+            assert ob.rel_fro(f64(Y), f64(A) @ W2) < TOL_BF16
+            dH, dX = rec[("B", k, j)]
+            _, dHr, _ = ob.backward_input(f64(dYs[(k, j)]), W1, W2, f64(H))
+            assert ob.rel_fro(f64(dH), dHr) < TOL_BF16
+            assert ob.rel_fro(f64(dX), f64(dH) @ W1.T) < TOL_BF16
+        r1 = np.zeros((h, f))
+        r2 = np.zeros((f, h))
+        for j in range(m):
+            _, A, _ = rec[("F", k, j)]
+            dH, _ = rec[("B", k, j)]
+            a, b, _, _ = ob.backward_weight(f64(Xs[(k, j)]), f64(A), f64(dH), f64(dYs[(k, j)]))
+            r1 += a
+            r2 += b
+        assert ob.rel_fro(f64(stages[k]["dW1"]), r1) < TOL_BF16
+        assert ob.rel_fro(f64(stages[k]["dW2"]), r2) < TOL_BF16
