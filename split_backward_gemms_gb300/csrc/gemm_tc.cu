@@ -138,6 +138,9 @@ struct EpiArgs {
     int act;
     int ksplit;  // CTAs per tile along K (1 = no split; CG = 1 only)
     int late_wait;  // wait for the previous kernel in the stream at exit, not at start
+    // L2 eviction priority of the A and B operand loads and of the output
+    // stores (0 normal, 1 evict first, 2 evict last; see choose_l2_hints)
+    int hint_a, hint_b, hint_out;
     unsigned int* err;
 };
 
@@ -429,14 +432,14 @@ __device__ __forceinline__ void staging_acquire(int lane) {
 // Hand a filled staging buffer to the TMA unit.
 template <bool REDUCE>
 __device__ __forceinline__ void staging_release(const CUtensorMap* tm, uint32_t stg, int lane,
-                                                int x, int y) {
+                                                int x, int y, uint64_t policy) {
     zbp::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
         if (REDUCE)
-            zbp::tma_reduce_add_2d(tm, stg, x, y);
+            zbp::tma_reduce_add_2d_hint(tm, stg, x, y, policy);
         else
-            zbp::tma_store_2d(tm, stg, x, y);
+            zbp::tma_store_2d_hint(tm, stg, x, y, policy);
         zbp::bulk_commit();
     }
 }
@@ -670,6 +673,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ------------------------------------------------ TMA producer
             uint32_t it = 0;
             bool ok = true;
+            const uint64_t pol_a = zbp::l2_policy(args.hint_a);
+            const uint64_t pol_b = zbp::l2_policy(args.hint_b);
             for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
                 int mb, nb;
                 tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
@@ -689,24 +694,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sb = sa + A_BYTES;
                     const int k0 = kb * BK;
                     if (leader) zbp::mbar_arrive_expect_tx(full_local, C::STAGE_BYTES * CG);
-                    auto load = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) {
+                    auto load = [&](uint32_t dst, const CUtensorMap* tm, int x, int y, uint64_t pol) {
                         if (PAIR)
-                            zbp::tma_load_2d_pair(dst, tm, full, x, y);
+                            zbp::tma_load_2d_pair_hint(dst, tm, full, x, y, pol);
                         else
-                            zbp::tma_load_2d(dst, tm, full, x, y);
+                            zbp::tma_load_2d_hint(dst, tm, full, x, y, pol);
                     };
                     if (A_MN) {
-                        load(sa, &tmA, m0, k0);
-                        load(sa + MN_ATOM_BYTES, &tmA, m0 + 64, k0);
+                        load(sa, &tmA, m0, k0, pol_a);
+                        load(sa + MN_ATOM_BYTES, &tmA, m0 + 64, k0, pol_a);
                     } else {
-                        load(sa, &tmA, k0, m0);
+                        load(sa, &tmA, k0, m0, pol_a);
                     }
                     if (B_MN) {
 #pragma unroll
                         for (int i = 0; i < C::B_ROWS / 64; ++i)
-                            load(sb + i * MN_ATOM_BYTES, &tmB, nb0 + 64 * i, k0);
+                            load(sb + i * MN_ATOM_BYTES, &tmB, nb0 + 64 * i, k0, pol_b);
                     } else {
-                        load(sb, &tmB, k0, nb0);
+                        load(sb, &tmB, k0, nb0, pol_b);
                     }
                 }
             }
@@ -852,6 +857,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int q = warp & 3;
             const int c_lo = (ew >> 2) * E::COLS;  // first tile column of this warp
             const uint32_t stg0 = zbp::smem_u32(staging + ew * 2 * E::BOX);
+            const uint64_t pol_out = zbp::l2_policy(args.hint_out);
             uint32_t flip = 0;
             uint32_t local = 0;
             for (int tile = cluster; tile < num_tiles; tile += clusters, ++local) {
@@ -902,9 +908,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         staging_acquire(lane);
                         stage_row(stg, lane, v);
                         if (args.accumulate)
-                            staging_release<true>(&tmO0, stg, lane, col0, row0);
+                            staging_release<true>(&tmO0, stg, lane, col0, row0, pol_out);
                         else
-                            staging_release<false>(&tmO0, stg, lane, col0, row0);
+                            staging_release<false>(&tmO0, stg, lane, col0, row0, pol_out);
                         if (!last_tile && pause_ns) __nanosleep(pause_ns);
                     }
                 } else {
@@ -951,7 +957,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         flip ^= 1u;
                         staging_acquire(lane);
                         stage_row64(stg, lane, w);
-                        staging_release<false>(&tmO0, stg, lane, col0, row0);
+                        staging_release<false>(&tmO0, stg, lane, col0, row0, pol_out);
                         if (EPI == zb::EPI_GELU_DUAL) {
                             if (args.act == ZB_ACT_GELU_TANH)
                                 gelu_pack<true, 32>(x, w);
@@ -961,7 +967,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             flip ^= 1u;
                             staging_acquire(lane);
                             stage_row64(stg, lane, w);
-                            staging_release<false>(&tmO1, stg, lane, col0, row0);
+                            staging_release<false>(&tmO1, stg, lane, col0, row0, pol_out);
                         }
                     }
                 }
@@ -1210,17 +1216,26 @@ zb_status dispatch(const zb::GemmBf16& g, const Maps& mp, const EpiArgs& ea, lon
     }
 }
 
-// CTA-group choice: the pair kernel when its 256x256 tiles fill at least one
-// wave of pairs, else one CTA per 128x256 tile (more CTAs for small problems).
-// ZB_GEMM_CTA_GROUP=1 or =2 in the environment forces one shape.
-int choose_cta_group(long long pair_tiles) {
+// CTA-group choice.  A pair and two single CTAs cover the same 256 rows on
+// the same two SMs, but the pair feeds each SM half of B's bytes (the MMA
+// reads the other half from the peer), so the pair is chosen whenever it is
+// not worse: always when its tiles fill a wave of pairs, and below that
+// unless the one-CTA kernel splits K (the split exchange lives in the
+// one-CTA kernel) or M fits in one 128-row block (a pair would compute
+// 128 rows of padding).  Measured against choosing the pair only for a full
+// wave: the P=4, h=1024 pipeline 1027 -> 1093 TF/s, 8192 x 1024 W +15 %,
+// 2048 x 2048 F and B +7 %.  ZB_GEMM_CTA_GROUP=1 or =2 in the environment
+// forces one shape.
+int choose_cta_group(long long pair_tiles, long long Mg, int ksplit) {
     static const int forced = [] {
         const char* v = std::getenv("ZB_GEMM_CTA_GROUP");
         return (v && (std::strcmp(v, "1") == 0 || std::strcmp(v, "2") == 0)) ? std::atoi(v) : 0;
     }();
     if (forced) return forced;
     const int pairs = sm_count() / 2;
-    return pair_tiles >= pairs ? 2 : 1;
+    if (pair_tiles >= pairs) return 2;
+    if (ksplit > 1 || Mg <= BM) return 1;
+    return 2;
 }
 
 // Split-K factor for a one-CTA-per-tile GEMM: the largest S in {2, 4}
@@ -1248,6 +1263,37 @@ int choose_split(long long tiles, long long num_kb) {
     return ks;
 }
 
+// L2 eviction priorities.  Tiles run in groups of GROUP_M M-blocks, M
+// fastest inside a group (tile_coords), so every wave of resident tiles
+// reads the A rows of its group again over the whole K range, and every
+// group reads the whole B operand again.  An operand whose re-read part fits
+// comfortably in L2 beside the streams (at most 48 MB: A's rows of one group,
+// or all of B when there are several groups) is kept (evict last); a larger
+// one, read once per group or too large to keep, goes first, so that it
+// does not push the kept one out; an output larger than 48 MB goes first
+// too (written once, read by a later kernel), a smaller one stays normal
+// (the next GEMM of the pass reads it at once).  At h=6144 this keeps X and
+// dY (37.7 MB) across the waves of the F1 and B1 GEMMs (DRAM reads 673 ->
+// 398 MB and 934 -> 815 MB per launch) and a group's 25 MB of A in the W
+// GEMMs.  ZB_GEMM_L2_HINTS=0 in the environment turns the hints off.
+void choose_l2_hints(const zb::GemmBf16& g, int cg, EpiArgs* ea) {
+    static const bool on = [] {
+        const char* v = std::getenv("ZB_GEMM_L2_HINTS");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
+    ea->hint_a = ea->hint_b = ea->hint_out = 0;
+    if (!on) return;
+    constexpr double kKeep = 48e6;
+    const long long group_rows = static_cast<long long>(Cfg<1>::GROUP_M) * BM * cg;
+    const long long groups = (g.Mg + group_rows - 1) / group_rows;
+    const double a_group = 2.0 * static_cast<double>(g.Mg < group_rows ? g.Mg : group_rows) * g.Kg;
+    const double b_all = 2.0 * static_cast<double>(g.Ng) * g.Kg;
+    const double out = (g.epi == zb::EPI_F32 ? 4.0 : 2.0) * static_cast<double>(g.Mg) * g.Ng;
+    ea->hint_a = a_group <= kKeep ? 2 : 1;
+    ea->hint_b = b_all > kKeep ? 1 : (groups > 1 ? 2 : 0);
+    ea->hint_out = out > kKeep ? 1 : 0;
+}
+
 }  // namespace
 
 namespace zb {
@@ -1268,7 +1314,9 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     if (sm_count() <= 0) return fail(ZB_ERR_CUDA, "cannot query the SM count");
 
     const long long pair_tiles = ((g.Mg + 2 * BM - 1) / (2 * BM)) * ((g.Ng + BN - 1) / BN);
-    const int cg = choose_cta_group(pair_tiles);
+    const long long tiles = ((g.Mg + BM - 1) / BM) * ((g.Ng + BN - 1) / BN);
+    const int ksplit = (g.epi != EPI_F32 && g.allow_split) ? choose_split(tiles, (g.Kg + BK - 1) / BK) : 1;
+    const int cg = choose_cta_group(pair_tiles, g.Mg, ksplit);
     const uint32_t b_rows = static_cast<uint32_t>(BN / cg);  // B columns per CTA
 
     std::string why;
@@ -1316,12 +1364,12 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     ea.act = g.act;
     ea.ksplit = 1;
     ea.late_wait = g.independent_of_prev && g.allow_pdl ? 1 : 0;
+    choose_l2_hints(g, cg, &ea);
     ea.err = err;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cg == 2) return dispatch<2>(g, mp, ea, pair_tiles, st);
-    const long long tiles = ((g.Mg + BM - 1) / BM) * ((g.Ng + BN - 1) / BN);
-    if (g.epi != EPI_F32 && g.allow_split) ea.ksplit = choose_split(tiles, (g.Kg + BK - 1) / BK);
+    ea.ksplit = ksplit;
     return dispatch<1>(g, mp, ea, tiles, st);
 }
 
