@@ -476,11 +476,11 @@ def setup_workload(zb, dev, name, schedule=None, streams=0, seed=1000):
     w.dY = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
     w.ops = make_ops(zb, w.sched, w.Pl, m, w.multi)
     w.blk = zb.make_block(M, h, f)
-    # multi-stage replays run their stages on P streams (stage-parallel)
-    # plus a W lane per stage where 2P streams fit (the P=4, h=1024
-    # pipeline: 995 TF/s on 4 streams, 1008 on 8); a one-stage replay puts
-    # its W passes on a second stream
-    n_streams = streams if streams > 0 else (min(2 * w.P, 8) if w.multi else 2)
+    # multi-stage replays run each stage's F, B and W ops on lanes of their
+    # own (3P streams; the P=4, h=1024 pipeline: 995 TF/s with a lane per
+    # stage, 1008-1069 with a W lane too, 1089 with separate F and B lanes);
+    # a one-stage replay puts its W passes on a second stream
+    n_streams = streams if streams > 0 else (min(3 * w.P, 12) if w.multi else 2)
     w.pl = zb.make_pipeline(w.P, m, w.blk, timing=True, streams=n_streams)
     w.need, w.peak_live = zb.zb_schedule_workspace_size(w.pl, w.ops)
     w.ws_t = torch.empty(max(w.need, 256), dtype=torch.uint8, device=dev)
@@ -575,8 +575,8 @@ def main():
                          "issued from the host on a copy stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--streams", type=int, default=0,
-                    help="streams of the replay (0: one per stage plus a W lane per stage when "
-                         "2P <= 8; a one-stage replay puts its W passes on a second stream)")
+                    help="streams of the replay (0: an F, a B and a W lane per stage for a "
+                         "pipeline, 3P <= 12; a one-stage replay puts its W passes on a second stream)")
     ap.add_argument("--e2e-result", choices=("stats", "dW"), default="stats",
                     help="what the e2e step reads back for the line's e2e value: the stages' "
                          "gradient statistics (sum of squares, NaN/Inf count; computed at the OPT "

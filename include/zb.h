@@ -286,7 +286,12 @@ typedef struct zb_pipeline {
                                   events and kept in list order, so a weight
                                   gradient GEMM fills the SMs that an F/B
                                   kernel's last partial wave leaves idle (the
-                                  one-stage replay with n = 2).  P = 1 and
+                                  one-stage replay with n = 2).  P > 1 and
+                                  n >= 3 P (3 P <= 12): each stage's B and
+                                  BW ops also leave its F stream for one of
+                                  their own (ordered after F(s,j) by an
+                                  event), so a stage's forwards do not queue
+                                  behind its backwards.  P = 1 and
                                   n >= 3: the F/B/BW ops of consecutive
                                   microbatches also alternate over n - 1
                                   streams (at most 7).  The call forks from

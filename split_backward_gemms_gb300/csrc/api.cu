@@ -437,16 +437,26 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     // consecutive microbatches over streams - 1 lanes (at most 7; the
     // microbatches are independent until their W) and keeps every W / OPT on
     // the last lane, in list order: each persistent GEMM then starts on the
-    // SMs that the previous one's partial last wave leaves idle.
+    // SMs that the previous one's partial last wave leaves idle.  With
+    // streams >= 3 P (3 P <= 12) a stage's B and BW ops also leave its F
+    // lane for a lane of their own (lanes[2 P + d]): a stage's next forward
+    // then starts as soon as its producers and its arena slots allow, instead
+    // of queueing behind a backward that waits for the next stage.
     const bool micro_lanes = pl->P == 1 && pl->streams >= 3;
-    const int nsd = micro_lanes ? std::min(pl->streams - 1, 7) : std::max(1, std::min(std::min(pl->streams, pl->P), 8));
-    const bool w_lanes = micro_lanes || (pl->streams >= 2 * pl->P && 2 * pl->P <= 8);
-    const int ns = nsd + (w_lanes ? (micro_lanes ? 1 : pl->P) : 0);
+    const bool fbw_lanes = !micro_lanes && pl->P > 1 && pl->streams >= 3 * pl->P && 3 * pl->P <= 12;
+    const int nsd = micro_lanes ? std::min(pl->streams - 1, 7)
+                    : fbw_lanes ? pl->P
+                                : std::max(1, std::min(std::min(pl->streams, pl->P), 8));
+    const bool w_lanes = micro_lanes || fbw_lanes || (pl->streams >= 2 * pl->P && 2 * pl->P <= 8);
+    const int ns = nsd + (w_lanes ? (micro_lanes ? 1 : pl->P) : 0) + (fbw_lanes ? pl->P : 0);
     std::vector<int> lane_of(n_ops, 0);
     for (size_t i = 0; i < n_ops; ++i) {
         const bool wk = vop[i].kind == ZB_OP_W || vop[i].kind == ZB_OP_OPT;
+        const bool bk = vop[i].kind == ZB_OP_B || vop[i].kind == ZB_OP_BW;
         if (micro_lanes)
             lane_of[i] = wk ? nsd : static_cast<int>(vop[i].micro % static_cast<uint32_t>(nsd));
+        else if (fbw_lanes)
+            lane_of[i] = wk ? nsd + dev[i] : bk ? 2 * nsd + dev[i] : dev[i];
         else
             lane_of[i] = (w_lanes && wk) ? nsd + dev[i] : dev[i] % nsd;
     }
@@ -503,6 +513,9 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
                 if (o.kind == ZB_OP_F && st > 0) deps.push_back(fwd_op[static_cast<size_t>(st - 1) * m + j]);
                 if ((o.kind == ZB_OP_B || o.kind == ZB_OP_BW) && st < P - 1)
                     deps.push_back(bwd_op[static_cast<size_t>(st + 1) * m + j]);
+                // its own forward (H, A): implied by list order on one lane,
+                // an event when B runs on a lane of its own
+                if (o.kind == ZB_OP_B || o.kind == ZB_OP_BW) deps.push_back(fwd_op[static_cast<size_t>(st) * m + j]);
                 if (o.kind == ZB_OP_W) deps.push_back(bwd_op[static_cast<size_t>(st) * m + j]);
             }
             for (int d : deps) {

@@ -393,12 +393,12 @@ def test_one_stage_lists_full_size_deferred_equals_eager(zb, kind, m, h):
 
 @pytest.mark.parametrize("P,m,M,h,kind,list_P,streams", [(1, 24, 3072, 6144, "ZBH2", 8, 2),
                                                         (1, 16, 3072, 4096, "ZBH1", 8, 2),
-                                                        (4, 8, 2048, 1024, "ZBH1", 4, 8)])
+                                                        (4, 8, 2048, 1024, "ZBH1", 4, 12)])
 def test_full_size_step_as_benchmarked(zb, P, m, M, h, kind, list_P, streams):
     """A step in the launch configuration the benchmark times: the h=6144
     stage (the stage-0 ZB-H2 list of an 8-stage ordering, m=24, seq 3072, an
     F/B lane and a W lane), the h=4096 stage (ZB-H1, m=16) and the P=4,
-    h=1024 pipeline (ZB-H1, m=8, a lane and a W lane per stage), each
+    h=1024 pipeline (ZB-H1, m=8, an F, a B and a W lane per stage), each
     captured once into a CUDA graph on a side
     stream after an eager warm-up and replayed twice.  Outputs and fp32
     weight gradients equal the serial eager replay's bit for bit (which the
@@ -508,7 +508,9 @@ def test_device_wait_timeout_is_reported_and_context_survives(zb):
 
 
 @pytest.mark.parametrize("kind,P,m,streams", [("ZBH1", 4, 8, 4), ("ZBH2", 4, 8, 4), ("1F1B", 4, 8, 4),
-                                              ("ZBH2", 8, 16, 3), ("ZBH1", 3, 5, 8), ("ZBH1", 4, 8, 8)])
+                                              ("ZBH2", 8, 16, 3), ("ZBH1", 3, 5, 8), ("ZBH1", 4, 8, 8),
+                                              ("ZBH1", 4, 8, 12), ("ZBH2", 4, 8, 12), ("1F1B", 4, 8, 12),
+                                              ("ZBH2", 3, 7, 9)])
 def test_stage_parallel_replay_is_bit_exact(zb, kind, P, m, streams):
     # Stages on several streams, ordered by events: same bits as the serial replay.
     M, h, f = 512, 256, 1024
@@ -657,7 +659,8 @@ def test_replay_reports_stage_grad_stats_and_injected_nan(zb):
                 assert bad > 0
 
 
-@pytest.mark.parametrize("P,m,streams,kind", [(4, 8, 4, "ZBH1"), (1, 6, 2, "ZBH2"), (2, 4, 1, "1F1B")])
+@pytest.mark.parametrize("P,m,streams,kind", [(4, 8, 4, "ZBH1"), (1, 6, 2, "ZBH2"), (2, 4, 1, "1F1B"),
+                                              (4, 8, 12, "ZBH1")])
 def test_replay_captured_in_a_cuda_graph(zb, P, m, streams, kind):
     # The executor only enqueues work (streams and events of its own are made
     # on first use, before the capture): a step captured into a CUDA graph and
