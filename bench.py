@@ -448,8 +448,14 @@ class Workload:
 
 def make_ops(zb, sched, Pl, m, multi):
     """The op list a workload replays: the whole pipeline, or the stage-0
-    list of a Pl-stage ordering replayed as one stage."""
-    ops = zb.zb_make_schedule(sched, Pl, m)
+    list of a Pl-stage ordering replayed as one stage.  ZB1P / ZB2P are the
+    heuristic scheduler's lists under p M_B and 2p M_B at equal pass times
+    (this block's M_W = M_B, so the memory ratio is 1)."""
+    if sched in ("ZB1P", "ZB2P"):
+        limit = Pl if sched == "ZB1P" else 2 * Pl
+        _, ops, _ = zb.zb_auto_schedule(Pl, m, 1.0, 1.0, 1.0, 0.0, limit, 1.0)
+    else:
+        ops = zb.zb_make_schedule(sched, Pl, m)
     if not multi:
         ops = [(k, 0, j) for k, s, j in ops if s == 0]
     return ops
@@ -535,12 +541,12 @@ def time_workload(zb, dev, w, steps, warmup, use_graph=True):
 
 def other_workloads(zb, dev, steps, warmup):
     """The other configurations in the same run, each as its own short
-    timed region: the P=4, h=1024 pipeline under 1F1B (fused backward) and
-    under ZB-H1 (split backward, W lanes), same streams and graphs, and the
-    h=4096 one-stage ZB-H1 step."""
+    timed region: the P=4, h=1024 pipeline under 1F1B (fused backward), under
+    ZB-H1 and ZB-H2 (split backward, W lanes) and under the heuristic ZB-2p,
+    same streams and graphs, and the h=4096 one-stage ZB-H1 step."""
     import torch
     out = {}
-    for name, sched in (("c2", "1F1B"), ("c2", "ZBH1"), ("c3", "ZBH1")):
+    for name, sched in (("c2", "1F1B"), ("c2", "ZBH1"), ("c2", "ZBH2"), ("c2", "ZB2P"), ("c3", "ZBH1")):
         w = setup_workload(zb, dev, name, sched)
         r = time_workload(zb, dev, w, steps, warmup)
         r.update({"workload": w.desc.split(",")[0] if name != "c2" else
@@ -560,7 +566,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="c4")
-    ap.add_argument("--schedule", choices=("1F1B", "ZBH1", "ZBH2"), default=None,
+    ap.add_argument("--schedule", choices=("1F1B", "ZBH1", "ZBH2", "ZB1P", "ZB2P"), default=None,
                     help="ordering to replay instead of the workload's own (c4: ZBH2, c3 and c2: ZBH1)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other configurations' short timed regions (the P=4, h=1024 "
@@ -856,6 +862,7 @@ def main():
             stream.wait_stream(side)
             return g
 
+        step_gpu_ms = []
         hybrid = graph is not None and args.e2e_mode == "hybrid"
         e2e_graphs = [capture_e2e(0), capture_e2e(1)] if graph is not None and not hybrid else None
         step_graphs = [capture_step(0), capture_step(1)] if hybrid else None
@@ -875,15 +882,20 @@ def main():
                 torch.cuda.synchronize()
                 return
             if e2e_graphs is not None:
-                # step 0's inputs, then each replay uploads the next step's
+                # step 0's inputs, then each replay uploads the next step's;
+                # events around each replay give its GPU time (diagnostic)
+                marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
                 with torch.cuda.stream(up_stream):
                     for j in range(m):
                         sets[0][0][j].copy_(pin[j], non_blocking=True)
                         sets[0][1][j].copy_(pin_g[j], non_blocking=True)
                 stream.wait_stream(up_stream)
+                marks[0].record(stream)
                 for k in range(steps):
                     e2e_graphs[k % 2].replay()
+                    marks[k + 1].record(stream)
                 torch.cuda.synchronize()
+                step_gpu_ms[:] = [marks[k].elapsed_time(marks[k + 1]) for k in range(steps)]
                 return
             for ev in done + down_done:
                 ev.record(stream)
@@ -932,6 +944,7 @@ def main():
                 "upload_alone_ms": upload_ms, "h2d_gb_per_s": h2d / (upload_ms * 1e6),
                 "mode": args.e2e_mode if graph is not None else "eager",
                 "clocks": e2e_clk,
+                "step_gpu_ms": [round(x, 2) for x in step_gpu_ms] or None,
                 "result": ("fp32 weight gradients" if want_dw else
                            "gradient statistics per stage (sum of squares, NaN/Inf count)"),
                 "timing": ("host wall clock around the steps; per step one CUDA graph: the step, "
