@@ -860,6 +860,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t pol_out = zbp::l2_policy(args.hint_out);
             uint32_t flip = 0;
             uint32_t local = 0;
+            uint64_t t_prev_full = 0;  // fp32 epilogue: when the previous accumulator was ready
             for (int tile = cluster; tile < num_tiles; tile += clusters, ++local) {
                 const uint32_t buf = local & 1u;
                 const uint32_t tr = local >> 1;
@@ -888,16 +889,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
                 const bool rows_live = row0 < args.Mg;
                 if (EPI == zb::EPI_F32) {
-                    // The fp32 stores (TMA reduce-adds) share the TMA unit with the
+                    // The fp32 stores (TMA reduce-adds; the L2 reads the old
+                    // dW from DRAM for each) share the TMA unit with the
                     // operand loads of the next tile: issued back to back they
-                    // queue ahead of those loads and starve the MMAs.  Spacing the
-                    // chunks over the tile (a pause that scales with the K loop,
-                    // ~5 ns per K block, at most 250 ns, none after the CTA's last
-                    // chunk) keeps the loads flowing.
+                    // queue ahead of those loads and starve the MMAs.  So the
+                    // chunks are paced over the next tile's MMAs: chunk c is
+                    // issued c x spacing after this accumulator was ready, with
+                    // spacing = 5/8 of the previous tile's MMA time (the time
+                    // between two accumulators becoming ready) / chunks, so
+                    // the reduce-adds spread over ~5/8 of a tile whatever the
+                    // clock and K; the first tile assumes 20 ns per K block.
+                    // Bounded: at most 20 us between chunks; no pacing on the
+                    // CTA's last tile.
+                    constexpr int CHUNKS = E::COLS / 32;
                     const bool last_tile = tile + clusters >= num_tiles;
-                    const unsigned pause_ns = static_cast<unsigned>(min(num_kb * 5, 250));
+                    uint64_t t_full = 0, spacing = 0;
+                    if (lane == 0) {
+                        t_full = zbp::globaltimer_ns();
+                        spacing = t_prev_full != 0 ? (t_full - t_prev_full) * 5 / (8 * CHUNKS)
+                                                   : static_cast<uint64_t>(num_kb) * 20;
+                        if (spacing > 20000) spacing = 20000;
+                        t_prev_full = t_full;
+                    }
 #pragma unroll 1
-                    for (int c = 0; c < E::COLS / 32; ++c) {
+                    for (int c = 0; c < CHUNKS; ++c) {
+                        if (c > 0 && !last_tile) {
+                            if (lane == 0) {
+                                const uint64_t target = t_full + static_cast<uint64_t>(c) * spacing;
+                                while (zbp::globaltimer_ns() < target) __nanosleep(64);
+                            }
+                            __syncwarp();
+                        }
                         uint32_t v[32];
                         zbp::tmem_ld_32x32b_x32(taddr + c_lo + c * 32, v);
                         zbp::tmem_ld_wait();
@@ -911,7 +933,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             staging_release<true>(&tmO0, stg, lane, col0, row0, pol_out);
                         else
                             staging_release<false>(&tmO0, stg, lane, col0, row0, pol_out);
-                        if (!last_tile && pause_ns) __nanosleep(pause_ns);
                     }
                 } else {
 #pragma unroll 1
