@@ -572,6 +572,9 @@ def main():
                     help="skip the other configurations' short timed regions (the P=4, h=1024 "
                          "pipeline under 1F1B and ZB-H1, the h=4096 step)")
     ap.add_argument("--extra-steps", type=int, default=10, help="timed steps of each other configuration")
+    ap.add_argument("--e2e-copies", choices=("one", "per-microbatch"), default="one",
+                    help="e2e uploads: one copy per tensor kind of a contiguous [m, M, h] input set, "
+                         "or one copy per microbatch tensor")
     ap.add_argument("--no-e2e-both", action="store_true",
                     help="measure e2e with the --e2e-result read-back only (default: both modes)")
     ap.add_argument("--e2e-steps", type=int, default=12)
@@ -775,8 +778,16 @@ def main():
     # full fp32 weight gradients.  Two input and gradient sets alternate so
     # that step k+1's upload and step k's read-back run on copy streams
     # while the other step computes.
-    pin = [x.cpu().pin_memory() for x in X0]
-    pin_g = [g.cpu().pin_memory() for g in dY]
+    one_copy = args.e2e_copies == "one"
+    if one_copy:
+        # each input set is one [m, M, h] buffer per tensor kind, uploaded
+        # with one copy each; the microbatches are views into it
+        pin_all = torch.stack(X0).cpu().pin_memory()
+        pin_g_all = torch.stack(dY).cpu().pin_memory()
+        pin, pin_g = list(pin_all.unbind(0)), list(pin_g_all.unbind(0))
+    else:
+        pin = [x.cpu().pin_memory() for x in X0]
+        pin_g = [g.cpu().pin_memory() for g in dY]
     h2d = sum(x.numel() * x.element_size() for x in pin + pin_g)
     up_stream = torch.cuda.Stream(device=dev)
     down_stream = torch.cuda.Stream(device=dev)
@@ -784,9 +795,18 @@ def main():
 
     def measure_e2e(want_dw):
         sets = []
+        whole = []  # one_copy: the [m, M, h] device buffers of each set
         for a in range(2):
-            Xs_ = X0 if a == 0 else [torch.empty_like(x) for x in X0]
-            Gs_ = dY if a == 0 else [torch.empty_like(g) for g in dY]
+            if one_copy:
+                xa = torch.empty((m,) + tuple(X0[0].shape), dtype=X0[0].dtype, device=dev)
+                ga = torch.empty((m,) + tuple(dY[0].shape), dtype=dY[0].dtype, device=dev)
+                xa.copy_(pin_all)
+                ga.copy_(pin_g_all)
+                whole.append((xa, ga))
+                Xs_, Gs_ = list(xa.unbind(0)), list(ga.unbind(0))
+            else:
+                Xs_ = X0 if a == 0 else [torch.empty_like(x) for x in X0]
+                Gs_ = dY if a == 0 else [torch.empty_like(g) for g in dY]
             Ws_ = [dict(w, dW1=torch.empty_like(w["dW1"]), dW2=torch.empty_like(w["dW2"])) for w in W]
             if not want_dw:
                 for w in Ws_:
@@ -803,13 +823,21 @@ def main():
         done = [torch.cuda.Event(), torch.cuda.Event()]
         down_done = [torch.cuda.Event(), torch.cuda.Event()]
 
+        def copy_in(a):
+            # this step's inputs from pinned host memory (on the current stream)
+            if one_copy:
+                whole[a][0].copy_(pin_all, non_blocking=True)
+                whole[a][1].copy_(pin_g_all, non_blocking=True)
+                return
+            for j in range(m):
+                sets[a][0][j].copy_(pin[j], non_blocking=True)
+                sets[a][1][j].copy_(pin_g[j], non_blocking=True)
+
         def upload(a):
             # set a's inputs were last read by the step two back (done[a])
             up_stream.wait_event(done[a])
             with torch.cuda.stream(up_stream):
-                for j in range(m):
-                    sets[a][0][j].copy_(pin[j], non_blocking=True)
-                    sets[a][1][j].copy_(pin_g[j], non_blocking=True)
+                copy_in(a)
                 in_ready[a].record(up_stream)
 
         def read_back(Ws):
@@ -834,9 +862,7 @@ def main():
                     fork.record(side)
                     up_stream.wait_event(fork)
                     with torch.cuda.stream(up_stream):
-                        for j in range(m):
-                            sets[1 - a][0][j].copy_(pin[j], non_blocking=True)
-                            sets[1 - a][1][j].copy_(pin_g[j], non_blocking=True)
+                        copy_in(1 - a)
                         joined = torch.cuda.Event()
                         joined.record(up_stream)
                     Xs_, Gs_, Ws_ = sets[a]
@@ -886,9 +912,7 @@ def main():
                 # events around each replay give its GPU time (diagnostic)
                 marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
                 with torch.cuda.stream(up_stream):
-                    for j in range(m):
-                        sets[0][0][j].copy_(pin[j], non_blocking=True)
-                        sets[0][1][j].copy_(pin_g[j], non_blocking=True)
+                    copy_in(0)
                 stream.wait_stream(up_stream)
                 marks[0].record(stream)
                 for k in range(steps):
@@ -922,9 +946,7 @@ def main():
         u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         u0.record(up_stream)
         with torch.cuda.stream(up_stream):
-            for j in range(m):
-                sets[0][0][j].copy_(pin[j], non_blocking=True)
-                sets[0][1][j].copy_(pin_g[j], non_blocking=True)
+            copy_in(0)
         u1.record(up_stream)
         torch.cuda.synchronize()
         upload_ms = u0.elapsed_time(u1)
@@ -943,6 +965,7 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                 "upload_alone_ms": upload_ms, "h2d_gb_per_s": h2d / (upload_ms * 1e6),
                 "mode": args.e2e_mode if graph is not None else "eager",
+                "copies": args.e2e_copies,
                 "clocks": e2e_clk,
                 "step_gpu_ms": [round(x, 2) for x in step_gpu_ms] or None,
                 "result": ("fp32 weight gradients" if want_dw else
