@@ -1,4 +1,4 @@
-"""Launch modes change timing only, never bits.
+"""Launch modes and copy policies change timing only, never bits.
 
 GEMMs that follow each other on one stream launch as programmatic dependents
 (their setup overlaps the previous GEMM's tail, their first global access
@@ -7,7 +7,8 @@ first, runs beside it and waits for it before exiting).  ZB_GEMM_PDL=0 turns tha
 turns it on inside every replay lane; the setting is read once per process,
 so each mode runs in a fresh process on the same seeded inputs: single passes
 (with and without split K) and replays on one lane, on an F/B lane beside a W
-lane, and on four stage lanes must give the same bits in every mode.  And a
+lane, on four stage lanes and on an F, a B and a W lane per stage must give
+the same bits in every mode.  And a
 process whose first library calls are made inside a CUDA graph capture (the
 split-K occupancy query and the programmatic launches among them) replays
 the graph to the bits of the same passes run eagerly.
@@ -66,7 +67,7 @@ def _child(out_path):
             res[f"pass{M}_{k}"] = _bits(v)
     # replays: one lane, F/B lane + W lane (one stage), four stage lanes
     for name, P, m, streams, kind in (("serial", 2, 4, 1, "ZBH1"), ("wlane", 1, 6, 2, "ZBH2"),
-                                      ("stages", 4, 8, 4, "ZBH1")):
+                                      ("stages", 4, 8, 4, "ZBH1"), ("fbw", 4, 8, 12, "ZBH2")):
         M, h, f = 512, 256, 1024
         stages, X0, dY = I.pipeline_draws(P, m, M, h, f, seed=P * 10 + m)
         wts = [{"W1": dev_bf16(s.W1), "W2": dev_bf16(s.W2), "dW1": empty_f32(h, f), "dW2": empty_f32(f, h)}
@@ -92,18 +93,26 @@ def _child(out_path):
     np.savez(out_path, **res)
 
 
-def test_programmatic_launches_change_no_bits(tmp_path):
+# Each mode: environment settings of a fresh process.  The L2 eviction
+# priorities of the GEMM's copies (ZB_GEMM_L2_HINTS=0 turns them off) only
+# decide where data sits in L2, and the W pass's paced reduce-adds only
+# decide when each is issued: neither may change a bit either.
+MODES = {"default": {}, "pdl0": {"ZB_GEMM_PDL": "0"}, "pdl1": {"ZB_GEMM_PDL": "1"},
+         "nohints": {"ZB_GEMM_L2_HINTS": "0"}}
+
+
+def test_launch_modes_change_no_bits(tmp_path):
     if not have_gpu():
         pytest.skip("no CUDA device")
     from split_backward_gemms_gb300 import build as B
     B.build()
     res = {}
-    for mode in ("default", "0", "1"):
+    for mode, extra in MODES.items():
         out = str(tmp_path / f"mode_{mode}.npz")
         env = dict(os.environ)
-        env.pop("ZB_GEMM_PDL", None)
-        if mode != "default":
-            env["ZB_GEMM_PDL"] = mode
+        for k in ("ZB_GEMM_PDL", "ZB_GEMM_L2_HINTS"):
+            env.pop(k, None)
+        env.update(extra)
         code = f"import tests.test_gpu_launch_modes as t; t._child({out!r})"
         r = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, capture_output=True, text=True,
                            timeout=600)
@@ -111,7 +120,7 @@ def test_programmatic_launches_change_no_bits(tmp_path):
         res[mode] = np.load(out)
     keys = res["default"].files
     assert len(keys) > 40
-    for mode in ("0", "1"):
+    for mode in MODES:
         assert res[mode].files == keys
         for k in keys:
             assert np.array_equal(res[mode][k], res["default"][k]), (mode, k)
