@@ -849,10 +849,12 @@ def main():
                     host_out[s_].copy_(Ws[s_]["grad_stats"], non_blocking=True)
 
         def capture_e2e(a):
-            # one graph per set: its step, in parallel the upload of the other
-            # set's inputs (for the next step), then the read-back of its
-            # result; replays follow each other on one stream, one host call
-            # per step
+            # one graph per set: its step and, in parallel branches, the
+            # upload of the other set's inputs (for the next step) and the
+            # read-back of the other set's result (the previous step's,
+            # complete when this graph starts); replays follow each other on
+            # one stream, one host call per step.  The last step's result is
+            # read back after the last replay (see e2e_run).
             g = torch.cuda.CUDAGraph()
             side = torch.cuda.Stream(device=dev)
             side.wait_stream(stream)
@@ -865,11 +867,16 @@ def main():
                         copy_in(1 - a)
                         joined = torch.cuda.Event()
                         joined.record(up_stream)
+                    down_stream.wait_event(fork)
+                    with torch.cuda.stream(down_stream):
+                        read_back(sets[1 - a][2])
+                        down_joined = torch.cuda.Event()
+                        down_joined.record(down_stream)
                     Xs_, Gs_, Ws_ = sets[a]
                     zb.zb_run_stage_schedule(pl, Ws_, Xs_, Gs_, None, None, ops_c, ws_t, ws_t.numel(), None,
                                              side)
-                    read_back(Ws_)
                     side.wait_event(joined)
+                    side.wait_event(down_joined)
             stream.wait_stream(side)
             return g
 
@@ -918,6 +925,9 @@ def main():
                 for k in range(steps):
                     e2e_graphs[k % 2].replay()
                     marks[k + 1].record(stream)
+                # the last step's result (the earlier ones were read back
+                # inside the following step's graph)
+                read_back(sets[(steps - 1) % 2][2])
                 torch.cuda.synchronize()
                 step_gpu_ms[:] = [marks[k].elapsed_time(marks[k + 1]) for k in range(steps)]
                 return
@@ -961,8 +971,12 @@ def main():
         e2e_s = reduce_max(time.perf_counter() - t0, dev, ws)
         e2e_clk = e2e_clocks.stop()
         zb.zb_sync_status(stream)
+        # graph mode reads back one result more than it runs steps (the first
+        # graph's branch reads the other set's buffers before any step wrote
+        # them): count every byte that crossed
+        d2h_step = d2h * (args.e2e_steps + 1) / args.e2e_steps if e2e_graphs is not None else d2h
         return {"value": job_rate(step_flops, args.e2e_steps, ws, e2e_s) / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h_step, "steps": args.e2e_steps,
                 "upload_alone_ms": upload_ms, "h2d_gb_per_s": h2d / (upload_ms * 1e6),
                 "mode": args.e2e_mode if graph is not None else "eager",
                 "copies": args.e2e_copies,
@@ -970,8 +984,9 @@ def main():
                 "step_gpu_ms": [round(x, 2) for x in step_gpu_ms] or None,
                 "result": ("fp32 weight gradients" if want_dw else
                            "gradient statistics per stage (sum of squares, NaN/Inf count)"),
-                "timing": ("host wall clock around the steps; per step one CUDA graph: the step, "
-                           "the next step's upload in a parallel branch, the read-back"
+                "timing": ("host wall clock around the steps; per step one CUDA graph: the step, in "
+                           "parallel branches the next step's upload and the previous step's read-back "
+                           "(the last step's read-back after the last graph)"
                            if e2e_graphs is not None else
                            "host wall clock around the steps; per step one CUDA graph (the step, "
                            "the read-back), the next step's upload issued from the host on a "
