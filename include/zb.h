@@ -38,8 +38,9 @@
  *    or writes what the other writes, unless the caller's buffers overlap,
  *    which the library checks) and ends only after it.  Environment:
  *    ZB_GEMM_PDL=0 disables this, ZB_GEMM_SPLIT_K=1 disables split K (see
- *    zb_block.flags), ZB_GEMM_CTA_GROUP=1|2 forces a GEMM tile shape; all
- *    are read once per process.
+ *    zb_block.flags), ZB_GEMM_CTA_GROUP=1|2 forces a GEMM tile shape,
+ *    ZB_GEMM_L2_HINTS=0 removes the L2 eviction priorities of the GEMMs'
+ *    copies; all are read once per process and none changes a result.
  *  - Errors: every call returns a zb_status; zb_last_error() returns a
  *    thread-local, human-readable message for the last failing call.
  *  - Threads and devices: calls may come from several host threads and for
@@ -53,7 +54,10 @@
  *  - Determinism: for fixed shapes the same inputs give the same output bits;
  *    the W pass adds each microbatch's product into the fp32 gradient with a
  *    fixed tile order, so deferred-W and fused-backward replays that visit
- *    microbatches in the same (ascending) order are bit-identical.
+ *    microbatches in the same (ascending) order are bit-identical.  Without
+ *    split K every output element is the ascending-K sum of its products in
+ *    either GEMM tile shape, so the bits do not depend on the shape the
+ *    problem's size selects either.
  */
 #ifndef ZB_GB300_H
 #define ZB_GB300_H
