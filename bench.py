@@ -718,16 +718,20 @@ def main():
         kms = kind_ms[i]
         kind_tf[name] = (4.0 * M * h * f * m * P * kind_steps / (kms / 1e3) / 1e12) if kms > 0 else None
     peaks = _peaks()
+    # the rate per GEMM: 2 M h f flops each, six GEMMs per stage and
+    # microbatch (a W pass's two run in one grouped launch, so GEMMs, not
+    # launches, are counted here)
     gemm_flops = 2.0 * M * h * f
-    avg_launch_ms = sums["gemm_ms"] / max(1, sums["gemm_launches"])
+    gemms = 6 * m * P * args.steps
+    avg_gemm_ms = sums["gemm_ms"] / max(1, gemms)
     overlapped = pl.streams > 1 or graph is not None
     if overlapped:
         # launches on different streams overlap (a W kernel starts in the
         # tail of an F/B kernel), so events around one launch also count the
         # time it waited for SMs: use the timed region's duration instead,
         # a lower bound on the kernel's own rate
-        avg_launch_ms = ms_max / max(1, sums["gemm_launches"])
-    achieved = gemm_flops / (avg_launch_ms / 1e3) / 1e12
+        avg_gemm_ms = ms_max / max(1, gemms)
+    achieved = gemm_flops / (avg_gemm_ms / 1e3) / 1e12
     roof_peak = peaks["bf16_sustained"]
     traffic = _profiled_traffic(args.workload)
 
@@ -1043,8 +1047,8 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": roof_peak,
                          "unit": "TFLOP/s", "frac": achieved / roof_peak, "traffic": traffic,
                          "kernel": "zb_gemm_bf16_tc_kernel (all six GEMMs of F/B/W)",
-                         "launch_duration": ("timed region / launches (streams overlap)" if overlapped
-                                             else "CUDA events around each launch"),
+                         "launch_duration": ("timed region / GEMMs (streams overlap)" if overlapped
+                                             else "CUDA events around each launch, per GEMM"),
                          "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
                          "frac_of_burst": achieved / peaks["bf16"]},
             "cpu_baseline": cpu,

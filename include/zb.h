@@ -34,13 +34,16 @@
  *    may start its setup before that one ends (programmatic dependent
  *    launch); it touches no memory until every earlier work item of the
  *    stream has completed, so stream order holds as usual.  One exception:
- *    zb_backward_weight's dW1 GEMM runs beside its dW2 GEMM (neither reads
- *    or writes what the other writes, unless the caller's buffers overlap,
- *    which the library checks) and ends only after it.  Environment:
+ *    zb_backward_weight's dW1 and dW2 GEMMs run at once (one grouped
+ *    launch, or the second launched beside the first), since neither reads
+ *    or writes what the other writes; when the caller's buffers overlap
+ *    (the library checks) they run one after the other.  Environment:
  *    ZB_GEMM_PDL=0 disables this, ZB_GEMM_SPLIT_K=1 disables split K (see
  *    zb_block.flags), ZB_GEMM_CTA_GROUP=1|2 forces a GEMM tile shape,
  *    ZB_GEMM_L2_HINTS=0 removes the L2 eviction priorities of the GEMMs'
- *    copies; all are read once per process and none changes a result.
+ *    copies, ZB_GEMM_GROUP_W=0 runs the W pass's two GEMMs as two launches
+ *    (by default one persistent launch runs both); all are read once per
+ *    process and none changes a result.
  *  - Errors: every call returns a zb_status; zb_last_error() returns a
  *    thread-local, human-readable message for the last failing call.
  *  - Threads and devices: calls may come from several host threads and for

@@ -286,23 +286,39 @@ zb_status backward_weight_impl(const zb_block& b, const void* X, const void* A, 
     g5.A = A; g5.lda = b.f; g5.a_mn = 1;
     g5.B = dY; g5.ldb = b.h; g5.b_mn = 1;
     g5.epi = EPI_F32; g5.out0 = dW2; g5.ld0 = b.h; g5.accumulate = accumulate;
-    zb_status s = run_gemm(g5, stream, rec);
-    if (s != ZB_OK) return s;
     GemmBf16 g6;  // dW1 (+)= X^T dH
     g6.Mg = b.h; g6.Ng = b.f; g6.Kg = b.M;
     g6.A = X; g6.lda = b.h; g6.a_mn = 1;
     g6.B = dH; g6.ldb = b.f; g6.b_mn = 1;
     g6.epi = EPI_F32; g6.out0 = dW1; g6.ld0 = b.f; g6.accumulate = accumulate;
-    // the two GEMMs share no output and neither reads the other's, so the
-    // second may run beside the first (unless the caller's buffers overlap)
+    // the two GEMMs share no output and neither reads the other's (unless
+    // the caller's buffers overlap), so they may run at once
+    bool independent;
     {
         const size_t hf4 = static_cast<size_t>(b.h) * b.f * 4;
         const size_t act_f = static_cast<size_t>(b.M) * b.f * 2, act_h = static_cast<size_t>(b.M) * b.h * 2;
-        g6.independent_of_prev = disjoint(dW1, hf4, dW2, hf4) && disjoint(dW1, hf4, A, act_f) &&
-                                 disjoint(dW1, hf4, dY, act_h) && disjoint(dW2, hf4, X, act_h) &&
-                                 disjoint(dW2, hf4, dH, act_f);
+        independent = disjoint(dW1, hf4, dW2, hf4) && disjoint(dW1, hf4, A, act_f) &&
+                      disjoint(dW1, hf4, dY, act_h) && disjoint(dW2, hf4, X, act_h) &&
+                      disjoint(dW2, hf4, dH, act_f);
     }
-    s = run_gemm(g6, stream, rec);
+    // one grouped launch for both (one setup, one tail; the second GEMM's
+    // tiles follow the first's in the same persistent kernel) when both take
+    // CTA pairs; else the second launches beside the first.
+    // ZB_GEMM_GROUP_W=0 in the environment keeps two launches.
+    static const bool group_w = [] {
+        const char* v = std::getenv("ZB_GEMM_GROUP_W");
+        return !(v && v[0] == '0');
+    }();
+    zb_status s;
+    if (group_w && independent && gemm_bf16_cta_group(g5) == 2 && gemm_bf16_cta_group(g6) == 2) {
+        g5.second = &g6;
+        s = run_gemm(g5, stream, rec);
+    } else {
+        s = run_gemm(g5, stream, rec);
+        if (s != ZB_OK) return s;
+        g6.independent_of_prev = independent;
+        s = run_gemm(g6, stream, rec);
+    }
     if (s != ZB_OK || !b.has_bias) return s;
     s = timed(rec, false, [&] { return colsum_bf16(dH, b.M, b.f, b.f, db1, accumulate, stream); });
     if (s != ZB_OK) return s;

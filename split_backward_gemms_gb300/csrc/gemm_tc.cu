@@ -141,6 +141,12 @@ struct EpiArgs {
     // L2 eviction priority of the A and B operand loads and of the output
     // stores (0 normal, 1 evict first, 2 evict last; see choose_l2_hints)
     int hint_a, hint_b, hint_out;
+    // fp32 epilogue with CTA pairs: a second problem (the W pass's other
+    // weight-gradient GEMM, same K and operand majors), its tiles after the
+    // first's; A, B and output maps tmA2, tmB2, tmO1
+    int groups;  // 1 or 2
+    int Mg2, Ng2;
+    int hint_a2, hint_b2;
     unsigned int* err;
 };
 
@@ -589,7 +595,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     zb_gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmO0,
-                           const __grid_constant__ CUtensorMap tmO1, const EpiArgs args) {
+                           const __grid_constant__ CUtensorMap tmO1,
+                           const __grid_constant__ CUtensorMap tmA2,
+                           const __grid_constant__ CUtensorMap tmB2, const EpiArgs args) {
     using C = Cfg<CG>;
     constexpr int STAGES = C::STAGES;
     constexpr bool PAIR = CG == 2;
@@ -612,7 +620,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int clusters = gridDim.x / cw;
     const int tiles_m = (args.Mg + C::TILE_M - 1) / C::TILE_M;
     const int tiles_n = (args.Ng + BN - 1) / BN;
-    const int num_tiles = tiles_m * tiles_n;
+    // a second problem (fp32 epilogue, CTA pairs): its tiles follow the first's
+    constexpr bool GROUPABLE = EPI == zb::EPI_F32 && PAIR;
+    const bool two = GROUPABLE && args.groups > 1;
+    const int tiles_1 = tiles_m * tiles_n;
+    const int tiles_m2 = two ? (args.Mg2 + C::TILE_M - 1) / C::TILE_M : 0;
+    const int tiles_n2 = two ? (args.Ng2 + BN - 1) / BN : 0;
+    const int num_tiles = tiles_1 + tiles_m2 * tiles_n2;
+    // problem of a tile (0 or 1) and its M / N block inside that problem
+    auto locate = [&](int tile, int& mb, int& nb) -> int {
+        if (two && tile >= tiles_1) {
+            tile_coords(tile - tiles_1, tiles_m2, tiles_n2, C::GROUP_M, mb, nb);
+            return 1;
+        }
+        tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
+        return 0;
+    };
     const int num_kb_all = (args.Kg + BK - 1) / BK;
     const int kb_lo = SPLITTABLE ? static_cast<int>(static_cast<long long>(kslice) * num_kb_all / ks) : 0;
     const int kb_hi =
@@ -637,7 +660,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         zbp::tma_prefetch_desc(&tmA);
         zbp::tma_prefetch_desc(&tmB);
         zbp::tma_prefetch_desc(&tmO0);
-        if (EPI == zb::EPI_GELU_DUAL) zbp::tma_prefetch_desc(&tmO1);
+        if (EPI == zb::EPI_GELU_DUAL || two) zbp::tma_prefetch_desc(&tmO1);
+        if (two) {
+            zbp::tma_prefetch_desc(&tmA2);
+            zbp::tma_prefetch_desc(&tmB2);
+        }
     }
     if (warp == 1) {
         if (PAIR) {
@@ -673,11 +700,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ------------------------------------------------ TMA producer
             uint32_t it = 0;
             bool ok = true;
-            const uint64_t pol_a = zbp::l2_policy(args.hint_a);
-            const uint64_t pol_b = zbp::l2_policy(args.hint_b);
+            const uint64_t pol_a1 = zbp::l2_policy(args.hint_a);
+            const uint64_t pol_b1 = zbp::l2_policy(args.hint_b);
+            const uint64_t pol_a2 = two ? zbp::l2_policy(args.hint_a2) : pol_a1;
+            const uint64_t pol_b2 = two ? zbp::l2_policy(args.hint_b2) : pol_b1;
             for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
                 int mb, nb;
-                tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
+                const int prob = locate(tile, mb, nb);
+                const CUtensorMap* tma = prob ? &tmA2 : &tmA;
+                const CUtensorMap* tmb = prob ? &tmB2 : &tmB;
+                const uint64_t pol_a = prob ? pol_a2 : pol_a1;
+                const uint64_t pol_b = prob ? pol_b2 : pol_b1;
                 const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
                 const int nb0 = nb * BN + static_cast<int>(rank) * C::B_ROWS;
                 for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
@@ -701,17 +734,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             zbp::tma_load_2d_hint(dst, tm, full, x, y, pol);
                     };
                     if (A_MN) {
-                        load(sa, &tmA, m0, k0, pol_a);
-                        load(sa + MN_ATOM_BYTES, &tmA, m0 + 64, k0, pol_a);
+                        load(sa, tma, m0, k0, pol_a);
+                        load(sa + MN_ATOM_BYTES, tma, m0 + 64, k0, pol_a);
                     } else {
-                        load(sa, &tmA, k0, m0, pol_a);
+                        load(sa, tma, k0, m0, pol_a);
                     }
                     if (B_MN) {
 #pragma unroll
                         for (int i = 0; i < C::B_ROWS / 64; ++i)
-                            load(sb + i * MN_ATOM_BYTES, &tmB, nb0 + 64 * i, k0, pol_b);
+                            load(sb + i * MN_ATOM_BYTES, tmb, nb0 + 64 * i, k0, pol_b);
                     } else {
-                        load(sb, &tmB, k0, nb0, pol_b);
+                        load(sb, tmb, k0, nb0, pol_b);
                     }
                 }
             }
@@ -865,7 +898,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t buf = local & 1u;
                 const uint32_t tr = local >> 1;
                 int mb, nb;
-                tile_coords(tile, tiles_m, tiles_n, C::GROUP_M, mb, nb);
+                const int prob = locate(tile, mb, nb);
+                const int Mg_t = prob ? args.Mg2 : args.Mg;  // this tile's problem
+                const int Ng_t = prob ? args.Ng2 : args.Ng;
+                const CUtensorMap* tmO_t = prob ? &tmO1 : &tmO0;
                 const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
                 const int n0 = nb * BN;
                 const int row0 = m0 + q * 32;
@@ -887,7 +923,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 zbp::tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
-                const bool rows_live = row0 < args.Mg;
+                const bool rows_live = row0 < Mg_t;
                 if (EPI == zb::EPI_F32) {
                     // The fp32 stores (TMA reduce-adds; the L2 reads the old
                     // dW from DRAM for each) share the TMA unit with the
@@ -924,15 +960,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         zbp::tmem_ld_32x32b_x32(taddr + c_lo + c * 32, v);
                         zbp::tmem_ld_wait();
                         const int col0 = n0 + c_lo + c * 32;
-                        if (!rows_live || col0 >= args.Ng) continue;
+                        if (!rows_live || col0 >= Ng_t) continue;
                         const uint32_t stg = stg0 + flip * E::BOX;
                         flip ^= 1u;
                         staging_acquire(lane);
                         stage_row(stg, lane, v);
                         if (args.accumulate)
-                            staging_release<true>(&tmO0, stg, lane, col0, row0, pol_out);
+                            staging_release<true>(tmO_t, stg, lane, col0, row0, pol_out);
                         else
-                            staging_release<false>(&tmO0, stg, lane, col0, row0, pol_out);
+                            staging_release<false>(tmO_t, stg, lane, col0, row0, pol_out);
                     }
                 } else {
 #pragma unroll 1
@@ -1096,7 +1132,7 @@ int sm_count() {
 }
 
 struct Maps {
-    CUtensorMap a, b, o0, o1;
+    CUtensorMap a, b, o0, o1, a2, b2;  // a2, b2: a grouped launch's second problem
 };
 
 // Persistent grid size in CTAs for a CTA-group shape (co-resident clusters x CG).
@@ -1205,7 +1241,7 @@ zb_status launch(const Maps& mp, EpiArgs ea, long long tiles, cudaStream_t st, b
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.o0, mp.o1, ea);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.o0, mp.o1, mp.a2, mp.b2, ea);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess)
         return zb::fail(ZB_ERR_CUDA, std::string("tensor-core GEMM launch: ") + cudaGetErrorString(e));
@@ -1366,6 +1402,34 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     }
     if (!ok) return fail(ZB_ERR_CUDA, why);
     if (f32_out && (g.ld0 % 4)) return fail(ZB_ERR_ALIGN, "fp32 output leading dimension must be a multiple of 4");
+    mp.a2 = mp.a;
+    mp.b2 = mp.b;
+    const GemmBf16* g2 = g.second;
+    if (g2) {
+        // a grouped launch: the second problem runs in the same persistent
+        // kernel, its tiles after the first's (fp32 epilogue, CTA pairs)
+        if (g.epi != EPI_F32 || g2->epi != EPI_F32 || g2->Kg != g.Kg || g2->a_mn != g.a_mn ||
+            g2->b_mn != g.b_mn || g2->accumulate != g.accumulate || g2->second || cg != 2)
+            return fail(ZB_ERR_INVALID_ARG, "grouped GEMM: the two problems must match (fp32, K, majors)");
+        if (g2->Mg <= 0 || g2->Ng <= 0 || g2->Mg > (1LL << 30) || g2->Ng > (1LL << 30))
+            return fail(ZB_ERR_SHAPE, "GEMM extents must be in [1, 2^30]");
+        if (g2->Ng % 8 || g2->lda % 8 || g2->ldb % 8 || g2->ld0 % 4)
+            return fail(ZB_ERR_ALIGN, "grouped GEMM: second problem's extents / leading dimensions");
+        if (!g2->A || !g2->B || !g2->out0) return fail(ZB_ERR_INVALID_ARG, "GEMM operand is NULL");
+        if (mis(g2->A) || mis(g2->B) || mis(g2->out0)) return fail(ZB_ERR_ALIGN, "GEMM pointers must be 16-byte aligned");
+        if (g2->a_mn)
+            ok = make_map(&mp.a2, g2->A, false, g2->Mg, g2->Kg, g2->lda, 64, BK, &why);
+        else
+            ok = make_map(&mp.a2, g2->A, false, g2->Kg, g2->Mg, g2->lda, BK, BM, &why);
+        if (ok) {
+            if (g2->b_mn)
+                ok = make_map(&mp.b2, g2->B, false, g2->Ng, g2->Kg, g2->ldb, 64, BK, &why);
+            else
+                ok = make_map(&mp.b2, g2->B, false, g2->Kg, g2->Ng, g2->ldb, BK, b_rows, &why);
+        }
+        if (ok) ok = make_map(&mp.o1, g2->out0, true, g2->Ng, g2->Mg, g2->ld0, 32, 32, &why, osw);
+        if (!ok) return fail(ZB_ERR_CUDA, why);
+    }
 
     unsigned int* err = device_error_word();
     if (!err) return ZB_ERR_CUDA;
@@ -1386,12 +1450,34 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream) {
     ea.ksplit = 1;
     ea.late_wait = g.independent_of_prev && g.allow_pdl ? 1 : 0;
     choose_l2_hints(g, cg, &ea);
+    ea.groups = 1;
+    ea.Mg2 = ea.Ng2 = 0;
+    ea.hint_a2 = ea.hint_b2 = 0;
+    long long tiles_all = pair_tiles;
+    if (g2) {
+        EpiArgs e2 = ea;
+        choose_l2_hints(*g2, cg, &e2);
+        ea.groups = 2;
+        ea.Mg2 = static_cast<int>(g2->Mg);
+        ea.Ng2 = static_cast<int>(g2->Ng);
+        ea.hint_a2 = e2.hint_a;
+        ea.hint_b2 = e2.hint_b;
+        tiles_all += ((g2->Mg + 2 * BM - 1) / (2 * BM)) * ((g2->Ng + BN - 1) / BN);
+    }
     ea.err = err;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cg == 2) return dispatch<2>(g, mp, ea, pair_tiles, st);
+    if (cg == 2) return dispatch<2>(g, mp, ea, tiles_all, st);
     ea.ksplit = ksplit;
     return dispatch<1>(g, mp, ea, tiles, st);
+}
+
+int gemm_bf16_cta_group(const GemmBf16& g) {
+    if (sm_count() <= 0 || g.Mg <= 0 || g.Ng <= 0 || g.Kg <= 0) return 1;
+    const long long pair_tiles = ((g.Mg + 2 * BM - 1) / (2 * BM)) * ((g.Ng + BN - 1) / BN);
+    const long long tiles = ((g.Mg + BM - 1) / BM) * ((g.Ng + BN - 1) / BN);
+    const int ksplit = (g.epi != EPI_F32 && g.allow_split) ? choose_split(tiles, (g.Kg + BK - 1) / BK) : 1;
+    return choose_cta_group(pair_tiles, g.Mg, ksplit);
 }
 
 }  // namespace zb

@@ -55,8 +55,15 @@ struct GemmBf16 {
     // waits for it just before exiting instead (its own completion then still
     // implies that kernel's, for whatever follows in the stream)
     int independent_of_prev = 0;
+    // a grouped launch: a second problem with the same epilogue (fp32
+    // only), K and operand majors, run by the same persistent kernel after
+    // this one's tiles (one launch for the W pass's two GEMMs); the two must
+    // not write what the other reads or writes
+    const GemmBf16* second = nullptr;
 };
 zb_status gemm_bf16_tc(const GemmBf16& g, void* stream);
+// The CTA group gemm_bf16_tc would choose for g (1 or 2).
+int gemm_bf16_cta_group(const GemmBf16& g);
 
 // fp32 FFMA GEMM (no TF32): C[m*ldc + n] (+)= sum_k A[m*sam + k*sak] * B[k*sbk + n*sbn]
 struct GemmF32 {

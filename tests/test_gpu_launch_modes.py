@@ -95,10 +95,12 @@ def _child(out_path):
 
 # Each mode: environment settings of a fresh process.  The L2 eviction
 # priorities of the GEMM's copies (ZB_GEMM_L2_HINTS=0 turns them off) only
-# decide where data sits in L2, and the W pass's paced reduce-adds only
-# decide when each is issued: neither may change a bit either.
+# decide where data sits in L2, the W pass's paced reduce-adds only decide
+# when each is issued, and its two GEMMs in one grouped launch
+# (ZB_GEMM_GROUP_W=0: two launches) compute every tile as before: none may
+# change a bit either.
 MODES = {"default": {}, "pdl0": {"ZB_GEMM_PDL": "0"}, "pdl1": {"ZB_GEMM_PDL": "1"},
-         "nohints": {"ZB_GEMM_L2_HINTS": "0"}}
+         "nohints": {"ZB_GEMM_L2_HINTS": "0"}, "twolaunchw": {"ZB_GEMM_GROUP_W": "0"}}
 
 
 def test_launch_modes_change_no_bits(tmp_path):
@@ -110,7 +112,7 @@ def test_launch_modes_change_no_bits(tmp_path):
     for mode, extra in MODES.items():
         out = str(tmp_path / f"mode_{mode}.npz")
         env = dict(os.environ)
-        for k in ("ZB_GEMM_PDL", "ZB_GEMM_L2_HINTS"):
+        for k in ("ZB_GEMM_PDL", "ZB_GEMM_L2_HINTS", "ZB_GEMM_GROUP_W"):
             env.pop(k, None)
         env.update(extra)
         code = f"import tests.test_gpu_launch_modes as t; t._child({out!r})"
