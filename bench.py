@@ -73,7 +73,7 @@ def _gemm_source_sha():
 
 
 def _profiled_traffic(workload):
-    """DRAM bytes per GEMM launch of the workload's step mix, from the ncu
+    """DRAM bytes per GEMM of the workload's step mix, from the ncu
     figures committed as data under profiles/ (gemm_tc_<workload>.json),
     while they were taken on the current GEMM source; else None."""
     path = os.path.join(ROOT, "profiles", f"gemm_tc_{workload}.json")
@@ -82,7 +82,7 @@ def _profiled_traffic(workload):
             d = json.load(fh)
         if d.get("source_sha") != _gemm_source_sha():
             return None
-        return float(d["traffic_bytes_per_launch"])
+        return float(d["traffic_bytes_per_gemm"])
     except (OSError, KeyError, TypeError, ValueError):
         return None
 
@@ -1046,6 +1046,7 @@ def main():
             "peak_live_bytes": peak_live, "workspace_bytes": need,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": roof_peak,
                          "unit": "TFLOP/s", "frac": achieved / roof_peak, "traffic": traffic,
+                         "traffic_per": "GEMM (2 M h f flops; a grouped W launch is two)",
                          "kernel": "zb_gemm_bf16_tc_kernel (all six GEMMs of F/B/W)",
                          "launch_duration": ("timed region / GEMMs (streams overlap)" if overlapped
                                              else "CUDA events around each launch, per GEMM"),
