@@ -45,7 +45,12 @@
 // Launched as a programmatic dependent of the previous GEMM in a stream, a
 // CTA runs its setup early and waits (griddepcontrol.wait) before its first
 // global access; a GEMM that touches nothing the previous one writes (the W
-// pass's second) waits only before it exits, and runs beside that one.
+// pass's second, when it has a launch of its own) waits only before it
+// exits, and runs beside that one.  By default the W pass's two GEMMs share
+// one launch instead (fp32 epilogue, CTA pairs): the second problem's tiles
+// follow the first's in the same persistent grid.
+// Every TMA copy carries an L2 eviction priority chosen per operand from
+// the raster order's re-reads (choose_l2_hints).
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets the
 // device error word, drains its in-flight copies and MMAs, frees TMEM and
 // returns.
