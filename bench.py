@@ -469,29 +469,43 @@ def setup_workload(zb, dev, name, schedule=None, streams=0, seed=1000):
     w.name = name
     w.h, w.f, w.M, w.m, sched, w.Pl, w.desc = WORKLOADS[name]
     w.sched = schedule or sched
+    if w.sched != sched:
+        w.desc += "; ordering replayed instead: " + w.sched
+        if w.sched in ("ZBV", "1F1B-I"):
+            w.desc += " (two chunks of one block per stage: 2P blocks)"
     w.multi = name == "c2"
     w.P = w.Pl if w.multi else 1
+    # ZB-V / interleaved 1F1B: two chunks per stage, one MLP block each, so
+    # the model is a chain of 2 P blocks (stage s holds two of them)
+    w.chunks = 2 if w.sched in ("ZBV", "1F1B-I") else 1
+    if w.chunks > 1 and not w.multi:
+        raise ValueError("two-chunk orderings are replayed on the pipeline workload only")
+    w.L = w.P * w.chunks
     h, f, M, m = w.h, w.f, w.M, w.m
     gen = torch.Generator(device=dev).manual_seed(seed)
     bf = torch.bfloat16
     w.W = [{"W1": (torch.randn(h, f, device=dev, generator=gen) * 0.02).to(bf),
             "W2": (torch.randn(f, h, device=dev, generator=gen) * 0.02).to(bf),
             "dW1": torch.zeros(h, f, device=dev), "dW2": torch.zeros(f, h, device=dev)}
-           for _ in range(w.P)]
+           for _ in range(w.L)]
     w.X0 = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
     w.dY = [torch.randn(M, h, device=dev, generator=gen).to(bf) for _ in range(m)]
-    w.ops = make_ops(zb, w.sched, w.Pl, m, w.multi)
+    if w.chunks > 1:
+        w.ops = zb.zb_make_interleaved_schedule(w.sched, w.Pl, w.chunks, m)
+    else:
+        w.ops = make_ops(zb, w.sched, w.Pl, m, w.multi)
     w.blk = zb.make_block(M, h, f)
     # multi-stage replays run each stage's F, B and W ops on lanes of their
     # own (3P streams; the P=4, h=1024 pipeline: 995 TF/s with a lane per
     # stage, 1008-1069 with a W lane too, 1089 with separate F and B lanes);
     # a one-stage replay puts its W passes on a second stream
     n_streams = streams if streams > 0 else (min(3 * w.P, 12) if w.multi else 2)
-    w.pl = zb.make_pipeline(w.P, m, w.blk, timing=True, streams=n_streams)
+    w.pl = zb.make_pipeline(w.P, m, w.blk, timing=True, streams=n_streams, chunks=w.chunks,
+                            layout=w.sched if w.chunks > 1 else zb.ZB_LAYOUT_CYCLIC)
     w.need, w.peak_live = zb.zb_schedule_workspace_size(w.pl, w.ops)
     w.ws_t = torch.empty(max(w.need, 256), dtype=torch.uint8, device=dev)
     w.ops_c = zb.ops_array(w.ops)
-    w.step_flops = 12.0 * M * h * f * m * w.P  # F, B and W: 4 M h f each per microbatch
+    w.step_flops = 12.0 * M * h * f * m * w.L  # F, B and W: 4 M h f each per microbatch and block
     return w
 
 
@@ -546,12 +560,18 @@ def other_workloads(zb, dev, steps, warmup):
     same streams and graphs, and the h=4096 one-stage ZB-H1 step."""
     import torch
     out = {}
-    for name, sched in (("c2", "1F1B"), ("c2", "ZBH1"), ("c2", "ZBH2"), ("c2", "ZB2P"), ("c3", "ZBH1")):
+    for name, sched in (("c2", "1F1B"), ("c2", "ZBH1"), ("c2", "ZBH2"), ("c2", "ZB2P"), ("c2", "1F1B-I"),
+                        ("c2", "ZBV"), ("c3", "ZBH1")):
         w = setup_workload(zb, dev, name, sched)
         r = time_workload(zb, dev, w, steps, warmup)
-        r.update({"workload": w.desc.split(",")[0] if name != "c2" else
-                  "P=4 stages h=1024 ffn=4096 microbatch 4x512 m=8, all stages on one GPU",
-                  "schedule": sched, "streams": w.pl.streams, "unit": UNIT,
+        if w.chunks > 1:
+            wl = ("P=4 stages x 2 chunks = 8 MLP blocks h=1024 ffn=4096, microbatch 4x512 m=8, all "
+                  "stages on one GPU")
+        elif name == "c2":
+            wl = "P=4 stages h=1024 ffn=4096 microbatch 4x512 m=8, all stages on one GPU"
+        else:
+            wl = w.desc.split(",")[0]
+        r.update({"workload": wl, "schedule": sched, "streams": w.pl.streams, "unit": UNIT,
                   "pct_of_burst_peak": 100.0 * r["value"] / _peaks()["bf16"]})
         out[f"{name}_{sched}"] = r
         del w
@@ -566,8 +586,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="c4")
-    ap.add_argument("--schedule", choices=("1F1B", "ZBH1", "ZBH2", "ZB1P", "ZB2P"), default=None,
-                    help="ordering to replay instead of the workload's own (c4: ZBH2, c3 and c2: ZBH1)")
+    ap.add_argument("--schedule", choices=("1F1B", "ZBH1", "ZBH2", "ZB1P", "ZB2P", "ZBV", "1F1B-I"), default=None,
+                    help="ordering to replay instead of the workload's own (c4: ZBH2, c3 and c2: ZBH1); "
+                         "ZBV and 1F1B-I (c2 only) give each stage two chunks of one block each")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other configurations' short timed regions (the P=4, h=1024 "
                          "pipeline under 1F1B and ZB-H1, the h=4096 step)")
@@ -632,7 +653,8 @@ def main():
 
     wk = setup_workload(zb, dev, args.workload, args.schedule, args.streams, seed=1000 + rank)
     h, f, M, m, sched, Pl, desc = wk.h, wk.f, wk.M, wk.m, wk.sched, wk.Pl, wk.desc
-    multi, P, W, X0, dY = wk.multi, wk.P, wk.W, wk.X0, wk.dY
+    # P counts MLP blocks (stages x chunks): per-block work, weights, results
+    multi, P, W, X0, dY = wk.multi, wk.L, wk.W, wk.X0, wk.dY
     blk, pl, need, peak_live, ws_t, ops_c = wk.blk, wk.pl, wk.need, wk.peak_live, wk.ws_t, wk.ops_c
     stream = torch.cuda.current_stream()
 
@@ -703,7 +725,8 @@ def main():
     if pl.streams > 1 or graph is not None:
         # per-pass times from a short serial replay: on overlapping streams an
         # op's events also count the time it waited for SMs
-        pl_serial = zb.make_pipeline(P, m, blk, timing=True, streams=1)
+        pl_serial = zb.make_pipeline(wk.P, m, blk, timing=True, streams=1, chunks=wk.chunks,
+                                     layout=wk.sched if wk.chunks > 1 else zb.ZB_LAYOUT_CYCLIC)
         st_serial = zb.zb_run_stats()
         step(st_serial, pl_serial)
         kind_ms, kind_steps = [0.0] * 4, 2
@@ -1034,7 +1057,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": desc, "h": h, "f": f, "M": M, "m": m, "P": P,
+            "config": {"workload": desc, "h": h, "f": f, "M": M, "m": m, "P": wk.P, "chunks": wk.chunks,
                        "schedule": sched, "list_from_P": Pl, "streams": pl.streams,
                        "cuda_graph": graph is not None,
                        "parallelism": "replicas" if ws > 1 else "single GPU",
