@@ -204,3 +204,45 @@ def test_chunked_replay_per_pass_against_oracle(zb, kind, P, v, m):
             r2 += b
         assert ob.rel_fro(f64(stages[k]["dW1"]), r1) < TOL_BF16
         assert ob.rel_fro(f64(stages[k]["dW2"]), r2) < TOL_BF16
+
+
+@pytest.mark.parametrize("kind", ["ZBV", "1F1B-I"])
+def test_chunked_pipeline_as_benchmarked(zb, kind):
+    """The two-chunk P=4, h=1024 pipeline (8 blocks, 4 x 512 tokens per
+    microbatch, m=8) in the launch configuration the benchmark times: 12
+    streams, one step captured into a CUDA graph and replayed twice, bit for
+    bit the serial eager replay of the same list."""
+    P, v, m, M, h = 4, 2, 8, 2048, 1024
+    f = 4 * h
+    L = P * v
+    blk = zb.make_block(M, h, f)
+    gen = torch.Generator(device="cuda").manual_seed(17)
+    bf = torch.bfloat16
+    wts = [{"W1": (torch.randn(h, f, device="cuda", generator=gen) * 0.02).to(bf),
+            "W2": (torch.randn(f, h, device="cuda", generator=gen) * 0.02).to(bf)} for _ in range(L)]
+    X0 = [torch.randn(M, h, device="cuda", generator=gen).to(bf) for _ in range(m)]
+    dY = [torch.randn(M, h, device="cuda", generator=gen).to(bf) for _ in range(m)]
+    ops = zb.zb_make_interleaved_schedule(kind, P, v, m)
+    ref = _replay(zb, zb.make_pipeline(P, m, blk, chunks=v, layout=kind), wts, X0, dY, ops, M, h, f)
+    pl = zb.make_pipeline(P, m, blk, chunks=v, layout=kind, streams=3 * P)
+    ws_bytes, _ = zb.zb_schedule_workspace_size(pl, ops)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stages = [dict(w, dW1=empty_f32(h, f), dW2=empty_f32(f, h)) for w in wts]
+    dX0 = [empty_bf16(M, h) for _ in range(m)]
+    Yl = [empty_bf16(M, h) for _ in range(m)]
+    ops_c = zb.ops_array(ops)
+    zb.zb_run_stage_schedule(pl, stages, X0, dY, dX0, Yl, ops_c, ws, ws_bytes)  # eager: makes the lanes
+    sync(zb)
+    for s in stages:
+        s["dW1"].fill_(float("nan"))
+        s["dW2"].fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            zb.zb_run_stage_schedule(pl, stages, X0, dY, dX0, Yl, ops_c, ws, ws_bytes, None, side)
+    for _ in range(2):
+        g.replay()
+        sync(zb)
+        _same((stages, dX0, Yl), ref)
