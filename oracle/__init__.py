@@ -13,8 +13,16 @@ Modules
                input-gradient B and the weight-gradient W, plus the
                single-linear special case and an fp64 pipeline chain.
 ``schedules``  1F1B / ZB-H1 / ZB-H2 event-graph generators (a list-scheduling
-               simulator), an event validator, bubble metrics, the closed
-               forms and the activation-memory ledger.
+               simulator), the heuristic ZB-1p / ZB-2p scheduler, an op-list
+               validator and a timed-trace checker built from the event
+               graph's dependency rules, bubble metrics, the closed forms and
+               the activation-memory ledger.
+``interleaved`` two-chunk orderings: interleaved 1F1B (cyclic assignment)
+               and ZB-V (V-shaped), their simulator, the gap-free search and
+               integer program, and the mapping onto the chain of virtual
+               stages.
+``optimizer``  AdamW, its algebraic inverse and the staged-reduce
+               post-update validation of the stages' optimizer steps.
 
 Sources are the three web pages on zero bubble pipeline parallelism:
   * "Zero Bubble Pipeline Parallelism" (paper-graph-ui summary of arXiv
