@@ -42,8 +42,11 @@
  *    zb_block.flags), ZB_GEMM_CTA_GROUP=1|2 forces a GEMM tile shape,
  *    ZB_GEMM_L2_HINTS=0 removes the L2 eviction priorities of the GEMMs'
  *    copies, ZB_GEMM_GROUP_W=0 runs the W pass's two GEMMs as two launches
- *    (by default one persistent launch runs both); all are read once per
- *    process and none changes a result.
+ *    (by default one persistent launch runs both), ZB_GEMM_HANDOFF=0 keeps
+ *    the long-K GeLU / GeLU' epilogues on every warp's own rows (by default
+ *    the warps that share SM schedulers with the copy and MMA warps hand
+ *    their accumulator chunks to the others); all are read once per process
+ *    and none changes a result.
  *  - Errors: every call returns a zb_status; zb_last_error() returns a
  *    thread-local, human-readable message for the last failing call.
  *  - Threads and devices: calls may come from several host threads and for

@@ -19,6 +19,12 @@
 //               and TMA tensor stores; the weight gradient is added in place
 //               with a TMA reduce-add (one fp32 add per element, in L2).
 // The two accumulators let the epilogue of tile t overlap the MMAs of t+1.
+// Warp w runs on SM sub-partition w mod 4 and may read only TMEM lane
+// quadrant w mod 4, so the epilogue warps of quadrants 0 and 1 share their
+// schedulers with the producer and MMA-issuer warps.  For the GeLU and
+// GeLU' epilogues of long-K problems (HAND, K >= 64 blocks) those four
+// warps only copy raw fp32 chunks from TMEM into shared memory, and the
+// warps of quadrants 2 and 3 do the arithmetic and stores of all rows.
 //
 // Two CTA-group shapes share the code:
 //   CG = 1  one CTA per 128x256 tile (M=128, N=256 MMAs), 4 stages of 48 KB;
@@ -120,12 +126,21 @@ struct SharedCtl {
     uint32_t tmem_base;
     int abort_flag;
     uint64_t xchg;  // split K: bytes of the other CTAs' slabs received
+    uint64_t hfull[4];   // hand-off epilogue: slot filled by the reader warp
+    uint64_t hempty[4];  // hand-off epilogue: slot read by the math warp
 };
+
+// With the hand-off epilogue the staging area (after the ring) holds 16 KiB
+// of TMA store boxes for its four math warps and four 4 KiB hand-off slots
+// (one per reader / math warp pair).
+constexpr uint32_t HAND_BOXES = 16 * 1024;
+constexpr uint32_t HAND_SLOT = 32 * 32 * 4;  // one raw fp32 chunk: 32 rows x 32 columns
+static_assert(HAND_BOXES + 4 * HAND_SLOT == STAGING_BYTES, "hand-off staging");
+static_assert(4 * 2 * 32 * 64 == HAND_BOXES, "hand-off store boxes");
 
 template <int CG>
 constexpr size_t smem_bytes() {
-    return 1024 + Cfg<CG>::STAGES * Cfg<CG>::STAGE_BYTES + STAGING_BYTES +
-           sizeof(SharedCtl<Cfg<CG>::STAGES>) + 64;
+    return 1024 + Cfg<CG>::STAGES * Cfg<CG>::STAGE_BYTES + STAGING_BYTES + sizeof(SharedCtl<Cfg<CG>::STAGES>) + 64;
 }
 static_assert(smem_bytes<1>() <= 232448, "shared memory budget (one CTA)");
 static_assert(smem_bytes<2>() <= 232448, "shared memory budget (CTA pair)");
@@ -595,7 +610,7 @@ __device__ __forceinline__ void split_reduce_store(const EpiArgs& args_in, uint3
     }
 }
 
-template <int EPI, int A_MN, int B_MN, int CG>
+template <int EPI, int A_MN, int B_MN, int CG, int HAND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     zb_gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -657,6 +672,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             zbp::mbar_init(zbp::smem_u32(&ctl->tempty[b]), EpiShape<EPI>::WARPS * CG);
         }
         zbp::mbar_init(zbp::smem_u32(&ctl->drain), 1);
+        if (HAND) {
+            for (int pp = 0; pp < 4; ++pp) {
+                zbp::mbar_init(zbp::smem_u32(&ctl->hfull[pp]), 1);
+                zbp::mbar_init(zbp::smem_u32(&ctl->hempty[pp]), 1);
+            }
+        }
         if (SPLITTABLE) zbp::mbar_init(zbp::smem_u32(&ctl->xchg), 1);
         ctl->abort_flag = 0;
         zbp::fence_mbar_init();
@@ -880,6 +901,174 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t bar = zbp::mapa_shared(zbp::smem_u32(&ctl->xchg), static_cast<uint32_t>(o));
                 zbp::bulk_copy_s2cluster(dst, base + static_cast<uint32_t>(o) * slab, slab, bar);
             }
+        }
+    } else if constexpr (HAND != 0) {
+        // ---------------------------------------- hand-off epilogue (HAND)
+        // Lane quadrants 0 and 1 of the accumulator can only be read by warps
+        // on schedulers 0 and 1, which also host the TMA-producer and
+        // MMA-issuer warps.  So here those warps (4, 5, 8, 9: "readers") only
+        // copy raw fp32 chunks from TMEM into shared-memory slots, and the
+        // warps on schedulers 2 and 3 (2, 3, 6, 7: "math") apply the GeLU /
+        // GeLU' epilogue and store both their own chunks and their partner's
+        // (pair p = 2 (q mod 2) + column half: warp 2 takes warp 4's, 3 takes
+        // 5's, 6 takes 8's, 7 takes 9's).  One slot per pair: the reader
+        // fills chunk c + 1 while its math warp finishes chunk c and its own
+        // chunk c + 1.  Every warp arrives on the accumulator's tempty
+        // barrier after its last chunk of the tile.
+        using E = EpiShape<EPI>;
+        constexpr int CH = E::COLS / 32;
+        const int ew = warp - 2;
+        if (ew < E::WARPS) {
+            const int q = warp & 3;
+            const int hf = ew >> 2;
+            const int c_lo = hf * E::COLS;
+            const int pr = (q & 1) * 2 + hf;
+            const bool reader = q < 2;
+            const uint32_t slot = zbp::smem_u32(staging + HAND_BOXES) + static_cast<uint32_t>(pr) * HAND_SLOT;
+            const int mi = hf * 2 + (q & 1);  // math warp index 0..3 (its staging boxes)
+            const uint32_t stg0 = zbp::smem_u32(staging) + static_cast<uint32_t>(mi) * 2u * E::BOX;
+            const uint64_t pol_out = zbp::l2_policy(args.hint_out);
+            uint32_t flip = 0;
+            uint32_t local = 0;
+            uint32_t k = 0;  // chunks handed off so far (the slot's phase)
+            bool ok = true;
+            // the GeLU / GeLU' epilogue of one 32-column chunk of row `row`
+            // (x: fp32 sums; hw: H for GeLU'), stored from row0c
+            auto finish = [&](float (&x)[32], const uint32_t (&hw)[16], int row0c, int col0) {
+                if (EPI == zb::EPI_GELU_DUAL && args.bias) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (col0 + g * 8 >= args.Ng) break;
+                        const uint4 b = *reinterpret_cast<const uint4*>(args.bias + col0 + g * 8);
+                        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 f2 = unpack_bf16x2(bw[i]);
+                            x[g * 8 + 2 * i] += f2.x;
+                            x[g * 8 + 2 * i + 1] += f2.y;
+                        }
+                    }
+                }
+                if (EPI == zb::EPI_GELU_BWD) {
+                    if (args.act == ZB_ACT_GELU_TANH)
+                        gelu_grad_mul<true, 32>(x, hw);
+                    else
+                        gelu_grad_mul<false, 32>(x, hw);
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+                uint32_t stg = stg0 + flip * E::BOX;
+                flip ^= 1u;
+                staging_acquire(lane);
+                stage_row64(stg, lane, w);
+                staging_release<false>(&tmO0, stg, lane, col0, row0c, pol_out);
+                if (EPI == zb::EPI_GELU_DUAL) {
+                    if (args.act == ZB_ACT_GELU_TANH)
+                        gelu_pack<true, 32>(x, w);
+                    else
+                        gelu_pack<false, 32>(x, w);
+                    stg = stg0 + flip * E::BOX;
+                    flip ^= 1u;
+                    staging_acquire(lane);
+                    stage_row64(stg, lane, w);
+                    staging_release<false>(&tmO1, stg, lane, col0, row0c, pol_out);
+                }
+            };
+            for (int tile = cluster; tile < num_tiles && ok; tile += clusters, ++local) {
+                const uint32_t buf = local & 1u;
+                const uint32_t tr = local >> 1;
+                int mb, nb;
+                locate(tile, mb, nb);
+                const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
+                const int n0 = nb * BN;
+                if (!reader && EPI == zb::EPI_GELU_BWD) {
+                    // warm L2 with this warp's parts of its own and its partner's rows of H
+                    const int ncols = min(E::COLS, args.Ng - n0 - c_lo);
+                    const int r_own = m0 + q * 32 + lane, r_hand = m0 + (q & 1) * 32 + lane;
+                    if (ncols > 0 && r_own < args.Mg)
+                        zbp::prefetch_l2(args.aux + static_cast<long long>(r_own) * args.ldaux + n0 + c_lo,
+                                         static_cast<uint32_t>(ncols) * 2u);
+                    if (ncols > 0 && r_hand < args.Mg)
+                        zbp::prefetch_l2(args.aux + static_cast<long long>(r_hand) * args.ldaux + n0 + c_lo,
+                                         static_cast<uint32_t>(ncols) * 2u);
+                }
+                if (!wait_bar<PAIR>(zbp::smem_u32(&ctl->tfull[buf]), tr & 1u, abort_flag, args.err,
+                                    ERR_WAIT_EPI, WAIT_LIMIT_NS, true))
+                    break;
+                zbp::tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
+                if (reader) {
+#pragma unroll 1
+                    for (int c = 0; c < CH; ++c, ++k) {
+                        if (!wait_bar<false>(zbp::smem_u32(&ctl->hempty[pr]), (k & 1u) ^ 1u, abort_flag,
+                                             args.err, ERR_WAIT_EPI, WAIT_LIMIT_NS, true)) {
+                            ok = false;
+                            break;
+                        }
+                        uint32_t v[32];
+                        zbp::tmem_ld_32x32b_x32(taddr + c_lo + c * 32, v);
+                        zbp::tmem_ld_wait();
+                        stage_row(slot, lane, v);  // one 128-byte row per lane, 128-byte swizzle
+                        __syncwarp();
+                        if (lane == 0) zbp::mbar_arrive(zbp::smem_u32(&ctl->hfull[pr]));
+                    }
+                } else {
+                    const int row0_own = m0 + q * 32, row0_hand = m0 + (q & 1) * 32;
+#pragma unroll 1
+                    for (int c = 0; c < CH && ok; ++c, ++k) {
+                        const int col0 = n0 + c_lo + c * 32;
+                        // own chunk, from TMEM
+                        {
+                            uint32_t hw[16];
+                            if (EPI == zb::EPI_GELU_BWD) load_h32(args, row0_own + lane, col0, hw);
+                            uint32_t v[32];
+                            zbp::tmem_ld_32x32b_x32(taddr + c_lo + c * 32, v);
+                            zbp::tmem_ld_wait();
+                            float x[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
+                            if (row0_own < args.Mg && col0 < args.Ng) finish(x, hw, row0_own, col0);
+                        }
+                        // the partner's chunk, from its slot
+                        {
+                            uint32_t hw[16];
+                            if (EPI == zb::EPI_GELU_BWD) load_h32(args, row0_hand + lane, col0, hw);
+                            if (!wait_bar<false>(zbp::smem_u32(&ctl->hfull[pr]), k & 1u, abort_flag,
+                                                 args.err, ERR_WAIT_EPI, WAIT_LIMIT_NS, true)) {
+                                ok = false;
+                                break;
+                            }
+                            float x[32];
+                            const uint32_t rowa = slot + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 f = zbp::ld_shared_v4(rowa + (static_cast<uint32_t>(j ^ (lane & 7)) << 4));
+                                x[4 * j] = f.x;
+                                x[4 * j + 1] = f.y;
+                                x[4 * j + 2] = f.z;
+                                x[4 * j + 3] = f.w;
+                            }
+                            __syncwarp();
+                            if (lane == 0) zbp::mbar_arrive(zbp::smem_u32(&ctl->hempty[pr]));
+                            if (row0_hand < args.Mg && col0 < args.Ng) finish(x, hw, row0_hand, col0);
+                        }
+                    }
+                }
+                if (!ok) break;
+                zbp::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t te = zbp::smem_u32(&ctl->tempty[buf]);
+                    if (PAIR)
+                        zbp::mbar_arrive_cluster(zbp::mapa_shared(te, 0));
+                    else
+                        zbp::mbar_arrive(te);
+                }
+            }
+            // the staging buffers must not be released while a bulk store reads them
+            if (lane == 0) zbp::bulk_wait<0>();
+            __syncwarp();
         }
     } else {
         // ---------------------------------------------------- epilogue
@@ -1141,9 +1330,9 @@ struct Maps {
 };
 
 // Persistent grid size in CTAs for a CTA-group shape (co-resident clusters x CG).
-template <int EPI, int A_MN, int B_MN, int CG>
+template <int EPI, int A_MN, int B_MN, int CG, int HAND>
 zb_status configure(int* max_ctas) {
-    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG>;
+    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG, HAND>;
     // per device; a first call racing another computes the same value
     static std::atomic<int> cached[64];
     int dev = 0;
@@ -1183,7 +1372,7 @@ zb_status configure(int* max_ctas) {
 // Co-resident clusters of `ks` one-tile CTAs (split K), per device.
 template <int EPI, int A_MN, int B_MN>
 int split_clusters(int ks) {
-    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, 1>;
+    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, 1, 0>;
     static std::atomic<int> cached[64][4];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1211,11 +1400,11 @@ int split_clusters(int ks) {
     return cached[dev][slot].load(std::memory_order_relaxed);
 }
 
-template <int EPI, int A_MN, int B_MN, int CG>
+template <int EPI, int A_MN, int B_MN, int CG, int HAND>
 zb_status launch(const Maps& mp, EpiArgs ea, long long tiles, cudaStream_t st, bool pdl) {
-    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG>;
+    auto kern = zb_gemm_bf16_tc_kernel<EPI, A_MN, B_MN, CG, HAND>;
     int max_ctas = 0;
-    zb_status s = configure<EPI, A_MN, B_MN, CG>(&max_ctas);
+    zb_status s = configure<EPI, A_MN, B_MN, CG, HAND>(&max_ctas);
     if (s != ZB_OK) return s;
     // a split pays only while every cluster of its grid is resident at once
     // (one tile each; a second wave of clusters would double the time)
@@ -1253,25 +1442,39 @@ zb_status launch(const Maps& mp, EpiArgs ea, long long tiles, cudaStream_t st, b
     return ZB_OK;
 }
 
-template <int EPI, int CG>
+template <int EPI, int CG, int HAND = 0>
 zb_status dispatch_major(int a_mn, int b_mn, const Maps& mp, const EpiArgs& ea, long long tiles,
                          cudaStream_t st, bool pdl) {
-    if (!a_mn && !b_mn) return launch<EPI, 0, 0, CG>(mp, ea, tiles, st, pdl);
-    if (!a_mn && b_mn) return launch<EPI, 0, 1, CG>(mp, ea, tiles, st, pdl);
-    if (a_mn && !b_mn) return launch<EPI, 1, 0, CG>(mp, ea, tiles, st, pdl);
-    return launch<EPI, 1, 1, CG>(mp, ea, tiles, st, pdl);
+    if (!a_mn && !b_mn) return launch<EPI, 0, 0, CG, HAND>(mp, ea, tiles, st, pdl);
+    if (!a_mn && b_mn) return launch<EPI, 0, 1, CG, HAND>(mp, ea, tiles, st, pdl);
+    if (a_mn && !b_mn) return launch<EPI, 1, 0, CG, HAND>(mp, ea, tiles, st, pdl);
+    return launch<EPI, 1, 1, CG, HAND>(mp, ea, tiles, st, pdl);
+}
+
+// The hand-off epilogue (GeLU / GeLU' on CTA pairs): only where a tile's K
+// loop outlasts the math warps' doubled epilogue share (K >= 64 blocks).
+// ZB_GEMM_HANDOFF=0 in the environment turns it off.
+bool use_handoff(const zb::GemmBf16& g) {
+    static const bool on = [] {
+        const char* v = std::getenv("ZB_GEMM_HANDOFF");
+        return !(v && v[0] == '0');
+    }();
+    return on && (g.Kg + BK - 1) / BK >= 64;
 }
 
 template <int CG>
 zb_status dispatch(const zb::GemmBf16& g, const Maps& mp, const EpiArgs& ea, long long tiles,
                    cudaStream_t st) {
     const bool pdl = g.allow_pdl != 0;
+    const bool hand = CG == 2 && use_handoff(g);
     switch (g.epi) {
         case zb::EPI_STORE_BF16:
             return dispatch_major<zb::EPI_STORE_BF16, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
         case zb::EPI_GELU_DUAL:
+            if (hand) return dispatch_major<zb::EPI_GELU_DUAL, 2, 1>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
             return dispatch_major<zb::EPI_GELU_DUAL, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
         case zb::EPI_GELU_BWD:
+            if (hand) return dispatch_major<zb::EPI_GELU_BWD, 2, 1>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
             return dispatch_major<zb::EPI_GELU_BWD, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
         case zb::EPI_F32: return dispatch_major<zb::EPI_F32, CG>(g.a_mn, g.b_mn, mp, ea, tiles, st, pdl);
         default: return zb::fail(ZB_ERR_INVALID_ARG, "unknown epilogue");

@@ -8,7 +8,8 @@ turns it on inside every replay lane; the setting is read once per process,
 so each mode runs in a fresh process on the same seeded inputs: single passes
 (with and without split K) and replays on one lane, on an F/B lane beside a W
 lane, on four stage lanes and on an F, a B and a W lane per stage must give
-the same bits in every mode.  And a
+the same bits in every mode (and long-K passes with and without the GeLU
+epilogues' hand-off between warps).  And a
 process whose first library calls are made inside a CUDA graph capture (the
 split-K occupancy query and the programmatic launches among them) replays
 the graph to the bits of the same passes run eagerly.
@@ -65,6 +66,24 @@ def _child(out_path):
         sync(zb)
         for k, v in dict(H=H, A=A, Y=Y, dH=dH, dX=dX, dW1=dW1, dW2=dW2, db1=db1, db2=db2).items():
             res[f"pass{M}_{k}"] = _bits(v)
+    # long K (>= 64 blocks of 64) on CTA pairs: the GeLU and GeLU' epilogues
+    # hand raw accumulator chunks from one warp to another (ragged edges,
+    # bias, both activations)
+    for M, h, f, act, bias in ((520, 4104, 1048, zb.ZB_ACT_GELU_ERF, True),
+                               (392, 4096, 776, zb.ZB_ACT_GELU_TANH, False)):
+        stages, X0, dY = I.pipeline_draws(1, 1, M, h, f, seed=M + h, bias=True)
+        st = stages[0]
+        X, G = dev_bf16(X0[0]), dev_bf16(dY[0])
+        W1, W2 = dev_bf16(st.W1), dev_bf16(st.W2)
+        b1, b2 = (dev_bf16(st.b1), dev_bf16(st.b2)) if bias else (None, None)
+        blk = zb.make_block(M, h, f, act=act, has_bias=bias, split_k=False)
+        H, A, Y = empty_bf16(M, f), empty_bf16(M, f), empty_bf16(M, h)
+        zb.zb_forward(blk, X, W1, W2, b1, b2, H, A, Y)
+        dH, dX = empty_bf16(M, f), empty_bf16(M, h)
+        zb.zb_backward_input(blk, G, W1, W2, H, dH, dX)
+        sync(zb)
+        for k, v in dict(H=H, A=A, Y=Y, dH=dH, dX=dX).items():
+            res[f"longk{M}_{k}"] = _bits(v)
     # replays: one lane, F/B lane + W lane (one stage), four stage lanes
     for name, P, m, streams, kind in (("serial", 2, 4, 1, "ZBH1"), ("wlane", 1, 6, 2, "ZBH2"),
                                       ("stages", 4, 8, 4, "ZBH1"), ("fbw", 4, 8, 12, "ZBH2")):
@@ -96,11 +115,14 @@ def _child(out_path):
 # Each mode: environment settings of a fresh process.  The L2 eviction
 # priorities of the GEMM's copies (ZB_GEMM_L2_HINTS=0 turns them off) only
 # decide where data sits in L2, the W pass's paced reduce-adds only decide
-# when each is issued, and its two GEMMs in one grouped launch
-# (ZB_GEMM_GROUP_W=0: two launches) compute every tile as before: none may
-# change a bit either.
+# when each is issued, its two GEMMs in one grouped launch
+# (ZB_GEMM_GROUP_W=0: two launches) compute every tile as before, and the
+# long-K GeLU epilogues' hand-off (ZB_GEMM_HANDOFF=0: every warp does its
+# own rows) only moves the same fp32 sums between warps: none may change a
+# bit either.
 MODES = {"default": {}, "pdl0": {"ZB_GEMM_PDL": "0"}, "pdl1": {"ZB_GEMM_PDL": "1"},
-         "nohints": {"ZB_GEMM_L2_HINTS": "0"}, "twolaunchw": {"ZB_GEMM_GROUP_W": "0"}}
+         "nohints": {"ZB_GEMM_L2_HINTS": "0"}, "twolaunchw": {"ZB_GEMM_GROUP_W": "0"},
+         "nohandoff": {"ZB_GEMM_HANDOFF": "0"}}
 
 
 def test_launch_modes_change_no_bits(tmp_path):
@@ -112,7 +134,7 @@ def test_launch_modes_change_no_bits(tmp_path):
     for mode, extra in MODES.items():
         out = str(tmp_path / f"mode_{mode}.npz")
         env = dict(os.environ)
-        for k in ("ZB_GEMM_PDL", "ZB_GEMM_L2_HINTS", "ZB_GEMM_GROUP_W"):
+        for k in ("ZB_GEMM_PDL", "ZB_GEMM_L2_HINTS", "ZB_GEMM_GROUP_W", "ZB_GEMM_HANDOFF"):
             env.pop(k, None)
         env.update(extra)
         code = f"import tests.test_gpu_launch_modes as t; t._child({out!r})"
