@@ -66,7 +66,7 @@ def _peaks():
 
 def _gemm_source_sha():
     h = hashlib.sha256()
-    for n in ("gemm_tc.cu", "ptx.cuh"):
+    for n in ("gemm_tc.cu", "gemm_core.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "split_backward_gemms_gb300", "csrc", n), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -461,7 +461,7 @@ def make_ops(zb, sched, Pl, m, multi):
     return ops
 
 
-def setup_workload(zb, dev, name, schedule=None, streams=0, seed=1000):
+def setup_workload(zb, dev, name, schedule=None, streams=0, seed=1000, executor="streams"):
     """Seeded synthetic weights (N(0, 0.02)), inputs and last-stage gradients
     (N(0, 1)) in HBM, the op list and a planned workspace."""
     import torch
@@ -500,8 +500,9 @@ def setup_workload(zb, dev, name, schedule=None, streams=0, seed=1000):
     # stage, 1008-1069 with a W lane too, 1089 with separate F and B lanes);
     # a one-stage replay puts its W passes on a second stream
     n_streams = streams if streams > 0 else (min(3 * w.P, 12) if w.multi else 2)
+    w.executor = executor
     w.pl = zb.make_pipeline(w.P, m, w.blk, timing=True, streams=n_streams, chunks=w.chunks,
-                            layout=w.sched if w.chunks > 1 else zb.ZB_LAYOUT_CYCLIC)
+                            layout=w.sched if w.chunks > 1 else zb.ZB_LAYOUT_CYCLIC, executor=executor)
     w.need, w.peak_live = zb.zb_schedule_workspace_size(w.pl, w.ops)
     w.ws_t = torch.empty(max(w.need, 256), dtype=torch.uint8, device=dev)
     w.ops_c = zb.ops_array(w.ops)
@@ -556,13 +557,17 @@ def time_workload(zb, dev, w, steps, warmup, use_graph=True):
 def other_workloads(zb, dev, steps, warmup):
     """The other configurations in the same run, each as its own short
     timed region: the P=4, h=1024 pipeline under 1F1B (fused backward), under
-    ZB-H1 and ZB-H2 (split backward, W lanes) and under the heuristic ZB-2p,
-    same streams and graphs, and the h=4096 one-stage ZB-H1 step."""
+    ZB-H1 and ZB-H2 (split backward, W lanes), under the heuristic ZB-2p and
+    the two-chunk orderings, same streams and graphs, and the h=4096
+    one-stage ZB-H1 step; then the same pipeline orderings and the h=4096
+    step with the persistent executor (one kernel per step)."""
     import torch
     out = {}
-    for name, sched in (("c2", "1F1B"), ("c2", "ZBH1"), ("c2", "ZBH2"), ("c2", "ZB2P"), ("c2", "1F1B-I"),
-                        ("c2", "ZBV"), ("c3", "ZBH1")):
-        w = setup_workload(zb, dev, name, sched)
+    runs = [("c2", s, "streams") for s in ("1F1B", "ZBH1", "ZBH2", "ZB2P", "1F1B-I", "ZBV")] + [("c3", "ZBH1", "streams")]
+    runs += [("c2", s, "persistent") for s in ("1F1B", "ZBH1", "ZBH2", "ZB2P", "1F1B-I", "ZBV")]
+    runs += [("c3", "ZBH1", "persistent")]
+    for name, sched, executor in runs:
+        w = setup_workload(zb, dev, name, sched, executor=executor)
         r = time_workload(zb, dev, w, steps, warmup)
         if w.chunks > 1:
             wl = ("P=4 stages x 2 chunks = 8 MLP blocks h=1024 ffn=4096, microbatch 4x512 m=8, all "
@@ -571,9 +576,11 @@ def other_workloads(zb, dev, steps, warmup):
             wl = "P=4 stages h=1024 ffn=4096 microbatch 4x512 m=8, all stages on one GPU"
         else:
             wl = w.desc.split(",")[0]
-        r.update({"workload": wl, "schedule": sched, "streams": w.pl.streams, "unit": UNIT,
+        r.update({"workload": wl, "schedule": sched, "executor": executor, "unit": UNIT,
                   "pct_of_burst_peak": 100.0 * r["value"] / _peaks()["bf16"]})
-        out[f"{name}_{sched}"] = r
+        if executor == "streams":
+            r["streams"] = w.pl.streams
+        out[f"{name}_{sched}" + ("_persistent" if executor == "persistent" else "")] = r
         del w
         torch.cuda.empty_cache()
     return out
@@ -604,6 +611,9 @@ def main():
                          "read-back; hybrid: a graph holds the step and read-back, the uploads are "
                          "issued from the host on a copy stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--executor", choices=("streams", "persistent"), default="streams",
+                    help="streams: one launch per GEMM on stream lanes; persistent: every GEMM of the "
+                         "step in one persistent kernel ordered on the device")
     ap.add_argument("--streams", type=int, default=0,
                     help="streams of the replay (0: an F, a B and a W lane per stage for a "
                          "pipeline, 3P <= 12; a one-stage replay puts its W passes on a second stream)")
@@ -651,7 +661,8 @@ def main():
         dist.barrier()
     from split_backward_gemms_gb300 import zb
 
-    wk = setup_workload(zb, dev, args.workload, args.schedule, args.streams, seed=1000 + rank)
+    wk = setup_workload(zb, dev, args.workload, args.schedule, args.streams, seed=1000 + rank,
+                        executor=args.executor)
     h, f, M, m, sched, Pl, desc = wk.h, wk.f, wk.M, wk.m, wk.sched, wk.Pl, wk.desc
     # P counts MLP blocks (stages x chunks): per-block work, weights, results
     multi, P, W, X0, dY = wk.multi, wk.L, wk.W, wk.X0, wk.dY
@@ -756,7 +767,8 @@ def main():
         avg_gemm_ms = ms_max / max(1, gemms)
     achieved = gemm_flops / (avg_gemm_ms / 1e3) / 1e12
     roof_peak = peaks["bf16_sustained"]
-    traffic = _profiled_traffic(args.workload)
+    # the recorded traffic is the one-launch kernels' (stream executor)
+    traffic = _profiled_traffic(args.workload) if args.executor == "streams" else None
 
     # ----------------------------------------------- projected P-stage pipeline
     # per-pass times measured above (executor CUDA events), fed to the
@@ -1058,7 +1070,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": desc, "h": h, "f": f, "M": M, "m": m, "P": wk.P, "chunks": wk.chunks,
-                       "schedule": sched, "list_from_P": Pl, "streams": pl.streams,
+                       "schedule": sched, "list_from_P": Pl, "streams": pl.streams, "executor": args.executor,
                        "cuda_graph": graph is not None,
                        "parallelism": "replicas" if ws > 1 else "single GPU",
                        "l2": l2_note},

@@ -181,6 +181,14 @@ typedef enum zb_schedule_kind {
  *           (stage i holds chunks i and 2p-i+1: summary §6 "ZB-V"). */
 typedef enum zb_layout { ZB_LAYOUT_CYCLIC = 0, ZB_LAYOUT_V = 1 } zb_layout;
 
+/* How zb_run_stage_schedule runs an op list's GEMMs (zb_pipeline.executor). */
+typedef enum zb_executor {
+    ZB_EXEC_STREAMS = 0,    /* one launch per GEMM, ordered by streams and
+                               events (zb_pipeline.streams)                  */
+    ZB_EXEC_PERSISTENT = 1  /* one persistent kernel for every GEMM of the
+                               list, ordered on the device                   */
+} zb_executor;
+
 /* Generate the one-GPU replay list of a handcrafted ordering for P stages and
  * m microbatches at equal pass times (T_F = T_B = T_W, no communication):
  *   1F1B : warm-up min(P-1-s, m) forwards, then F / fused BW alternation;
@@ -315,6 +323,27 @@ typedef struct zb_pipeline {
                                   then per virtual stage, in chain order     */
     int32_t layout;            /* zb_layout (V requires chunks = 2); ignored
                                   for one chunk                              */
+    int32_t executor;          /* zb_executor.  ZB_EXEC_PERSISTENT: one
+                                  persistent kernel on CTA pairs (every SM)
+                                  runs all GEMMs of the list; a GEMM's
+                                  tiles start once every earlier GEMM whose
+                                  buffers it reads or overwrites (or that
+                                  reads what it overwrites) has stored all
+                                  of its tiles, tracked by counters in the
+                                  workspace.  Same bits as the serial
+                                  replay.  bf16 blocks without bias only
+                                  (else ZB_ERR_UNSUPPORTED); `streams` is
+                                  ignored; OPT statistics follow the kernel
+                                  on `stream`; the workspace also holds the
+                                  kernel's tables (zb_schedule_workspace_size
+                                  counts them), written on `stream` by
+                                  small kernels before it.  Kernels of
+                                  other streams delay it (it waits for all
+                                  of its CTA pairs' SMs); its waits are
+                                  bounded like every device wait.  With
+                                  timing, total_ms and gemm_ms cover the
+                                  kernel and its table upload; the per-op
+                                  times are 0, n_gemm_launches is 1.     */
 } zb_pipeline;
 
 typedef struct zb_stage_params {

@@ -161,8 +161,15 @@ thread_local bool g_in_replay = false;
 // CTAs keep other stages' GEMMs off free SMs there (the P=4, h=1024 pipeline
 // on four streams: 956 -> 938 TF/s).
 thread_local bool g_pdl_lanes = true;
+// A persistent replay is being planned: GEMMs are recorded, not launched.
+thread_local std::vector<GemmBf16>* g_record = nullptr;
 
 zb_status run_gemm(const GemmBf16& g, void* stream, Recorder* rec) {
+    if (g_record) {
+        g_record->push_back(g);
+        g_record->back().second = nullptr;
+        return ZB_OK;
+    }
     if (g_gemm_counter) ++*g_gemm_counter;
     GemmBf16 h = g;
     // programmatic dependent launch where the lanes allow it, and with no
@@ -186,6 +193,7 @@ bool disjoint(const void* a, size_t na, const void* b, size_t nb) {
 int split_allowed(const zb_block& b) { return !g_in_replay && !(b.flags & ZB_BLOCK_NO_SPLIT_K); }
 
 zb_status run_gemm32(const GemmF32& g, void* stream, Recorder* rec) {
+    if (g_record) return fail(ZB_ERR_UNSUPPORTED, "fp32 GEMM in a persistent replay");
     if (g_gemm_counter) ++*g_gemm_counter;
     return timed(rec, true, [&] { return gemm_f32_simt(g, stream); });
 }
@@ -310,7 +318,7 @@ zb_status backward_weight_impl(const zb_block& b, const void* X, const void* A, 
         return !(v && v[0] == '0');
     }();
     zb_status s;
-    if (group_w && independent && gemm_bf16_cta_group(g5) == 2 && gemm_bf16_cta_group(g6) == 2) {
+    if (group_w && !g_record && independent && gemm_bf16_cta_group(g5) == 2 && gemm_bf16_cta_group(g6) == 2) {
         g5.second = &g6;
         s = run_gemm(g5, stream, rec);
     } else {
@@ -445,6 +453,129 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         return ws + static_cast<size_t>(plan.row_slots) * plan.row_bytes + static_cast<size_t>(slot) * plan.ffn_bytes;
     };
 
+    // one op's passes on `lane` (recorded instead of launched while a
+    // persistent replay is being planned)
+    std::vector<char> w_started(P, 0);
+    auto run_op = [&](size_t i, cudaStream_t lane, Recorder* recp) -> zb_status {
+        zb_status s = ZB_OK;
+        const zb_op& o = vop[i];
+        const int st = o.stage, j = static_cast<int>(o.micro);
+        const zb_stage_params& p = stages[st];
+        void* lane_v = static_cast<void*>(lane);
+        const void* X = st == 0 ? X0[j] : row_ptr(plan.at(st, j, BUF_X));
+        const void* dY = st == P - 1 ? dY_last[j] : row_ptr(plan.at(st, j, BUF_DY));
+        void* H = mlp ? ffn_ptr(plan.at(st, j, BUF_H)) : nullptr;
+        void* A = mlp ? ffn_ptr(plan.at(st, j, BUF_A)) : nullptr;
+        void* dH = mlp ? ffn_ptr(plan.at(st, j, BUF_DH)) : nullptr;
+        auto run_b = [&]() -> zb_status {
+            void* dX;
+            if (st > 0) dX = row_ptr(plan.at(st - 1, j, BUF_DY));
+            else dX = has_dx ? dX0_out[j] : row_ptr(plan.tmp_slot[i]);
+            return backward_input_impl(b, dY, p.W1, p.W2, H, dH, dX, lane_v, recp);
+        };
+        auto run_w = [&]() -> zb_status {
+            const int acc = (pl->zero_grads && !w_started[st]) ? 0 : 1;
+            w_started[st] = 1;
+            const void* Xw = X;
+            return backward_weight_impl(b, Xw, A, dH, dY, p.dW1, p.dW2, p.db1, p.db2, acc, lane_v, recp);
+        };
+        switch (o.kind) {
+            case ZB_OP_F: {
+                void* Y;
+                if (st < P - 1) Y = row_ptr(plan.at(st + 1, j, BUF_X));
+                else Y = has_y ? Y_last_out[j] : row_ptr(plan.tmp_slot[i]);
+                s = forward_impl(b, X, p.W1, p.W2, p.b1, p.b2, H, A, Y, lane_v, recp);
+                break;
+            }
+            case ZB_OP_B: s = run_b(); break;
+            case ZB_OP_W: s = run_w(); break;
+            case ZB_OP_BW:
+                s = run_b();
+                if (s == ZB_OK) s = run_w();
+                break;
+            case ZB_OP_OPT:
+                if (p.grad_stats) {
+                    const float* bufs[4];
+                    uint64_t counts[4];
+                    int nb = 0;
+                    const uint64_t hf = static_cast<uint64_t>(b.h) * static_cast<uint64_t>(b.f);
+                    bufs[nb] = p.dW1; counts[nb++] = hf;
+                    if (mlp) { bufs[nb] = p.dW2; counts[nb++] = hf; }
+                    if (b.has_bias) {
+                        bufs[nb] = p.db1; counts[nb++] = static_cast<uint64_t>(b.f);
+                        if (mlp) { bufs[nb] = p.db2; counts[nb++] = static_cast<uint64_t>(b.h); }
+                    }
+                    void* scratch = ws + plan.stats_offset + static_cast<size_t>(st) * plan.stats_bytes;
+                    s = timed(recp, false, [&] {
+                        return zb_grad_stats(bufs, counts, nb, p.grad_stats, scratch, plan.stats_bytes, lane_v);
+                    });
+                }
+                break;
+            default: break;
+        }
+        return s;
+    };
+
+
+    if (pl->executor == ZB_EXEC_PERSISTENT) {
+        // Every GEMM of the list in one persistent kernel on `stream`
+        // (replay_tc.cu), then the OPT ops' statistics in list order (an OPT
+        // follows all of its stage's W, so it reads the final gradients).
+        if (b.dtype != ZB_DT_BF16 || b.has_bias)
+            return fail(ZB_ERR_UNSUPPORTED, "the persistent executor replays bf16 blocks without bias");
+        size_t njobs = 0, ntiles = 0;
+        s = replay_count(b, vop.data(), n_ops, &njobs, &ntiles);
+        if (s != ZB_OK) return s;
+        const size_t toff = (plan.workspace_bytes + 255) & ~static_cast<size_t>(255);
+        const size_t tbytes = replay_table_bytes(njobs, ntiles);
+        if (!workspace) return fail(ZB_ERR_WORKSPACE, "workspace is NULL");
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(ZB_ERR_ALIGN, "workspace must be 256-byte aligned");
+        if (ws_bytes < toff + tbytes)
+            return fail(ZB_ERR_WORKSPACE, "workspace too small: need " + std::to_string(toff + tbytes) + " bytes");
+        cudaStream_t st0 = static_cast<cudaStream_t>(stream);
+        std::vector<GemmBf16> jobs;
+        g_record = &jobs;
+        g_in_replay = true;
+        for (size_t i = 0; i < n_ops && s == ZB_OK; ++i)
+            if (vop[i].kind != ZB_OP_OPT) s = run_op(i, st0, nullptr);
+        g_record = nullptr;
+        g_in_replay = false;
+        if (s != ZB_OK) return s;
+        if (jobs.size() != njobs) return fail(ZB_ERR_UNSUPPORTED, "persistent replay: GEMM count mismatch");
+        Recorder trec;  // the replay kernel (with its table upload) as one span
+        trec.st = st0;
+        trec.on = pl->timing != 0 && stats != nullptr;
+        s = event_pool(&trec.pool);
+        if (s != ZB_OK) return s;
+        s = timed(&trec, true, [&] { return replay_persistent(jobs, ws + toff, tbytes, stream, nullptr); });
+        if (s != ZB_OK) return s;
+        for (size_t i = 0; i < n_ops && s == ZB_OK; ++i)
+            if (vop[i].kind == ZB_OP_OPT) s = run_op(i, st0, nullptr);
+        if (s != ZB_OK) return s;
+        if (stats) {
+            stats->workspace_bytes = toff + tbytes;
+            stats->peak_live_bytes = plan.peak_live_bytes;
+            stats->n_ops = static_cast<uint32_t>(n_ops);
+            stats->n_gemm_launches = jobs.empty() ? 0u : 1u;
+            stats->total_ms = 0.0;
+            for (double& k : stats->kind_ms) k = 0.0;
+            stats->gemm_ms = 0.0;
+            if (trec.on && !trec.spans.empty()) {
+                const auto& sp = trec.spans.front();
+                cudaError_t e = cudaEventSynchronize((*trec.pool)[sp.b]);
+                if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("timing sync: ") + cudaGetErrorString(e));
+                float t = 0.f;
+                cudaEventElapsedTime(&t, (*trec.pool)[sp.a], (*trec.pool)[sp.b]);
+                stats->total_ms = stats->gemm_ms = static_cast<double>(t);
+            }
+            if (stats->op_ms)
+                for (size_t i = 0; i < n_ops; ++i) stats->op_ms[i] = 0.f;
+        }
+        clear_error();
+        return ZB_OK;
+    }
+    if (pl->executor != ZB_EXEC_STREAMS) return fail(ZB_ERR_INVALID_ARG, "unknown pipeline.executor");
+
     // Streams: ops of stage (device) d run on lanes[d % nsd]; lanes[0] is the
     // caller's stream.  With streams >= 2 P (at most 8) each stage's W and
     // OPT ops get a lane of their own (lanes[nsd + d]): a weight-gradient
@@ -509,15 +640,12 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
     g_gemm_counter = &gemms;
     g_in_replay = true;
     g_pdl_lanes = ns == 1 || (w_lanes && !micro_lanes && nsd == 1);
-    std::vector<char> w_started(P, 0);
     std::vector<int> last_w_op(P, -1);  // latest W / BW of each stage, for OPT
 
     for (size_t i = 0; i < n_ops && s == ZB_OK; ++i) {
         const zb_op& o = vop[i];  // stage = virtual stage of the chain
         const int st = o.stage, j = static_cast<int>(o.micro);
-        const zb_stage_params& p = stages[st];
         cudaStream_t lane = lanes[lane_of[i]];
-        void* lane_v = static_cast<void*>(lane);
         rec.st = lane;
         if (ns > 1) {
             // wait for producers and slot releases that ran on other lanes
@@ -545,57 +673,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
             if (s != ZB_OK) break;
         }
         op_span[i].first = rec.spans.size();
-        const void* X = st == 0 ? X0[j] : row_ptr(plan.at(st, j, BUF_X));
-        const void* dY = st == P - 1 ? dY_last[j] : row_ptr(plan.at(st, j, BUF_DY));
-        void* H = mlp ? ffn_ptr(plan.at(st, j, BUF_H)) : nullptr;
-        void* A = mlp ? ffn_ptr(plan.at(st, j, BUF_A)) : nullptr;
-        void* dH = mlp ? ffn_ptr(plan.at(st, j, BUF_DH)) : nullptr;
-        auto run_b = [&]() -> zb_status {
-            void* dX;
-            if (st > 0) dX = row_ptr(plan.at(st - 1, j, BUF_DY));
-            else dX = has_dx ? dX0_out[j] : row_ptr(plan.tmp_slot[i]);
-            return backward_input_impl(b, dY, p.W1, p.W2, H, dH, dX, lane_v, &rec);
-        };
-        auto run_w = [&]() -> zb_status {
-            const int acc = (pl->zero_grads && !w_started[st]) ? 0 : 1;
-            w_started[st] = 1;
-            const void* Xw = X;
-            return backward_weight_impl(b, Xw, A, dH, dY, p.dW1, p.dW2, p.db1, p.db2, acc, lane_v, &rec);
-        };
-        switch (o.kind) {
-            case ZB_OP_F: {
-                void* Y;
-                if (st < P - 1) Y = row_ptr(plan.at(st + 1, j, BUF_X));
-                else Y = has_y ? Y_last_out[j] : row_ptr(plan.tmp_slot[i]);
-                s = forward_impl(b, X, p.W1, p.W2, p.b1, p.b2, H, A, Y, lane_v, &rec);
-                break;
-            }
-            case ZB_OP_B: s = run_b(); break;
-            case ZB_OP_W: s = run_w(); break;
-            case ZB_OP_BW:
-                s = run_b();
-                if (s == ZB_OK) s = run_w();
-                break;
-            case ZB_OP_OPT:
-                if (p.grad_stats) {
-                    const float* bufs[4];
-                    uint64_t counts[4];
-                    int nb = 0;
-                    const uint64_t hf = static_cast<uint64_t>(b.h) * static_cast<uint64_t>(b.f);
-                    bufs[nb] = p.dW1; counts[nb++] = hf;
-                    if (mlp) { bufs[nb] = p.dW2; counts[nb++] = hf; }
-                    if (b.has_bias) {
-                        bufs[nb] = p.db1; counts[nb++] = static_cast<uint64_t>(b.f);
-                        if (mlp) { bufs[nb] = p.db2; counts[nb++] = static_cast<uint64_t>(b.h); }
-                    }
-                    void* scratch = ws + plan.stats_offset + static_cast<size_t>(st) * plan.stats_bytes;
-                    s = timed(&rec, false, [&] {
-                        return zb_grad_stats(bufs, counts, nb, p.grad_stats, scratch, plan.stats_bytes, lane_v);
-                    });
-                }
-                break;
-            default: break;
-        }
+        s = run_op(i, lane, &rec);
         op_span[i].second = rec.spans.size();
         if (o.kind == ZB_OP_W || o.kind == ZB_OP_BW) last_w_op[st] = static_cast<int>(i);
         if (ns > 1 && s == ZB_OK) {

@@ -609,6 +609,12 @@ extern "C" zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_
     // sizing assumes no caller output buffers (the largest arena)
     st = zb::plan_arena(chain, vops.data(), n_ops, false, false, &plan);
     *bytes = plan.workspace_bytes;
+    if (st == ZB_OK && pl->executor == ZB_EXEC_PERSISTENT) {
+        // the persistent kernel's tables follow the arena (256-byte aligned)
+        size_t njobs = 0, ntiles = 0;
+        st = zb::replay_count(pl->blk, vops.data(), n_ops, &njobs, &ntiles);
+        *bytes = ((plan.workspace_bytes + 255) & ~static_cast<size_t>(255)) + zb::replay_table_bytes(njobs, ntiles);
+    }
     if (peak_live_bytes) *peak_live_bytes = plan.peak_live_bytes;
     if (st != ZB_OK) return st;
     zb::clear_error();

@@ -65,6 +65,21 @@ zb_status gemm_bf16_tc(const GemmBf16& g, void* stream);
 // The CTA group gemm_bf16_tc would choose for g (1 or 2).
 int gemm_bf16_cta_group(const GemmBf16& g);
 
+// Persistent replay (replay_tc.cu): every GEMM of an op list in one
+// persistent launch on CTA pairs, in the order the dependencies between the
+// GEMMs' byte ranges allow (jobs in list order; no grouped records).  The
+// tables go into `table` (256-byte aligned, replay_table_bytes bytes for
+// the list's GEMM and tile counts).
+struct ReplayInfo {
+    size_t jobs = 0, tiles = 0, maps = 0, deps = 0, pairs = 0, table_bytes = 0, upload_launches = 0;
+    double est_makespan_kb = 0.0;  // simulated makespan, in one K block's MMA time on a pair
+};
+zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size_t table_bytes, void* stream,
+                            ReplayInfo* info);
+// GEMMs and CTA-pair tiles an op list replays (for the table size).
+zb_status replay_count(const zb_block& b, const zb_op* ops, size_t n_ops, size_t* njobs, size_t* ntiles);
+size_t replay_table_bytes(size_t njobs, size_t ntiles);
+
 // fp32 FFMA GEMM (no TF32): C[m*ldc + n] (+)= sum_k A[m*sam + k*sak] * B[k*sbk + n*sbn]
 struct GemmF32 {
     int64_t Mg = 0, Ng = 0, Kg = 0;

@@ -47,6 +47,8 @@ ZB_SCHED_1F1B, ZB_SCHED_ZBH1, ZB_SCHED_ZBH2, ZB_SCHED_1F1B_I, ZB_SCHED_ZBV = ran
 SCHED_IDS = {"1F1B": ZB_SCHED_1F1B, "ZBH1": ZB_SCHED_ZBH1, "ZBH2": ZB_SCHED_ZBH2,
              "1F1B-I": ZB_SCHED_1F1B_I, "ZBV": ZB_SCHED_ZBV}
 ZB_LAYOUT_CYCLIC, ZB_LAYOUT_V = range(2)
+ZB_EXEC_STREAMS, ZB_EXEC_PERSISTENT = range(2)
+EXECUTOR_OF = {"streams": ZB_EXEC_STREAMS, "persistent": ZB_EXEC_PERSISTENT}
 LAYOUT_OF = {"1F1B-I": ZB_LAYOUT_CYCLIC, "ZBV": ZB_LAYOUT_V}
 
 
@@ -63,7 +65,8 @@ class zb_op(C.Structure):
 class zb_pipeline(C.Structure):
     _fields_ = [("P", C.c_int32), ("m", C.c_int32), ("blk", zb_block),
                 ("mem_limit_bytes", C.c_uint64), ("zero_grads", C.c_int32), ("timing", C.c_int32),
-                ("streams", C.c_int32), ("chunks", C.c_int32), ("layout", C.c_int32)]
+                ("streams", C.c_int32), ("chunks", C.c_int32), ("layout", C.c_int32),
+                ("executor", C.c_int32)]
 
 
 class zb_stage_params(C.Structure):
@@ -367,11 +370,13 @@ def zb_selftest_wait_timeout(limit_ns: int, stream=None):
 
 
 def make_pipeline(P, m, blk, mem_limit_bytes=0, zero_grads=True, timing=False,
-                  streams=1, chunks=1, layout=ZB_LAYOUT_CYCLIC) -> zb_pipeline:
+                  streams=1, chunks=1, layout=ZB_LAYOUT_CYCLIC, executor=ZB_EXEC_STREAMS) -> zb_pipeline:
     if isinstance(layout, str):
         layout = LAYOUT_OF[layout]
+    if isinstance(executor, str):
+        executor = EXECUTOR_OF[executor]
     return zb_pipeline(P, m, blk, mem_limit_bytes, 1 if zero_grads else 0, 1 if timing else 0,
-                       int(streams), int(chunks), int(layout))
+                       int(streams), int(chunks), int(layout), int(executor))
 
 
 def zb_schedule_workspace_size(pl, ops):
