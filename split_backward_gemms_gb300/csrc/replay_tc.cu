@@ -70,15 +70,17 @@ static_assert(sizeof(RJob) == 128, "job record");
 
 // Per-tile trace record (ZB_REPLAY_TRACE=1): written at the end of the
 // caller's workspace.  entry and pair and the simulated start come from the
-// host; the times (global timer, ns) from the kernel: when the pair's
-// producer reached the tile, when its dependencies were complete, and when
-// the leader CTA's first epilogue warp signalled it.
+// host; the times (global timer, ns) from the kernel, all in the leader CTA:
+// when its producer reached the tile and when the tile's dependencies were
+// complete; when its MMA issuer had the accumulator and when it committed
+// the last K block; when its first epilogue warp had the accumulator, had
+// issued its last store, and signalled the tile.
 struct TraceRec {
     uint32_t entry, pair;
     int64_t sim_start;
-    uint64_t t_reach, t_ready, t_signal;
+    uint64_t t_reach, t_ready, t_mma0, t_mma1, t_epi0, t_epi1, t_signal;
 };
-static_assert(sizeof(TraceRec) == 40, "trace record");
+static_assert(sizeof(TraceRec) == 72, "trace record");
 
 // Up to PARAM_MAPS distinct tensor maps travel in the launch parameters
 // (the one-launch kernel's place for them); more stay in global memory.
@@ -375,6 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
                     break;
                 }
                 zbp::tc_fence_after();
+                if (rp.trace) rp.trace[e].t_mma0 = zbp::globaltimer_ns();
                 const uint32_t d_tmem = tmem_base + buf * ACC_COLS;
                 switch (majors) {
                     case 0: ok = mma_tile<0, 0>(ctl, smem, it, num_kb, d_tmem, abort_flag, abort_all, rp.err); break;
@@ -384,6 +387,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
                 }
                 if (!ok) break;
                 zbp::tc_commit_pair_multicast(zbp::smem_u32(&ctl->tfull[buf]), 0x3);
+                if (rp.trace) rp.trace[e].t_mma1 = zbp::globaltimer_ns();
             }
             // every MMA issued here completes before TMEM is released
             zbp::tc_commit_pair(zbp::smem_u32(&ctl->drain));
@@ -452,6 +456,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
                              WAIT_LIMIT_NS, true))
                 break;
             zbp::tc_fence_after();
+            const bool tr_epi = rp.trace != nullptr && leader && warp == 2 && lane == 0;
+            if (tr_epi) rp.trace[e].t_epi0 = zbp::globaltimer_ns();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
             if (epi == zb::EPI_F32) {
                 const bool pace = e + 1 < e_hi;
@@ -539,6 +545,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
                     }
                 }
             }
+            if (tr_epi) rp.trace[e].t_epi1 = zbp::globaltimer_ns();
             zbp::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -971,7 +978,8 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
         std::vector<TraceRec> tr(ntiles);
         size_t e = 0;
         for (int p = 0; p < npairs; ++p)
-            for (size_t k = 0; k < lists[p].size(); ++k, ++e) tr[e] = TraceRec{lists[p][k], static_cast<uint32_t>(p), starts[p][k], 0, 0, 0};
+            for (size_t k = 0; k < lists[p].size(); ++k, ++e)
+                tr[e] = TraceRec{lists[p][k], static_cast<uint32_t>(p), starts[p][k], 0, 0, 0, 0, 0, 0, 0};
         cudaError_t te = cudaMemcpyAsync(trace, tr.data(), ntiles * sizeof(TraceRec), cudaMemcpyHostToDevice, st);
         if (te == cudaSuccess) te = cudaStreamSynchronize(st);
         if (te != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("trace setup: ") + cudaGetErrorString(te));
