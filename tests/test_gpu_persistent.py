@@ -8,8 +8,9 @@ tile is the one-launch kernel's tile and the accumulating weight-gradient
 GEMMs of a stage keep their list order, so outputs and gradients are the
 serial replay's bit for bit: handcrafted and heuristic orderings, one stage
 and several, ragged shapes and M below one 128-row block (a one-CTA tile in
-the serial replay), chunked (ZB-V) lists, gradient statistics at OPT,
-accumulation into existing gradients, and a CUDA graph.  The serial replay
+the serial replay), chunked (ZB-V and interleaved 1F1B) lists, both GeLU
+forms, gradient statistics at OPT, accumulation into existing gradients, the
+allocation-free entry point, and a CUDA graph.  The serial replay
 is checked against the fp64 oracle elsewhere; one case here is also
 compared with the rounding-emulating oracle chain directly.
 """
@@ -94,6 +95,9 @@ def _same_bits(a, b, stats=False):
 CASES = [
     # kind, P, m, M, h, f, chunks
     ("ZBH1", 4, 8, 512, 256, 1024, 1),
+    ("ZB1P", 4, 8, 512, 256, 1024, 1),
+    ("ZBH2", 8, 16, 256, 256, 512, 1),
+    ("1F1B-I", 2, 4, 512, 256, 1024, 2),  # two chunks per stage, cyclic
     ("ZBH2", 4, 8, 512, 256, 1024, 1),
     ("1F1B", 4, 8, 512, 256, 1024, 1),
     ("ZB2P", 4, 8, 512, 256, 1024, 1),
@@ -111,7 +115,7 @@ def test_persistent_replay_is_the_serial_replay(zb, kind, P, m, M, h, f, chunks)
     blk = zb.make_block(M, h, f)
     wts, X0, dY = _setup(L, m, M, h, f, seed=7 * P + m + M)
     ops = _ops(zb, kind, P, m, chunks)
-    extra = dict(chunks=chunks, layout="ZBV") if chunks > 1 else {}
+    extra = dict(chunks=chunks, layout=kind) if chunks > 1 else {}
     ref = _replay(zb, zb.make_pipeline(P, m, blk, **extra), wts, X0, dY, ops, M, h, f, stats_bufs=True)
     st = zb.zb_run_stats()
     got = _replay(zb, zb.make_pipeline(P, m, blk, executor="persistent", **extra), wts, X0, dY, ops, M, h, f,
@@ -122,6 +126,39 @@ def test_persistent_replay_is_the_serial_replay(zb, kind, P, m, M, h, f, chunks)
     got2 = _replay(zb, zb.make_pipeline(P, m, blk, executor="persistent", **extra), wts, X0, dY, ops, M, h, f,
                    stats_bufs=True)
     _same_bits(ref, got2)
+
+
+@pytest.mark.parametrize("act", ["tanh", "erf"])
+def test_persistent_replay_activation_forms(zb, act):
+    # the runtime-selected GeLU / GeLU' epilogues, both activation forms
+    P, m, M, h, f = 2, 4, 520, 264, 1048
+    blk = zb.make_block(M, h, f, act=zb.ZB_ACT_GELU_TANH if act == "tanh" else zb.ZB_ACT_GELU_ERF)
+    wts, X0, dY = _setup(P, m, M, h, f, seed=17)
+    ops = zb.zb_make_schedule("ZBH2", P, m)
+    ref = _replay(zb, zb.make_pipeline(P, m, blk), wts, X0, dY, ops, M, h, f)
+    got = _replay(zb, zb.make_pipeline(P, m, blk, executor="persistent"), wts, X0, dY, ops, M, h, f)
+    _same_bits(ref, got)
+
+
+def test_persistent_replay_without_workspace_argument(zb):
+    # the allocation-free entry point (library-owned static arena) with the
+    # persistent executor: its tables fit the static arena too
+    P, m, M, h, f = 2, 4, 256, 256, 1024
+    blk = zb.make_block(M, h, f)
+    wts, X0, dY = _setup(P, m, M, h, f, seed=23)
+    ops = zb.zb_make_schedule("ZBH1", P, m)
+    ref = _replay(zb, zb.make_pipeline(P, m, blk), wts, X0, dY, ops, M, h, f)
+    pl = zb.make_pipeline(P, m, blk, executor="persistent")
+    need, _ = zb.zb_schedule_workspace_size(pl, ops)
+    assert need <= zb.ZB_STATIC_ARENA_BYTES
+    stages = [dict(w, dW1=empty_f32(h, f), dW2=empty_f32(f, h)) for w in wts]
+    dX0 = [empty_bf16(M, h) for _ in range(m)]
+    Yl = [empty_bf16(M, h) for _ in range(m)]
+    st = zb.zb_run_stats()
+    zb.zb_run_stage_schedule_static(pl, stages, X0, dY, dX0, Yl, ops, st)
+    sync(zb)
+    assert st.n_gemm_launches == 1
+    _same_bits(ref, (stages, dX0, Yl))
 
 
 def test_persistent_replay_accumulates_into_existing_gradients(zb):
