@@ -385,6 +385,37 @@ typedef struct zb_run_stats {
 zb_status zb_schedule_workspace_size(const zb_pipeline* pl, const zb_op* ops, size_t n_ops,
                                      size_t* bytes, size_t* peak_live_bytes);
 
+/* The host plan of a persistent replay (zb_pipeline.executor =
+ * ZB_EXEC_PERSISTENT; `pl->executor` itself is ignored here), for inspection
+ * and tests; host only, no device is touched.  The op list is validated and
+ * its GEMMs recorded as zb_run_stage_schedule would run them, with every
+ * stage parameter, input and workspace buffer at a distinct stand-in
+ * address (no caller output buffers), for `pairs` CTA pairs (1..128; a
+ * GB300 has 76).  GEMMs are numbered in list order: an F op gives H = X W1
+ * (with A = GeLU(H)) then Y = A W2, a B op dH then dX, a W op dW2 then dW1,
+ * a BW op its B then its W (a single-linear block: one GEMM per pass).
+ *   info   counts: GEMMs, 256 x 256 tiles, dependency edges kept after the
+ *          transitive reduction, pairs, the simulated makespan in K blocks
+ *          of one pair, the priority rule (by_chain 1: longest chain of work
+ *          after the GEMM; 0: list order), the longest tile list of a pair.
+ *   edges  optional, 2 * (*n_edges) int32: (consumer, producer) GEMM index
+ *          pairs of the kept dependencies; *n_edges holds the capacity on
+ *          entry and the count on return (ZB_ERR_INVALID_ARG if the
+ *          capacity is smaller; n_edges NULL: edges not returned).
+ * Errors as zb_run_stage_schedule (list, shapes, bias: ZB_ERR_UNSUPPORTED),
+ * and ZB_ERR_UNSUPPORTED if the plan fails its deadlock-freedom check (every
+ * tile must start, in the simulation, after every tile of the GEMMs it
+ * depends on and after its pair's earlier tiles). */
+typedef struct zb_persistent_plan_info {
+    uint64_t gemms, tiles, deps, pairs;
+    double est_makespan_kblocks;
+    int32_t by_chain;
+    int32_t reserved;
+    uint64_t max_tiles_per_pair;
+} zb_persistent_plan_info;
+zb_status zb_persistent_plan(const zb_pipeline* pl, const zb_op* ops, size_t n_ops, int32_t pairs,
+                             zb_persistent_plan_info* info, int32_t* edges, size_t* n_edges);
+
 /* Replay an op list over P stages on one GPU.
  *   stages[L]       weights and fp32 gradient buffers per (virtual) stage,
  *                   in chain order; L = P, or chunks * P with chunks > 1;

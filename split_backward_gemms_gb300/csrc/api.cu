@@ -163,6 +163,12 @@ thread_local bool g_in_replay = false;
 thread_local bool g_pdl_lanes = true;
 // A persistent replay is being planned: GEMMs are recorded, not launched.
 thread_local std::vector<GemmBf16>* g_record = nullptr;
+// zb_persistent_plan: stop after the host plan (no device work at all).
+struct PlanOnly {
+    int pairs = 0;
+    ReplayPlan plan;
+};
+thread_local PlanOnly* g_plan_only = nullptr;
 
 zb_status run_gemm(const GemmBf16& g, void* stream, Recorder* rec) {
     if (g_record) {
@@ -339,6 +345,66 @@ zb_status backward_weight_impl(const zb_block& b, const void* X, const void* A, 
 using namespace zb;
 
 extern "C" const char* zb_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" zb_status zb_persistent_plan(const zb_pipeline* pl, const zb_op* ops, size_t n_ops, int32_t pairs,
+                                        zb_persistent_plan_info* info, int32_t* edges, size_t* n_edges) {
+    if (!pl || !info) return fail(ZB_ERR_INVALID_ARG, "pipeline or info is NULL");
+    if (pairs < 1 || pairs > 128) return fail(ZB_ERR_INVALID_ARG, "pairs must be in [1, 128]");
+    zb_pipeline p = *pl;
+    p.executor = ZB_EXEC_PERSISTENT;
+    p.timing = 0;
+    const int L = p.P * (p.chunks > 1 ? p.chunks : 1);
+    if (p.P < 1 || p.m < 1 || L > 4096 || p.m > (1 << 20)) return fail(ZB_ERR_SHAPE, "P and m out of range");
+    // distinct, aligned stand-in addresses for every buffer of the call (never
+    // dereferenced): 2^36 bytes apart, far above the workspace's
+    const uintptr_t unit = uintptr_t(1) << 36;
+    uintptr_t next = uintptr_t(1) << 44;
+    auto fake = [&]() { const uintptr_t a = next; next += unit; return reinterpret_cast<void*>(a); };
+    std::vector<zb_stage_params> st(L);
+    for (auto& sp : st) {
+        sp.W1 = fake(); sp.W2 = fake(); sp.b1 = fake(); sp.b2 = fake();
+        sp.dW1 = static_cast<float*>(fake()); sp.dW2 = static_cast<float*>(fake());
+        sp.db1 = static_cast<float*>(fake()); sp.db2 = static_cast<float*>(fake());
+        sp.grad_stats = nullptr;
+    }
+    std::vector<const void*> x0(p.m), dy(p.m);
+    for (int j = 0; j < p.m; ++j) {
+        x0[j] = fake();
+        dy[j] = fake();
+    }
+    PlanOnly po;
+    po.pairs = pairs;
+    g_plan_only = &po;
+    zb_status s = zb_run_stage_schedule(&p, st.data(), x0.data(), dy.data(), nullptr, nullptr, ops, n_ops,
+                                        reinterpret_cast<void*>(uintptr_t(1) << 40), SIZE_MAX / 4, nullptr, nullptr);
+    g_plan_only = nullptr;
+    if (s != ZB_OK) return s;
+    const ReplayPlan& pp = po.plan;
+    info->gemms = pp.tiles.size();
+    info->tiles = pp.ntiles;
+    info->deps = pp.ndeps;
+    info->pairs = static_cast<uint64_t>(pairs);
+    info->est_makespan_kblocks = static_cast<double>(pp.makespan) / 16.0;
+    info->by_chain = pp.by_level ? 1 : 0;
+    info->max_tiles_per_pair = 0;
+    for (const auto& l : pp.lists) info->max_tiles_per_pair = std::max<uint64_t>(info->max_tiles_per_pair, l.size());
+    if (n_edges) {
+        const size_t cap = *n_edges;
+        size_t k = 0;
+        for (size_t j = 0; j < pp.deps.size(); ++j)
+            for (int d : pp.deps[j]) {
+                if (edges && k < cap) {
+                    edges[2 * k] = static_cast<int32_t>(j);
+                    edges[2 * k + 1] = d;
+                }
+                ++k;
+            }
+        *n_edges = k;
+        if (edges && k > cap) return fail(ZB_ERR_INVALID_ARG, "edges: capacity too small");
+    }
+    clear_error();
+    return ZB_OK;
+}
 
 extern "C" const char* zb_version(void) { return "zb-gb300 0.1 sm_103a"; }
 
@@ -542,6 +608,7 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         g_in_replay = false;
         if (s != ZB_OK) return s;
         if (jobs.size() != njobs) return fail(ZB_ERR_UNSUPPORTED, "persistent replay: GEMM count mismatch");
+        if (g_plan_only) return plan_replay(jobs, g_plan_only->pairs, &g_plan_only->plan);
         Recorder trec;  // the replay kernel (with its table upload) as one span
         trec.st = st0;
         trec.on = pl->timing != 0 && stats != nullptr;

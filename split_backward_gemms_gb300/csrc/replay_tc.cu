@@ -707,40 +707,19 @@ zb_status replay_count(const zb_block& b, const zb_op* ops, size_t n_ops, size_t
     return ZB_OK;
 }
 
-zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size_t table_bytes, void* stream,
-                            ReplayInfo* info) {
+// The host plan of a persistent replay: every GEMM's tiles, its
+// dependencies (transitive reduction of the byte-range conflicts), the tile
+// lists of the CTA pairs from the list-scheduling simulation, and the check
+// that the order cannot deadlock.  No device access.
+zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan* plan) {
     const size_t nj = jobs.size();
-    if (info) *info = ReplayInfo{};
+    *plan = ReplayPlan{};
     if (nj == 0) return ZB_OK;
     if (nj > MAX_JOBS) return fail(ZB_ERR_UNSUPPORTED, "persistent replay: too many GEMMs in one op list");
-    const int npairs = replay_pairs();
-    if (npairs <= 0) return fail(ZB_ERR_UNSUPPORTED, "persistent replay: no co-resident CTA pairs");
-    unsigned int* err = device_error_word();
-    if (!err) return ZB_ERR_CUDA;
+    if (npairs <= 0 || npairs > MAX_PAIRS) return fail(ZB_ERR_INVALID_ARG, "persistent replay: pair count");
     auto mis = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
-
-    // -------------------------------------------- tensor maps, job records
-    std::vector<CUtensorMap> maps;
-    std::unordered_map<std::string, int> map_index;
-    std::string why;
-    auto add_map = [&](int* idx, const void* base, bool f32, uint64_t inner, uint64_t outer, uint64_t ld,
-                       uint32_t bi, uint32_t bo, CUtensorMapSwizzle sw) -> bool {
-        CUtensorMap m;
-        std::memset(&m, 0, sizeof(m));
-        if (!make_map(&m, base, f32, inner, outer, ld, bi, bo, &why, sw)) return false;
-        const std::string key(reinterpret_cast<const char*>(&m), sizeof(m));
-        auto f = map_index.find(key);
-        if (f != map_index.end()) {
-            *idx = f->second;
-            return true;
-        }
-        *idx = static_cast<int>(maps.size());
-        maps.push_back(m);
-        map_index.emplace(key, *idx);
-        return true;
-    };
-    std::vector<RJob> rj(nj);
-    std::vector<long long> tiles(nj);
+    std::vector<long long>& tiles = plan->tiles;
+    tiles.assign(nj, 0);
     std::vector<std::vector<Range>> reads(nj), writes(nj);
     size_t ntiles = 0;
     for (size_t j = 0; j < nj; ++j) {
@@ -757,49 +736,12 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
         if (g.epi == EPI_GELU_DUAL && !g.out1) return fail(ZB_ERR_INVALID_ARG, "GeLU dual store needs out1");
         if (g.epi == EPI_GELU_BWD && !g.aux) return fail(ZB_ERR_INVALID_ARG, "GeLU' epilogue needs H");
         if (g.epi == EPI_F32 && g.bias) return fail(ZB_ERR_UNSUPPORTED, "persistent replay: bias of an fp32 GEMM");
-        RJob& J = rj[j];
-        std::memset(&J, 0, sizeof(J));
-        J.Mg = static_cast<int>(g.Mg);
-        J.Ng = static_cast<int>(g.Ng);
-        J.Kg = static_cast<int>(g.Kg);
-        J.epi = g.epi;
-        J.a_mn = g.a_mn;
-        J.b_mn = g.b_mn;
-        J.act = g.act;
-        J.accumulate = g.accumulate;
-        J.tiles_m = static_cast<int>((g.Mg + 2 * BM - 1) / (2 * BM));
-        J.tiles_n = static_cast<int>((g.Ng + BN - 1) / BN);
-        tiles[j] = static_cast<long long>(J.tiles_m) * J.tiles_n;
+        const bool f32_out = g.epi == EPI_F32;
+        if (f32_out && (g.ld0 % 4)) return fail(ZB_ERR_ALIGN, "fp32 output leading dimension must be a multiple of 4");
+        tiles[j] = pair_tiles_of(g.Mg, g.Ng);
         if (tiles[j] > static_cast<long long>(ENTRY_TILE_MASK) + 1)
             return fail(ZB_ERR_UNSUPPORTED, "persistent replay: too many tiles in one GEMM");
         ntiles += static_cast<size_t>(tiles[j]);
-        J.ldaux = g.ldaux;
-        J.aux = static_cast<const __nv_bfloat16*>(g.aux);
-        J.bias = static_cast<const __nv_bfloat16*>(g.bias);
-        EpiArgs ea;
-        choose_l2_hints(g, 2, &ea);
-        J.hint_a = ea.hint_a;
-        J.hint_b = ea.hint_b;
-        J.hint_out = ea.hint_out;
-        bool ok;
-        if (g.a_mn)
-            ok = add_map(&J.map_a, g.A, false, g.Mg, g.Kg, g.lda, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
-        else
-            ok = add_map(&J.map_a, g.A, false, g.Kg, g.Mg, g.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
-        if (ok) {
-            if (g.b_mn)
-                ok = add_map(&J.map_b, g.B, false, g.Ng, g.Kg, g.ldb, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
-            else
-                ok = add_map(&J.map_b, g.B, false, g.Kg, g.Ng, g.ldb, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
-        }
-        const bool f32_out = g.epi == EPI_F32;
-        if (f32_out && (g.ld0 % 4)) return fail(ZB_ERR_ALIGN, "fp32 output leading dimension must be a multiple of 4");
-        const CUtensorMapSwizzle osw = f32_out ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        if (ok) ok = add_map(&J.map_o0, g.out0, f32_out, g.Ng, g.Mg, g.ld0, 32, 32, osw);
-        J.map_o1 = J.map_o0;
-        if (ok && g.epi == EPI_GELU_DUAL) ok = add_map(&J.map_o1, g.out1, false, g.Ng, g.Mg, g.ld1, 32, 32, osw);
-        if (!ok) return fail(ZB_ERR_CUDA, why);
-        J.target = static_cast<uint32_t>(tiles[j]) * SIGNALS_PER_TILE;
         // byte ranges read and written
         reads[j].push_back(g.a_mn ? range_of(g.A, g.Kg, g.Mg, g.lda, 2) : range_of(g.A, g.Mg, g.Kg, g.lda, 2));
         reads[j].push_back(g.b_mn ? range_of(g.B, g.Kg, g.Ng, g.ldb, 2) : range_of(g.B, g.Ng, g.Kg, g.ldb, 2));
@@ -809,6 +751,7 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
         if (f32_out && g.accumulate) reads[j].push_back(writes[j].back());
         if (g.epi == EPI_GELU_DUAL) writes[j].push_back(range_of(g.out1, g.Mg, g.Ng, g.ld1, 2));
     }
+    plan->ntiles = ntiles;
 
     // -------------------------------------------- dependencies
     // j depends on i < j when i writes what j reads or writes, or reads what
@@ -816,7 +759,8 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
     // reduction over the closure bitsets)
     const size_t words = (nj + 63) / 64;
     std::vector<uint64_t> closure(nj * words, 0);
-    std::vector<std::vector<int>> deps(nj);
+    std::vector<std::vector<int>>& deps = plan->deps;
+    deps.assign(nj, {});
     size_t ndeps = 0;
     for (size_t j = 0; j < nj; ++j) {
         std::vector<uint64_t> cover(words, 0);
@@ -839,8 +783,6 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
         for (size_t w = 0; w < words; ++w) cj[w] = cover[w];
         if (deps[j].size() > DEPS_PER_JOB)
             return fail(ZB_ERR_UNSUPPORTED, "persistent replay: a GEMM with more than 16 direct dependencies");
-        rj[j].dep0 = static_cast<int>(ndeps);
-        rj[j].ndeps = static_cast<int>(deps[j].size());
         ndeps += deps[j].size();
     }
 
@@ -891,8 +833,10 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
     using Slot = std::pair<int64_t, int>;  // (free at, pair)
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
     for (int p = 0; p < npairs; ++p) free_at.push({0, p});
-    std::vector<std::vector<uint32_t>> lists(npairs);
-    std::vector<std::vector<int64_t>> starts(npairs);
+    std::vector<std::vector<uint32_t>>& lists = plan->lists;
+    std::vector<std::vector<int64_t>>& starts = plan->starts;
+    lists.assign(npairs, {});
+    starts.assign(npairs, {});
     size_t assigned = 0;
     while (assigned < ntiles) {
         const Slot sl = free_at.top();
@@ -945,6 +889,98 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
     }
     int64_t makespan = 0;
     for (size_t j = 0; j < nj; ++j) makespan = std::max(makespan, finish[j]);
+    plan->ndeps = ndeps;
+    plan->makespan = makespan;
+    plan->by_level = by_level;
+    return ZB_OK;
+}
+
+zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size_t table_bytes, void* stream,
+                            ReplayInfo* info) {
+    const size_t nj = jobs.size();
+    if (info) *info = ReplayInfo{};
+    if (nj == 0) return ZB_OK;
+    const int npairs = replay_pairs();
+    if (npairs <= 0) return fail(ZB_ERR_UNSUPPORTED, "persistent replay: no co-resident CTA pairs");
+    ReplayPlan plan;
+    zb_status ps = plan_replay(jobs, npairs, &plan);
+    if (ps != ZB_OK) return ps;
+    const std::vector<long long>& tiles = plan.tiles;
+    const std::vector<std::vector<int>>& deps = plan.deps;
+    const std::vector<std::vector<uint32_t>>& lists = plan.lists;
+    const std::vector<std::vector<int64_t>>& starts = plan.starts;
+    const size_t ntiles = plan.ntiles, ndeps = plan.ndeps;
+    const int64_t makespan = plan.makespan;
+    unsigned int* err = device_error_word();
+    if (!err) return ZB_ERR_CUDA;
+
+    // -------------------------------------------- tensor maps, job records
+    std::vector<CUtensorMap> maps;
+    std::unordered_map<std::string, int> map_index;
+    std::string why;
+    auto add_map = [&](int* idx, const void* base, bool f32, uint64_t inner, uint64_t outer, uint64_t ld,
+                       uint32_t bi, uint32_t bo, CUtensorMapSwizzle sw) -> bool {
+        CUtensorMap m;
+        std::memset(&m, 0, sizeof(m));
+        if (!make_map(&m, base, f32, inner, outer, ld, bi, bo, &why, sw)) return false;
+        const std::string key(reinterpret_cast<const char*>(&m), sizeof(m));
+        auto f = map_index.find(key);
+        if (f != map_index.end()) {
+            *idx = f->second;
+            return true;
+        }
+        *idx = static_cast<int>(maps.size());
+        maps.push_back(m);
+        map_index.emplace(key, *idx);
+        return true;
+    };
+    std::vector<RJob> rj(nj);
+    size_t dep0 = 0;
+    for (size_t j = 0; j < nj; ++j) {
+        const GemmBf16& g = jobs[j];
+        RJob& J = rj[j];
+        std::memset(&J, 0, sizeof(J));
+        J.Mg = static_cast<int>(g.Mg);
+        J.Ng = static_cast<int>(g.Ng);
+        J.Kg = static_cast<int>(g.Kg);
+        J.epi = g.epi;
+        J.a_mn = g.a_mn;
+        J.b_mn = g.b_mn;
+        J.act = g.act;
+        J.accumulate = g.accumulate;
+        J.tiles_m = static_cast<int>((g.Mg + 2 * BM - 1) / (2 * BM));
+        J.tiles_n = static_cast<int>((g.Ng + BN - 1) / BN);
+        J.dep0 = static_cast<int>(dep0);
+        J.ndeps = static_cast<int>(deps[j].size());
+        dep0 += deps[j].size();
+        J.ldaux = g.ldaux;
+        J.aux = static_cast<const __nv_bfloat16*>(g.aux);
+        J.bias = static_cast<const __nv_bfloat16*>(g.bias);
+        EpiArgs ea;
+        choose_l2_hints(g, 2, &ea);
+        J.hint_a = ea.hint_a;
+        J.hint_b = ea.hint_b;
+        J.hint_out = ea.hint_out;
+        bool ok;
+        if (g.a_mn)
+            ok = add_map(&J.map_a, g.A, false, g.Mg, g.Kg, g.lda, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+        else
+            ok = add_map(&J.map_a, g.A, false, g.Kg, g.Mg, g.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (ok) {
+            if (g.b_mn)
+                ok = add_map(&J.map_b, g.B, false, g.Ng, g.Kg, g.ldb, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+            else
+                ok = add_map(&J.map_b, g.B, false, g.Kg, g.Ng, g.ldb, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+        const bool f32_out = g.epi == EPI_F32;
+        const CUtensorMapSwizzle osw = f32_out ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        if (ok) ok = add_map(&J.map_o0, g.out0, f32_out, g.Ng, g.Mg, g.ld0, 32, 32, osw);
+        J.map_o1 = J.map_o0;
+        if (ok && g.epi == EPI_GELU_DUAL) ok = add_map(&J.map_o1, g.out1, false, g.Ng, g.Mg, g.ld1, 32, 32, osw);
+        if (!ok) return fail(ZB_ERR_CUDA, why);
+        J.target = static_cast<uint32_t>(tiles[j]) * SIGNALS_PER_TILE;
+    }
+
 
     // -------------------------------------------- tables and launch
     const Layout L = table_layout(maps.size(), nj, ndeps, ntiles);

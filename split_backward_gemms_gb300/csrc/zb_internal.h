@@ -76,6 +76,20 @@ struct ReplayInfo {
 };
 zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size_t table_bytes, void* stream,
                             ReplayInfo* info);
+// The host plan of a persistent replay (no device access): tiles per GEMM,
+// dependencies (reduced), the CTA pairs' tile lists (job << 18 | tile, in
+// order) with their simulated starts (1/16 of a K block's MMA time), the
+// simulated makespan and the priority rule used; checked deadlock-free.
+struct ReplayPlan {
+    std::vector<long long> tiles;
+    size_t ntiles = 0, ndeps = 0;
+    std::vector<std::vector<int>> deps;
+    std::vector<std::vector<uint32_t>> lists;
+    std::vector<std::vector<int64_t>> starts;
+    int64_t makespan = 0;
+    bool by_level = false;
+};
+zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan* plan);
 // GEMMs and CTA-pair tiles an op list replays (for the table size).
 zb_status replay_count(const zb_block& b, const zb_op* ops, size_t n_ops, size_t* njobs, size_t* ntiles);
 size_t replay_table_bytes(size_t njobs, size_t ntiles);

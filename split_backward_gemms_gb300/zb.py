@@ -379,6 +379,25 @@ def make_pipeline(P, m, blk, mem_limit_bytes=0, zero_grads=True, timing=False,
                        int(streams), int(chunks), int(layout), int(executor))
 
 
+class zb_persistent_plan_info(C.Structure):
+    _fields_ = [("gemms", C.c_uint64), ("tiles", C.c_uint64), ("deps", C.c_uint64), ("pairs", C.c_uint64),
+                ("est_makespan_kblocks", C.c_double), ("by_chain", C.c_int32), ("reserved", C.c_int32),
+                ("max_tiles_per_pair", C.c_uint64)]
+
+
+def zb_persistent_plan(pl, ops, pairs=76):
+    """Host plan of a persistent replay: (info, [(consumer, producer), ...])."""
+    arr = ops if isinstance(ops, C.Array) else ops_array(ops)
+    info = zb_persistent_plan_info()
+    n = C.c_size_t(0)
+    _check(LIB.zb_persistent_plan(C.byref(pl), arr, len(arr), int(pairs), C.byref(info), None, C.byref(n)),
+           "zb_persistent_plan")
+    edges = (C.c_int32 * (2 * max(n.value, 1)))()
+    _check(LIB.zb_persistent_plan(C.byref(pl), arr, len(arr), int(pairs), C.byref(info), edges, C.byref(n)),
+           "zb_persistent_plan")
+    return info, [(edges[2 * k], edges[2 * k + 1]) for k in range(n.value)]
+
+
 def zb_schedule_workspace_size(pl, ops):
     """Returns (workspace_bytes, peak_live_bytes)."""
     arr = ops if isinstance(ops, C.Array) else ops_array(ops)
