@@ -13,9 +13,12 @@
 // reads the output the previous one wrote).
 //
 // The host assigns the tiles to the persistent grid's CTA pairs with a
-// list-scheduling simulation (estimated tile times, critical path first);
-// each pair runs its list in order with the one-launch kernel's roles (TMA
-// producer, MMA issuer, 8 epilogue warps, two TMEM accumulators).  Before a
+// list-scheduling simulation (estimated tile times; priority to the earliest
+// GEMM in list order where most tiles belong to GEMMs of two or more waves,
+// else to the longest chain of work after a GEMM); each pair runs its list
+// in order with the one-launch kernel's roles (TMA producer, MMA issuer, 8
+// epilogue warps, two TMEM accumulators), the producer's and MMA issuer's K
+// loops instantiated per operand-major pair.  Before a
 // pair loads a job's first tile, its producers wait (bounded) until every
 // job that job depends on has signalled all of its tiles: a GPU-scope
 // acquire load of each dependency's completion counter; each epilogue warp
@@ -25,10 +28,12 @@
 // own pair, so the unfinished tile that starts first in the simulation can
 // always proceed; the host checks that order before every launch.
 //
-// Tables (tensor maps, job records, dependency lists, per-pair tile lists)
-// go into the caller's workspace, written by small kernels that carry them
-// as launch parameters, so a replay captured in a CUDA graph holds no
-// pointer to host memory.
+// Tables (job records, dependency lists, per-pair tile lists; the tensor
+// maps too when there are more than fit the launch parameters) go into the
+// caller's workspace, written by small kernels that carry them as launch
+// parameters, so a replay captured in a CUDA graph holds no pointer to host
+// memory.  ZB_REPLAY_TRACE=1 adds per-tile timestamps (TraceRec) at the end
+// of the workspace (eager replays).
 #include <algorithm>
 #include <cstdio>
 #include <cstdint>
