@@ -665,15 +665,27 @@ int replay_pairs() {
     return n;
 }
 
-// Estimated time of one tile (units of 1/16 of a K block's MMAs): its K
-// loop, or its epilogue where that is longer (the GeLU epilogues of a short
-// K loop), plus a fixed cost.
+// Estimated time of one tile (units of 1/16 of a K block's MMA time at the
+// tensor peak): its K loop at the rate tiles of the P=4, h=1024 pipeline
+// were traced at (1.45 x the peak: the operand stream of a CTA pair runs
+// behind the tensor pipe at these sizes), or its epilogue and completion
+// signal where those are longer (the GeLU epilogues of a K = 1024 tile: ~7
+// us), plus a fixed cost.
 int64_t tile_cost(const zb::GemmBf16& g) {
     const int64_t kb = (g.Kg + BK - 1) / BK;
-    const int64_t epi = g.epi == zb::EPI_GELU_DUAL ? 18 : g.epi == zb::EPI_GELU_BWD ? 22 : g.epi == zb::EPI_F32 ? 10 : 6;
-    return (std::max(kb, epi) + 1) * 16;
+    const int64_t epi = g.epi == zb::EPI_GELU_DUAL ? 40 : g.epi == zb::EPI_GELU_BWD ? 44 : g.epi == zb::EPI_F32 ? 16 : 10;
+    return std::max(kb * 23, epi * 16) + 4 * 16;
 }
-constexpr int64_t READY_LATENCY = 2 * 16;  // a signal's trip to the waiting pair
+// Simulated time from a GEMM's last tile to its dependents' first: the
+// completion signal, its detection and a cold operand pipeline, plus the
+// slack that keeps a pair's static list from stalling on tiles that run late.
+// Chosen by measurement on the P=4, h=1024 pipeline, for the longest-chain
+// priority (mean of ZB-H1, ZB-H2, 1F1B, ZB-2p and ZB-V, TF/s): 2 K blocks
+// 1190, 20 1224, 45 1234, 70 1246, 100 1258, 150 1229.  With list order
+// (GEMMs of several waves, each on every pair in turn) 2 K blocks: there a
+// larger one only moves later GEMMs' tiles into the current one's waves.
+constexpr int64_t READY_LATENCY_CHAIN = 100 * 16;
+constexpr int64_t READY_LATENCY_LIST = 2 * 16;
 
 }  // namespace
 
@@ -792,18 +804,9 @@ zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan*
     }
 
     // -------------------------------------------- tile assignment
-    // bottom level: the longest chain of job spans (its tiles spread over
-    // all pairs) from the job to the end
     std::vector<std::vector<int>> succ(nj);
     for (size_t j = 0; j < nj; ++j)
         for (int d : deps[j]) succ[d].push_back(static_cast<int>(j));
-    std::vector<int64_t> cost(nj), level(nj, 0);
-    for (size_t j = 0; j < nj; ++j) cost[j] = tile_cost(jobs[j]);
-    for (size_t j = nj; j-- > 0;) {
-        int64_t tail = 0;
-        for (int s : succ[j]) tail = std::max(tail, level[s] + READY_LATENCY);
-        level[j] = (tiles[j] + npairs - 1) / npairs * cost[j] + tail;
-    }
     // Which ready job a free pair takes.  Where most tiles belong to GEMMs
     // of at least two waves of tiles (the large one-stage steps): the
     // earliest in list order, so that each GEMM runs on every pair, its
@@ -823,6 +826,17 @@ zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan*
     for (size_t j = 0; j < nj; ++j)
         if (tiles[j] >= 2LL * npairs) big_tiles += tiles[j];
     const bool by_level = forced ? forced == 1 : 2 * big_tiles < static_cast<long long>(ntiles);
+    const int64_t ready_latency = by_level ? READY_LATENCY_CHAIN : READY_LATENCY_LIST;
+    // bottom level: the longest chain of job spans (its tiles spread over
+    // all pairs) from the job to the end
+    std::vector<int64_t> cost(nj), level(nj, 0);
+    for (size_t j = 0; j < nj; ++j) cost[j] = tile_cost(jobs[j]);
+    for (size_t j = nj; j-- > 0;) {
+        int64_t tail = 0;
+        for (int s : succ[j]) tail = std::max(tail, level[s] + ready_latency);
+        level[j] = (tiles[j] + npairs - 1) / npairs * cost[j] + tail;
+    }
+
     auto prio = [&](int a, int b) {
         if (by_level && level[a] != level[b]) return level[a] > level[b];
         return a < b;
@@ -872,7 +886,7 @@ zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan*
             for (int s : succ[best]) {
                 if (--deps_left[s] == 0) {
                     int64_t r = 0;
-                    for (int d : deps[s]) r = std::max(r, finish[d] + READY_LATENCY);
+                    for (int d : deps[s]) r = std::max(r, finish[d] + ready_latency);
                     ready_at[s] = r;
                     ready.push_back(s);
                 }
