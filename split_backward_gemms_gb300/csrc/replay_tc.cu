@@ -12,21 +12,25 @@
 // accumulating weight-gradient GEMMs of a stage stay in list order (each
 // reads the output the previous one wrote).
 //
-// The host assigns the tiles to the persistent grid's CTA pairs with a
-// list-scheduling simulation (estimated tile times; priority to the earliest
-// GEMM in list order where most tiles belong to GEMMs of two or more waves,
-// else to the longest chain of work after a GEMM); each pair runs its list
-// in order with the one-launch kernel's roles (TMA producer, MMA issuer, 8
-// epilogue warps, two TMEM accumulators), the producer's and MMA issuer's K
-// loops instantiated per operand-major pair.  Before a
+// The host orders all tiles by a list-scheduling simulation of the
+// persistent grid's CTA pairs (estimated tile times; priority to the
+// earliest GEMM in list order where most tiles belong to GEMMs of two or
+// more waves, else to the longest chain of work after a GEMM).  On the
+// device each CTA pair takes the next tile of that order (an atomic counter)
+// whenever its producer is free and runs it with the one-launch kernel's
+// roles (TMA producer, MMA issuer, 8 epilogue warps, two TMEM
+// accumulators), the producer's and MMA issuer's K loops instantiated per
+// operand-major pair; the leader CTA's producer hands each entry to the
+// other roles of both CTAs through a small ring in shared memory.  Before a
 // pair loads a job's first tile, its producers wait (bounded) until every
 // job that job depends on has signalled all of its tiles: a GPU-scope
 // acquire load of each dependency's completion counter; each epilogue warp
 // adds 1 to its job's counter with a release once its tile's stores have
-// completed.  Deadlock freedom: in the simulation every tile starts after
-// every tile of the jobs it depends on and after every earlier tile of its
-// own pair, so the unfinished tile that starts first in the simulation can
-// always proceed; the host checks that order before every launch.
+// completed.  Deadlock freedom: in the order every tile comes after every
+// tile of the jobs it depends on (the host checks this before every
+// launch), and tiles are handed out as a prefix of the order, so the
+// earliest unfinished tile has been taken, its dependencies and its pair's
+// earlier tiles are finished, and it can always proceed.
 //
 // Tables (job records, dependency lists, per-pair tile lists; the tensor
 // maps too when there are more than fit the launch parameters) go into the
@@ -55,7 +59,7 @@ constexpr size_t DEPS_PER_JOB = 16;  // table room per job (after reduction)
 constexpr int EPI_WARPS = 8;
 constexpr uint32_t SIGNALS_PER_TILE = 2 * EPI_WARPS;  // every epilogue warp of both CTAs
 // fp32 reduce-adds of a weight-gradient tile: chunk c is issued c x (K
-// blocks x this) ns after the accumulator is ready (not on a pair's last tile)
+// blocks x this) ns after the accumulator is ready
 constexpr uint64_t PACE_NS_PER_KB = 50;
 
 // One GEMM of the replay as the kernel reads it (global memory).
@@ -95,16 +99,23 @@ struct RParams {
     const CUtensorMap* maps;  // global copy (used when nparam == 0)
     const RJob* jobs;
     const int* deps;
-    const int* list_off;      // pair p runs entries[list_off[p] .. list_off[p + 1])
-    const uint32_t* entries;
-    uint32_t* done;           // per job; done[njobs]: this launch's abort word
+    const uint32_t* entries;  // every tile, in the simulation's start order
+    uint32_t* done;           // per job; done[njobs]: this launch's abort word,
+                              // done[njobs + 1]: the next entry to hand out
     unsigned int* err;
     TraceRec* trace;          // or nullptr
     int njobs;
+    int ntiles;
     int nparam;               // maps held in pmaps below (0: all in global memory)
     CUtensorMap pmaps[PARAM_MAPS];
 };
 static_assert(sizeof(RParams) <= 32000, "launch parameter size");
+
+// A CTA pair takes its tiles one at a time from the global order (an atomic
+// counter); the leader's producer hands each entry to the pair's other roles
+// through a ring of RING slots in both CTAs' shared memory.
+constexpr int RING = 4;
+constexpr uint32_t RING_READERS = 2 + 2 * EPI_WARPS;  // other producer, MMA issuer, epilogue warps
 
 template <int STAGES>
 struct RCtl {
@@ -113,6 +124,9 @@ struct RCtl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t tfill[RING];  // slot k mod RING holds the pair's k-th entry (both CTAs)
+    uint64_t tfree[RING];  // leader CTA: every reader has read the slot
+    int tslot[RING];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -184,6 +198,44 @@ __device__ bool wait_deps(const RParams& rp, const RJob* J, volatile int* abort_
     }
     zbp::fence_proxy_async_global();
     return true;
+}
+
+__device__ __forceinline__ void st_shared_cluster_s32(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// The leader's producer: the pair's k-th entry (-1: none left; -2: abort),
+// published to both CTAs' slot k mod RING.
+template <int STAGES>
+__device__ __forceinline__ int ring_put(RCtl<STAGES>* ctl, uint32_t k, const RParams& rp, volatile int* abort_flag,
+                                        volatile uint32_t* abort_all) {
+    const uint32_t r = k % RING, use = k / RING;
+    if (!rwait<true>(zbp::smem_u32(&ctl->tfree[r]), (use & 1u) ^ 1u, abort_flag, abort_all, rp.err,
+                     ERR_WAIT_PRODUCER, WAIT_LIMIT_NS, true))
+        return -2;
+    int e = static_cast<int>(atomicAdd(rp.done + rp.njobs + 1, 1u));
+    if (e >= rp.ntiles) e = -1;
+    const uint32_t slot = zbp::smem_u32(&ctl->tslot[r]);
+    const uint32_t fill = zbp::smem_u32(&ctl->tfill[r]);
+    ctl->tslot[r] = e;
+    st_shared_cluster_s32(zbp::mapa_shared(slot, 1), e);
+    zbp::mbar_arrive(fill);
+    zbp::mbar_arrive_cluster(zbp::mapa_shared(fill, 1));  // release: orders the remote store
+    return e;
+}
+
+// Any other role: the pair's k-th entry from slot k mod RING, then the slot
+// is released to the leader's producer.
+template <int STAGES>
+__device__ __forceinline__ int ring_take(RCtl<STAGES>* ctl, uint32_t k, const RParams& rp, volatile int* abort_flag,
+                                         volatile uint32_t* abort_all, unsigned code) {
+    const uint32_t r = k % RING, use = k / RING;
+    if (!rwait<true>(zbp::smem_u32(&ctl->tfill[r]), use & 1u, abort_flag, abort_all, rp.err, code, WAIT_LIMIT_NS,
+                     true))
+        return -2;
+    const int e = *reinterpret_cast<volatile int*>(&ctl->tslot[r]);
+    zbp::mbar_arrive_cluster(zbp::mapa_shared(zbp::smem_u32(&ctl->tfree[r]), 0));
+    return e;
 }
 
 __device__ __forceinline__ void load_h32r(const __nv_bfloat16* aux, long long ldaux, int Mg, int Ng, int row,
@@ -278,8 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
     const int lane = threadIdx.x & 31;
     const uint32_t rank = zbp::cluster_ctarank();
     const bool leader = rank == 0;
-    const int pair = static_cast<int>(blockIdx.x >> 1);
-    const int e_lo = rp.list_off[pair], e_hi = rp.list_off[pair + 1];
+    const uint32_t pair = blockIdx.x >> 1;
     volatile uint32_t* abort_all = rp.done + rp.njobs;
     const CUtensorMap* maps = rp.nparam > 0 ? rp.pmaps : rp.maps;
 
@@ -293,6 +344,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
             zbp::mbar_init(zbp::smem_u32(&ctl->tempty[b]), SIGNALS_PER_TILE);
         }
         zbp::mbar_init(zbp::smem_u32(&ctl->drain), 1);
+        for (int r = 0; r < RING; ++r) {
+            zbp::mbar_init(zbp::smem_u32(&ctl->tfill[r]), 1);
+            zbp::mbar_init(zbp::smem_u32(&ctl->tfree[r]), RING_READERS);
+        }
         ctl->abort_flag = 0;
         zbp::fence_mbar_init();
     }
@@ -313,7 +368,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
             uint32_t it = 0;
             bool ok = true;
             int cur = -1;
-            for (int e = e_lo; e < e_hi && ok; ++e) {
+            for (uint32_t k = 0; ok; ++k) {
+                const int e = leader ? ring_put(ctl, k, rp, abort_flag, abort_all)
+                                     : ring_take(ctl, k, rp, abort_flag, abort_all, ERR_WAIT_PRODUCER);
+                if (e < 0) {
+                    ok = e == -1;
+                    break;
+                }
                 const uint32_t ent = rp.entries[e];
                 const int job = static_cast<int>(ent >> ENTRY_JOB_SHIFT);
                 const int tile = static_cast<int>(ent & ENTRY_TILE_MASK);
@@ -321,7 +382,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
                 const CUtensorMap* tma = maps + J->map_a;
                 const CUtensorMap* tmb = maps + J->map_b;
                 const bool tr_on = rp.trace != nullptr && leader;
-                if (tr_on) rp.trace[e].t_reach = zbp::globaltimer_ns();
+                if (tr_on) {
+                    rp.trace[e].pair = pair;
+                    rp.trace[e].t_reach = zbp::globaltimer_ns();
+                }
                 if (job != cur) {
                     if (!wait_deps(rp, J, abort_flag)) {
                         ok = false;
@@ -368,9 +432,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer
             uint32_t it = 0;
-            uint32_t local = 0;
             bool ok = true;
-            for (int e = e_lo; e < e_hi && ok; ++e, ++local) {
+            for (uint32_t local = 0; ok; ++local) {
+                const int e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_MMA);
+                if (e < 0) break;
                 const RJob* J = rp.jobs + (rp.entries[e] >> ENTRY_JOB_SHIFT);
                 const int majors = (J->a_mn << 1) | J->b_mn;
                 const int num_kb = (J->Kg + BK - 1) / BK;
@@ -411,9 +476,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
         const int c_lo = (ew >> 2) * 128;
         const uint32_t region = zbp::smem_u32(staging) + static_cast<uint32_t>(ew) * 4096u;
         uint32_t flip = 0;
-        uint32_t local = 0;
         int cur = -1;
-        for (int e = e_lo; e < e_hi; ++e, ++local) {
+        for (uint32_t local = 0;; ++local) {
+            int e = 0;
+            if (lane == 0) e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_EPI);
+            e = __shfl_sync(0xffffffffu, e, 0);
+            if (e < 0) break;
             const uint32_t ent = rp.entries[e];
             const int job = static_cast<int>(ent >> ENTRY_JOB_SHIFT);
             const int tile = static_cast<int>(ent & ENTRY_TILE_MASK);
@@ -465,12 +533,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
             if (tr_epi) rp.trace[e].t_epi0 = zbp::globaltimer_ns();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
             if (epi == zb::EPI_F32) {
-                const bool pace = e + 1 < e_hi;
                 const uint64_t spacing = static_cast<uint64_t>((J->Kg + BK - 1) / BK) * PACE_NS_PER_KB;
                 const uint64_t t_full = zbp::globaltimer_ns();
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    if (c > 0 && pace) {
+                    if (c > 0) {
                         if (lane == 0) {
                             const uint64_t target = t_full + static_cast<uint64_t>(c) * spacing;
                             while (zbp::globaltimer_ns() < target) __nanosleep(64);
@@ -606,7 +673,7 @@ bool trace_on() {
 }
 
 struct Layout {
-    size_t maps, jobs, deps, offs, entries, done, total;
+    size_t maps, jobs, deps, entries, done, total;
 };
 
 Layout table_layout(size_t nmaps, size_t njobs, size_t ndeps, size_t ntiles) {
@@ -614,10 +681,9 @@ Layout table_layout(size_t nmaps, size_t njobs, size_t ndeps, size_t ntiles) {
     L.maps = 0;
     L.jobs = align256(L.maps + nmaps * sizeof(CUtensorMap));
     L.deps = align256(L.jobs + njobs * sizeof(RJob));
-    L.offs = align256(L.deps + ndeps * sizeof(int));
-    L.entries = align256(L.offs + (MAX_PAIRS + 1) * sizeof(int));
+    L.entries = align256(L.deps + ndeps * sizeof(int));
     L.done = align256(L.entries + ntiles * sizeof(uint32_t));
-    L.total = align256(L.done + (njobs + 1) * sizeof(uint32_t));
+    L.total = align256(L.done + (njobs + 2) * sizeof(uint32_t));
     return L;
 }
 
@@ -908,6 +974,24 @@ zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan*
     }
     int64_t makespan = 0;
     for (size_t j = 0; j < nj; ++j) makespan = std::max(makespan, finish[j]);
+    // the order the pairs take the tiles in (each pair the next one when it
+    // is free): by simulated start, so every tile comes after every tile of
+    // the GEMMs it depends on (checked above)
+    {
+        std::vector<std::pair<std::pair<int64_t, int>, uint32_t>> all;
+        all.reserve(ntiles);
+        for (int p = 0; p < npairs; ++p)
+            for (size_t k = 0; k < lists[p].size(); ++k) all.push_back({{starts[p][k], p}, lists[p][k]});
+        std::sort(all.begin(), all.end());
+        plan->order.resize(all.size());
+        plan->order_start.resize(all.size());
+        plan->order_pair.resize(all.size());
+        for (size_t i = 0; i < all.size(); ++i) {
+            plan->order[i] = all[i].second;
+            plan->order_start[i] = all[i].first.first;
+            plan->order_pair[i] = static_cast<uint32_t>(all[i].first.second);
+        }
+    }
     plan->ndeps = ndeps;
     plan->makespan = makespan;
     plan->by_level = by_level;
@@ -926,8 +1010,6 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
     if (ps != ZB_OK) return ps;
     const std::vector<long long>& tiles = plan.tiles;
     const std::vector<std::vector<int>>& deps = plan.deps;
-    const std::vector<std::vector<uint32_t>>& lists = plan.lists;
-    const std::vector<std::vector<int64_t>>& starts = plan.starts;
     const size_t ntiles = plan.ntiles, ndeps = plan.ndeps;
     const int64_t makespan = plan.makespan;
     unsigned int* err = device_error_word();
@@ -1014,15 +1096,7 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
         int* dp = reinterpret_cast<int*>(img.data() + L.deps);
         for (size_t j = 0; j < nj; ++j)
             for (int d : deps[j]) *dp++ = d;
-        int* op = reinterpret_cast<int*>(img.data() + L.offs);
-        uint32_t* ep = reinterpret_cast<uint32_t*>(img.data() + L.entries);
-        int off = 0;
-        for (int p = 0; p < npairs; ++p) {
-            op[p] = off;
-            std::memcpy(ep + off, lists[p].data(), lists[p].size() * sizeof(uint32_t));
-            off += static_cast<int>(lists[p].size());
-        }
-        op[npairs] = off;
+        std::memcpy(img.data() + L.entries, plan.order.data(), ntiles * sizeof(uint32_t));
     }
     uint8_t* base = static_cast<uint8_t*>(table);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1031,10 +1105,8 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
         // the records go at the very end of the table area, host fields set
         trace = reinterpret_cast<TraceRec*>(base + table_bytes - trace_bytes);
         std::vector<TraceRec> tr(ntiles);
-        size_t e = 0;
-        for (int p = 0; p < npairs; ++p)
-            for (size_t k = 0; k < lists[p].size(); ++k, ++e)
-                tr[e] = TraceRec{lists[p][k], static_cast<uint32_t>(p), starts[p][k], 0, 0, 0, 0, 0, 0, 0};
+        for (size_t e = 0; e < ntiles; ++e)
+            tr[e] = TraceRec{plan.order[e], plan.order_pair[e], plan.order_start[e], 0, 0, 0, 0, 0, 0, 0};
         cudaError_t te = cudaMemcpyAsync(trace, tr.data(), ntiles * sizeof(TraceRec), cudaMemcpyHostToDevice, st);
         if (te == cudaSuccess) te = cudaStreamSynchronize(st);
         if (te != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("trace setup: ") + cudaGetErrorString(te));
@@ -1052,7 +1124,7 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
             if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("table upload: ") + cudaGetErrorString(e));
         }
     }
-    cudaError_t e = cudaMemsetAsync(base + L.done, 0, (nj + 1) * sizeof(uint32_t), st);
+    cudaError_t e = cudaMemsetAsync(base + L.done, 0, (nj + 2) * sizeof(uint32_t), st);
     if (e != cudaSuccess) return fail(ZB_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
 
     std::vector<RParams> rpv(1);  // ~31 KB: not on the stack
@@ -1061,12 +1133,12 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
     rp.maps = reinterpret_cast<const CUtensorMap*>(base + L.maps);
     rp.jobs = reinterpret_cast<const RJob*>(base + L.jobs);
     rp.deps = reinterpret_cast<const int*>(base + L.deps);
-    rp.list_off = reinterpret_cast<const int*>(base + L.offs);
     rp.entries = reinterpret_cast<const uint32_t*>(base + L.entries);
     rp.done = reinterpret_cast<uint32_t*>(base + L.done);
     rp.err = err;
     rp.trace = trace;
     rp.njobs = static_cast<int>(nj);
+    rp.ntiles = static_cast<int>(ntiles);
     static const bool param_maps = [] {
         const char* v = std::getenv("ZB_REPLAY_PARAM_MAPS");
         return !(v && v[0] == '0');

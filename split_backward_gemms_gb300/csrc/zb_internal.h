@@ -86,6 +86,11 @@ struct ReplayPlan {
     std::vector<std::vector<int>> deps;
     std::vector<std::vector<uint32_t>> lists;
     std::vector<std::vector<int64_t>> starts;
+    // every tile in the order the pairs take them (simulated start, then
+    // pair), with its simulated start and pair
+    std::vector<uint32_t> order;
+    std::vector<int64_t> order_start;
+    std::vector<uint32_t> order_pair;
     int64_t makespan = 0;
     bool by_level = false;
 };
