@@ -343,7 +343,8 @@ typedef struct zb_pipeline {
                                   bounded like every device wait.  With
                                   timing, total_ms and gemm_ms cover the
                                   kernel and its table upload; the per-op
-                                  times are 0, n_gemm_launches is 1.     */
+                                  times are 0; n_gemm_launches counts the
+                                  replay kernel and the upload kernels.  */
 } zb_pipeline;
 
 typedef struct zb_stage_params {
@@ -361,7 +362,9 @@ typedef struct zb_run_stats {
     uint64_t workspace_bytes;   /* arena bytes used by this op list            */
     uint64_t peak_live_bytes;   /* ledger peak of live saved activations       */
     uint32_t n_ops;             /* ops replayed (OPT included)                 */
-    uint32_t n_gemm_launches;   /* tensor-core / FFMA GEMM launches enqueued   */
+    uint32_t n_gemm_launches;   /* tensor-core / FFMA GEMM launches enqueued
+                                   (persistent executor: its replay kernel and
+                                   the kernels that write its tables)         */
     double total_ms;            /* timing: first op start to last op end       */
     double kind_ms[4];          /* timing: summed op time per F, B, W, BW      */
     double gemm_ms;             /* timing: summed GEMM kernel time             */

@@ -614,7 +614,8 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
         trec.on = pl->timing != 0 && stats != nullptr;
         s = event_pool(&trec.pool);
         if (s != ZB_OK) return s;
-        s = timed(&trec, true, [&] { return replay_persistent(jobs, ws + toff, tbytes, stream, nullptr); });
+        ReplayInfo rinfo;
+        s = timed(&trec, true, [&] { return replay_persistent(jobs, ws + toff, tbytes, stream, &rinfo); });
         if (s != ZB_OK) return s;
         for (size_t i = 0; i < n_ops && s == ZB_OK; ++i)
             if (vop[i].kind == ZB_OP_OPT) s = run_op(i, st0, nullptr);
@@ -623,7 +624,8 @@ extern "C" zb_status zb_run_stage_schedule(const zb_pipeline* pl, const zb_stage
             stats->workspace_bytes = toff + tbytes;
             stats->peak_live_bytes = plan.peak_live_bytes;
             stats->n_ops = static_cast<uint32_t>(n_ops);
-            stats->n_gemm_launches = jobs.empty() ? 0u : 1u;
+            // the replay kernel and the kernels that write its tables
+            stats->n_gemm_launches = jobs.empty() ? 0u : static_cast<uint32_t>(1 + rinfo.upload_launches);
             stats->total_ms = 0.0;
             for (double& k : stats->kind_ms) k = 0.0;
             stats->gemm_ms = 0.0;
