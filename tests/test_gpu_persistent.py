@@ -140,6 +140,20 @@ def test_persistent_replay_activation_forms(zb, act):
     _same_bits(ref, got)
 
 
+def test_persistent_replay_single_linear_block(zb):
+    # the single-linear block (no activation): plain-store and fp32 GEMMs only
+    P, m, M, h = 2, 4, 520, 264
+    blk = zb.make_block(M, h, h, act=zb.ZB_ACT_NONE)
+    wts, X0, dY = _setup(P, m, M, h, h, seed=29)
+    ops = zb.zb_make_schedule("ZBH1", P, m)
+    ref = _replay(zb, zb.make_pipeline(P, m, blk), wts, X0, dY, ops, M, h, h)
+    got = _replay(zb, zb.make_pipeline(P, m, blk, executor="persistent"), wts, X0, dY, ops, M, h, h)
+    for p_, q_ in zip(ref[0], got[0]):
+        assert torch.equal(_bits(p_["dW1"]), _bits(q_["dW1"]))
+    for p_, q_ in zip(ref[1] + ref[2], got[1] + got[2]):
+        assert torch.equal(_bits(p_), _bits(q_))
+
+
 def test_persistent_replay_without_workspace_argument(zb):
     # the allocation-free entry point (library-owned static arena) with the
     # persistent executor: its tables fit the static arena too
