@@ -12,7 +12,9 @@
  * ("Pipeline Schedules: GPipe, 1F1B and Zero Bubble", section "Zero bubble:
  * split the backward pass").  A per-stage F/B/W executor replays 1F1B, ZB-H1
  * and ZB-H2 orderings for all P stages serially on one GPU (summary §3.4
- * "Handcrafted Schedule ZB-H1 / ZB-H2", Table 2).
+ * "Handcrafted Schedule ZB-H1 / ZB-H2", Table 2): one launch per GEMM on
+ * streams and events, or every GEMM of the list in one persistent kernel
+ * that orders them on the device (zb_pipeline.executor).
  *
  * Conventions for every entry point
  * ---------------------------------
