@@ -58,9 +58,12 @@ constexpr int MAX_PAIRS = 128;
 constexpr size_t DEPS_PER_JOB = 16;  // table room per job (after reduction)
 constexpr int EPI_WARPS = 8;
 constexpr uint32_t SIGNALS_PER_TILE = 2 * EPI_WARPS;  // every epilogue warp of both CTAs
-// fp32 reduce-adds of a weight-gradient tile: chunk c is issued c x (K
-// blocks x this) ns after the accumulator is ready
-constexpr uint64_t PACE_NS_PER_KB = 50;
+// fp32 reduce-adds of a weight-gradient tile: epilogue warp w (0..7) issues
+// its chunk c (0..3) (8 c + w) x (K blocks x this) ns after the accumulator
+// is ready, so the CTA's 32 reduce-adds of 4 KiB are evenly spaced over ~5/8
+// of the tile's MMA time instead of leaving in bursts that queue ahead of the
+// operand loads in the TMA unit
+constexpr uint64_t PACE_NS_PER_KB = 7;
 
 // One GEMM of the replay as the kernel reads it (global memory).
 struct alignas(128) RJob {
@@ -537,9 +540,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
                 const uint64_t t_full = zbp::globaltimer_ns();
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    if (c > 0) {
+                    const uint64_t slot = static_cast<uint64_t>(c * 8 + ew);
+                    if (slot > 0) {
                         if (lane == 0) {
-                            const uint64_t target = t_full + static_cast<uint64_t>(c) * spacing;
+                            const uint64_t target = t_full + slot * spacing;
                             while (zbp::globaltimer_ns() < target) __nanosleep(64);
                         }
                         __syncwarp();
