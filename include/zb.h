@@ -47,8 +47,13 @@
  *    (by default one persistent launch runs both), ZB_GEMM_HANDOFF=0 keeps
  *    the long-K GeLU / GeLU' epilogues on every warp's own rows (by default
  *    the warps that share SM schedulers with the copy and MMA warps hand
- *    their accumulator chunks to the others); all are read once per process
- *    and none changes a result.
+ *    their accumulator chunks to the others).  For the persistent executor
+ *    (zb_pipeline.executor): ZB_REPLAY_PRIORITY=list|level forces the rule
+ *    that orders its tiles, ZB_REPLAY_PARAM_MAPS=0 keeps its tensor maps in
+ *    the workspace instead of the launch parameters, ZB_REPLAY_TRACE=1 writes
+ *    per-tile timestamps at the end of the workspace (eager replays; the
+ *    size query then counts them).  All are read once per process and none
+ *    changes a result.
  *  - Errors: every call returns a zb_status; zb_last_error() returns a
  *    thread-local, human-readable message for the last failing call.
  *  - Threads and devices: calls may come from several host threads and for
