@@ -60,9 +60,9 @@ constexpr int EPI_WARPS = 8;
 constexpr uint32_t SIGNALS_PER_TILE = 2 * EPI_WARPS;  // every epilogue warp of both CTAs
 // fp32 reduce-adds of a weight-gradient tile: epilogue warp w (0..7) issues
 // its chunk c (0..3) (8 c + w) x (K blocks x this) ns after the accumulator
-// is ready, so the CTA's 32 reduce-adds of 4 KiB are evenly spaced over ~5/8
-// of the tile's MMA time instead of leaving in bursts that queue ahead of the
-// operand loads in the TMA unit
+// is ready, so the CTA's 32 reduce-adds of 4 KiB are evenly spaced over about
+// half of the tile's MMA time instead of leaving in bursts that queue ahead
+// of the operand loads in the TMA unit
 constexpr uint64_t PACE_NS_PER_KB = 7;
 
 // One GEMM of the replay as the kernel reads it (global memory).
@@ -81,8 +81,9 @@ struct alignas(128) RJob {
 static_assert(sizeof(RJob) == 128, "job record");
 
 // Per-tile trace record (ZB_REPLAY_TRACE=1): written at the end of the
-// caller's workspace.  entry and pair and the simulated start come from the
-// host; the times (global timer, ns) from the kernel, all in the leader CTA:
+// caller's workspace, one per entry of the order.  entry and the simulated
+// start come from the host, pair from the kernel (the pair that took the
+// tile), and the times (global timer, ns) too, all in the leader CTA:
 // when its producer reached the tile and when the tile's dependencies were
 // complete; when its MMA issuer had the accumulator and when it committed
 // the last K block; when its first epilogue warp had the accumulator, had
