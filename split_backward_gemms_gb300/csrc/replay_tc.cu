@@ -32,8 +32,8 @@
 // earliest unfinished tile has been taken, its dependencies and its pair's
 // earlier tiles are finished, and it can always proceed.
 //
-// Tables (job records, dependency lists, per-pair tile lists; the tensor
-// maps too when there are more than fit the launch parameters) go into the
+// Tables (job records, dependency lists, the tile order; the tensor maps
+// too when there are more than fit the launch parameters) go into the
 // caller's workspace, written by small kernels that carry them as launch
 // parameters, so a replay captured in a CUDA graph holds no pointer to host
 // memory.  ZB_REPLAY_TRACE=1 adds per-tile timestamps (TraceRec) at the end
@@ -748,8 +748,9 @@ int64_t tile_cost(const zb::GemmBf16& g) {
     return std::max(kb * 23, epi * 16) + 4 * 16;
 }
 // Simulated time from a GEMM's last tile to its dependents' first: the
-// completion signal, its detection and a cold operand pipeline, plus the
-// slack that keeps a pair's static list from stalling on tiles that run late.
+// completion signal, its detection and a cold operand pipeline, plus slack
+// for tiles that run late, so that the order seldom puts a tile ahead of the
+// moment a pair could start it.
 // Chosen by measurement on the P=4, h=1024 pipeline, for the longest-chain
 // priority (mean of ZB-H1, ZB-H2, 1F1B, ZB-2p and ZB-V, TF/s): 2 K blocks
 // 1190, 20 1224, 45 1234, 70 1246, 100 1258, 150 1229.  With list order
@@ -797,8 +798,9 @@ zb_status replay_count(const zb_block& b, const zb_op* ops, size_t n_ops, size_t
 
 // The host plan of a persistent replay: every GEMM's tiles, its
 // dependencies (transitive reduction of the byte-range conflicts), the tile
-// lists of the CTA pairs from the list-scheduling simulation, and the check
-// that the order cannot deadlock.  No device access.
+// lists of the CTA pairs from the list-scheduling simulation, the global
+// order of all tiles by simulated start that the kernel hands out, and the
+// check that this order cannot deadlock.  No device access.
 zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan* plan) {
     const size_t nj = jobs.size();
     *plan = ReplayPlan{};
