@@ -16,21 +16,26 @@
 // persistent grid's CTA pairs (estimated tile times; priority to the
 // earliest GEMM in list order where most tiles belong to GEMMs of two or
 // more waves, else to the longest chain of work after a GEMM).  On the
-// device each CTA pair takes the next tile of that order (an atomic counter)
-// whenever its producer is free and runs it with the one-launch kernel's
-// roles (TMA producer, MMA issuer, 8 epilogue warps, two TMEM
-// accumulators), the producer's and MMA issuer's K loops instantiated per
-// operand-major pair; the leader CTA's producer hands each entry to the
-// other roles of both CTAs through a small ring in shared memory.  Before a
-// pair loads a job's first tile, its producers wait (bounded) until every
-// job that job depends on has signalled all of its tiles: a GPU-scope
-// acquire load of each dependency's completion counter; each epilogue warp
+// device each CTA pair runs its tiles with the one-launch kernel's roles
+// (TMA producer, MMA issuer, 8 epilogue warps, two TMEM accumulators), the
+// producer's and MMA issuer's K loops instantiated per operand-major pair,
+// plus a scheduler warp in the leader CTA.  The scheduler takes the pair's
+// next tile of the order (an atomic counter) as soon as the producer has
+// started on the current one, reads its entry and job record, and waits
+// (bounded) until every job that job depends on has signalled all of its
+// tiles: a GPU-scope acquire load of each dependency's completion counter.
+// It then hands the entry to the producers, the MMA issuer and the epilogue
+// warps of both CTAs through a small ring in shared memory (a cluster-scope
+// release / acquire, which carries the acquire on to them), so the
+// producer's first loads of a tile follow its last loads of the one before
+// without a round trip to global memory in between.  Each epilogue warp
 // adds 1 to its job's counter with a release once its tile's stores have
 // completed.  Deadlock freedom: in the order every tile comes after every
 // tile of the jobs it depends on (the host checks this before every
-// launch), and tiles are handed out as a prefix of the order, so the
-// earliest unfinished tile has been taken, its dependencies and its pair's
-// earlier tiles are finished, and it can always proceed.
+// launch), and tiles are taken as a prefix of the order, each pair running
+// its own in the order taken, so the earliest unfinished tile has been
+// taken, its dependencies and its pair's earlier tiles are finished, and it
+// can always proceed.
 //
 // Tables (job records, dependency lists, the tile order; the tensor maps
 // too when there are more than fit the launch parameters) go into the
@@ -84,7 +89,7 @@ static_assert(sizeof(RJob) == 128, "job record");
 // caller's workspace, one per entry of the order.  entry and the simulated
 // start come from the host, pair from the kernel (the pair that took the
 // tile), and the times (global timer, ns) too, all in the leader CTA:
-// when its producer reached the tile and when the tile's dependencies were
+// when its scheduler took the tile and when the tile's dependencies were
 // complete; when its MMA issuer had the accumulator and when it committed
 // the last K block; when its first epilogue warp had the accumulator, had
 // issued its last store, and signalled the tile.
@@ -116,10 +121,15 @@ struct RParams {
 static_assert(sizeof(RParams) <= 32000, "launch parameter size");
 
 // A CTA pair takes its tiles one at a time from the global order (an atomic
-// counter); the leader's producer hands each entry to the pair's other roles
-// through a ring of RING slots in both CTAs' shared memory.
+// counter); the leader's scheduler warp hands each entry to the pair's other
+// roles through a ring of RING slots in both CTAs' shared memory.
 constexpr int RING = 4;
-constexpr uint32_t RING_READERS = 2 + 2 * EPI_WARPS;  // other producer, MMA issuer, epilogue warps
+constexpr uint32_t RING_READERS = 3 + 2 * EPI_WARPS;  // both producers, MMA issuer, epilogue warps
+constexpr int SCHED_WARP = 2 + EPI_WARPS;
+constexpr int REPLAY_THREADS = NUM_THREADS + 32;  // the one-launch roles and the scheduler warp
+// ring slot's second word: the tile's K-block count and operand majors (the
+// MMA issuer then reads no global memory between tiles)
+constexpr uint32_t INFO_KB_MASK = (1u << 28) - 1u;
 
 template <int STAGES>
 struct RCtl {
@@ -130,13 +140,17 @@ struct RCtl {
     uint64_t drain;
     uint64_t tfill[RING];  // slot k mod RING holds the pair's k-th entry (both CTAs)
     uint64_t tfree[RING];  // leader CTA: every reader has read the slot
-    int tslot[RING];
+    int tslot[RING];       // index into the order (-1: none left; -2: abort)
+    uint32_t tent[RING];   // the order's entry there (job << 18 | tile)
+    uint32_t tinfo[RING];  // K blocks | majors << 28
+    int ptaken;            // leader CTA: entries its producer has taken
     uint32_t tmem_base;
     int abort_flag;
 };
-static_assert(smem_bytes<2>() >= 1024 + Cfg<2>::STAGES * Cfg<2>::STAGE_BYTES + STAGING_BYTES +
-                                     sizeof(RCtl<Cfg<2>::STAGES>),
-              "replay kernel shared memory");
+constexpr size_t replay_smem_bytes() {
+    return 1024 + Cfg<2>::STAGES * Cfg<2>::STAGE_BYTES + STAGING_BYTES + sizeof(RCtl<Cfg<2>::STAGES>) + 64;
+}
+static_assert(replay_smem_bytes() <= 232448, "replay kernel shared memory");
 
 // Bounded wait on a local mbarrier phase (cluster-scope acquire where the
 // arrivals come from the other CTA of the pair); gives up on this CTA's or
@@ -208,38 +222,71 @@ __device__ __forceinline__ void st_shared_cluster_s32(uint32_t addr, int v) {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// The leader's producer: the pair's k-th entry (-1: none left; -2: abort),
-// published to both CTAs' slot k mod RING.
+// The leader's scheduler: the pair's k-th entry (e: index into the order,
+// -1: none left; ent and info when e >= 0), published to both
+// CTAs' slot k mod RING once every reader has read the slot's previous use.
 template <int STAGES>
-__device__ __forceinline__ int ring_put(RCtl<STAGES>* ctl, uint32_t k, const RParams& rp, volatile int* abort_flag,
-                                        volatile uint32_t* abort_all) {
+__device__ __forceinline__ bool ring_publish(RCtl<STAGES>* ctl, uint32_t k, int e, uint32_t ent, uint32_t info,
+                                             const RParams& rp, volatile int* abort_flag,
+                                             volatile uint32_t* abort_all) {
     const uint32_t r = k % RING, use = k / RING;
     if (!rwait<true>(zbp::smem_u32(&ctl->tfree[r]), (use & 1u) ^ 1u, abort_flag, abort_all, rp.err,
                      ERR_WAIT_PRODUCER, WAIT_LIMIT_NS, true))
-        return -2;
-    int e = static_cast<int>(atomicAdd(rp.done + rp.njobs + 1, 1u));
-    if (e >= rp.ntiles) e = -1;
-    const uint32_t slot = zbp::smem_u32(&ctl->tslot[r]);
+        return false;
     const uint32_t fill = zbp::smem_u32(&ctl->tfill[r]);
     ctl->tslot[r] = e;
-    st_shared_cluster_s32(zbp::mapa_shared(slot, 1), e);
+    ctl->tent[r] = ent;
+    ctl->tinfo[r] = info;
+    st_shared_cluster_s32(zbp::mapa_shared(zbp::smem_u32(&ctl->tslot[r]), 1), e);
+    st_shared_cluster_s32(zbp::mapa_shared(zbp::smem_u32(&ctl->tent[r]), 1), static_cast<int>(ent));
+    st_shared_cluster_s32(zbp::mapa_shared(zbp::smem_u32(&ctl->tinfo[r]), 1), static_cast<int>(info));
     zbp::mbar_arrive(fill);
-    zbp::mbar_arrive_cluster(zbp::mapa_shared(fill, 1));  // release: orders the remote store
-    return e;
+    zbp::mbar_arrive_cluster(zbp::mapa_shared(fill, 1));  // release: orders the remote stores
+    return true;
 }
 
-// Any other role: the pair's k-th entry from slot k mod RING, then the slot
-// is released to the leader's producer.
+// Every other role: the pair's k-th entry from slot k mod RING (its order
+// index; *ent and *info with it), then the slot is released to the
+// scheduler.  The wait is an acquire at cluster scope, so what the
+// scheduler saw before publishing (the dependencies' results) is seen here.
 template <int STAGES>
 __device__ __forceinline__ int ring_take(RCtl<STAGES>* ctl, uint32_t k, const RParams& rp, volatile int* abort_flag,
-                                         volatile uint32_t* abort_all, unsigned code) {
+                                         volatile uint32_t* abort_all, unsigned code, uint32_t* ent, uint32_t* info) {
     const uint32_t r = k % RING, use = k / RING;
     if (!rwait<true>(zbp::smem_u32(&ctl->tfill[r]), use & 1u, abort_flag, abort_all, rp.err, code, WAIT_LIMIT_NS,
                      true))
         return -2;
     const int e = *reinterpret_cast<volatile int*>(&ctl->tslot[r]);
+    *ent = *reinterpret_cast<volatile uint32_t*>(&ctl->tent[r]);
+    *info = *reinterpret_cast<volatile uint32_t*>(&ctl->tinfo[r]);
     zbp::mbar_arrive_cluster(zbp::mapa_shared(zbp::smem_u32(&ctl->tfree[r]), 0));
     return e;
+}
+
+// The scheduler: bounded wait until the leader's producer has taken `k`
+// entries (the scheduler runs at most one tile ahead of it).
+__device__ bool wait_taken(volatile int* ptaken, int k, volatile int* abort_flag, volatile uint32_t* abort_all,
+                           unsigned int* err) {
+    if (*ptaken >= k) return true;
+    const uint64_t t0 = zbp::globaltimer_ns();
+    uint32_t spins = 0;
+    while (*ptaken < k) {
+        __nanosleep(20);
+        if ((++spins & 15u) == 0) {
+            const uint64_t waited = zbp::globaltimer_ns() - t0;
+            if (*abort_flag || (waited > 20000 && *abort_all)) {
+                *abort_flag = 1;
+                return false;
+            }
+            if (waited > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                *abort_all = 1;
+                atomicOr(err, ERR_WAIT_PRODUCER);
+                return false;
+            }
+        }
+    }
+    return true;
 }
 
 __device__ __forceinline__ void load_h32r(const __nv_bfloat16* aux, long long ldaux, int Mg, int Ng, int row,
@@ -321,7 +368,7 @@ __device__ __forceinline__ bool mma_tile(RCtl<STAGES>* ctl, uint8_t* smem, uint3
     return true;
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __grid_constant__ RParams rp) {
+__global__ void __launch_bounds__(REPLAY_THREADS, 1) zb_replay_tc_kernel(const __grid_constant__ RParams rp) {
     using C = Cfg<2>;
     constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -353,6 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
             zbp::mbar_init(zbp::smem_u32(&ctl->tfree[r]), RING_READERS);
         }
         ctl->abort_flag = 0;
+        ctl->ptaken = 0;
         zbp::fence_mbar_init();
     }
     if (warp == 1) {
@@ -373,28 +421,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
             bool ok = true;
             int cur = -1;
             for (uint32_t k = 0; ok; ++k) {
-                const int e = leader ? ring_put(ctl, k, rp, abort_flag, abort_all)
-                                     : ring_take(ctl, k, rp, abort_flag, abort_all, ERR_WAIT_PRODUCER);
+                uint32_t ent = 0, info = 0;
+                const int e = ring_take(ctl, k, rp, abort_flag, abort_all, ERR_WAIT_PRODUCER, &ent, &info);
                 if (e < 0) {
                     ok = e == -1;
                     break;
                 }
-                const uint32_t ent = rp.entries[e];
+                if (leader) *reinterpret_cast<volatile int*>(&ctl->ptaken) = static_cast<int>(k) + 1;
                 const int job = static_cast<int>(ent >> ENTRY_JOB_SHIFT);
                 const int tile = static_cast<int>(ent & ENTRY_TILE_MASK);
                 const RJob* J = rp.jobs + job;
                 const CUtensorMap* tma = maps + J->map_a;
                 const CUtensorMap* tmb = maps + J->map_b;
-                const bool tr_on = rp.trace != nullptr && leader;
-                if (tr_on) {
-                    rp.trace[e].pair = pair;
-                    rp.trace[e].t_reach = zbp::globaltimer_ns();
-                }
                 if (job != cur) {
-                    if (!wait_deps(rp, J, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    // the scheduler's acquire of the job's dependencies reached
+                    // this thread through the ring; its TMA reads follow it
+                    zbp::fence_proxy_async_global();
                     if (rp.nparam == 0) {
                         zbp::fence_tensormap_acquire(tma);
                         zbp::fence_tensormap_acquire(tmb);
@@ -403,15 +445,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
                     zbp::tma_prefetch_desc(tmb);
                     cur = job;
                 }
-                if (tr_on) rp.trace[e].t_ready = zbp::globaltimer_ns();
-                const int a_mn = J->a_mn, b_mn = J->b_mn;
+                const int a_mn = static_cast<int>(info >> 29) & 1, b_mn = static_cast<int>(info >> 28) & 1;
                 const uint64_t pol_a = zbp::l2_policy(J->hint_a);
                 const uint64_t pol_b = zbp::l2_policy(J->hint_b);
                 int mb, nb;
                 tile_coords(tile, J->tiles_m, J->tiles_n, C::GROUP_M, mb, nb);
                 const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
                 const int nb0 = nb * BN + static_cast<int>(rank) * C::B_ROWS;
-                const int num_kb = (J->Kg + BK - 1) / BK;
+                const int num_kb = static_cast<int>(info & INFO_KB_MASK);
                 switch ((a_mn << 1) | b_mn) {
                     case 0: ok = load_tile<0, 0>(ctl, smem, it, num_kb, tma, tmb, m0, nb0, pol_a, pol_b, leader,
                                                  abort_flag, abort_all, rp.err); break;
@@ -438,11 +479,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
             uint32_t it = 0;
             bool ok = true;
             for (uint32_t local = 0; ok; ++local) {
-                const int e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_MMA);
+                uint32_t ent = 0, info = 0;
+                const int e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_MMA, &ent, &info);
                 if (e < 0) break;
-                const RJob* J = rp.jobs + (rp.entries[e] >> ENTRY_JOB_SHIFT);
-                const int majors = (J->a_mn << 1) | J->b_mn;
-                const int num_kb = (J->Kg + BK - 1) / BK;
+                const int majors = static_cast<int>(info >> 28) & 3;
+                const int num_kb = static_cast<int>(info & INFO_KB_MASK);
                 const uint32_t buf = local & 1u;
                 const uint32_t tr = local >> 1;
                 if (!rwait<true>(zbp::smem_u32(&ctl->tempty[buf]), (tr & 1u) ^ 1u, abort_flag, abort_all, rp.err,
@@ -468,7 +509,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
             rwait<true>(zbp::smem_u32(&ctl->drain), 0, abort_flag, abort_all, rp.err, ERR_WAIT_MMA, DRAIN_LIMIT_NS,
                         false);
         }
-    } else {
+    } else if (warp < SCHED_WARP) {
         // ---------------------------------------------------- epilogue
         // Warp w reads TMEM lanes 32 (w mod 4) .. + 31 (rows of this CTA's
         // 128), columns [128 h, 128 h + 128) of the tile with h = (w - 2) / 4,
@@ -483,10 +524,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
         int cur = -1;
         for (uint32_t local = 0;; ++local) {
             int e = 0;
-            if (lane == 0) e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_EPI);
+            uint32_t ent = 0, info = 0;
+            if (lane == 0) e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_EPI, &ent, &info);
             e = __shfl_sync(0xffffffffu, e, 0);
+            ent = __shfl_sync(0xffffffffu, ent, 0);
+            __syncwarp();  // orders every lane's reads after lane 0's acquire
             if (e < 0) break;
-            const uint32_t ent = rp.entries[e];
             const int job = static_cast<int>(ent >> ENTRY_JOB_SHIFT);
             const int tile = static_cast<int>(ent & ENTRY_TILE_MASK);
             const RJob* J = rp.jobs + job;
@@ -494,18 +537,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
             const CUtensorMap* tmo0 = maps + J->map_o0;
             const CUtensorMap* tmo1 = maps + J->map_o1;
             if (job != cur) {
-                // already satisfied (this CTA's producer waited); orders this
-                // warp's stores and H loads after the producers' results
-                int good = 1;
+                // the scheduler's acquire of the job's dependencies reached
+                // lane 0 through the ring; its TMA stores follow it
                 if (lane == 0) {
-                    good = wait_deps(rp, J, abort_flag) ? 1 : 0;
-                    if (good && rp.nparam == 0) {
+                    zbp::fence_proxy_async_global();
+                    if (rp.nparam == 0) {
                         zbp::fence_tensormap_acquire(tmo0);
                         if (epi == zb::EPI_GELU_DUAL) zbp::fence_tensormap_acquire(tmo1);
                     }
                 }
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) break;
                 cur = job;
             }
             const uint32_t buf = local & 1u;
@@ -638,6 +678,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) zb_replay_tc_kernel(const __gr
         // the staging boxes must not be released while a bulk store reads them
         if (lane == 0) zbp::bulk_wait<0>();
         __syncwarp();
+    } else if (lane == 0 && leader) {
+        // ---------------------------------------------------- scheduler
+        // Takes the pair's k-th tile once the producer has taken the
+        // (k-1)-th (one tile of lookahead: the pair claims no more of the
+        // order than it can start on), waits for the tile's dependencies
+        // when its job changes, and publishes it.
+        int cur = -1;
+        for (uint32_t k = 0;; ++k) {
+            if (!wait_taken(&ctl->ptaken, static_cast<int>(k), abort_flag, abort_all, rp.err)) break;
+            int e = static_cast<int>(atomicAdd(rp.done + rp.njobs + 1, 1u));
+            uint32_t ent = 0, info = 0;
+            if (e >= rp.ntiles) {
+                e = -1;
+            } else {
+                ent = rp.entries[e];
+                const int job = static_cast<int>(ent >> ENTRY_JOB_SHIFT);
+                const RJob* J = rp.jobs + job;
+                if (rp.trace) {
+                    rp.trace[e].pair = pair;
+                    rp.trace[e].t_reach = zbp::globaltimer_ns();
+                }
+                if (job != cur) {
+                    if (!wait_deps(rp, J, abort_flag)) break;
+                    cur = job;
+                }
+                const uint32_t num_kb = static_cast<uint32_t>((J->Kg + BK - 1) / BK);
+                info = num_kb | static_cast<uint32_t>((J->a_mn << 1) | J->b_mn) << 28;
+                if (rp.trace) rp.trace[e].t_ready = zbp::globaltimer_ns();
+            }
+            if (!ring_publish(ctl, k, e, ent, info, rp, abort_flag, abort_all)) break;
+            if (e < 0) break;
+        }
     }
 
     __syncthreads();
@@ -713,12 +785,12 @@ int replay_pairs() {
     if (n) return n;
     auto kern = zb_replay_tc_kernel;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<2>())) != cudaSuccess)
+                             static_cast<int>(replay_smem_bytes())) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 256, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<2>();
+    cfg.blockDim = dim3(REPLAY_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = replay_smem_bytes();
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -1156,8 +1228,8 @@ zb_status replay_persistent(const std::vector<GemmBf16>& jobs, void* table, size
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * npairs, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<2>();
+    cfg.blockDim = dim3(REPLAY_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = replay_smem_bytes();
     cfg.stream = st;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
