@@ -127,8 +127,9 @@ constexpr int RING = 4;
 constexpr uint32_t RING_READERS = 3 + 2 * EPI_WARPS;  // both producers, MMA issuer, epilogue warps
 constexpr int SCHED_WARP = 2 + EPI_WARPS;
 constexpr int REPLAY_THREADS = NUM_THREADS + 32;  // the one-launch roles and the scheduler warp
-// ring slot's second word: the tile's K-block count and operand majors (the
-// MMA issuer then reads no global memory between tiles)
+// ring slot's info word: the tile's K-block count and operand majors (with
+// the slot's tile coordinates, tensor maps and L2 hints, the producers and
+// the MMA issuer read no global memory between tiles)
 constexpr uint32_t INFO_KB_MASK = (1u << 28) - 1u;
 
 template <int STAGES>
@@ -143,6 +144,10 @@ struct RCtl {
     int tslot[RING];       // index into the order (-1: none left; -2: abort)
     uint32_t tent[RING];   // the order's entry there (job << 18 | tile)
     uint32_t tinfo[RING];  // K blocks | majors << 28
+    int tm0[RING];         // the tile's first row (pair) and column
+    int tn0[RING];
+    uint32_t tmaps[RING];  // operand tensor maps: A | B << 16
+    uint32_t thints[RING]; // L2 hints: A | B << 8
     int ptaken;            // leader CTA: entries its producer has taken
     uint32_t tmem_base;
     int abort_flag;
@@ -223,10 +228,18 @@ __device__ __forceinline__ void st_shared_cluster_s32(uint32_t addr, int v) {
 }
 
 // The leader's scheduler: the pair's k-th entry (e: index into the order,
-// -1: none left; ent and info when e >= 0), published to both
+// -1: none left; t when e >= 0), published to both
 // CTAs' slot k mod RING once every reader has read the slot's previous use.
+// What the ring carries for one tile besides its order index.
+struct RingTile {
+    uint32_t ent, info;  // the order's entry; K blocks | majors << 28
+    int m0, n0;          // the pair's first row and column of the tile
+    uint32_t maps;       // operand tensor maps: A | B << 16
+    uint32_t hints;      // L2 hints of A and B: A | B << 8
+};
+
 template <int STAGES>
-__device__ __forceinline__ bool ring_publish(RCtl<STAGES>* ctl, uint32_t k, int e, uint32_t ent, uint32_t info,
+__device__ __forceinline__ bool ring_publish(RCtl<STAGES>* ctl, uint32_t k, int e, const RingTile& t,
                                              const RParams& rp, volatile int* abort_flag,
                                              volatile uint32_t* abort_all) {
     const uint32_t r = k % RING, use = k / RING;
@@ -235,30 +248,43 @@ __device__ __forceinline__ bool ring_publish(RCtl<STAGES>* ctl, uint32_t k, int 
         return false;
     const uint32_t fill = zbp::smem_u32(&ctl->tfill[r]);
     ctl->tslot[r] = e;
-    ctl->tent[r] = ent;
-    ctl->tinfo[r] = info;
-    st_shared_cluster_s32(zbp::mapa_shared(zbp::smem_u32(&ctl->tslot[r]), 1), e);
-    st_shared_cluster_s32(zbp::mapa_shared(zbp::smem_u32(&ctl->tent[r]), 1), static_cast<int>(ent));
-    st_shared_cluster_s32(zbp::mapa_shared(zbp::smem_u32(&ctl->tinfo[r]), 1), static_cast<int>(info));
+    ctl->tent[r] = t.ent;
+    ctl->tinfo[r] = t.info;
+    ctl->tm0[r] = t.m0;
+    ctl->tn0[r] = t.n0;
+    ctl->tmaps[r] = t.maps;
+    ctl->thints[r] = t.hints;
+    auto remote = [&](const void* p, int v) { st_shared_cluster_s32(zbp::mapa_shared(zbp::smem_u32(p), 1), v); };
+    remote(&ctl->tslot[r], e);
+    remote(&ctl->tent[r], static_cast<int>(t.ent));
+    remote(&ctl->tinfo[r], static_cast<int>(t.info));
+    remote(&ctl->tm0[r], t.m0);
+    remote(&ctl->tn0[r], t.n0);
+    remote(&ctl->tmaps[r], static_cast<int>(t.maps));
+    remote(&ctl->thints[r], static_cast<int>(t.hints));
     zbp::mbar_arrive(fill);
     zbp::mbar_arrive_cluster(zbp::mapa_shared(fill, 1));  // release: orders the remote stores
     return true;
 }
 
 // Every other role: the pair's k-th entry from slot k mod RING (its order
-// index; *ent and *info with it), then the slot is released to the
+// index; *t with it), then the slot is released to the
 // scheduler.  The wait is an acquire at cluster scope, so what the
 // scheduler saw before publishing (the dependencies' results) is seen here.
 template <int STAGES>
 __device__ __forceinline__ int ring_take(RCtl<STAGES>* ctl, uint32_t k, const RParams& rp, volatile int* abort_flag,
-                                         volatile uint32_t* abort_all, unsigned code, uint32_t* ent, uint32_t* info) {
+                                         volatile uint32_t* abort_all, unsigned code, RingTile* t) {
     const uint32_t r = k % RING, use = k / RING;
     if (!rwait<true>(zbp::smem_u32(&ctl->tfill[r]), use & 1u, abort_flag, abort_all, rp.err, code, WAIT_LIMIT_NS,
                      true))
         return -2;
     const int e = *reinterpret_cast<volatile int*>(&ctl->tslot[r]);
-    *ent = *reinterpret_cast<volatile uint32_t*>(&ctl->tent[r]);
-    *info = *reinterpret_cast<volatile uint32_t*>(&ctl->tinfo[r]);
+    t->ent = *reinterpret_cast<volatile uint32_t*>(&ctl->tent[r]);
+    t->info = *reinterpret_cast<volatile uint32_t*>(&ctl->tinfo[r]);
+    t->m0 = *reinterpret_cast<volatile int*>(&ctl->tm0[r]);
+    t->n0 = *reinterpret_cast<volatile int*>(&ctl->tn0[r]);
+    t->maps = *reinterpret_cast<volatile uint32_t*>(&ctl->tmaps[r]);
+    t->hints = *reinterpret_cast<volatile uint32_t*>(&ctl->thints[r]);
     zbp::mbar_arrive_cluster(zbp::mapa_shared(zbp::smem_u32(&ctl->tfree[r]), 0));
     return e;
 }
@@ -421,18 +447,16 @@ __global__ void __launch_bounds__(REPLAY_THREADS, 1) zb_replay_tc_kernel(const _
             bool ok = true;
             int cur = -1;
             for (uint32_t k = 0; ok; ++k) {
-                uint32_t ent = 0, info = 0;
-                const int e = ring_take(ctl, k, rp, abort_flag, abort_all, ERR_WAIT_PRODUCER, &ent, &info);
+                RingTile t;
+                const int e = ring_take(ctl, k, rp, abort_flag, abort_all, ERR_WAIT_PRODUCER, &t);
                 if (e < 0) {
                     ok = e == -1;
                     break;
                 }
                 if (leader) *reinterpret_cast<volatile int*>(&ctl->ptaken) = static_cast<int>(k) + 1;
-                const int job = static_cast<int>(ent >> ENTRY_JOB_SHIFT);
-                const int tile = static_cast<int>(ent & ENTRY_TILE_MASK);
-                const RJob* J = rp.jobs + job;
-                const CUtensorMap* tma = maps + J->map_a;
-                const CUtensorMap* tmb = maps + J->map_b;
+                const int job = static_cast<int>(t.ent >> ENTRY_JOB_SHIFT);
+                const CUtensorMap* tma = maps + (t.maps & 0xffffu);
+                const CUtensorMap* tmb = maps + (t.maps >> 16);
                 if (job != cur) {
                     // the scheduler's acquire of the job's dependencies reached
                     // this thread through the ring; its TMA reads follow it
@@ -445,14 +469,12 @@ __global__ void __launch_bounds__(REPLAY_THREADS, 1) zb_replay_tc_kernel(const _
                     zbp::tma_prefetch_desc(tmb);
                     cur = job;
                 }
-                const int a_mn = static_cast<int>(info >> 29) & 1, b_mn = static_cast<int>(info >> 28) & 1;
-                const uint64_t pol_a = zbp::l2_policy(J->hint_a);
-                const uint64_t pol_b = zbp::l2_policy(J->hint_b);
-                int mb, nb;
-                tile_coords(tile, J->tiles_m, J->tiles_n, C::GROUP_M, mb, nb);
-                const int m0 = mb * C::TILE_M + static_cast<int>(rank) * BM;
-                const int nb0 = nb * BN + static_cast<int>(rank) * C::B_ROWS;
-                const int num_kb = static_cast<int>(info & INFO_KB_MASK);
+                const int a_mn = static_cast<int>(t.info >> 29) & 1, b_mn = static_cast<int>(t.info >> 28) & 1;
+                const uint64_t pol_a = zbp::l2_policy(static_cast<int>(t.hints & 0xffu));
+                const uint64_t pol_b = zbp::l2_policy(static_cast<int>((t.hints >> 8) & 0xffu));
+                const int m0 = t.m0 + static_cast<int>(rank) * BM;
+                const int nb0 = t.n0 + static_cast<int>(rank) * C::B_ROWS;
+                const int num_kb = static_cast<int>(t.info & INFO_KB_MASK);
                 switch ((a_mn << 1) | b_mn) {
                     case 0: ok = load_tile<0, 0>(ctl, smem, it, num_kb, tma, tmb, m0, nb0, pol_a, pol_b, leader,
                                                  abort_flag, abort_all, rp.err); break;
@@ -479,11 +501,11 @@ __global__ void __launch_bounds__(REPLAY_THREADS, 1) zb_replay_tc_kernel(const _
             uint32_t it = 0;
             bool ok = true;
             for (uint32_t local = 0; ok; ++local) {
-                uint32_t ent = 0, info = 0;
-                const int e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_MMA, &ent, &info);
+                RingTile t;
+                const int e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_MMA, &t);
                 if (e < 0) break;
-                const int majors = static_cast<int>(info >> 28) & 3;
-                const int num_kb = static_cast<int>(info & INFO_KB_MASK);
+                const int majors = static_cast<int>(t.info >> 28) & 3;
+                const int num_kb = static_cast<int>(t.info & INFO_KB_MASK);
                 const uint32_t buf = local & 1u;
                 const uint32_t tr = local >> 1;
                 if (!rwait<true>(zbp::smem_u32(&ctl->tempty[buf]), (tr & 1u) ^ 1u, abort_flag, abort_all, rp.err,
@@ -524,14 +546,15 @@ __global__ void __launch_bounds__(REPLAY_THREADS, 1) zb_replay_tc_kernel(const _
         int cur = -1;
         for (uint32_t local = 0;; ++local) {
             int e = 0;
-            uint32_t ent = 0, info = 0;
-            if (lane == 0) e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_EPI, &ent, &info);
+            RingTile t{};
+            if (lane == 0) e = ring_take(ctl, local, rp, abort_flag, abort_all, ERR_WAIT_EPI, &t);
             e = __shfl_sync(0xffffffffu, e, 0);
-            ent = __shfl_sync(0xffffffffu, ent, 0);
+            const uint32_t ent = __shfl_sync(0xffffffffu, t.ent, 0);
+            const int m0 = __shfl_sync(0xffffffffu, t.m0, 0) + static_cast<int>(rank) * BM;
+            const int n0 = __shfl_sync(0xffffffffu, t.n0, 0);
             __syncwarp();  // orders every lane's reads after lane 0's acquire
             if (e < 0) break;
             const int job = static_cast<int>(ent >> ENTRY_JOB_SHIFT);
-            const int tile = static_cast<int>(ent & ENTRY_TILE_MASK);
             const RJob* J = rp.jobs + job;
             const int epi = J->epi, Mg = J->Mg, Ng = J->Ng;
             const CUtensorMap* tmo0 = maps + J->map_o0;
@@ -550,10 +573,6 @@ __global__ void __launch_bounds__(REPLAY_THREADS, 1) zb_replay_tc_kernel(const _
             }
             const uint32_t buf = local & 1u;
             const uint32_t tr = local >> 1;
-            int mb, nb;
-            tile_coords(tile, J->tiles_m, J->tiles_n, Cfg<2>::GROUP_M, mb, nb);
-            const int m0 = mb * Cfg<2>::TILE_M + static_cast<int>(rank) * BM;
-            const int n0 = nb * BN;
             const int row0 = m0 + q * 32;
             const int row = row0 + lane;
             const bool rows_live = row0 < Mg;
@@ -688,11 +707,11 @@ __global__ void __launch_bounds__(REPLAY_THREADS, 1) zb_replay_tc_kernel(const _
         for (uint32_t k = 0;; ++k) {
             if (!wait_taken(&ctl->ptaken, static_cast<int>(k), abort_flag, abort_all, rp.err)) break;
             int e = static_cast<int>(atomicAdd(rp.done + rp.njobs + 1, 1u));
-            uint32_t ent = 0, info = 0;
+            RingTile t{};
             if (e >= rp.ntiles) {
                 e = -1;
             } else {
-                ent = rp.entries[e];
+                const uint32_t ent = rp.entries[e];
                 const int job = static_cast<int>(ent >> ENTRY_JOB_SHIFT);
                 const RJob* J = rp.jobs + job;
                 if (rp.trace) {
@@ -704,10 +723,17 @@ __global__ void __launch_bounds__(REPLAY_THREADS, 1) zb_replay_tc_kernel(const _
                     cur = job;
                 }
                 const uint32_t num_kb = static_cast<uint32_t>((J->Kg + BK - 1) / BK);
-                info = num_kb | static_cast<uint32_t>((J->a_mn << 1) | J->b_mn) << 28;
+                int mb, nb;
+                tile_coords(static_cast<int>(ent & ENTRY_TILE_MASK), J->tiles_m, J->tiles_n, Cfg<2>::GROUP_M, mb, nb);
+                t.ent = ent;
+                t.info = num_kb | static_cast<uint32_t>((J->a_mn << 1) | J->b_mn) << 28;
+                t.m0 = mb * Cfg<2>::TILE_M;
+                t.n0 = nb * BN;
+                t.maps = static_cast<uint32_t>(J->map_a) | static_cast<uint32_t>(J->map_b) << 16;
+                t.hints = static_cast<uint32_t>(J->hint_a) | static_cast<uint32_t>(J->hint_b) << 8;
                 if (rp.trace) rp.trace[e].t_ready = zbp::globaltimer_ns();
             }
-            if (!ring_publish(ctl, k, e, ent, info, rp, abort_flag, abort_all)) break;
+            if (!ring_publish(ctl, k, e, t, rp, abort_flag, abort_all)) break;
             if (e < 0) break;
         }
     }
