@@ -7,10 +7,11 @@ with its own have stored all of theirs (counters in the workspace).  Every
 tile is the one-launch kernel's tile and the accumulating weight-gradient
 GEMMs of a stage keep their list order, so outputs and gradients are the
 serial replay's bit for bit: handcrafted and heuristic orderings, one stage
-and several, ragged shapes and M below one 128-row block (a one-CTA tile in
-the serial replay), chunked (ZB-V and interleaved 1F1B) lists, both GeLU
-forms, gradient statistics at OPT, accumulation into existing gradients, the
-allocation-free entry point, and a CUDA graph.  The serial replay
+and several, plans by longest chain and in list order, ragged shapes and M
+below one 128-row block (a one-CTA tile in the serial replay), chunked (ZB-V
+and interleaved 1F1B) lists, both GeLU forms, gradient statistics at OPT,
+accumulation into existing gradients, the allocation-free entry point, and a
+CUDA graph.  The serial replay
 is checked against the fp64 oracle elsewhere; one case here is also
 compared with the rounding-emulating oracle chain directly.
 """
@@ -126,6 +127,22 @@ def test_persistent_replay_is_the_serial_replay(zb, kind, P, m, M, h, f, chunks)
     got2 = _replay(zb, zb.make_pipeline(P, m, blk, executor="persistent", **extra), wts, X0, dY, ops, M, h, f,
                    stats_bufs=True)
     _same_bits(ref, got2)
+
+
+def test_persistent_replay_in_list_order(zb):
+    # GEMMs of two or more waves of tiles (M=2048, h=2048, f=8192: H/A, dH,
+    # dW1 and dW2 have 256 tiles of 256 x 256 for 76 CTA pairs) make the plan
+    # give priority to list order, as for the large one-stage steps, instead
+    # of the longest chain; the replay is still the serial replay bit for bit
+    P, m, M, h, f = 1, 6, 2048, 2048, 8192
+    blk = zb.make_block(M, h, f)
+    ops = _ops(zb, "ZBH2", P, m, 1)
+    info, _ = zb.zb_persistent_plan(zb.make_pipeline(P, m, blk), ops, pairs=76)
+    assert info.by_chain == 0 and info.gemms == 6 * m
+    wts, X0, dY = _setup(P, m, M, h, f, seed=91)
+    ref = _replay(zb, zb.make_pipeline(P, m, blk), wts, X0, dY, ops, M, h, f)
+    got = _replay(zb, zb.make_pipeline(P, m, blk, executor="persistent"), wts, X0, dY, ops, M, h, f)
+    _same_bits(ref, got)
 
 
 @pytest.mark.parametrize("act", ["tanh", "erf"])
