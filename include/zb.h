@@ -569,7 +569,11 @@ zb_status zb_post_validated_adamw(int32_t P, const double* const* stage_state,
 
 /* Synchronise `stream`, then report (and clear) the device error word of the
  * current device: ZB_ERR_TIMEOUT if a bounded device wait gave up,
- * ZB_ERR_CUDA if the stream reported an error, else ZB_OK. */
+ * ZB_ERR_CUDA if the stream reported an error, else ZB_OK.  zb_last_error()
+ * then gives the word, whose bits name the role whose wait gave up: 1 a TMA
+ * producer (or the persistent replay's tile scheduler), 2 an MMA issuer, 4
+ * an epilogue warp, 8 the persistent replay's wait for a GEMM it depends on,
+ * 1 << 31 zb_selftest_wait_timeout. */
 zb_status zb_sync_status(void* stream);
 
 /* Self-test of the device-side timeout path: launches one thread that waits
