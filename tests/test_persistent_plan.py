@@ -14,7 +14,8 @@ library generates, that
   (its dX is this stage's dY), dX after dH, W after the F and B it reads, the
   fp32 accumulation of a stage's W GEMMs in list order;
 * the priority rule follows the GEMM sizes (list order for multi-wave GEMMs,
-  longest chain for small ones), and the plan holds for one pair as well.
+  longest chain for small ones), and the plan holds for one pair as well;
+* the workspace size query counts the kernel's tables on top of the arena.
 The order-safety check itself runs inside the library on every plan.
 """
 
@@ -145,3 +146,21 @@ def test_plan_errors(zb):
     bad = [op for op in ops if op[0] != "W"]  # W missing: not a legal replay
     with pytest.raises(zb.ZBError):
         zb.zb_persistent_plan(zb.make_pipeline(2, 2, zb.make_block(256, 256, 1024)), bad)
+
+
+def test_workspace_holds_the_replay_tables(zb):
+    # the persistent executor's workspace is the stream executor's arena plus
+    # the kernel's tables: per GEMM up to four tensor maps (128 bytes each),
+    # a 128-byte job record, up to 16 dependency entries and a counter; per
+    # tile one entry of the order
+    for (P, m, M, h, f) in ((4, 8, 2048, 1024, 4096), (2, 4, 520, 264, 1048)):
+        ops = zb.zb_make_schedule("ZBH1", P, m)
+        blk = zb.make_block(M, h, f)
+        ws_s, peak_s = zb.zb_schedule_workspace_size(zb.make_pipeline(P, m, blk), ops)
+        ws_p, peak_p = zb.zb_schedule_workspace_size(zb.make_pipeline(P, m, blk, executor="persistent"), ops)
+        info, _ = zb.zb_persistent_plan(zb.make_pipeline(P, m, blk), ops)
+        nj, nt = info.gemms, info.tiles
+        assert peak_p == peak_s
+        extra = ws_p - ws_s
+        assert extra >= nj * (4 * 128 + 128 + 16 * 4 + 4) + nt * 4
+        assert extra <= nj * (4 * 128 + 128 + 16 * 4 + 4) + nt * 4 + 8 * 256
