@@ -1027,6 +1027,12 @@ zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan*
     std::vector<std::vector<int64_t>>& starts = plan->starts;
     lists.assign(npairs, {});
     starts.assign(npairs, {});
+    plan->order.clear();
+    plan->order_start.clear();
+    plan->order_pair.clear();
+    plan->order.reserve(ntiles);
+    plan->order_start.reserve(ntiles);
+    plan->order_pair.reserve(ntiles);
     size_t assigned = 0;
     while (assigned < ntiles) {
         const Slot sl = free_at.top();
@@ -1047,8 +1053,12 @@ zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan*
             continue;
         }
         const long long tile = next_tile[best]++;
-        lists[sl.second].push_back((static_cast<uint32_t>(best) << ENTRY_JOB_SHIFT) | static_cast<uint32_t>(tile));
+        const uint32_t ent = (static_cast<uint32_t>(best) << ENTRY_JOB_SHIFT) | static_cast<uint32_t>(tile);
+        lists[sl.second].push_back(ent);
         starts[sl.second].push_back(t);
+        plan->order.push_back(ent);
+        plan->order_start.push_back(t);
+        plan->order_pair.push_back(static_cast<uint32_t>(sl.second));
         last_start[best] = std::max(last_start[best], t);
         finish[best] = std::max(finish[best], t + cost[best]);
         ++assigned;
@@ -1080,9 +1090,16 @@ zb_status plan_replay(const std::vector<GemmBf16>& jobs, int npairs, ReplayPlan*
     int64_t makespan = 0;
     for (size_t j = 0; j < nj; ++j) makespan = std::max(makespan, finish[j]);
     // the order the pairs take the tiles in (each pair the next one when it
-    // is free): by simulated start, so every tile comes after every tile of
-    // the GEMMs it depends on (checked above)
-    {
+    // is free): by simulated start, then pair, so every tile comes after
+    // every tile of the GEMMs it depends on (checked above).  The simulation
+    // assigns tiles in that order already (its free pairs leave the heap by
+    // time, then pair, and re-enter later); sorted only if that ever fails.
+    bool in_order = true;
+    for (size_t i = 1; i < plan->order.size() && in_order; ++i)
+        in_order = plan->order_start[i - 1] < plan->order_start[i] ||
+                   (plan->order_start[i - 1] == plan->order_start[i] &&
+                    plan->order_pair[i - 1] < plan->order_pair[i]);
+    if (!in_order) {
         std::vector<std::pair<std::pair<int64_t, int>, uint32_t>> all;
         all.reserve(ntiles);
         for (int p = 0; p < npairs; ++p)
