@@ -9,6 +9,8 @@ library generates, that
 * the GEMM and tile counts are those of the list (6 GEMMs per stage and
   microbatch of the MLP block: H/A, Y, dH, dX, dW2, dW1);
 * every data dependency of the split backward is implied by the kept edges
+  (for one chunk per stage and, along the chain of virtual stages, for the
+  two- and three-chunk ZB-V and interleaved 1F1B lists)
   (each edge points backwards in list order): the next stage's forward after
   this stage's Y, B after the stage's own F (H) and after the next stage's B
   (its dX is this stage's dY), dX after dH, W after the F and B it reads, the
@@ -164,3 +166,48 @@ def test_workspace_holds_the_replay_tables(zb):
         extra = ws_p - ws_s
         assert extra >= nj * (4 * 128 + 128 + 16 * 4 + 4) + nt * 4
         assert extra <= nj * (4 * 128 + 128 + 16 * 4 + 4) + nt * 4 + 8 * 256
+
+
+def _vstage(kind, P, op):
+    """Virtual stage of a chunked op: cyclic (chunk c of stage s is c P + s)
+    or V (chunk 0 of stage s is s, chunk 1 is 2P - 1 - s)."""
+    _, s, c, _ = op
+    if kind == "ZBV":
+        return s if c == 0 else 2 * P - 1 - s
+    return c * P + s
+
+
+@pytest.mark.parametrize("kind,P,v,m", [("ZBV", 2, 2, 4), ("ZBV", 3, 2, 6), ("1F1B-I", 2, 2, 4), ("1F1B-I", 2, 3, 4)])
+def test_chunked_plan_keeps_every_data_dependency(zb, kind, P, v, m):
+    # the same rules along the chain of L = v P virtual stages
+    M, h, f = 256, 256, 1024
+    ops = zb.zb_make_interleaved_schedule(kind, P, v, m)
+    L = v * P
+    pl = zb.make_pipeline(P, m, zb.make_block(M, h, f), chunks=v, layout=kind)
+    info, edges = zb.zb_persistent_plan(pl, ops, pairs=76)
+    g = []
+    for op in ops:
+        if op[0] == "OPT":  # no GEMM
+            continue
+        k, s, j = op[0], _vstage(kind, P, op), op[3]
+        g += {"F": [("F1", s, j), ("F2", s, j)], "B": [("B1", s, j), ("B2", s, j)],
+              "W": [("W2", s, j), ("W1", s, j)],
+              "BW": [("B1", s, j), ("B2", s, j), ("W2", s, j), ("W1", s, j)]}[k]
+    assert info.gemms == len(g) == 6 * L * m
+    assert all(p < c for c, p in edges)
+    clo = _reach(len(g), edges)
+    at = {x: i for i, x in enumerate(g)}
+    for (name, s, j), i in at.items():
+        need = {"F1": [("F2", s - 1, j)] if s > 0 else [],
+                "F2": [("F1", s, j)],
+                "B1": [("F1", s, j)] + ([("B2", s + 1, j)] if s < L - 1 else []),
+                "B2": [("B1", s, j)],
+                "W2": [("F1", s, j)] + ([("B2", s + 1, j)] if s < L - 1 else []),
+                "W1": [("B1", s, j)] + ([("F2", s - 1, j)] if s > 0 else [])}[name]
+        for x in need:
+            assert at[x] in clo[i], (kind, (name, s, j), x)
+    for name in ("W2", "W1"):
+        for s in range(L):
+            seq = [i for i, x in enumerate(g) if x[0] == name and x[1] == s]
+            for a, b in zip(seq, seq[1:]):
+                assert a in clo[b], (kind, name, s)
