@@ -8,13 +8,13 @@ library generates, that
 
 * the GEMM and tile counts are those of the list (6 GEMMs per stage and
   microbatch of the MLP block: H/A, Y, dH, dX, dW2, dW1);
-* every data dependency of the split backward is implied by the kept edges
-  (for one chunk per stage and, along the chain of virtual stages, for the
-  two- and three-chunk ZB-V and interleaved 1F1B lists)
-  (each edge points backwards in list order): the next stage's forward after
+* every data dependency of the split backward is implied by the kept edges,
+  each pointing backwards in list order: the next stage's forward after
   this stage's Y, B after the stage's own F (H) and after the next stage's B
   (its dX is this stage's dY), dX after dH, W after the F and B it reads, the
-  fp32 accumulation of a stage's W GEMMs in list order;
+  fp32 accumulation of a stage's W GEMMs in list order; for the two- and
+  three-chunk ZB-V and interleaved 1F1B lists the same along the chain of
+  virtual stages;
 * the priority rule follows the GEMM sizes (list order for multi-wave GEMMs,
   longest chain for small ones), and the plan holds for one pair as well;
 * the workspace size query counts the kernel's tables on top of the arena.
