@@ -343,6 +343,24 @@ def test_auto_scheduler_reproduces_printed_bubbles(row):
     assert max(S.mem_peaks(ev, P, mw)) <= limit + 1e-9
 
 
+@pytest.mark.parametrize("row", _rows("table5_consistency.txt"), ids=lambda r: f"{r[0]}-{r[2]}-{r[10]}")
+def test_other_printed_bubbles_are_consistent(row):
+    # rows whose own profiled times the pages do not print (see the fixture):
+    # close to the printed value, not exact
+    name, P, m, tf, tb, tw, tc, h, a, s_, kind, pct, tol = row
+    P, m, h, a, s_ = int(P), int(m), int(h), int(a), int(s_)
+    t = S.Times(float(tf), float(tb), float(tw), float(tc))
+    mw = 32 * h / (34 * h + 5 * a * s_)
+    if kind in ("ZB1P", "ZB2P"):
+        limit = P if kind == "ZB1P" else 2 * P
+        ev, ops, _ = S.auto_schedule_search(P, m, t, limit, mw)
+        assert max(S.mem_peaks(ev, P, mw)) <= limit + 1e-9
+    else:
+        ev, ops = S.make_schedule(kind, P, m, t)
+    assert S.validate_ops(ops, P, m)
+    assert abs(100 * S.bubble_rate(ev, P, m, t) - float(pct)) <= float(tol)
+
+
 @pytest.mark.parametrize("P,m", [(2, 4), (4, 8), (4, 24), (8, 16), (8, 24), (3, 9)])
 def test_zb1p_equals_zbh1_and_zb2p_equals_zbh2_at_equal_times(P, m):
     # ZB-1p matches ZB-H1 under the 1F1B memory limit; with 2P M_B the
