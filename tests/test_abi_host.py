@@ -224,6 +224,17 @@ def test_auto_scheduler_reproduces_printed_bubbles(zb):
         assert ops == ref_ops
 
 
+@pytest.mark.parametrize("P,m", [(2, 6), (4, 8), (6, 18), (8, 24)])
+def test_auto_scheduler_at_the_zero_bubble_threshold(zb, P, m):
+    # the same lists as the oracle at (2P-1) M_B (zero bubble at equal times)
+    # and one M_B below it (a bubble of at most one forward pass)
+    for limit in (2 * P - 1, 2 * P - 2):
+        res, ops, _ = zb.zb_auto_schedule(P, m, 1.0, 1.0, 1.0, 0.0, limit, 0.5)
+        ev, ref_ops, _ = S.auto_schedule_search(P, m, S.Times(), limit, 0.5)
+        assert ops == ref_ops and res.cost == S.cost(ev, P)
+        assert (res.cost == 3 * m) == (limit == 2 * P - 1)
+
+
 def test_auto_scheduler_rejects_bad_budget(zb):
     with pytest.raises(zb.ZBError) as e:
         zb.zb_auto_schedule(4, 8, 1, 1, 1, 0, 0.5)

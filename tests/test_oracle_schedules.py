@@ -361,6 +361,21 @@ def test_other_printed_bubbles_are_consistent(row):
     assert abs(100 * S.bubble_rate(ev, P, m, t) - float(pct)) <= float(tol)
 
 
+@pytest.mark.parametrize("P,m", [(2, 6), (3, 9), (4, 8), (4, 12), (6, 18), (8, 24)])
+def test_zero_bubble_memory_threshold_at_equal_times(P, m):
+    # "Memory Limit vs. Bubble Rate": the bubble vanishes at a budget of
+    # ((p-1)(T_B + 2 T_comm) + p T_F) / T_F M_B, which is (2p-1) M_B at
+    # T_F = T_B and no communication; below it a small bubble of at most a
+    # forward pass's time remains in the makespan
+    t = S.Times()
+    ev, ops, _ = S.auto_schedule_search(P, m, t, 2 * P - 1, 0.5)
+    assert S.validate_ops(ops, P, m)
+    assert S.cost(ev, P) == 3 * m and S.bubble_rate(ev, P, m, t) == 0.0
+    ev, ops, _ = S.auto_schedule_search(P, m, t, 2 * P - 2, 0.5)
+    assert 3 * m < S.cost(ev, P) <= 3 * m + t.F
+    assert max(S.mem_peaks(ev, P, 0.5)) <= 2 * P - 2 + 1e-9
+
+
 @pytest.mark.parametrize("P,m", [(2, 4), (4, 8), (4, 24), (8, 16), (8, 24), (3, 9)])
 def test_zb1p_equals_zbh1_and_zb2p_equals_zbh2_at_equal_times(P, m):
     # ZB-1p matches ZB-H1 under the 1F1B memory limit; with 2P M_B the
