@@ -308,6 +308,22 @@ def test_memory_ledger_peaks():
     assert peak[0] == P * M_B
 
 
+@pytest.mark.parametrize("P,m", [(2, 4), (4, 8), (4, 12), (8, 16), (8, 24)])
+@pytest.mark.parametrize("mw", [0.375, 0.5, 0.8])
+def test_per_stage_peak_of_the_memory_model(P, m, mw):
+    # "The Memory Model": stage i (from 1) peaks at (p-i+1) M_B + (i-1) M_W
+    # once B and W are separate passes, which is the split 1F1B order ZB-H1;
+    # the fused 1F1B never holds an M_W (its W runs inside BW), so its stages
+    # peak at (p-i+1) M_B
+    _, ops = S.make_schedule("ZBH1", P, m)
+    peak, final = S.memory_ledger(ops, P, 1.0, mw)
+    assert peak == pytest.approx([(P - s) + s * mw for s in range(P)])
+    assert final == pytest.approx([0.0] * P, abs=1e-9)
+    _, ops = S.make_schedule("1F1B", P, m)
+    peak, _ = S.memory_ledger(ops, P, 1.0, mw)
+    assert peak == pytest.approx([float(P - s) for s in range(P)])
+
+
 def test_comm_time_delays_dependents():
     t = S.Times(1.0, 1.0, 1.0, comm=0.25)
     ev, _ = S.make_schedule("ZBH1", 3, 6, t)
