@@ -560,15 +560,23 @@ def other_workloads(zb, dev, steps, warmup):
     ZB-H1 and ZB-H2 (split backward, W lanes), under the heuristic ZB-2p and
     the two-chunk orderings, same streams and graphs, and the h=4096
     one-stage ZB-H1 step; then the same pipeline orderings and the h=4096
-    step with the persistent executor (one kernel per step)."""
+    step with the persistent executor (one kernel per step).  A configuration
+    that fails is reported with its error; the others and the main result
+    stand."""
     import torch
     out = {}
     runs = [("c2", s, "streams") for s in ("1F1B", "ZBH1", "ZBH2", "ZB2P", "1F1B-I", "ZBV")] + [("c3", "ZBH1", "streams")]
     runs += [("c2", s, "persistent") for s in ("1F1B", "ZBH1", "ZBH2", "ZB2P", "1F1B-I", "ZBV")]
     runs += [("c3", "ZBH1", "persistent")]
     for name, sched, executor in runs:
-        w = setup_workload(zb, dev, name, sched, executor=executor)
-        r = time_workload(zb, dev, w, steps, warmup)
+        key = f"{name}_{sched}" + ("_persistent" if executor == "persistent" else "")
+        try:
+            w = setup_workload(zb, dev, name, sched, executor=executor)
+            r = time_workload(zb, dev, w, steps, warmup)
+        except Exception as exc:  # noqa: BLE001  (reported in the line; the main result stands)
+            out[key] = {"schedule": sched, "executor": executor, "error": f"{type(exc).__name__}: {exc}"[:300]}
+            torch.cuda.empty_cache()
+            continue
         if w.chunks > 1:
             wl = ("P=4 stages x 2 chunks = 8 MLP blocks h=1024 ffn=4096, microbatch 4x512 m=8, all "
                   "stages on one GPU")
@@ -580,7 +588,7 @@ def other_workloads(zb, dev, steps, warmup):
                   "pct_of_burst_peak": 100.0 * r["value"] / _peaks()["bf16"]})
         if executor == "streams":
             r["streams"] = w.pl.streams
-        out[f"{name}_{sched}" + ("_persistent" if executor == "persistent" else "")] = r
+        out[key] = r
         del w
         torch.cuda.empty_cache()
     return out
