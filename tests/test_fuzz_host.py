@@ -1,0 +1,76 @@
+"""Property-based comparison of the library's host schedulers with the oracle.
+
+Random pipeline depths, microbatch counts, pass times and communication
+times (dyadic, so both sides add exactly the same floating-point values):
+the C++ simulators of the handcrafted and the multi-chunk orderings and the
+C++ heuristic scheduler return the oracle's op lists and costs, every list
+passes the oracle's validator, and the heuristic respects its memory limit.
+CPU only (hypothesis; skipped where it is not installed).
+"""
+
+import pytest
+
+hypothesis = pytest.importorskip("hypothesis")
+from hypothesis import given, settings, strategies as st  # noqa: E402
+
+from oracle import schedules as S  # noqa: E402
+from split_backward_gemms_gb300 import build as B  # noqa: E402
+
+B.build()
+from split_backward_gemms_gb300 import zb  # noqa: E402
+
+dyadic = st.integers(min_value=1, max_value=24).map(lambda k: k / 8)
+comm = st.integers(min_value=0, max_value=8).map(lambda k: k / 16)
+
+
+@st.composite
+def pipelines(draw):
+    P = draw(st.integers(min_value=1, max_value=8))
+    m = draw(st.integers(min_value=1, max_value=3 * P + 3))
+    return P, m
+
+
+@settings(max_examples=400, deadline=None)
+@given(pipelines(), st.sampled_from(S.SCHEDULES), dyadic, dyadic, dyadic, comm)
+def test_simulator_matches_oracle(pm, kind, tf, tb, tw, tc):
+    P, m = pm
+    t = S.Times(tf, tb, tw, tc)
+    ev, ref_ops = S.make_schedule(kind, P, m, t)
+    res, ops = zb.zb_simulate_schedule(kind, P, m, tf, tb, tw, tc, want_ops=True)
+    assert ops == ref_ops
+    assert res.cost == S.cost(ev, P)
+    assert S.validate_ops(ops, P, m)
+
+
+@settings(max_examples=300, deadline=None)
+@given(pipelines(), st.integers(min_value=0, max_value=8), dyadic, dyadic, dyadic, comm,
+       st.sampled_from([0.25, 0.375, 0.5, 0.75, 1.0]))
+def test_auto_scheduler_matches_oracle(pm, extra, tf, tb, tw, tc, mw):
+    P, m = pm
+    limit = P + extra * P / 8  # between the 1F1B budget and twice it
+    t = S.Times(tf, tb, tw, tc)
+    ev, ref_ops, ref_h = S.auto_schedule_search(P, m, t, limit, mw)
+    res, ops, hyper = zb.zb_auto_schedule(P, m, tf, tb, tw, tc, limit, mw)
+    assert ops == ref_ops and hyper == ref_h
+    assert res.cost == S.cost(ev, P)
+    assert S.validate_ops(ops, P, m)
+    assert max(S.mem_peaks(ev, P, mw)) <= limit + 1e-9
+
+
+@settings(max_examples=300, deadline=None)
+@given(st.sampled_from(["ZBV", "1F1B-I"]), st.integers(min_value=1, max_value=6),
+       st.integers(min_value=2, max_value=3), st.integers(min_value=1, max_value=4),
+       dyadic, dyadic, dyadic, comm)
+def test_interleaved_simulator_matches_oracle(kind, P, v, k, tf, tb, tw, tc):
+    from oracle import interleaved as IL
+    if kind == "ZBV":
+        v, m = 2, k * P - (k % 2)  # odd and even microbatch counts, from P - 1 up
+        m = max(m, 1)
+    else:
+        m = k * P  # whole groups of P microbatches
+    t = S.Times(tf, tb, tw, tc)
+    ev, ref_ops = IL.make_interleaved_schedule(kind, P, v, m, t)
+    res, ops = zb.zb_simulate_interleaved_schedule(kind, P, v, m, tf, tb, tw, tc, want_ops=True)
+    assert ops == ref_ops
+    assert abs(res.bubble_rate - IL.bubble_rate(ev, P, m, t)) < 1e-12
+    assert IL.validate_interleaved(kind, P, v, m, ops)
