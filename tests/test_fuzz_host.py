@@ -4,8 +4,10 @@ Random pipeline depths, microbatch counts, pass times and communication
 times (dyadic, so both sides add exactly the same floating-point values):
 the C++ simulators of the handcrafted and the multi-chunk orderings and the
 C++ heuristic scheduler return the oracle's op lists and costs, every list
-passes the oracle's validator, and the heuristic respects its memory limit.
-CPU only (hypothesis; skipped where it is not installed).
+passes the oracle's validator, and the heuristic respects its memory limit;
+the persistent executor's host plan of random lists, for any number of CTA
+pairs, keeps every data dependency (and passes its own deadlock check).  CPU
+only (hypothesis; skipped where it is not installed).
 """
 
 import pytest
@@ -74,3 +76,34 @@ def test_interleaved_simulator_matches_oracle(kind, P, v, k, tf, tb, tw, tc):
     assert ops == ref_ops
     assert abs(res.bubble_rate - IL.bubble_rate(ev, P, m, t)) < 1e-12
     assert IL.validate_interleaved(kind, P, v, m, ops)
+
+
+@settings(max_examples=60, deadline=None)
+@given(st.sampled_from(["1F1B", "ZBH1", "ZBH2", "ZB1P", "ZB2P"]), pipelines(),
+       st.sampled_from([(96, 256, 512), (256, 256, 1024), (520, 264, 1048), (2048, 1024, 4096)]),
+       st.integers(min_value=1, max_value=76))
+def test_persistent_plan_keeps_every_data_dependency(kind, pm, shape, pairs):
+    # the persistent executor's host plan on random lists: every data
+    # dependency of the split backward implied by its kept edges
+    from tests.test_persistent_plan import _gemms, _reach
+    P, m = pm
+    M, h, f = shape
+    if kind in ("ZB1P", "ZB2P"):
+        limit = P if kind == "ZB1P" else 2 * P
+        _, ops, _ = zb.zb_auto_schedule(P, m, 1.0, 1.0, 1.0, 0.0, limit, 1.0)
+    else:
+        ops = zb.zb_make_schedule(kind, P, m)
+    info, edges = zb.zb_persistent_plan(zb.make_pipeline(P, m, zb.make_block(M, h, f)), ops, pairs=pairs)
+    g = _gemms(ops)
+    assert info.gemms == len(g) == 6 * P * m and all(p < c for c, p in edges)
+    clo = _reach(len(g), edges)
+    at = {x: i for i, x in enumerate(g)}
+    for (name, s, j), i in at.items():
+        need = {"F1": [("F2", s - 1, j)] if s > 0 else [],
+                "F2": [("F1", s, j)],
+                "B1": [("F1", s, j)] + ([("B2", s + 1, j)] if s < P - 1 else []),
+                "B2": [("B1", s, j)],
+                "W2": [("F1", s, j)] + ([("B2", s + 1, j)] if s < P - 1 else []),
+                "W1": [("B1", s, j)] + ([("F2", s - 1, j)] if s > 0 else [])}[name]
+        for x in need:
+            assert at[x] in clo[i], (kind, (name, s, j), x)
