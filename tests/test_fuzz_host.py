@@ -6,8 +6,10 @@ the C++ simulators of the handcrafted and the multi-chunk orderings and the
 C++ heuristic scheduler return the oracle's op lists and costs, every list
 passes the oracle's validator, and the heuristic respects its memory limit;
 the persistent executor's host plan of random lists, for any number of CTA
-pairs, keeps every data dependency (and passes its own deadlock check).  CPU
-only (hypothesis; skipped where it is not installed).
+pairs, keeps every data dependency (and passes its own deadlock check); the
+oracle's trace checker accepts every simulated step and rejects it once one
+pass starts before a producer has ended.  CPU only (hypothesis; skipped
+where it is not installed).
 """
 
 import pytest
@@ -107,3 +109,37 @@ def test_persistent_plan_keeps_every_data_dependency(kind, pm, shape, pairs):
                 "W1": [("B1", s, j)] + ([("F2", s - 1, j)] if s > 0 else [])}[name]
         for x in need:
             assert at[x] in clo[i], (kind, (name, s, j), x)
+
+
+@settings(max_examples=150, deadline=None)
+@given(pipelines(), st.sampled_from(S.SCHEDULES), dyadic, dyadic, dyadic, comm, st.data())
+def test_trace_checker_accepts_simulated_and_rejects_early_starts(pm, kind, tf, tb, tw, tc, data):
+    # every simulated step passes the oracle's trace checker, with and without
+    # the trace's own dependency claims; moving one pass so that it starts
+    # before one of its producers has ended (same length) is rejected
+    P, m = pm
+    t = S.Times(tf, tb, tw, tc)
+    ev, _ = S.make_schedule(kind, P, m, t)
+    evs = S.events_as_dicts(ev)
+    r = S.check_trace(evs, P)
+    assert abs(r["bubble_eq3"] - S.bubble_rate(ev, P, m, t)) < 1e-12
+    bare = [{k: v for k, v in e.items() if k != "dependsOn"} for e in evs]
+    assert S.check_trace(bare, P) == r
+    with_producer = [e for e in evs if e["dependsOn"]]
+    if not with_producer:
+        return
+    victim = data.draw(st.sampled_from(with_producer))
+    ends = {e["id"]: e["end"] for e in evs}
+    latest = max(ends[p] for p in victim["dependsOn"])
+    shift = victim["start"] - latest + data.draw(st.sampled_from([0.0625, 0.25, 1.0]))
+    moved = []
+    for e in bare:
+        e = dict(e)
+        if e["id"] == victim["id"]:
+            e["start"], e["end"] = e["start"] - shift, e["end"] - shift
+        moved.append(e)
+    if victim["start"] - shift < 0:
+        return  # the move would leave the trace's time range
+    with pytest.raises(S.ScheduleError) as ei:
+        S.check_trace(moved, P)
+    assert ei.value.code in ("early_consumer", "stage_collision")
