@@ -1,4 +1,4 @@
-"""Property-based comparison of the library's host schedulers with the oracle.
+"""Property-based tests of the host schedulers, the planner and the oracle.
 
 Random pipeline depths, microbatch counts, pass times and communication
 times (dyadic, so both sides add exactly the same floating-point values):
@@ -8,7 +8,8 @@ passes the oracle's validator, and the heuristic respects its memory limit;
 the persistent executor's host plan of random lists, for any number of CTA
 pairs, keeps every data dependency (and passes its own deadlock check); the
 oracle's trace checker accepts every simulated step and rejects it once one
-pass starts before a producer has ended.  CPU only (hypothesis; skipped
+pass starts before a producer has ended; the fp64 block's gradients match
+central differences on random tiny shapes.  CPU only (hypothesis; skipped
 where it is not installed).
 """
 
@@ -143,3 +144,37 @@ def test_trace_checker_accepts_simulated_and_rejects_early_starts(pm, kind, tf, 
     with pytest.raises(S.ScheduleError) as ei:
         S.check_trace(moved, P)
     assert ei.value.code in ("early_consumer", "stage_collision")
+
+
+@settings(max_examples=60, deadline=None)
+@given(st.integers(1, 6), st.integers(1, 5), st.integers(1, 8), st.sampled_from(["gelu_erf", "gelu_tanh"]),
+       st.booleans(), st.integers(0, 2**31 - 1))
+def test_block_oracle_gradients_match_finite_differences(M, h, f, act, bias, seed):
+    # the fp64 block's B and W against central differences of L = sum(Y * G)
+    # on random tiny shapes (calculus, not the oracle, fixes the gradients)
+    import numpy as np
+    from oracle import block as ob
+    rng = np.random.default_rng(seed)
+    X, G = rng.standard_normal((M, h)), rng.standard_normal((M, h))
+    W1, W2 = rng.standard_normal((h, f)) * 0.7, rng.standard_normal((f, h)) * 0.7
+    b1 = rng.standard_normal(f) * 0.3 if bias else None
+    b2 = rng.standard_normal(h) * 0.3 if bias else None
+    H, A, _ = ob.forward(X, W1, W2, b1, b2, act)
+    _, dH, dX = ob.backward_input(G, W1, W2, H, act)
+    dW1, dW2, db1, db2 = ob.backward_weight(X, A, dH, G, act)
+
+    def loss():
+        return float(np.sum(ob.forward(X, W1, W2, b1, b2, act)[2] * G))
+
+    params = [(dX, X), (dW1, W1), (dW2, W2)] + ([(db1, b1), (db2, b2)] if bias else [])
+    for got, p in params:
+        fd = np.zeros_like(p)
+        for i in np.ndindex(p.shape):
+            old = p[i]
+            p[i] = old + 1e-6
+            lp = loss()
+            p[i] = old - 1e-6
+            lm = loss()
+            p[i] = old
+            fd[i] = (lp - lm) / 2e-6
+        assert np.abs(got - fd).max() <= 1e-6 * max(1.0, np.abs(fd).max())
